@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GMM EM step on GB300.
+
+One step = one EM iteration over the whole workload (prepare, E-step with
+log-sum-exp, statistics, reduction, M-step), inputs resident in HBM.
+Prints ONE JSON line (rank 0).  Workloads are the synthetic ones of
+datagen.WORKLOADS; the default is the 10M-point, D=128, K=256 fp16 diagonal
+EM workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline] [--no-e2e]
+
+--impl reference times the fp64 CPU oracle (the reference this path is
+checked against) on a bounded sample of the same workload, on the host
+cores.  Under torchrun (N > 1) each rank runs an independent replica of the
+workload on its own GPU (the EM step is not sharded here): scaling "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused EM step N*K pairs/s (1 x GB300)"
+UNIT = "pairs/s"
+DEFAULT_WORKLOAD = "embed_diag"
+COV_NAMES = {0: "full", 1: "diag", 2: "iso"}
+XNAMES = {0: "f32", 1: "f16", 2: "bf16"}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                sm_max_mhz=2070.0, source="fallback")
+
+
+# ---------------------------------------------------------------- work model
+
+def work_model(wl):
+    """Algorithmic flops / bytes of one EM step and of each kernel (per launch).
+    Diagonal / isotropic: 4D flops per point-component pair for the log-density
+    ([x, x^2] . [mu/var, -1/(2 var)]) and 4D for the statistics; full: D(D+1)
+    for the triangular solve and D(D+1) + 2D for the statistics."""
+    N, D, K = wl.N, wl.D, wl.K
+    esz = 4 if wl.dtype == 0 else 2
+    pairs = N * K
+    if wl.cov_type == 0:
+        e_flops, s_flops = D * (D + 1), D * (D + 1) + 2 * D
+        pbytes = 4 * K * (1 + D + D * D)
+    else:
+        e_flops, s_flops = 4 * D, 4 * D
+        pbytes = 4 * K * (1 + 2 * D)
+    x_bytes = N * D * esz
+    return dict(
+        pairs=pairs,
+        step_flops=pairs * (e_flops + s_flops),
+        step_bytes=x_bytes + 2 * pbytes,
+        x_bytes=x_bytes,
+        kernels={
+            # two-pass CUDA-core path: the LSE pass computes every log-density;
+            # the statistics pass recomputes them and accumulates the moments
+            "lse_kernel": dict(flops=pairs * e_flops, bytes=x_bytes + 4 * N),
+            "stats_kernel": dict(flops=pairs * (e_flops + s_flops), bytes=x_bytes + 4 * N),
+        })
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception as e:  # no nvidia-smi
+            log("clock sampling unavailable:", e)
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                     power=float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                                     hw=parts[5], hw_th=parts[6], sw_th=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_th", "hw_thermal_slowdown"),
+                              ("sw_th", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in rows),
+                    sm_max_mhz=max(r["sm_max"] for r in rows), samples=len(rows),
+                    reasons=sorted(reasons))
+
+
+# ---------------------------------------------------------------- helpers
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu capture, if the kernel's
+    sources are unchanged since it was taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(kernel, {}).get(workload)
+    if not rec:
+        return None
+    if rec.get("src_sha") != source_sha():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def source_sha():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "soft_clustering_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_sample_run(wl, mix, seconds):
+    """The oracle (as it stands) on the first n' points of the workload, one
+    EM iteration from theta_0; n' sized for about `seconds` of work.
+    Returns (pairs_per_s, n', threads, seconds_taken)."""
+    import datagen
+    import oracle
+    n_cal = min(wl.N, 256)
+    bits = datagen.points(mix, 0, n_cal)
+    theta = datagen.init_params(mix)
+    t0 = time.perf_counter()
+    oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype)
+    per_point = max((time.perf_counter() - t0) / n_cal, 1e-9)
+    n = int(min(wl.N, max(n_cal, seconds / per_point)))
+    bits = datagen.points(mix, 0, n)
+    t0 = time.perf_counter()
+    oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype)
+    dt = time.perf_counter() - t0
+    return n * wl.K / dt, n, oracle.max_threads(), dt
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, wl):
+    """The fp64 oracle timed on the host cores on a bounded sample per step."""
+    import datagen
+    import oracle
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    mix = datagen.planted(wl)
+    total_steps = args.steps + args.warmup
+    per_step_s = max(2.0, min(20.0, 150.0 / max(total_steps, 1)))
+    _, n, threads, _ = cpu_sample_run(wl, mix, per_step_s)
+    bits = datagen.points(mix, 0, n)
+    theta = datagen.init_params(mix)
+    pi, mu, cov = theta
+    for _ in range(args.warmup):
+        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype)
+        times.append(time.perf_counter() - t0)
+        pi, mu, cov = r["pi"], r["mu"], r["cov"]
+    ms = 1e3 * sum(times) / len(times)
+    value = n * wl.K / (ms / 1e3)
+    sample = "first %d of %d points, one EM iteration per step (fp64 oracle)" % (n, wl.N)
+    line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=config_dict(wl, extra=dict(sample_points=n)),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=threads, kind="oracle",
+                                  sample=sample),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(wl, extra=None):
+    d = dict(workload=wl.name, N=wl.N, D=wl.D, K=wl.K, cov=COV_NAMES[wl.cov_type],
+             x_dtype=XNAMES[wl.dtype], l2="inputs larger than L2 (X is %.2f GB > 129 MB)"
+             % (wl.N * wl.D * (4 if wl.dtype == 0 else 2) / 1e9))
+    if extra:
+        d.update(extra)
+    return d
+
+
+def run_ours(args, wl):
+    import torch
+    import datagen
+    import soft_clustering_gb300 as G
+    from soft_clustering_gb300 import build as gbuild
+    from soft_clustering_gb300.torch_api import GMMState
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        gbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    G.lib()
+    peaks = measured_peaks()
+    wm = work_model(wl)
+
+    # inputs: drawn straight into HBM (same bits the host generator gives)
+    mix = datagen.planted(wl)
+    keep, ptrs = datagen.upload_tables(mix, device=dev)
+    esz = 4 if wl.dtype == 0 else 2
+    X = torch.empty(wl.N * wl.D * esz, dtype=torch.uint8, device=dev)
+    datagen.device_points(mix, 0, wl.N, X.data_ptr(), torch.cuda.current_stream().cuda_stream,
+                          ptrs)
+    theta0 = datagen.init_params(mix)
+    torch.cuda.synchronize()
+
+    st = GMMState(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, device=dev)
+    st.set_params(*theta0)
+    for _ in range(args.warmup):
+        st.step(X)
+    torch.cuda.synchronize()
+    status = st.device_status()
+    if status != 0:
+        log("device status after warm-up:", G.status_string(status))
+
+    # timed region: device-resident X, CUDA events on the launching stream
+    G.gmm_profile_reset()
+    G.gmm_profile_enable(True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        st.step(X)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    G.gmm_profile_enable(False)
+    prof = G.gmm_profile_read()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = st.device_status()
+    ll = float(st.loglik.item())
+    value = world * wm["pairs"] / (ms / 1e3)
+    launches = sum(n for (_, n) in prof.values())
+
+    # dominant kernel roofline, measured live in the timed region
+    top = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
+    roof = None
+    if top:
+        tot_ms, n_launch = prof[top]
+        avg_s = tot_ms / n_launch / 1e3
+        km = wm["kernels"].get(top)
+        # CUDA-core fp32 kernels: ALU peak = 152 SMs x 128 lanes x 2 flops x max SM clock
+        alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        if km:
+            achieved = km["flops"] / avg_s / 1e12
+            roof = dict(bound="alu", achieved=achieved, peak=alu_peak, unit="TFLOP/s",
+                        frac=achieved / alu_peak, traffic=traffic_for(top, wl.name),
+                        kernel=top, avg_launch_ms=tot_ms / n_launch,
+                        peak_source="fp32 FMA lanes x clock (derived)")
+    step_roof_s = max(wm["step_flops"] / (peaks["bf16_tflops"] * 1e12),
+                      wm["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
+
+    # end to end through the host-buffer entry point: X streamed from pinned
+    # host memory every step, log-likelihood read back every step
+    e2e = None
+    if not args.no_e2e:
+        chunk = max(1, min(wl.N, (256 << 20) // (wl.D * esz)))
+        st2 = GMMState(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, device=dev, chunk_rows=chunk)
+        st2.set_params(*theta0)
+        host = torch.empty(wl.N * wl.D * esz, dtype=torch.uint8, pin_memory=True)
+        host.copy_(X)
+        ll_host = torch.zeros(1, dtype=torch.float64, pin_memory=True)
+        del X
+        torch.cuda.empty_cache()
+        st2.step_host(host, loglik_host=ll_host)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            st2.step_host(host, loglik_host=ll_host)
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = dict(value=world * wm["pairs"] / e2e_s, unit=UNIT,
+                   h2d_bytes_per_step=wm["x_bytes"], d2h_bytes_per_step=8,
+                   ms_per_step=e2e_s * 1e3, chunk_rows=chunk)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, thr, dt = cpu_sample_run(wl, mix, 15.0)
+        cpu = dict(value=v, unit=UNIT, cores=thr, kind="oracle",
+                   sample="first %d of %d points, one EM iteration from theta_0, %.1f s" %
+                   (n, wl.N, dt))
+
+    if rank == 0:
+        line = dict(
+            metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+            warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+            vs_baseline=None, dtype="f32", data="synthetic",
+            config=config_dict(wl, extra=dict(
+                iters_per_s=1e3 / ms, parallelism="replicas" if world > 1 else "single",
+                loglik=ll, device_status=G.status_string(status),
+                step_roofline=dict(flops=wm["step_flops"], bytes=wm["step_bytes"],
+                                   roofline_ms=step_roof_s * 1e3,
+                                   frac=step_roof_s * 1e3 / ms,
+                                   peaks="bf16 %.1f TFLOP/s, HBM %.1f GB/s (%s)" % (
+                                       peaks["bf16_tflops"], peaks["hbm_gbs"], peaks["source"])),
+                kernels={k: dict(ms_per_launch=v[0] / v[1], launches=v[1])
+                         for k, v in prof.items()})),
+            roofline=roof, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clk)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    import datagen
+    wl = datagen.WORKLOADS[args.workload]
+    if wl.m:
+        raise SystemExit("assignment workloads are benchmarked by bench_assign (not yet)")
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,416 @@
+// gmm_api.cu - the C ABI declared in include/gmm.h: argument checks,
+// workspace layout and the order of kernel launches for one EM iteration.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "gmm_internal.cuh"
+
+namespace gmm {
+
+cudaError_t launch_prepare(const gmm_params* p, int D, int K, int cov, float ridge_rel,
+                           void* prepared, DeviceStatus* st, cudaStream_t s);
+cudaError_t simt_lse(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                     const void* prepared, float* lse, double* ll_part, int m, int32_t* ids,
+                     float* gamma, DeviceStatus* st, cudaStream_t s);
+cudaError_t simt_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                       const void* prepared, const float* lse, int parts, double* part,
+                       int accumulate, cudaStream_t s);
+int simt_stat_chunk(int D, int cov);
+cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
+                         const float* centre, const int32_t* prep_flags, float var_floor,
+                         float min_s0, gmm_params* p, int32_t* flags_out, cudaStream_t s);
+cudaError_t launch_ll_finalize(const double* ll_part, int64_t n, double* out, int accumulate,
+                               cudaStream_t s);
+
+namespace {
+
+constexpr int kLseRows = 128;      // rows per block of the LSE kernel
+constexpr int kTargetCtas = 608;   // 4 x 152 SMs: statistics blocks per launch
+constexpr int kMaxK = 1 << 16;
+
+bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
+size_t esize(int xdtype) { return xdtype == GMM_F32 ? 4 : 2; }
+
+// Point partitions of the statistics kernel: enough blocks to fill the GPU,
+// fixed by the sizes alone so the reduction order never depends on the device.
+int stat_parts(int64_t N, int D, int K, int cov) {
+  const int kc = simt_stat_chunk(D, cov);
+  const int64_t chunks = (K + kc - 1) / kc;
+  int64_t p = (kTargetCtas + chunks - 1) / chunks;
+  const int64_t tiles = (N + 63) / 64;
+  if (p > tiles) p = tiles;
+  if (p < 1) p = 1;
+  return (int)p;
+}
+
+struct WsLayout {
+  size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_stage,
+      bytes;
+  int parts;
+  int64_t lse_rows;
+};
+
+// rows: rows processed per launch (N, or the chunk size of the host path);
+// stage_bytes: host path staging buffers (0 otherwise).
+WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_bytes) {
+  WsLayout W;
+  size_t o = 0;
+  W.off_status = o; o = align_up(o + sizeof(DeviceStatus));
+  W.off_prep = o;   o = align_up(o + PreparedLayout::make(D, K, cov).bytes);
+  W.lse_rows = rows;
+  W.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)rows);
+  W.off_llpart = o; o = align_up(o + sizeof(double) * (size_t)((rows + kLseRows - 1) / kLseRows));
+  W.off_ll = o;     o = align_up(o + sizeof(double));
+  W.parts = stat_parts(rows, D, K, cov);
+  W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)W.parts * K * stat_width(D, cov));
+  W.off_flags = o;  o = align_up(o + sizeof(int32_t) * K);
+  W.off_stage = o;  o = align_up(o + stage_bytes);
+  W.bytes = o;
+  (void)N;
+  return W;
+}
+
+gmm_status check_common(const void* X, gmm_dtype xdtype, int64_t N, int D, int K, int cov) {
+  if (!X || N < 1 || K < 1 || K > kMaxK) return GMM_ERR_INVALID_ARG;
+  if (xdtype < GMM_F32 || xdtype > GMM_BF16) return GMM_ERR_INVALID_ARG;
+  if (cov < GMM_COV_FULL || cov > GMM_COV_ISO) return GMM_ERR_INVALID_ARG;
+  if (!valid_d(D)) return D > 0 ? GMM_ERR_UNSUPPORTED : GMM_ERR_INVALID_ARG;
+  return GMM_OK;
+}
+
+gmm_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return GMM_OK;
+  fprintf(stderr, "libgmm: CUDA error %s\n", cudaGetErrorString(e));
+  return GMM_ERR_CUDA;
+}
+
+#define GMM_TRY(expr)                                  \
+  do {                                                 \
+    gmm_status _s = cuda_status(expr);                 \
+    if (_s != GMM_OK) return _s;                       \
+  } while (0)
+
+// ---------------------------------------------------------------- profiler
+// When enabled, every kernel launch of the library is bracketed by two CUDA
+// events recorded on the launching stream; gmm_profile_read sums them per
+// kernel.  Off by default (no events recorded).
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_pending;
+std::vector<cudaEvent_t> g_prof_pool;
+struct ProfSum { const char* name; double ms; long launches; };
+std::vector<ProfSum> g_prof_sum;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) { cudaEvent_t e = g_prof_pool.back(); g_prof_pool.pop_back(); return e; }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct ProfScope {
+  const char* name; cudaStream_t s; cudaEvent_t a = nullptr;
+  ProfScope(const char* n, cudaStream_t st) : name(n), s(st) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (g_prof_on) { a = prof_event(); cudaEventRecord(a, s); }
+  }
+  ~ProfScope() {
+    if (!a) return;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    cudaEvent_t b = prof_event();
+    cudaEventRecord(b, s);
+    g_prof_pending.push_back({name, a, b});
+  }
+};
+
+#define GMM_PROF(name) ProfScope _prof_scope(name, s)
+
+// The E-step and statistics for one block of rows, accumulating into the
+// workspace partials (accumulate = 0 for the first block of an iteration).
+gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int K, int cov,
+                      const WsLayout& W, void* ws, float* lse, int accumulate, cudaStream_t s) {
+  DeviceStatus* st = at<DeviceStatus>(ws, W.off_status);
+  const void* prep = at<char>(ws, W.off_prep);
+  double* llp = at<double>(ws, W.off_llpart);
+  {
+    GMM_PROF("lse_kernel");
+    GMM_TRY(simt_lse(X, xdtype, rows, D, K, cov, prep, lse, llp, 0, nullptr, nullptr, st, s));
+  }
+  {
+    GMM_PROF("ll_finalize_kernel");
+    GMM_TRY(launch_ll_finalize(llp, (rows + kLseRows - 1) / kLseRows, at<double>(ws, W.off_ll),
+                               accumulate, s));
+  }
+  {
+    GMM_PROF("stats_kernel");
+    GMM_TRY(simt_stats(X, xdtype, rows, D, K, cov, prep, lse, W.parts,
+                       at<double>(ws, W.off_part), accumulate, s));
+  }
+  return GMM_OK;
+}
+
+// Library-owned copy stream and events of the host path (one set per device).
+struct HostPathRes {
+  cudaStream_t copy = nullptr;
+  cudaEvent_t copied[2] = {nullptr, nullptr};
+  cudaEvent_t consumed[2] = {nullptr, nullptr};
+};
+std::mutex g_res_mu;
+HostPathRes g_res[64];
+
+gmm_status host_res(HostPathRes** out) {
+  int dev = 0;
+  GMM_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return GMM_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_res_mu);
+  HostPathRes& r = g_res[dev];
+  if (!r.copy) {
+    GMM_TRY(cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking));
+    for (int i = 0; i < 2; ++i) {
+      GMM_TRY(cudaEventCreateWithFlags(&r.copied[i], cudaEventDisableTiming));
+      GMM_TRY(cudaEventCreateWithFlags(&r.consumed[i], cudaEventDisableTiming));
+    }
+  }
+  *out = &r;
+  return GMM_OK;
+}
+
+}  // namespace
+}  // namespace gmm
+
+using namespace gmm;
+
+extern "C" {
+
+gmm_opts gmm_default_opts(void) {
+  gmm_opts o;
+  o.ridge_rel = 0.0f;
+  o.var_floor = 0.0f;
+  o.min_s0 = 1e-3f;
+  o.flags = 0;
+  return o;
+}
+
+const char* gmm_status_string(gmm_status s) {
+  switch (s) {
+    case GMM_OK: return "GMM_OK";
+    case GMM_ERR_INVALID_ARG: return "GMM_ERR_INVALID_ARG";
+    case GMM_ERR_UNSUPPORTED: return "GMM_ERR_UNSUPPORTED";
+    case GMM_ERR_NOT_PD: return "GMM_ERR_NOT_PD";
+    case GMM_ERR_NONFINITE: return "GMM_ERR_NONFINITE";
+    case GMM_ERR_WORKSPACE: return "GMM_ERR_WORKSPACE";
+    case GMM_ERR_TIMEOUT: return "GMM_ERR_TIMEOUT";
+    case GMM_ERR_CUDA: return "GMM_ERR_CUDA";
+  }
+  return "unknown gmm_status";
+}
+
+size_t gmm_prepared_bytes(int D, int K, gmm_cov_type cov) {
+  if (!valid_d(D) || K < 1 || K > kMaxK || cov < GMM_COV_FULL || cov > GMM_COV_ISO) return 0;
+  return PreparedLayout::make(D, K, cov).bytes;
+}
+
+size_t gmm_workspace_bytes(int64_t N, int D, int K, gmm_cov_type cov, gmm_dtype xdtype) {
+  if (N < 1 || !valid_d(D) || K < 1 || K > kMaxK || cov < GMM_COV_FULL || cov > GMM_COV_ISO ||
+      xdtype < GMM_F32 || xdtype > GMM_BF16)
+    return 0;
+  return ws_layout(N, N, D, K, cov, 0).bytes;
+}
+
+size_t gmm_workspace_bytes_host(int64_t N, int D, int K, gmm_cov_type cov, gmm_dtype xdtype,
+                                int64_t chunk_rows) {
+  if (chunk_rows < 1 || gmm_workspace_bytes(N, D, K, cov, xdtype) == 0) return 0;
+  int64_t rows = chunk_rows < N ? chunk_rows : N;
+  size_t stage = 2 * align_up((size_t)rows * D * esize(xdtype));
+  return ws_layout(N, rows, D, K, cov, stage).bytes;
+}
+
+gmm_status gmm_prepare(const gmm_params* p, int D, int K, gmm_cov_type cov, const gmm_opts* opts,
+                       void* prepared, int32_t* flags_dev, void* stream) {
+  if (!p || !p->pi || !p->mu || !p->cov || !prepared || K < 1 || K > kMaxK) return GMM_ERR_INVALID_ARG;
+  if (cov < GMM_COV_FULL || cov > GMM_COV_ISO) return GMM_ERR_INVALID_ARG;
+  if (!valid_d(D)) return D > 0 ? GMM_ERR_UNSUPPORTED : GMM_ERR_INVALID_ARG;
+  gmm_opts o = opts ? *opts : gmm_default_opts();
+  cudaStream_t s = (cudaStream_t)stream;
+  {
+    GMM_PROF("prepare_kernel");
+    GMM_TRY(launch_prepare(p, D, K, cov, o.ridge_rel, prepared, nullptr, s));
+  }
+  if (flags_dev) {
+    PreparedLayout L = PreparedLayout::make(D, K, cov);
+    GMM_TRY(cudaMemcpyAsync(flags_dev, at<char>(prepared, L.off_flags), sizeof(int32_t) * K,
+                            cudaMemcpyDeviceToDevice, s));
+  }
+  return GMM_OK;
+}
+
+gmm_status gmm_em_step(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
+                       gmm_params* params, gmm_cov_type cov, const gmm_opts* opts, void* ws,
+                       size_t ws_bytes, double* loglik_dev, float* lse_dev, int32_t* flags_dev,
+                       void* stream) {
+  gmm_status c = check_common(X, xdtype, N, D, K, cov);
+  if (c != GMM_OK) return c;
+  if (!params || !params->pi || !params->mu || !params->cov || !ws || !loglik_dev)
+    return GMM_ERR_INVALID_ARG;
+  if (((uintptr_t)X & 15) || ((uintptr_t)ws & 255)) return GMM_ERR_INVALID_ARG;
+  WsLayout W = ws_layout(N, N, D, K, cov, 0);
+  if (ws_bytes < W.bytes) return GMM_ERR_WORKSPACE;
+  gmm_opts o = opts ? *opts : gmm_default_opts();
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus* st = at<DeviceStatus>(ws, W.off_status);
+  void* prep = at<char>(ws, W.off_prep);
+  PreparedLayout PL = PreparedLayout::make(D, K, cov);
+  GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
+  {
+    GMM_PROF("prepare_kernel");
+    GMM_TRY(launch_prepare(params, D, K, cov, o.ridge_rel, prep, st, s));
+  }
+  float* lse = lse_dev ? lse_dev : at<float>(ws, W.off_lse);
+  gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, 0, s);
+  if (r != GMM_OK) return r;
+  {
+    GMM_PROF("mstep_kernel");
+    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), W.parts, N, D, K, cov,
+                         at<float>(prep, PL.off_mu), at<int32_t>(prep, PL.off_flags), o.var_floor,
+                         o.min_s0, params, flags_dev ? flags_dev : at<int32_t>(ws, W.off_flags),
+                         s));
+  }
+  GMM_TRY(cudaMemcpyAsync(loglik_dev, at<double>(ws, W.off_ll), sizeof(double),
+                          cudaMemcpyDeviceToDevice, s));
+  return GMM_OK;
+}
+
+gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int D, int K,
+                            gmm_params* params, gmm_cov_type cov, const gmm_opts* opts, void* ws,
+                            size_t ws_bytes, int64_t chunk_rows, double* loglik_dev,
+                            double* loglik_host, int32_t* flags_dev, void* stream) {
+  gmm_status c = check_common(X_host, xdtype, N, D, K, cov);
+  if (c != GMM_OK) return c;
+  if (!params || !params->pi || !params->mu || !params->cov || !ws || !loglik_dev ||
+      chunk_rows < 1 || ((uintptr_t)ws & 255))
+    return GMM_ERR_INVALID_ARG;
+  const int64_t rows = chunk_rows < N ? chunk_rows : N;
+  const size_t stage_one = align_up((size_t)rows * D * esize(xdtype));
+  WsLayout W = ws_layout(N, rows, D, K, cov, 2 * stage_one);
+  if (ws_bytes < W.bytes) return GMM_ERR_WORKSPACE;
+  HostPathRes* res = nullptr;
+  gmm_status rr = host_res(&res);
+  if (rr != GMM_OK) return rr;
+  gmm_opts o = opts ? *opts : gmm_default_opts();
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus* st = at<DeviceStatus>(ws, W.off_status);
+  void* prep = at<char>(ws, W.off_prep);
+  PreparedLayout PL = PreparedLayout::make(D, K, cov);
+  char* stage[2] = {at<char>(ws, W.off_stage), at<char>(ws, W.off_stage + stage_one)};
+  GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
+  {
+    GMM_PROF("prepare_kernel");
+    GMM_TRY(launch_prepare(params, D, K, cov, o.ridge_rel, prep, st, s));
+  }
+  // The copy stream may start only after earlier work on `s` that used the
+  // staging buffers is done.
+  GMM_TRY(cudaEventRecord(res->consumed[0], s));
+  GMM_TRY(cudaEventRecord(res->consumed[1], s));
+  const int64_t nchunks = (N + rows - 1) / rows;
+  const size_t esz = esize(xdtype);
+  for (int64_t ci = 0; ci < nchunks; ++ci) {
+    const int b = (int)(ci & 1);
+    const int64_t r0 = ci * rows;
+    const int64_t rn = (N - r0) < rows ? (N - r0) : rows;
+    GMM_TRY(cudaStreamWaitEvent(res->copy, res->consumed[b], 0));
+    GMM_TRY(cudaMemcpyAsync(stage[b], (const char*)X_host + (size_t)r0 * D * esz,
+                            (size_t)rn * D * esz, cudaMemcpyHostToDevice, res->copy));
+    GMM_TRY(cudaEventRecord(res->copied[b], res->copy));
+    GMM_TRY(cudaStreamWaitEvent(s, res->copied[b], 0));
+    gmm_status r = estep_rows(stage[b], xdtype, rn, D, K, cov, W, ws, at<float>(ws, W.off_lse),
+                              ci > 0, s);
+    if (r != GMM_OK) return r;
+    GMM_TRY(cudaEventRecord(res->consumed[b], s));
+  }
+  {
+    GMM_PROF("mstep_kernel");
+    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), W.parts, N, D, K, cov,
+                         at<float>(prep, PL.off_mu), at<int32_t>(prep, PL.off_flags), o.var_floor,
+                         o.min_s0, params, flags_dev ? flags_dev : at<int32_t>(ws, W.off_flags),
+                         s));
+  }
+  GMM_TRY(cudaMemcpyAsync(loglik_dev, at<double>(ws, W.off_ll), sizeof(double),
+                          cudaMemcpyDeviceToDevice, s));
+  if (loglik_host)
+    GMM_TRY(cudaMemcpyAsync(loglik_host, at<double>(ws, W.off_ll), sizeof(double),
+                            cudaMemcpyDeviceToHost, s));
+  GMM_TRY(cudaStreamSynchronize(s));
+  return GMM_OK;
+}
+
+gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
+                           const void* prepared, gmm_cov_type cov, int m, int32_t* ids,
+                           float* gamma, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  gmm_status c = check_common(X, xdtype, N, D, K, cov);
+  if (c != GMM_OK) return c;
+  if (!prepared || !ids || !gamma || !ws || m < 1 || m > 8 || m > K) return GMM_ERR_INVALID_ARG;
+  if (((uintptr_t)X & 15) || ((uintptr_t)ws & 255)) return GMM_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(DeviceStatus)) return GMM_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus* st = static_cast<DeviceStatus*>(ws);
+  GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
+  GMM_PROF("lse_topm_kernel");
+  GMM_TRY(simt_lse(X, xdtype, N, D, K, cov, prepared, lse, nullptr, m, ids, gamma, st, s));
+  return GMM_OK;
+}
+
+void gmm_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+int gmm_profile_read(const char** names, double* ms_total, long* launches, int max_kernels) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (ProfRec& r : g_prof_pending) {
+    float ms = 0.f;
+    cudaEventSynchronize(r.b);
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    size_t i = 0;
+    for (; i < g_prof_sum.size(); ++i)
+      if (strcmp(g_prof_sum[i].name, r.name) == 0) break;
+    if (i == g_prof_sum.size()) g_prof_sum.push_back({r.name, 0.0, 0});
+    g_prof_sum[i].ms += ms;
+    g_prof_sum[i].launches += 1;
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_pending.clear();
+  int n = (int)g_prof_sum.size();
+  for (int i = 0; i < n && i < max_kernels; ++i) {
+    if (names) names[i] = g_prof_sum[i].name;
+    if (ms_total) ms_total[i] = g_prof_sum[i].ms;
+    if (launches) launches[i] = g_prof_sum[i].launches;
+  }
+  return n;
+}
+
+void gmm_profile_reset(void) {
+  const char* dummy[1];
+  gmm_profile_read(dummy, nullptr, nullptr, 0);
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_sum.clear();
+}
+
+gmm_status gmm_last_device_status(void* ws, void* stream) {
+  if (!ws) return GMM_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus h;
+  GMM_TRY(cudaStreamSynchronize(s));
+  GMM_TRY(cudaMemcpy(&h, ws, sizeof(DeviceStatus), cudaMemcpyDeviceToHost));
+  return (gmm_status)h.code;
+}
+
+}  // extern "C"

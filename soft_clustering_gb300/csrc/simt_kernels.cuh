@@ -1,0 +1,388 @@
+// simt_kernels.cuh - fp32 CUDA-core path of the fused EM step (all covariance
+// types).  It is the general path (any K, all three covariance types, small
+// problems where a tensor-core tile would be mostly padding) and the exact
+// yardstick the tensor-core kernels are tested beside.
+//
+// Two passes over X, no N x K buffer:
+//   lse_kernel:   one thread per point; l_nk for every component in the
+//                 centred form (x - mu) with an online max/sum over k
+//                 ("low-precision GMM operator" notes, sec. 3.2 fused
+//                 distance + posterior, sec. 4.2 log-sum-exp); writes LSE_n,
+//                 a per-block log-likelihood partial and, for assignment,
+//                 the top-m components.
+//   stats_kernel: grid (component chunk, point partition); recomputes l_nk
+//                 for its chunk, g = exp(l - LSE_n), and accumulates
+//                 [s0, sum g (x-mu), sum g (x-mu)^2 or (x-mu)(x-mu)^T]
+//                 (Flash-GMM summary, Method: online sufficient statistics)
+//                 about the input mean, fp32 per 64-point tile, fp64 across
+//                 tiles, into a per-block partial.
+#pragma once
+#include <math.h>
+
+#include <type_traits>
+
+#include "gmm_internal.cuh"
+
+namespace gmm {
+
+namespace simt {
+
+constexpr int kLseThreads = 128;
+constexpr int kStatThreads = 256;
+constexpr int kStatTile = 64;
+
+// Components per chunk of the statistics kernel, chosen so that a thread
+// owns at most ~9 (diag) accumulators.
+template <int D, int COV>
+struct StatShape {
+  static constexpr int F = COV == GMM_COV_FULL ? 1 + D + D * (D + 1) / 2 : 1 + 2 * D;
+  static constexpr int KC = COV == GMM_COV_FULL ? (D >= 64 ? 1 : (D == 32 ? 4 : 16))
+                                                 : (D == 128 ? 8 : (D == 64 ? 16 : (D == 32 ? 32 : 64)));
+  static constexpr int SLOTS = (KC * F + kStatThreads - 1) / kStatThreads;
+};
+
+// Components per shared-memory chunk of the LSE kernel.
+template <int D, int COV>
+struct LseShape {
+  static constexpr int P = COV == GMM_COV_FULL ? D * D : (COV == GMM_COV_DIAG ? D : 1);
+  static constexpr int KC = COV == GMM_COV_FULL ? (D == 128 ? 1 : (D == 64 ? 2 : 8)) : 16;
+};
+
+template <int XT, int D>
+__device__ __forceinline__ void load_row(const void* X, int64_t n, float* x) {
+#pragma unroll
+  for (int d = 0; d < D; ++d) x[d] = load_x<XT>(X, (size_t)n * D + d);
+}
+
+// log joint of one component for a point held in registers (diag / iso).
+template <int D, int COV>
+__device__ __forceinline__ float logj_diag(const float* x, const float* mu, const float* prec,
+                                           float c) {
+  float acc = 0.f;
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    float t = x[d] - mu[d];
+    float w = COV == GMM_COV_DIAG ? prec[d] : prec[0];
+    acc = fmaf(t * t, w, acc);
+  }
+  return c - 0.5f * acc;
+}
+
+// Full: z = W (x - mu), d^2 = z.z, with W lower triangular.
+template <int D>
+__device__ __forceinline__ float logj_full(const float* y, const float* W, float c) {
+  float acc = 0.f;
+  // fully unrolled up to D = 64 so y[] stays in registers
+#pragma unroll(D <= 64 ? D : 4)
+  for (int i = 0; i < D; ++i) {
+    float z = 0.f;
+#pragma unroll(D <= 64 ? D : 1)
+    for (int j = 0; j <= i; ++j) z = fmaf(W[i * D + j], y[j], z);
+    acc = fmaf(z, z, acc);
+  }
+  return c - 0.5f * acc;
+}
+
+template <int D, int COV, int XT>
+__global__ void __launch_bounds__(kLseThreads)
+lse_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict__ prepared,
+           PreparedLayout L, float* __restrict__ lse_out, double* __restrict__ ll_part, int m,
+           int32_t* __restrict__ ids, float* __restrict__ gamma, DeviceStatus* st) {
+  using S = LseShape<D, COV>;
+  extern __shared__ float sm[];
+  float* s_mu = sm;                      // KC*D
+  float* s_prec = s_mu + S::KC * D;      // KC*P
+  float* s_c = s_prec + S::KC * S::P;    // KC
+  __shared__ double red[kLseThreads / 32];
+
+  const int64_t n = (int64_t)blockIdx.x * kLseThreads + threadIdx.x;
+  const bool valid = n < N;
+  const float* g_c = at<float>(prepared, L.off_c);
+  const float* g_mu = at<float>(prepared, L.off_mu);
+  const float* g_prec = at<float>(prepared, L.off_prec);
+
+  float x[D];
+  if (COV != GMM_COV_FULL) {
+    if (valid) load_row<XT, D>(X, n, x);
+    else
+#pragma unroll
+      for (int d = 0; d < D; ++d) x[d] = 0.f;
+  }
+  float run_m = -INFINITY, run_s = 0.f;
+  float tv[8];
+  int ti[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { tv[j] = -INFINITY; ti[j] = 0x7fffffff; }
+
+  for (int k0 = 0; k0 < K; k0 += S::KC) {
+    const int kc = min(S::KC, K - k0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kc * D; i += kLseThreads) s_mu[i] = g_mu[(size_t)k0 * D + i];
+    for (int i = threadIdx.x; i < kc * S::P; i += kLseThreads)
+      s_prec[i] = g_prec[(size_t)k0 * S::P + i];
+    for (int i = threadIdx.x; i < kc; i += kLseThreads) s_c[i] = g_c[k0 + i];
+    __syncthreads();
+    if (!valid) continue;
+    for (int kk = 0; kk < kc; ++kk) {
+      const float c = s_c[kk];
+      if (c == -INFINITY) continue;
+      float l;
+      if constexpr (COV == GMM_COV_FULL) {
+        float y[D];
+#pragma unroll
+        for (int d = 0; d < D; ++d) y[d] = load_x<XT>(X, (size_t)n * D + d) - s_mu[kk * D + d];
+        l = logj_full<D>(y, s_prec + kk * S::P, c);
+      } else {
+        l = logj_diag<D, COV>(x, s_mu + kk * D, s_prec + kk * S::P, c);
+      }
+      // online log-sum-exp (running max, rescaled sum)
+      if (l > run_m) {
+        run_s = run_s * expf(run_m - l) + 1.f;
+        run_m = l;
+      } else {
+        run_s += expf(l - run_m);
+      }
+      if (m > 0 && l > tv[m - 1]) {
+        // insertion into the descending top-m list; a value equal to an
+        // entry goes after it, so ties keep the lower component first
+        const int k = k0 + kk;
+        bool placed = false;
+#pragma unroll
+        for (int t = 7; t >= 1; --t) {
+          if (t < m && !placed) {
+            if (l > tv[t - 1]) { tv[t] = tv[t - 1]; ti[t] = ti[t - 1]; }
+            else { tv[t] = l; ti[t] = k; placed = true; }
+          }
+        }
+        if (!placed) { tv[0] = l; ti[0] = k; }
+      }
+    }
+  }
+  double lsev = 0.0;
+  if (valid) {
+    const float lse = run_m + logf(run_s);
+    if (lse_out) lse_out[n] = lse;
+    if (!isfinite(lse)) raise_status(st, GMM_ERR_NONFINITE);
+    lsev = (double)lse;
+    for (int j = 0; j < m; ++j) {
+      ids[n * m + j] = ti[j] == 0x7fffffff ? -1 : ti[j];
+      gamma[n * m + j] = tv[j] == -INFINITY ? 0.f : expf(tv[j] - lse);
+    }
+  }
+  if (ll_part) {
+    lsev = warp_sum(lsev);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lsev;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double s = 0.0;
+      for (int i = 0; i < kLseThreads / 32; ++i) s += red[i];
+      ll_part[blockIdx.x] = s;
+    }
+  }
+}
+
+template <int D, int COV, int XT>
+__global__ void __launch_bounds__(kStatThreads)
+stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict__ prepared,
+             PreparedLayout L, const float* __restrict__ lse, int64_t rows_per_part,
+             double* __restrict__ part, int accumulate) {
+  using SS = StatShape<D, COV>;
+  constexpr int KC = SS::KC, F = SS::F, SLOTS = SS::SLOTS, T = kStatTile;
+  constexpr int P = LseShape<D, COV>::P;
+  constexpr int XS = D + 1;  // padded row of the x tile
+  extern __shared__ float sm[];
+  float* s_x = sm;                    // T*XS
+  float* s_g = s_x + T * XS;          // T*KC
+  float* s_mu = s_g + T * KC;         // KC*D
+  float* s_prec = s_mu + KC * D;      // KC*P
+  float* s_c = s_prec + KC * P;       // KC
+  float* s_y = s_c + KC;              // full only: T*KC*D   (y = x - mu)
+  short* s_pair = (short*)(s_y + (COV == GMM_COV_FULL ? T * KC * D : 0));  // full: 2 shorts per s2 entry
+
+  const int k0 = blockIdx.x * KC;
+  const int kc = min(KC, K - k0);
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_part;
+  const int64_t r1 = min(N, r0 + rows_per_part);
+
+  for (int i = threadIdx.x; i < kc * D; i += kStatThreads)
+    s_mu[i] = at<float>(prepared, L.off_mu)[(size_t)k0 * D + i];
+  for (int i = threadIdx.x; i < kc * P; i += kStatThreads)
+    s_prec[i] = at<float>(prepared, L.off_prec)[(size_t)k0 * P + i];
+  for (int i = threadIdx.x; i < kc; i += kStatThreads) s_c[i] = at<float>(prepared, L.off_c)[k0 + i];
+  if constexpr (COV == GMM_COV_FULL) {
+    for (int e = threadIdx.x; e < D * (D + 1) / 2; e += kStatThreads) {
+      // e enumerates the lower triangle row by row: (a, b) with b <= a
+      int a = (int)((sqrtf(8.f * e + 1.f) - 1.f) * 0.5f);
+      while ((a + 1) * (a + 2) / 2 <= e) ++a;
+      while (a * (a + 1) / 2 > e) --a;
+      int b = e - a * (a + 1) / 2;
+      s_pair[2 * e] = (short)a;
+      s_pair[2 * e + 1] = (short)b;
+    }
+  }
+
+  double accd[SLOTS];
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) accd[s] = 0.0;
+
+  for (int64_t t0 = r0; t0 < r1; t0 += T) {
+    const int tn = (int)min((int64_t)T, r1 - t0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * D; i += kStatThreads) {
+      int r = i / D, d = i % D;
+      s_x[r * XS + d] = r < tn ? load_x<XT>(X, (size_t)(t0 + r) * D + d) : 0.f;
+    }
+    __syncthreads();
+    // responsibilities of this chunk for the tile
+    for (int pidx = threadIdx.x; pidx < T * KC; pidx += kStatThreads) {
+      const int r = pidx / KC, kk = pidx % KC;
+      float g = 0.f;
+      if (r < tn && kk < kc && s_c[kk] != -INFINITY) {
+        float l;
+        if constexpr (COV == GMM_COV_FULL) {
+          float y[D];
+#pragma unroll
+          for (int d = 0; d < D; ++d) {
+            y[d] = s_x[r * XS + d] - s_mu[kk * D + d];
+            s_y[(r * KC + kk) * D + d] = y[d];
+          }
+          l = logj_full<D>(y, s_prec + kk * P, s_c[kk]);
+        } else {
+          float acc = 0.f;
+#pragma unroll 8
+          for (int d = 0; d < D; ++d) {
+            float tt = s_x[r * XS + d] - s_mu[kk * D + d];
+            float w = COV == GMM_COV_DIAG ? s_prec[kk * P + d] : s_prec[kk * P];
+            acc = fmaf(tt * tt, w, acc);
+          }
+          l = s_c[kk] - 0.5f * acc;
+        }
+        g = expf(l - lse[t0 + r]);
+      }
+      s_g[r * KC + kk] = g;
+    }
+    __syncthreads();
+    // accumulate [1, y, y^2 | y y^T] weighted by g over the tile
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+      const int f = threadIdx.x + s * kStatThreads;
+      if (f >= kc * F) continue;
+      const int kk = f / F, feat = f % F;
+      float acc = 0.f;
+      if (feat == 0) {
+        for (int r = 0; r < tn; ++r) acc += s_g[r * KC + kk];
+      } else if (COV != GMM_COV_FULL) {
+        const int d = (feat - 1) % D;
+        const bool sq = feat > D;
+        const float mu_d = s_mu[kk * D + d];
+        for (int r = 0; r < tn; ++r) {
+          float y = s_x[r * XS + d] - mu_d;
+          acc = fmaf(s_g[r * KC + kk], sq ? y * y : y, acc);
+        }
+      } else {
+        if (feat <= D) {
+          const int d = feat - 1;
+          for (int r = 0; r < tn; ++r) acc = fmaf(s_g[r * KC + kk], s_y[(r * KC + kk) * D + d], acc);
+        } else {
+          const int e = feat - 1 - D;
+          const int a = s_pair[2 * e], b = s_pair[2 * e + 1];
+          for (int r = 0; r < tn; ++r) {
+            const float* y = s_y + (r * KC + kk) * D;
+            acc = fmaf(s_g[r * KC + kk], y[a] * y[b], acc);
+          }
+        }
+      }
+      accd[s] += (double)acc;
+    }
+  }
+  // per-block partial [P][K][F]
+  double* out = part + (size_t)blockIdx.y * K * F;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int f = threadIdx.x + s * kStatThreads;
+    if (f >= kc * F) continue;
+    const int kk = f / F, feat = f % F;
+    double* o = out + (size_t)(k0 + kk) * F + feat;
+    *o = accumulate ? *o + accd[s] : accd[s];
+  }
+}
+
+template <int D, int COV, int XT>
+size_t lse_smem() {
+  using S = LseShape<D, COV>;
+  return sizeof(float) * (S::KC * D + S::KC * S::P + S::KC);
+}
+
+template <int D, int COV, int XT>
+size_t stat_smem() {
+  using SS = StatShape<D, COV>;
+  constexpr int P = LseShape<D, COV>::P;
+  size_t f = (size_t)kStatTile * (D + 1) + kStatTile * SS::KC + SS::KC * D + SS::KC * P + SS::KC;
+  if (COV == GMM_COV_FULL) f += (size_t)kStatTile * SS::KC * D;
+  size_t b = f * sizeof(float);
+  if (COV == GMM_COV_FULL) b += sizeof(short) * 2 * (D * (D + 1) / 2);
+  return b;
+}
+
+template <int D, int COV, int XT>
+cudaError_t run_lse(const void* X, int64_t N, int K, const void* prepared, const PreparedLayout& L,
+                    float* lse, double* ll_part, int m, int32_t* ids, float* gamma,
+                    DeviceStatus* st, cudaStream_t s) {
+  size_t smem = lse_smem<D, COV, XT>();
+  auto kern = lse_kernel<D, COV, XT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int64_t blocks = (N + kLseThreads - 1) / kLseThreads;
+  kern<<<(unsigned)blocks, kLseThreads, smem, s>>>(X, N, K, prepared, L, lse, ll_part, m, ids, gamma, st);
+  return cudaGetLastError();
+}
+
+template <int D, int COV, int XT>
+cudaError_t run_stats(const void* X, int64_t N, int K, const void* prepared,
+                      const PreparedLayout& L, const float* lse, int parts, double* part,
+                      int accumulate, cudaStream_t s) {
+  using SS = StatShape<D, COV>;
+  size_t smem = stat_smem<D, COV, XT>();
+  auto kern = stats_kernel<D, COV, XT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int64_t rows = (N + parts - 1) / parts;
+  rows = (rows + kStatTile - 1) / kStatTile * kStatTile;
+  dim3 grid((K + SS::KC - 1) / SS::KC, parts);
+  kern<<<grid, kStatThreads, smem, s>>>(X, N, K, prepared, L, lse, rows, part, accumulate);
+  return cudaGetLastError();
+}
+
+}  // namespace simt
+
+template <int V>
+using IC = std::integral_constant<int, V>;
+
+// Calls fn(IC<cov>, IC<xdtype>) for the runtime pair.
+template <typename Fn>
+cudaError_t dispatch_cx(int cov, int xt, Fn&& fn) {
+  auto by_x = [&](auto Cc) -> cudaError_t {
+    switch (xt) {
+      case GMM_F32: return fn(Cc, IC<GMM_F32>{});
+      case GMM_F16: return fn(Cc, IC<GMM_F16>{});
+      default: return fn(Cc, IC<GMM_BF16>{});
+    }
+  };
+  switch (cov) {
+    case GMM_COV_FULL: return by_x(IC<GMM_COV_FULL>{});
+    case GMM_COV_DIAG: return by_x(IC<GMM_COV_DIAG>{});
+    default: return by_x(IC<GMM_COV_ISO>{});
+  }
+}
+
+// One instantiation unit per D (simt_d*.cu) defines these two.
+template <int D>
+cudaError_t simt_lse_d(const void* X, int xdtype, int64_t N, int K, int cov, const void* prepared,
+                       float* lse, double* ll_part, int m, int32_t* ids, float* gamma,
+                       DeviceStatus* st, cudaStream_t s);
+template <int D>
+cudaError_t simt_stats_d(const void* X, int xdtype, int64_t N, int K, int cov,
+                         const void* prepared, const float* lse, int parts, double* part,
+                         int accumulate, cudaStream_t s);
+
+}  // namespace gmm

@@ -1,0 +1,79 @@
+"""Parity criteria for the CUDA path against the fp64 oracle.
+
+Tolerances (fixed for this path):
+  * log-likelihood: relative error <= 1e-4 per iteration;
+  * updated means and covariance entries: |gpu - ref| / max(|ref|, 1e-3 * scale)
+    <= 2e-3, scale = max |ref| over that parameter array;
+  * weights: absolute error <= 1e-5;
+  * top-1 assignment agreement >= 99.9%, points whose two best oracle
+    responsibilities differ by less than 1e-6 excluded.
+On failure the report gives the diagnostics the ops-debug page recommends
+(sec. 3.2): cosine similarity, max abs error with its index and the
+P50/P95/P99 of the relative error.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+LL_RTOL = 1e-4
+PARAM_RTOL = 2e-3
+PARAM_FLOOR = 1e-3
+PI_ATOL = 1e-5
+TOP1_MIN = 0.999
+TIE_EPS = 1e-6
+
+
+def diagnostics(got, ref):
+    got = np.asarray(got, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    err = np.abs(got - ref)
+    i = int(np.argmax(err)) if err.size else 0
+    rel = err / np.maximum(np.abs(ref), 1e-300)
+    denom = np.linalg.norm(got) * np.linalg.norm(ref)
+    cos = float(got @ ref / denom) if denom > 0 else float("nan")
+    p = np.percentile(rel, [50, 95, 99]) if rel.size else [0, 0, 0]
+    return dict(cosine=cos, max_abs=float(err[i]) if err.size else 0.0, argmax=i,
+                got=float(got[i]) if err.size else 0.0, ref=float(ref[i]) if err.size else 0.0,
+                p50=float(p[0]), p95=float(p[1]), p99=float(p[2]))
+
+
+def scaled_rel_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = float(np.abs(ref).max()) if ref.size else 0.0
+    return np.abs(got - ref) / np.maximum(np.abs(ref), PARAM_FLOOR * scale + 1e-300)
+
+
+def compare_step(gpu, ref, what=""):
+    """gpu/ref: dicts with pi, mu, cov, ll.  Returns a list of failure strings."""
+    fails = []
+    ll_err = abs(gpu["ll"] - ref["ll"]) / max(abs(ref["ll"]), 1e-300)
+    if not ll_err <= LL_RTOL:
+        fails.append("%s LL rel err %.3g (gpu %.10g ref %.10g)" % (what, ll_err, gpu["ll"], ref["ll"]))
+    pe = np.abs(np.asarray(gpu["pi"]) - np.asarray(ref["pi"]))
+    if not (pe <= PI_ATOL).all():
+        fails.append("%s pi abs err %.3g at %d %s" % (what, pe.max(), int(pe.argmax()),
+                                                     diagnostics(gpu["pi"], ref["pi"])))
+    for name in ("mu", "cov"):
+        e = scaled_rel_err(gpu[name], ref[name])
+        if not (e <= PARAM_RTOL).all():
+            idx = np.unravel_index(int(np.argmax(e)), e.shape)
+            fails.append("%s %s scaled rel err %.3g at %s (gpu %.8g ref %.8g) %s" % (
+                what, name, e.max(), idx, np.asarray(gpu[name])[idx], np.asarray(ref[name])[idx],
+                diagnostics(gpu[name], ref[name])))
+    return fails
+
+
+def top1_agreement(ids_gpu, ids_ref, gamma_ref):
+    """Fraction of non-tied points whose top-1 component agrees."""
+    ids_gpu = np.asarray(ids_gpu)
+    ids_ref = np.asarray(ids_ref)
+    g = np.asarray(gamma_ref)
+    if g.shape[1] >= 2:
+        keep = (g[:, 0] - g[:, 1]) >= TIE_EPS
+    else:
+        keep = np.ones(len(g), dtype=bool)
+    if not keep.any():
+        return 1.0, 0
+    agree = (ids_gpu[keep, 0] == ids_ref[keep, 0]).mean()
+    return float(agree), int(keep.sum())

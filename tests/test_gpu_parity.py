@@ -1,0 +1,244 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded inputs.
+
+Sizes are ones the oracle finishes in seconds, spanning several tiles with a
+ragged tail.  Per-step parity feeds both sides the same fp32 parameters
+(the oracle's own trajectory, rounded to fp32 - never values from the GPU);
+trajectory parity lets each side iterate on its own from theta_0.
+"""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+import parity
+from gpu_util import f32, gpu_step, make_state, oracle_step, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from soft_clustering_gb300 import build
+    build.build()
+
+
+def _workload(name, n=None, **over):
+    wl = datagen.WORKLOADS[name]
+    if n is not None:
+        wl = wl.with_n(n)
+    for k, v in over.items():
+        setattr(wl, k, v)
+    return wl
+
+
+def _run_parity(wl, iters, trajectory=True):
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    theta0 = f32(datagen.init_params(mix, bits))
+    Xd = to_device(bits, wl.dtype)
+    state = make_state(wl)
+    fails = []
+    # per step: both sides start each step from the oracle's (fp32-rounded) parameters
+    theta = theta0
+    for t in range(iters):
+        ref = oracle_step(bits, wl.dtype, theta, wl.cov_type)
+        assert ref["status"] == 0
+        got = gpu_step(state, Xd, theta)
+        assert got["status"] == 0, got["status"]
+        fails += parity.compare_step(got, ref, "%s step %d" % (wl.name, t))
+        theta = f32((ref["pi"], ref["mu"], ref["cov"]))
+    # trajectory: each side on its own from theta_0
+    if trajectory:
+        ref_theta = theta0
+        state.set_params(*theta0)
+        for t in range(iters):
+            ref = oracle_step(bits, wl.dtype, ref_theta, wl.cov_type)
+            state.step(Xd)
+            pi, mu, cov = state.params_numpy()
+            got = dict(pi=pi, mu=mu, cov=cov, ll=float(state.loglik.item()))
+            fails += parity.compare_step(got, ref, "%s trajectory %d" % (wl.name, t))
+            ref_theta = (ref["pi"], ref["mu"], ref["cov"])
+    assert not fails, "\n".join(fails[:10])
+
+
+def test_tiny_diag_full_size():
+    """N=4096, D=16, K=8, fp32 X, 10 iterations (full size)."""
+    _run_parity(_workload("tiny_diag"), 10)
+
+
+def test_full_cov_subset():
+    _run_parity(_workload("full_cov", n=20_000 + 37), 4)
+
+
+def test_embed_diag_subset():
+    _run_parity(_workload("embed_diag", n=12_000 + 61), 3)
+
+
+def test_large_diag_subset_bf16():
+    _run_parity(_workload("large_diag", n=8_000 + 5), 2)
+
+
+def test_large_iso_subset_bf16():
+    _run_parity(_workload("large_diag", n=8_000 + 5, cov_type=datagen.COV_ISO, K=64), 3)
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("cov", [datagen.COV_FULL, datagen.COV_DIAG, datagen.COV_ISO])
+@pytest.mark.parametrize("xdtype", [datagen.F32, datagen.F16, datagen.BF16])
+def test_shapes_dtypes(D, cov, xdtype):
+    """Every (D, covariance, dtype) on a ragged N and a K that is not a
+    multiple of any chunk."""
+    kind = datagen.MIX_FULL if cov == datagen.COV_FULL else datagen.MIX_DIAG
+    recipe = (dict(mean_sd=2.0, ridge=0.2, alpha=2.0) if kind == datagen.MIX_FULL else
+              dict(mean_sd=2.0, sd_mode=0, lo=0.3, hi=1.5, alpha=2.0))
+    wl = datagen.Workload("shape", 100 + D + 7 * cov + 31 * xdtype, 1000 + 3, D, 11, xdtype, cov,
+                          1, kind, recipe)
+    _run_parity(wl, 1, trajectory=False)
+
+
+def test_assign_topm_subset():
+    wl = _workload("ivf_assign", n=6_000 + 13)
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    pi, mu, var = datagen.planted_params_f16(mix)
+    st, ids_ref, gam_ref, lse_ref = oracle.topm(bits, pi, mu, var, wl.cov_type, wl.m,
+                                                xdtype=wl.dtype)
+    assert st == 0
+    from soft_clustering_gb300.torch_api import Assigner
+    a = Assigner(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, wl.m)
+    a.prepare(pi, mu, var)
+    a.assign(to_device(bits, wl.dtype))
+    assert a.device_status() == 0
+    ids = a.ids.cpu().numpy()
+    gam = a.gamma.cpu().numpy().astype(np.float64)
+    lse = a.lse.cpu().numpy().astype(np.float64)
+    agree, kept = parity.top1_agreement(ids, ids_ref, gam_ref)
+    assert agree >= parity.TOP1_MIN, (agree, kept)
+    assert np.abs(lse - lse_ref).max() <= 1e-4 * np.abs(lse_ref).max()
+    same = ids == ids_ref
+    assert np.abs(gam - gam_ref)[same].max() < 2e-4
+    assert (np.diff(np.where(ids >= 0, 0, 1), axis=1) >= 0).all()
+
+
+def test_deterministic():
+    wl = _workload("embed_diag", n=5_000)
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    theta = f32(datagen.init_params(mix, bits))
+    Xd = to_device(bits, wl.dtype)
+    s = make_state(wl)
+    a = gpu_step(s, Xd, theta)
+    b = gpu_step(s, Xd, theta)
+    for k in ("pi", "mu", "cov"):
+        assert (a[k] == b[k]).all(), k
+    assert a["ll"] == b["ll"]
+
+
+def test_no_device_allocation_in_step():
+    """The library allocates nothing: free device memory is unchanged by a
+    step (torch's allocator is not involved in the call)."""
+    wl = _workload("embed_diag", n=50_000)
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    theta = f32(datagen.init_params(mix, bits))
+    Xd = to_device(bits, wl.dtype)
+    s = make_state(wl)
+    gpu_step(s, Xd, theta)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    gpu_step(s, Xd, theta)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert s.ws_bytes < wl.N * wl.K * 4
+
+
+def test_host_streaming_matches():
+    wl = _workload("embed_diag", n=30_000 + 9)
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    theta = f32(datagen.init_params(mix, bits))
+    ref = oracle_step(bits, wl.dtype, theta, wl.cov_type)
+    s = make_state(wl, chunk_rows=7_000)
+    s.set_params(*theta)
+    host = torch.from_numpy(bits.view(np.int16)).pin_memory()
+    ll_host = np.zeros(1)
+    s.step_host(host, loglik_host=ll_host)
+    assert s.device_status() == 0
+    pi, mu, cov = s.params_numpy()
+    fails = parity.compare_step(dict(pi=pi, mu=mu, cov=cov, ll=float(ll_host[0])), ref, "host")
+    assert not fails, fails
+
+
+def test_edge_cases_small():
+    """N = 1, K = 1, a single tile, and K larger than N."""
+    for N, K in [(1, 1), (1, 3), (5, 1), (127, 2), (129, 200)]:
+        wl = datagen.Workload("edge", 77 + N + K, N, 16, K, datagen.F32, datagen.COV_DIAG, 1,
+                              datagen.MIX_DIAG, dict(mean_sd=1.0, sd_mode=0, lo=0.5, hi=1.0,
+                                                     alpha=1.0))
+        mix = datagen.planted(wl)
+        bits = datagen.points(mix, 0, N)
+        pi = np.full(K, 1.0 / K, dtype=np.float32)
+        mu = (mix.mu.astype(np.float32) * 0.5)
+        var = np.ones((K, 16), dtype=np.float32)
+        ref = oracle_step(bits, wl.dtype, (pi, mu, var), wl.cov_type)
+        got = gpu_step(make_state(wl), to_device(bits, wl.dtype), (pi, mu, var))
+        fails = parity.compare_step(got, ref, "N=%d K=%d" % (N, K))
+        assert not fails, fails
+        assert (got["flags"] == ref["flags"]).all(), (got["flags"], ref["flags"])
+
+
+def test_empty_floor_notpd_flags():
+    """Empty component (mean far away), variance floor, and a covariance that
+    is not positive definite: same flags and parameters as the oracle."""
+    rng = np.random.default_rng(5)
+    N, D, K = 2000, 16, 4
+    X = (rng.standard_normal((N, D))).astype(np.float32)
+    pi = np.full(K, 0.25, dtype=np.float32)
+    mu = np.zeros((K, D), dtype=np.float32)
+    mu[1] = 1e4  # takes no responsibility -> empty
+    mu[2] = 0.5
+    var = np.ones((K, D), dtype=np.float32)
+    var[3, 0] = 0.0  # ridge retry (1e-3 tr/D) repairs it
+    opts = dict(var_floor=0.9, min_s0=1e-3)
+    wl = datagen.Workload("flags", 0, N, D, K, datagen.F32, datagen.COV_DIAG, 1, 0, {})
+    ref = oracle_step(X, datagen.F32, (pi, mu, var), wl.cov_type, opts=opts)
+    s = make_state(wl)
+    s.opts.var_floor = 0.9
+    got = gpu_step(s, to_device(X, datagen.F32), (pi, mu, var))
+    assert (got["flags"] == ref["flags"]).all(), (got["flags"], ref["flags"])
+    assert got["flags"][1] & oracle.FLAG_EMPTY and got["flags"][3] & oracle.FLAG_RIDGE
+    fails = parity.compare_step(got, ref, "flags")
+    assert not fails, fails
+    # not positive definite even after the retry: status NOT_PD, component excluded
+    var2 = var.copy()
+    var2[3, :] = -1.0
+    got = gpu_step(s, to_device(X, datagen.F32), (pi, mu, var2))
+    assert got["status"] == 3 and got["flags"][3] & oracle.FLAG_NOT_PD
+
+
+def test_nonfinite_input_reported():
+    N, D, K = 300, 16, 2
+    X = np.random.default_rng(1).standard_normal((N, D)).astype(np.float32)
+    X[17, 3] = np.nan
+    wl = datagen.Workload("nan", 0, N, D, K, datagen.F32, datagen.COV_DIAG, 1, 0, {})
+    s = make_state(wl)
+    got = gpu_step(s, to_device(X, datagen.F32),
+                   (np.full(K, 0.5, np.float32), np.zeros((K, D), np.float32),
+                    np.ones((K, D), np.float32)))
+    assert got["status"] == 4  # GMM_ERR_NONFINITE
+
+
+def test_invalid_workspace_and_alignment():
+    import soft_clustering_gb300 as G
+    wl = _workload("tiny_diag", n=256)
+    s = make_state(wl)
+    X = torch.zeros(wl.N * wl.D + 1, dtype=torch.float32, device="cuda")
+    st = G.gmm_em_step(X, wl.dtype, wl.N, wl.D, wl.K, s.pi, s.mu, s.cov, wl.cov_type, s.ws,
+                       s.ws_bytes - 1, s.loglik, raise_on_error=False)
+    assert st == G.GMM_ERR_WORKSPACE
+    st = G.gmm_em_step(X.data_ptr() + 4, wl.dtype, wl.N, wl.D, wl.K, s.pi, s.mu, s.cov,
+                       wl.cov_type, s.ws, s.ws_bytes, s.loglik, raise_on_error=False)
+    assert st == G.GMM_ERR_INVALID_ARG
