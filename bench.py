@@ -192,13 +192,14 @@ def cpu_sample_run(wl, mix, seconds):
     n_cal = min(wl.N, 256)
     bits = datagen.points(mix, 0, n_cal)
     theta = datagen.init_params(mix)
+    opts = datagen.em_opts(theta)
     t0 = time.perf_counter()
-    oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype)
+    oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype, opts=opts)
     per_point = max((time.perf_counter() - t0) / n_cal, 1e-9)
     n = int(min(wl.N, max(n_cal, seconds / per_point)))
     bits = datagen.points(mix, 0, n)
     t0 = time.perf_counter()
-    oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype)
+    oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype, opts=opts)
     dt = time.perf_counter() - t0
     return n * wl.K / dt, n, oracle.max_threads(), dt
 
@@ -218,13 +219,14 @@ def run_reference(args, wl):
     _, n, threads, _ = cpu_sample_run(wl, mix, per_step_s)
     bits = datagen.points(mix, 0, n)
     theta = datagen.init_params(mix)
+    opts = datagen.em_opts(theta)
     pi, mu, cov = theta
     for _ in range(args.warmup):
-        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype)
+        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype, opts=opts)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype)
+        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype, opts=opts)
         times.append(time.perf_counter() - t0)
         pi, mu, cov = r["pi"], r["mu"], r["cov"]
     ms = 1e3 * sum(times) / len(times)
@@ -282,7 +284,10 @@ def run_ours(args, wl):
     theta0 = datagen.init_params(mix)
     torch.cuda.synchronize()
 
+    opts = datagen.em_opts(theta0)
     st = GMMState(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, device=dev)
+    for k, v in opts.items():
+        setattr(st.opts, k, v)
     st.set_params(*theta0)
     for _ in range(args.warmup):
         st.step(X)
@@ -345,6 +350,8 @@ def run_ours(args, wl):
     if not args.no_e2e:
         chunk = max(1, min(wl.N, (256 << 20) // (wl.D * esz)))
         st2 = GMMState(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, device=dev, chunk_rows=chunk)
+        for k, v in opts.items():
+            setattr(st2.opts, k, v)
         st2.set_params(*theta0)
         host = torch.empty(wl.N * wl.D * esz, dtype=torch.uint8, pin_memory=True)
         host.copy_(X)
@@ -403,9 +410,13 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--n", type=int, default=None,
+                    help="override the number of points (small profiling cases)")
     args = ap.parse_args(argv)
     import datagen
     wl = datagen.WORKLOADS[args.workload]
+    if args.n:
+        wl = wl.with_n(args.n)
     if wl.m:
         raise SystemExit("assignment workloads are benchmarked by bench_assign (not yet)")
     if args.impl == "reference":

@@ -295,6 +295,17 @@ def init_params(mix: Mixture, prefix_rows: np.ndarray | None = None):
     return (pi.astype(np.float32), mu.astype(np.float32), np.ascontiguousarray(c, dtype=np.float32))
 
 
+def em_opts(theta0, min_s0=0.5):
+    """Caller-side EM options for a workload started from theta0: a variance
+    floor of 1e-6 times the mean initial (global) variance, the empty
+    threshold, no ridge.  Values are rounded to fp32 (the C ABI's type) so
+    every side applies the same numbers."""
+    cov = np.asarray(theta0[2], dtype=np.float64)
+    v = np.mean(np.diagonal(cov, axis1=1, axis2=2)) if cov.ndim == 3 else np.mean(cov)
+    return dict(ridge_rel=0.0, var_floor=float(np.float32(1e-6 * v)),
+                min_s0=float(np.float32(min_s0)))
+
+
 def planted_params_f16(mix: Mixture):
     """A trained model stored in fp16 (the assignment workload): the planted
     weights, centres and variances rounded to fp16, widened to float32."""

@@ -82,7 +82,9 @@ typedef struct {
   int flags;
 } gmm_opts;
 
-/* Defaults: ridge_rel 0, var_floor 0, min_s0 1e-3, flags 0. */
+/* Defaults: ridge_rel 0, var_floor 0, min_s0 0.5, flags 0.  (A component
+ * holding less than half of one point's worth of responsibility has no mean
+ * the data determine: it is a weighted average of a few far tail points.) */
 gmm_opts gmm_default_opts(void);
 
 /* Human-readable name of a status code (static string). */

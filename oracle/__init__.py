@@ -28,9 +28,9 @@ COV_FULL, COV_DIAG, COV_ISO = 0, 1, 2
 OK, INVALID, NOT_PD, NONFINITE, NOMEM = 0, 1, 3, 4, 8
 FLAG_RIDGE, FLAG_NOT_PD, FLAG_FLOOR, FLAG_EMPTY = 1, 2, 4, 8
 
-# Defaults of the readings: no ridge unless needed, no floor, empty below
-# 1e-3 of one point's responsibility.
-DEFAULT_OPTS = dict(ridge_rel=0.0, var_floor=0.0, min_s0=1e-3)
+# Defaults of the readings: no ridge unless needed, no floor, a component is
+# empty below half of one point's worth of responsibility.
+DEFAULT_OPTS = dict(ridge_rel=0.0, var_floor=0.0, min_s0=0.5)
 
 
 def build(src: str | None = None, out: str | None = None, extra=()) -> str:

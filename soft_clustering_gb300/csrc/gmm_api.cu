@@ -194,7 +194,7 @@ gmm_opts gmm_default_opts(void) {
   gmm_opts o;
   o.ridge_rel = 0.0f;
   o.var_floor = 0.0f;
-  o.min_s0 = 1e-3f;
+  o.min_s0 = 0.5f;
   o.flags = 0;
   return o;
 }

@@ -6,10 +6,10 @@
 // partitions in a fixed order, so two runs give the same bits.  The update
 // is the maximum-likelihood one from the sufficient statistics (Flash-GMM
 // summary, Method: parameters updated directly from s0, s1, s2):
-//   pi' = s0/N,  mu' = c + S1/s0,  Sigma' = S2/s0 - (S1/s0)(S1/s0)^T,
-// where S1, S2 are the first and second moments about the centre c the
-// statistics were accumulated around (the input mean), so the subtraction
-// loses nothing to cancellation.
+//   pi' = s0/N,  mu' = c + S1/s0,  Sigma' = M2/s0,
+// where S1 is the first moment about the centre c the statistics were taken
+// around (the input mean) and M2 the second moment about the weighted mean
+// itself, so no large moments cancel.
 #include <math.h>
 
 #include "gmm_internal.cuh"
@@ -18,8 +18,13 @@ namespace gmm {
 
 namespace {
 
-// part: [P][K][F] fp64.  centre: the mean the statistics are taken about
-// (fp32 [K*D]).  Updates params in place.  dynamic smem: F doubles.
+// part: [P][K][F] fp64, each partial [S0 | S1 about the centre c | M2 about
+// the partial's own mean].  The partials are merged in partition order:
+// S0 and S1 are summed; M2 = sum_p [M2_p + S0_p (m_p - m)(m_p - m)^T] with
+// m_p = S1_p / S0_p and m = S1 / S0 (the pairwise update of Chan, Golub and
+// LeVeque, applied to all partitions at once).  centre: the mean the
+// statistics were taken about (fp32 [K*D]).  Updates params in place.
+// dynamic smem: F doubles.
 __global__ void mstep_kernel(const double* __restrict__ part, int parts, int64_t N, int D, int K,
                              int cov, const float* __restrict__ centre,
                              const int32_t* __restrict__ prep_flags, float var_floor,
@@ -28,14 +33,38 @@ __global__ void mstep_kernel(const double* __restrict__ part, int parts, int64_t
   extern __shared__ double s[];
   const int k = blockIdx.x;
   const int F = stat_width(D, cov);
-  for (int f = threadIdx.x; f < F; f += blockDim.x) {
+  auto P_ = [&](int p, int f) { return part[((size_t)p * K + k) * F + f]; };
+  for (int f = threadIdx.x; f <= D; f += blockDim.x) {
     double acc = 0.0;
-    for (int p = 0; p < parts; ++p) acc += part[((size_t)p * K + k) * F + f];
+    for (int p = 0; p < parts; ++p) acc += P_(p, f);
     s[f] = acc;
   }
   __syncthreads();
   const double s0 = s[0];
   const bool empty = !(s0 >= (double)min_s0) || !(s0 > 0.0);
+  const int nm2 = cov == GMM_COV_FULL ? D * (D + 1) / 2 : D;
+  for (int e = threadIdx.x; e < nm2; e += blockDim.x) {
+    int a, b;
+    if (cov == GMM_COV_FULL) {
+      a = (int)((sqrt(8.0 * e + 1.0) - 1.0) * 0.5);
+      while ((a + 1) * (a + 2) / 2 <= e) ++a;
+      while (a * (a + 1) / 2 > e) --a;
+      b = e - a * (a + 1) / 2;
+    } else {
+      a = b = e;
+    }
+    double acc = 0.0;
+    if (s0 > 0.0) {
+      const double ma = s[1 + a] / s0, mb = s[1 + b] / s0;
+      for (int p = 0; p < parts; ++p) {
+        const double c0 = P_(p, 0);
+        acc += P_(p, 1 + D + e);
+        if (c0 > 0.0) acc += c0 * (P_(p, 1 + a) / c0 - ma) * (P_(p, 1 + b) / c0 - mb);
+      }
+    }
+    s[1 + D + e] = acc;
+  }
+  __syncthreads();
   __shared__ int s_floor;
   if (threadIdx.x == 0) s_floor = 0;
   __syncthreads();
@@ -45,36 +74,29 @@ __global__ void mstep_kernel(const double* __restrict__ part, int parts, int64_t
     const float* c = centre + (size_t)k * D;
     if (cov == GMM_COV_FULL) {
       float* S = covp + (size_t)k * D * D;
-      // s layout: [s0 | S1 (D) | S2 lower triangle, row by row]
       for (int e = threadIdx.x; e < D * (D + 1) / 2; e += blockDim.x) {
         int a = (int)((sqrt(8.0 * e + 1.0) - 1.0) * 0.5);
         while ((a + 1) * (a + 2) / 2 <= e) ++a;
         while (a * (a + 1) / 2 > e) --a;
         const int b = e - a * (a + 1) / 2;
-        const double da = s[1 + a] * inv, db = s[1 + b] * inv;
-        double v = s[1 + D + e] * inv - da * db;
+        double v = s[1 + D + e] * inv;
         if (a == b && v < (double)var_floor) { v = var_floor; floored = 1; }
         S[(size_t)a * D + b] = (float)v;
         S[(size_t)b * D + a] = (float)v;
       }
     } else if (cov == GMM_COV_DIAG) {
       for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        const double dd = s[1 + d] * inv;
-        double v = s[1 + D + d] * inv - dd * dd;
+        double v = s[1 + D + d] * inv;
         if (v < (double)var_floor) { v = var_floor; floored = 1; }
         covp[(size_t)k * D + d] = (float)v;
       }
     } else if (threadIdx.x == 0) {
       double acc = 0.0;
-      for (int d = 0; d < D; ++d) {
-        const double dd = s[1 + d] * inv;
-        acc += s[1 + D + d] * inv - dd * dd;
-      }
-      double v = acc / D;
+      for (int d = 0; d < D; ++d) acc += s[1 + D + d];
+      double v = acc * inv / D;
       if (v < (double)var_floor) { v = var_floor; floored = 1; }
       covp[k] = (float)v;
     }
-    __syncthreads();  // every thread has read mu (centre is the prepared copy)
     for (int d = threadIdx.x; d < D; d += blockDim.x)
       mu[(size_t)k * D + d] = (float)((double)c[d] + s[1 + d] * inv);
   }

@@ -55,32 +55,56 @@ __device__ __forceinline__ void load_row(const void* X, int64_t n, float* x) {
 }
 
 // log joint of one component for a point held in registers (diag / iso).
+// d^2 = sum_d (x_d - mu_d)^2 w_d is summed in 8 interleaved fp32 partial sums
+// combined pairwise: the rounding error of the sum (the dominant error of the
+// log-density) drops about threefold against one running sum.
 template <int D, int COV>
 __device__ __forceinline__ float logj_diag(const float* x, const float* mu, const float* prec,
                                            float c) {
-  float acc = 0.f;
+  constexpr int NP = D >= 64 ? 8 : 4;
+  float p[NP];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) p[i] = 0.f;
 #pragma unroll
   for (int d = 0; d < D; ++d) {
     float t = x[d] - mu[d];
     float w = COV == GMM_COV_DIAG ? prec[d] : prec[0];
-    acc = fmaf(t * t, w, acc);
+    p[d % NP] = fmaf(t * t, w, p[d % NP]);
   }
-  return c - 0.5f * acc;
+#pragma unroll
+  for (int h = NP / 2; h > 0; h /= 2)
+#pragma unroll
+    for (int i = 0; i < h; ++i) p[i] += p[i + h];
+  return c - 0.5f * p[0];
 }
 
-// Full: z = W (x - mu), d^2 = z.z, with W lower triangular.
+// Full: z = W (x - mu), d^2 = z.z, with W lower triangular.  Each z_i is
+// summed in 4 interleaved partial sums; d^2 is accumulated with Neumaier's
+// compensated summation.
 template <int D>
 __device__ __forceinline__ float logj_full(const float* y, const float* W, float c) {
-  float acc = 0.f;
+  float s = 0.f, comp = 0.f;
   // fully unrolled up to D = 64 so y[] stays in registers
 #pragma unroll(D <= 64 ? D : 4)
   for (int i = 0; i < D; ++i) {
-    float z = 0.f;
-#pragma unroll(D <= 64 ? D : 1)
-    for (int j = 0; j <= i; ++j) z = fmaf(W[i * D + j], y[j], z);
-    acc = fmaf(z, z, acc);
+    float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+    const float* Wi = W + i * D;
+    int j = 0;
+#pragma unroll(D <= 64 ? D / 4 : 1)
+    for (; j + 3 <= i; j += 4) {
+      z0 = fmaf(Wi[j], y[j], z0);
+      z1 = fmaf(Wi[j + 1], y[j + 1], z1);
+      z2 = fmaf(Wi[j + 2], y[j + 2], z2);
+      z3 = fmaf(Wi[j + 3], y[j + 3], z3);
+    }
+    for (; j <= i; ++j) z0 = fmaf(Wi[j], y[j], z0);
+    const float z = (z0 + z1) + (z2 + z3);
+    const float q = z * z;
+    const float t = s + q;
+    comp += fabsf(s) >= fabsf(q) ? (s - t) + q : (q - t) + s;
+    s = t;
   }
-  return c - 0.5f * acc;
+  return c - 0.5f * (s + comp);
 }
 
 template <int D, int COV, int XT>
@@ -181,6 +205,13 @@ lse_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict_
   }
 }
 
+// Statistics of one component chunk over one point partition.  Per 64-point
+// tile: responsibilities, the tile's weighted count t0 and first moment t1
+// about the fixed centre c_k, then the tile's second moment M2_t about the
+// tile's own weighted mean, merged into the block's running sums with Chan,
+// Golub and LeVeque's pairwise update (M2 += M2_t + d d^T S0 t0 / (S0 + t0),
+// d = tile mean - running mean) in fp64.  Output per block and component:
+// [S0 | S1 about c_k | M2 about the block mean].
 template <int D, int COV, int XT>
 __global__ void __launch_bounds__(kStatThreads)
 stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict__ prepared,
@@ -190,14 +221,18 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   constexpr int KC = SS::KC, F = SS::F, SLOTS = SS::SLOTS, T = kStatTile;
   constexpr int P = LseShape<D, COV>::P;
   constexpr int XS = D + 1;  // padded row of the x tile
-  extern __shared__ float sm[];
-  float* s_x = sm;                    // T*XS
+  extern __shared__ double smd[];
+  double* s_r0 = smd;                 // KC     running S0 of this block
+  double* s_r1 = s_r0 + KC;           // KC*D   running S1 of this block
+  float* s_x = (float*)(s_r1 + KC * D);  // T*XS
   float* s_g = s_x + T * XS;          // T*KC
   float* s_mu = s_g + T * KC;         // KC*D
   float* s_prec = s_mu + KC * D;      // KC*P
   float* s_c = s_prec + KC * P;       // KC
-  float* s_y = s_c + KC;              // full only: T*KC*D   (y = x - mu)
-  short* s_pair = (short*)(s_y + (COV == GMM_COV_FULL ? T * KC * D : 0));  // full: 2 shorts per s2 entry
+  float* s_t0 = s_c + KC;             // KC     tile sums
+  float* s_t1 = s_t0 + KC;            // KC*D
+  float* s_y = s_t1 + KC * D;         // full only: T*KC*D   (y = x - c)
+  short* s_pair = (short*)(s_y + (COV == GMM_COV_FULL ? T * KC * D : 0));
 
   const int k0 = blockIdx.x * KC;
   const int kc = min(KC, K - k0);
@@ -209,6 +244,7 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   for (int i = threadIdx.x; i < kc * P; i += kStatThreads)
     s_prec[i] = at<float>(prepared, L.off_prec)[(size_t)k0 * P + i];
   for (int i = threadIdx.x; i < kc; i += kStatThreads) s_c[i] = at<float>(prepared, L.off_c)[k0 + i];
+  for (int i = threadIdx.x; i < KC * (D + 1); i += kStatThreads) smd[i] = 0.0;
   if constexpr (COV == GMM_COV_FULL) {
     for (int e = threadIdx.x; e < D * (D + 1) / 2; e += kStatThreads) {
       // e enumerates the lower triangle row by row: (a, b) with b <= a
@@ -222,15 +258,16 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   }
 
   double accd[SLOTS];
+  float tsum[SLOTS];
 #pragma unroll
-  for (int s = 0; s < SLOTS; ++s) accd[s] = 0.0;
+  for (int s = 0; s < SLOTS; ++s) { accd[s] = 0.0; tsum[s] = 0.f; }
 
-  for (int64_t t0 = r0; t0 < r1; t0 += T) {
-    const int tn = (int)min((int64_t)T, r1 - t0);
+  for (int64_t t0r = r0; t0r < r1; t0r += T) {
+    const int tn = (int)min((int64_t)T, r1 - t0r);
     __syncthreads();
     for (int i = threadIdx.x; i < T * D; i += kStatThreads) {
       int r = i / D, d = i % D;
-      s_x[r * XS + d] = r < tn ? load_x<XT>(X, (size_t)(t0 + r) * D + d) : 0.f;
+      s_x[r * XS + d] = r < tn ? load_x<XT>(X, (size_t)(t0r + r) * D + d) : 0.f;
     }
     __syncthreads();
     // responsibilities of this chunk for the tile
@@ -248,62 +285,145 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
           }
           l = logj_full<D>(y, s_prec + kk * P, s_c[kk]);
         } else {
-          float acc = 0.f;
+          // same summation order as logj_diag, so both passes agree
+          constexpr int NP = D >= 64 ? 8 : 4;
+          float pp[NP];
+#pragma unroll
+          for (int i = 0; i < NP; ++i) pp[i] = 0.f;
 #pragma unroll 8
           for (int d = 0; d < D; ++d) {
             float tt = s_x[r * XS + d] - s_mu[kk * D + d];
             float w = COV == GMM_COV_DIAG ? s_prec[kk * P + d] : s_prec[kk * P];
-            acc = fmaf(tt * tt, w, acc);
+            pp[d % NP] = fmaf(tt * tt, w, pp[d % NP]);
           }
-          l = s_c[kk] - 0.5f * acc;
+#pragma unroll
+          for (int h = NP / 2; h > 0; h /= 2)
+#pragma unroll
+            for (int i = 0; i < h; ++i) pp[i] += pp[i + h];
+          l = s_c[kk] - 0.5f * pp[0];
         }
-        g = expf(l - lse[t0 + r]);
+        g = expf(l - lse[t0r + r]);
       }
       s_g[r * KC + kk] = g;
     }
     __syncthreads();
-    // accumulate [1, y, y^2 | y y^T] weighted by g over the tile
+    // phase A: tile count and first moment about the centre
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
       const int f = threadIdx.x + s * kStatThreads;
       if (f >= kc * F) continue;
       const int kk = f / F, feat = f % F;
+      if (feat > D) continue;
       float acc = 0.f;
       if (feat == 0) {
         for (int r = 0; r < tn; ++r) acc += s_g[r * KC + kk];
-      } else if (COV != GMM_COV_FULL) {
-        const int d = (feat - 1) % D;
-        const bool sq = feat > D;
-        const float mu_d = s_mu[kk * D + d];
-        for (int r = 0; r < tn; ++r) {
-          float y = s_x[r * XS + d] - mu_d;
-          acc = fmaf(s_g[r * KC + kk], sq ? y * y : y, acc);
-        }
+        s_t0[kk] = acc;
       } else {
-        if (feat <= D) {
-          const int d = feat - 1;
+        const int d = feat - 1;
+        if constexpr (COV == GMM_COV_FULL) {
           for (int r = 0; r < tn; ++r) acc = fmaf(s_g[r * KC + kk], s_y[(r * KC + kk) * D + d], acc);
         } else {
-          const int e = feat - 1 - D;
-          const int a = s_pair[2 * e], b = s_pair[2 * e + 1];
-          for (int r = 0; r < tn; ++r) {
-            const float* y = s_y + (r * KC + kk) * D;
-            acc = fmaf(s_g[r * KC + kk], y[a] * y[b], acc);
-          }
+          const float c_d = s_mu[kk * D + d];
+          for (int r = 0; r < tn; ++r) acc = fmaf(s_g[r * KC + kk], s_x[r * XS + d] - c_d, acc);
+        }
+        s_t1[kk * D + d] = acc;
+      }
+      tsum[s] = acc;
+    }
+    __syncthreads();
+    // phase B: second moment about the tile mean, merged (Chan et al.)
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+      const int f = threadIdx.x + s * kStatThreads;
+      if (f >= kc * F) continue;
+      const int kk = f / F, feat = f % F;
+      if (feat <= D) continue;
+      const float t0 = s_t0[kk];
+      if (!(t0 > 0.f)) continue;
+      int a, b;
+      if constexpr (COV == GMM_COV_FULL) {
+        const int e = feat - 1 - D;
+        a = s_pair[2 * e];
+        b = s_pair[2 * e + 1];
+      } else {
+        a = b = feat - 1 - D;
+      }
+      const float ma = s_t1[kk * D + a] / t0, mb = s_t1[kk * D + b] / t0;
+      float m2 = 0.f;
+      if constexpr (COV == GMM_COV_FULL) {
+        for (int r = 0; r < tn; ++r) {
+          const float* y = s_y + (r * KC + kk) * D;
+          m2 = fmaf(s_g[r * KC + kk], (y[a] - ma) * (y[b] - mb), m2);
+        }
+      } else {
+        const float c_d = s_mu[kk * D + a];
+        for (int r = 0; r < tn; ++r) {
+          const float u = (s_x[r * XS + a] - c_d) - ma;
+          m2 = fmaf(s_g[r * KC + kk], u * u, m2);
         }
       }
-      accd[s] += (double)acc;
+      const double R0 = s_r0[kk];
+      double corr = 0.0;
+      if (R0 > 0.0) {
+        const double da = (double)ma - s_r1[kk * D + a] / R0;
+        const double db = (double)mb - s_r1[kk * D + b] / R0;
+        corr = da * db * (R0 * (double)t0 / (R0 + (double)t0));
+      }
+      accd[s] += (double)m2 + corr;
+    }
+    __syncthreads();
+    // phase C: running count and first moment
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+      const int f = threadIdx.x + s * kStatThreads;
+      if (f >= kc * F) continue;
+      const int kk = f / F, feat = f % F;
+      if (feat > D) continue;
+      accd[s] += (double)tsum[s];
+      if (feat == 0) s_r0[kk] = accd[s];
+      else s_r1[kk * D + feat - 1] = accd[s];
     }
   }
-  // per-block partial [P][K][F]
+  // per-block partial [P][K][F]; with `accumulate` the block's sums are
+  // merged into the partial already there (same pairwise rule)
   double* out = part + (size_t)blockIdx.y * K * F;
+  __syncthreads();
+  double outv[SLOTS];
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int f = threadIdx.x + s * kStatThreads;
+    outv[s] = accd[s];
+    if (f >= kc * F || !accumulate) continue;
+    const int kk = f / F, feat = f % F;
+    const double* o = out + (size_t)(k0 + kk) * F;
+    if (feat <= D) {
+      outv[s] = o[feat] + accd[s];
+    } else {
+      int a, b;
+      if constexpr (COV == GMM_COV_FULL) {
+        const int e = feat - 1 - D;
+        a = s_pair[2 * e];
+        b = s_pair[2 * e + 1];
+      } else {
+        a = b = feat - 1 - D;
+      }
+      const double S0o = o[0], S0n = s_r0[kk];
+      double corr = 0.0;
+      if (S0o > 0.0 && S0n > 0.0) {
+        const double da = s_r1[kk * D + a] / S0n - o[1 + a] / S0o;
+        const double db = s_r1[kk * D + b] / S0n - o[1 + b] / S0o;
+        corr = da * db * (S0o * S0n / (S0o + S0n));
+      }
+      outv[s] = o[feat] + accd[s] + corr;
+    }
+  }
+  __syncthreads();
 #pragma unroll
   for (int s = 0; s < SLOTS; ++s) {
     const int f = threadIdx.x + s * kStatThreads;
     if (f >= kc * F) continue;
     const int kk = f / F, feat = f % F;
-    double* o = out + (size_t)(k0 + kk) * F + feat;
-    *o = accumulate ? *o + accd[s] : accd[s];
+    out[(size_t)(k0 + kk) * F + feat] = outv[s];
   }
 }
 
@@ -317,9 +437,11 @@ template <int D, int COV, int XT>
 size_t stat_smem() {
   using SS = StatShape<D, COV>;
   constexpr int P = LseShape<D, COV>::P;
-  size_t f = (size_t)kStatTile * (D + 1) + kStatTile * SS::KC + SS::KC * D + SS::KC * P + SS::KC;
+  size_t b = sizeof(double) * (size_t)SS::KC * (D + 1);
+  size_t f = (size_t)kStatTile * (D + 1) + kStatTile * SS::KC + SS::KC * D + SS::KC * P + SS::KC +
+             SS::KC + SS::KC * D;
   if (COV == GMM_COV_FULL) f += (size_t)kStatTile * SS::KC * D;
-  size_t b = f * sizeof(float);
+  b += f * sizeof(float);
   if (COV == GMM_COV_FULL) b += sizeof(short) * 2 * (D * (D + 1) / 2);
   return b;
 }

@@ -25,7 +25,13 @@ def make_state(wl, chunk_rows=None):
     return GMMState(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, chunk_rows=chunk_rows)
 
 
-def gpu_step(state: GMMState, Xd, params, want_lse=False):
+def set_opts(state: GMMState, opts):
+    for k, v in (opts or {}).items():
+        setattr(state.opts, k, v)
+
+
+def gpu_step(state: GMMState, Xd, params, want_lse=False, opts=None):
+    set_opts(state, opts)
     state.set_params(*params)
     lse = torch.empty(state.N, dtype=torch.float32, device="cuda") if want_lse else None
     state.step(Xd, lse=lse)

@@ -21,6 +21,11 @@ PARAM_FLOOR = 1e-3
 PI_ATOL = 1e-5
 TOP1_MIN = 0.999
 TIE_EPS = 1e-6
+# Trajectories (each side iterating on its own from theta_0) are held to the
+# per-iteration LL bound and to a 10x wider parameter band: a parameter that
+# depends on a few boundary points amplifies last-bit differences of the
+# previous iterate, so the strict bound is a per-step (same input) bound.
+TRAJ_PARAM_RTOL = 2e-2
 
 
 def diagnostics(got, ref):
@@ -44,9 +49,16 @@ def scaled_rel_err(got, ref):
     return np.abs(got - ref) / np.maximum(np.abs(ref), PARAM_FLOOR * scale + 1e-300)
 
 
-def compare_step(gpu, ref, what=""):
-    """gpu/ref: dicts with pi, mu, cov, ll.  Returns a list of failure strings."""
+def compare_step(gpu, ref, what="", min_s0=None, param_rtol=PARAM_RTOL):
+    """gpu/ref: dicts with pi, mu, cov, ll.  Returns a list of failure strings.
+    With min_s0 (and ref['s0']), components whose oracle s0 lies within 1e-4
+    (relative) of the empty threshold are left out of the mean/covariance
+    check: there the empty-or-not decision rests on rounding."""
     fails = []
+    keep = None
+    if min_s0 is not None and "s0" in ref:
+        s0 = np.asarray(ref["s0"])
+        keep = np.abs(s0 - min_s0) > 1e-4 * max(min_s0, 1e-30)
     ll_err = abs(gpu["ll"] - ref["ll"]) / max(abs(ref["ll"]), 1e-300)
     if not ll_err <= LL_RTOL:
         fails.append("%s LL rel err %.3g (gpu %.10g ref %.10g)" % (what, ll_err, gpu["ll"], ref["ll"]))
@@ -56,7 +68,9 @@ def compare_step(gpu, ref, what=""):
                                                      diagnostics(gpu["pi"], ref["pi"])))
     for name in ("mu", "cov"):
         e = scaled_rel_err(gpu[name], ref[name])
-        if not (e <= PARAM_RTOL).all():
+        if keep is not None:
+            e = e * keep.reshape((-1,) + (1,) * (e.ndim - 1))
+        if not (e <= param_rtol).all():
             idx = np.unravel_index(int(np.argmax(e)), e.shape)
             fails.append("%s %s scaled rel err %.3g at %s (gpu %.8g ref %.8g) %s" % (
                 what, name, e.max(), idx, np.asarray(gpu[name])[idx], np.asarray(ref[name])[idx],

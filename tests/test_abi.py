@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_default_opts_and_strings(lib):
     o = G.gmm_default_opts()
-    assert o.ridge_rel == 0.0 and o.var_floor == 0.0 and abs(o.min_s0 - 1e-3) < 1e-9
+    assert o.ridge_rel == 0.0 and o.var_floor == 0.0 and o.min_s0 == 0.5
     assert G.status_string(G.GMM_ERR_NOT_PD) == "GMM_ERR_NOT_PD"
 
 

@@ -12,7 +12,7 @@ import torch
 import datagen
 import oracle
 import parity
-from gpu_util import f32, gpu_step, make_state, oracle_step, to_device
+from gpu_util import f32, gpu_step, make_state, oracle_step, set_opts, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -38,28 +38,30 @@ def _run_parity(wl, iters, trajectory=True):
     mix = datagen.planted(wl)
     bits = datagen.points(mix, 0, wl.N)
     theta0 = f32(datagen.init_params(mix, bits))
+    opts = datagen.em_opts(theta0)
     Xd = to_device(bits, wl.dtype)
     state = make_state(wl)
     fails = []
     # per step: both sides start each step from the oracle's (fp32-rounded) parameters
     theta = theta0
     for t in range(iters):
-        ref = oracle_step(bits, wl.dtype, theta, wl.cov_type)
+        ref = oracle_step(bits, wl.dtype, theta, wl.cov_type, opts=opts)
         assert ref["status"] == 0
-        got = gpu_step(state, Xd, theta)
+        got = gpu_step(state, Xd, theta, opts=opts)
         assert got["status"] == 0, got["status"]
-        fails += parity.compare_step(got, ref, "%s step %d" % (wl.name, t))
+        fails += parity.compare_step(got, ref, "%s step %d" % (wl.name, t), opts["min_s0"])
         theta = f32((ref["pi"], ref["mu"], ref["cov"]))
     # trajectory: each side on its own from theta_0
     if trajectory:
         ref_theta = theta0
         state.set_params(*theta0)
         for t in range(iters):
-            ref = oracle_step(bits, wl.dtype, ref_theta, wl.cov_type)
+            ref = oracle_step(bits, wl.dtype, ref_theta, wl.cov_type, opts=opts)
             state.step(Xd)
             pi, mu, cov = state.params_numpy()
             got = dict(pi=pi, mu=mu, cov=cov, ll=float(state.loglik.item()))
-            fails += parity.compare_step(got, ref, "%s trajectory %d" % (wl.name, t))
+            fails += parity.compare_step(got, ref, "%s trajectory %d" % (wl.name, t),
+                                         opts["min_s0"], parity.TRAJ_PARAM_RTOL)
             ref_theta = (ref["pi"], ref["mu"], ref["cov"])
     assert not fails, "\n".join(fails[:10])
 
@@ -160,15 +162,18 @@ def test_host_streaming_matches():
     mix = datagen.planted(wl)
     bits = datagen.points(mix, 0, wl.N)
     theta = f32(datagen.init_params(mix, bits))
-    ref = oracle_step(bits, wl.dtype, theta, wl.cov_type)
+    opts = datagen.em_opts(theta)
+    ref = oracle_step(bits, wl.dtype, theta, wl.cov_type, opts=opts)
     s = make_state(wl, chunk_rows=7_000)
+    set_opts(s, opts)
     s.set_params(*theta)
     host = torch.from_numpy(bits.view(np.int16)).pin_memory()
     ll_host = np.zeros(1)
     s.step_host(host, loglik_host=ll_host)
     assert s.device_status() == 0
     pi, mu, cov = s.params_numpy()
-    fails = parity.compare_step(dict(pi=pi, mu=mu, cov=cov, ll=float(ll_host[0])), ref, "host")
+    fails = parity.compare_step(dict(pi=pi, mu=mu, cov=cov, ll=float(ll_host[0])), ref, "host",
+                                opts["min_s0"])
     assert not fails, fails
 
 
@@ -183,9 +188,11 @@ def test_edge_cases_small():
         pi = np.full(K, 1.0 / K, dtype=np.float32)
         mu = (mix.mu.astype(np.float32) * 0.5)
         var = np.ones((K, 16), dtype=np.float32)
-        ref = oracle_step(bits, wl.dtype, (pi, mu, var), wl.cov_type)
-        got = gpu_step(make_state(wl), to_device(bits, wl.dtype), (pi, mu, var))
-        fails = parity.compare_step(got, ref, "N=%d K=%d" % (N, K))
+        # one point has zero variance: the floor makes the update defined
+        opts = dict(var_floor=1e-6, min_s0=0.5)
+        ref = oracle_step(bits, wl.dtype, (pi, mu, var), wl.cov_type, opts=opts)
+        got = gpu_step(make_state(wl), to_device(bits, wl.dtype), (pi, mu, var), opts=opts)
+        fails = parity.compare_step(got, ref, "N=%d K=%d" % (N, K), 0.5)
         assert not fails, fails
         assert (got["flags"] == ref["flags"]).all(), (got["flags"], ref["flags"])
 
@@ -202,12 +209,11 @@ def test_empty_floor_notpd_flags():
     mu[2] = 0.5
     var = np.ones((K, D), dtype=np.float32)
     var[3, 0] = 0.0  # ridge retry (1e-3 tr/D) repairs it
-    opts = dict(var_floor=0.9, min_s0=1e-3)
+    opts = dict(var_floor=0.9, min_s0=0.5)
     wl = datagen.Workload("flags", 0, N, D, K, datagen.F32, datagen.COV_DIAG, 1, 0, {})
     ref = oracle_step(X, datagen.F32, (pi, mu, var), wl.cov_type, opts=opts)
     s = make_state(wl)
-    s.opts.var_floor = 0.9
-    got = gpu_step(s, to_device(X, datagen.F32), (pi, mu, var))
+    got = gpu_step(s, to_device(X, datagen.F32), (pi, mu, var), opts=opts)
     assert (got["flags"] == ref["flags"]).all(), (got["flags"], ref["flags"])
     assert got["flags"][1] & oracle.FLAG_EMPTY and got["flags"][3] & oracle.FLAG_RIDGE
     fails = parity.compare_step(got, ref, "flags")
