@@ -224,7 +224,9 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   extern __shared__ double smd[];
   double* s_r0 = smd;                 // KC     running S0 of this block
   double* s_r1 = s_r0 + KC;           // KC*D   running S1 of this block
-  float* s_x = (float*)(s_r1 + KC * D);  // T*XS
+  double* s_rm = s_r1 + KC * D;       // KC*D   running mean S1 / S0
+  double* s_fac = s_rm + KC * D;      // KC     this tile's correction weight
+  float* s_x = (float*)(s_fac + KC);  // T*XS
   float* s_g = s_x + T * XS;          // T*KC
   float* s_mu = s_g + T * KC;         // KC*D
   float* s_prec = s_mu + KC * D;      // KC*P
@@ -244,7 +246,7 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   for (int i = threadIdx.x; i < kc * P; i += kStatThreads)
     s_prec[i] = at<float>(prepared, L.off_prec)[(size_t)k0 * P + i];
   for (int i = threadIdx.x; i < kc; i += kStatThreads) s_c[i] = at<float>(prepared, L.off_c)[k0 + i];
-  for (int i = threadIdx.x; i < KC * (D + 1); i += kStatThreads) smd[i] = 0.0;
+  for (int i = threadIdx.x; i < KC * (2 * D + 2); i += kStatThreads) smd[i] = 0.0;
   if constexpr (COV == GMM_COV_FULL) {
     for (int e = threadIdx.x; e < D * (D + 1) / 2; e += kStatThreads) {
       // e enumerates the lower triangle row by row: (a, b) with b <= a
@@ -271,8 +273,10 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
     }
     __syncthreads();
     // responsibilities of this chunk for the tile
+    // lanes of a warp share one component (broadcast reads of its
+    // parameters) and walk consecutive rows of the padded x tile
     for (int pidx = threadIdx.x; pidx < T * KC; pidx += kStatThreads) {
-      const int r = pidx / KC, kk = pidx % KC;
+      const int kk = pidx / T, r = pidx % T;
       float g = 0.f;
       if (r < tn && kk < kc && s_c[kk] != -INFINITY) {
         float l;
@@ -318,6 +322,9 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
       if (feat == 0) {
         for (int r = 0; r < tn; ++r) acc += s_g[r * KC + kk];
         s_t0[kk] = acc;
+        // weight of the pairwise correction: S0 t0 / (S0 + t0)
+        const double R0 = s_r0[kk];
+        s_fac[kk] = (R0 > 0.0 && acc > 0.f) ? R0 * (double)acc / (R0 + (double)acc) : 0.0;
       } else {
         const int d = feat - 1;
         if constexpr (COV == GMM_COV_FULL) {
@@ -362,14 +369,11 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
           m2 = fmaf(s_g[r * KC + kk], u * u, m2);
         }
       }
-      const double R0 = s_r0[kk];
-      double corr = 0.0;
-      if (R0 > 0.0) {
-        const double da = (double)ma - s_r1[kk * D + a] / R0;
-        const double db = (double)mb - s_r1[kk * D + b] / R0;
-        corr = da * db * (R0 * (double)t0 / (R0 + (double)t0));
-      }
-      accd[s] += (double)m2 + corr;
+      // s_rm holds the running mean (S1 / S0) of the tiles merged so far
+      const double fac = s_fac[kk];
+      const double da = (double)ma - s_rm[kk * D + a];
+      const double db = (double)mb - s_rm[kk * D + b];
+      accd[s] += (double)m2 + da * db * fac;
     }
     __syncthreads();
     // phase C: running count and first moment
@@ -382,6 +386,12 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
       accd[s] += (double)tsum[s];
       if (feat == 0) s_r0[kk] = accd[s];
       else s_r1[kk * D + feat - 1] = accd[s];
+    }
+    __syncthreads();
+    // running mean for the next tile's correction
+    for (int i = threadIdx.x; i < kc * D; i += kStatThreads) {
+      const double r0 = s_r0[i / D];
+      s_rm[i] = r0 > 0.0 ? s_r1[i] / r0 : 0.0;
     }
   }
   // per-block partial [P][K][F]; with `accumulate` the block's sums are
@@ -437,7 +447,7 @@ template <int D, int COV, int XT>
 size_t stat_smem() {
   using SS = StatShape<D, COV>;
   constexpr int P = LseShape<D, COV>::P;
-  size_t b = sizeof(double) * (size_t)SS::KC * (D + 1);
+  size_t b = sizeof(double) * (size_t)SS::KC * (2 * D + 2);
   size_t f = (size_t)kStatTile * (D + 1) + kStatTile * SS::KC + SS::KC * D + SS::KC * P + SS::KC +
              SS::KC + SS::KC * D;
   if (COV == GMM_COV_FULL) f += (size_t)kStatTile * SS::KC * D;
