@@ -179,6 +179,38 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
 gmm_status gmm_last_device_status(void* ws, void* stream);
 
 /*
+ * gmm_em_step_noalloc - gmm_em_step for callers that cannot allocate device
+ * memory.  The source pages have no counterpart: this entry point exists for
+ * callers that are handed only their input and output buffers - plugins
+ * running inside another framework's memory budget, code that must not call
+ * cudaMalloc after start-up - and so cannot provide the `ws` workspace that
+ * gmm_em_step needs.
+ *
+ * Same arithmetic and outputs as gmm_em_step (same kernels, same reduction
+ * order).  X, params, loglik_dev, lse_dev (N floats, required here) and
+ * flags_dev (optional) are the caller's device buffers.  All other scratch
+ * lives in one 64 MiB array built into the library's device image: every
+ * GPU that loads the library holds it until the process exits, and nothing
+ * is allocated by this call.  The scratch needed is about
+ * N/16 + 8*P*K*F + 4*K*(D+2) + prepared-parameter bytes (P statistics blocks,
+ * F = 1+2D, or 1+D+D(D+1)/2 for full covariance); sizes that need more than
+ * 64 MiB are rejected with GMM_ERR_WORKSPACE (and a message on stderr)
+ * before anything is queued.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture.  Every call shares the one
+ * array, so calls that overlap on the GPU (other streams, other host
+ * threads) race: serialise them.  The call synchronises `stream` and
+ * returns the first device-side condition of this call (GMM_ERR_NOT_PD,
+ * GMM_ERR_NONFINITE) or GMM_OK.
+ */
+gmm_status gmm_em_step_noalloc(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
+                               gmm_params* params, gmm_cov_type cov, const gmm_opts* opts,
+                               double* loglik_dev, float* lse_dev, int32_t* flags_dev,
+                               void* stream);
+
+/*
  * Per-kernel timing ("launch / device / sync" breakdown of the ops-debug
  * page, sec. 4.2).  gmm_profile_enable(1): every kernel the library launches
  * is bracketed by two CUDA events recorded on its own stream (adds two event

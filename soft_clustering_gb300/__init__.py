@@ -25,7 +25,7 @@ EXPORTS = (
     "gmm_default_opts", "gmm_status_string", "gmm_workspace_bytes", "gmm_prepared_bytes",
     "gmm_prepare", "gmm_em_step", "gmm_workspace_bytes_host", "gmm_em_step_host",
     "gmm_assign_topm", "gmm_last_device_status", "gmm_profile_enable", "gmm_profile_read",
-    "gmm_profile_reset",
+    "gmm_profile_reset", "gmm_em_step_noalloc",
 )
 
 
@@ -73,6 +73,8 @@ def lib():
                                        vp, sz, i64, vp, vp, vp, vp]
         L.gmm_assign_topm.argtypes = [vp, i32, i64, i32, i32, vp, i32, i32, vp, vp, vp, vp, sz, vp]
         L.gmm_last_device_status.argtypes = [vp, vp]
+        L.gmm_em_step_noalloc.argtypes = [vp, i32, i64, i32, i32, P(gmm_params), i32,
+                                          P(gmm_opts), vp, vp, vp, vp]
         L.gmm_profile_enable.argtypes = [i32]
         L.gmm_profile_enable.restype = None
         L.gmm_profile_read.argtypes = [P(ctypes.c_char_p), P(ctypes.c_double), P(ctypes.c_long),
@@ -80,7 +82,7 @@ def lib():
         L.gmm_profile_read.restype = i32
         L.gmm_profile_reset.restype = None
         for f in ("gmm_prepare", "gmm_em_step", "gmm_em_step_host", "gmm_assign_topm",
-                  "gmm_last_device_status"):
+                  "gmm_last_device_status", "gmm_em_step_noalloc"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -176,6 +178,19 @@ def gmm_assign_topm(X, xdtype, N, D, K, prepared, cov_type, m, ids, gamma, lse, 
     st = lib().gmm_assign_topm(_ptr(X), xdtype, N, D, K, _ptr(prepared), cov_type, m, _ptr(ids),
                                _ptr(gamma), _ptr(lse), _ptr(ws), ws_bytes, _stream(stream))
     return _check(st, "gmm_assign_topm", raise_on_error)
+
+
+def gmm_em_step_noalloc(X, xdtype, N, D, K, pi, mu, cov, cov_type, loglik, lse, flags=None,
+                        opts=None, stream=None, raise_on_error=True):
+    """The EM step without a workspace, for callers that cannot allocate
+    device memory (scratch is a fixed 64 MiB array inside the library).
+    Synchronises the stream; returns the call's status."""
+    p = make_params(pi, mu, cov)
+    o = opts if opts is not None else gmm_default_opts()
+    st = lib().gmm_em_step_noalloc(_ptr(X), xdtype, N, D, K, ctypes.byref(p), cov_type,
+                                   ctypes.byref(o), _ptr(loglik), _ptr(lse), _ptr(flags),
+                                   _stream(stream))
+    return _check(st, "gmm_em_step_noalloc", raise_on_error)
 
 
 def gmm_last_device_status(ws, stream=None) -> int:

@@ -184,6 +184,11 @@ gmm_status host_res(HostPathRes** out) {
 }
 
 }  // namespace
+
+// The statistics partition count the entry points above use, for other
+// translation units that launch the same kernels.
+int stat_parts_for(int64_t N, int D, int K, int cov) { return stat_parts(N, D, K, cov); }
+
 }  // namespace gmm
 
 using namespace gmm;
