@@ -25,7 +25,7 @@ EXPORTS = (
     "gmm_default_opts", "gmm_status_string", "gmm_workspace_bytes", "gmm_prepared_bytes",
     "gmm_prepare", "gmm_em_step", "gmm_workspace_bytes_host", "gmm_em_step_host",
     "gmm_assign_topm", "gmm_last_device_status", "gmm_profile_enable", "gmm_profile_read",
-    "gmm_profile_reset", "gmm_em_step_noalloc",
+    "gmm_profile_reset", "gmm_em_step_noalloc", "gmm_debug_tc_gemm",
 )
 
 
@@ -75,6 +75,8 @@ def lib():
         L.gmm_last_device_status.argtypes = [vp, vp]
         L.gmm_em_step_noalloc.argtypes = [vp, i32, i64, i32, i32, P(gmm_params), i32,
                                           P(gmm_opts), vp, vp, vp, vp]
+        L.gmm_debug_tc_gemm.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+        L.gmm_debug_tc_gemm.restype = i32
         L.gmm_profile_enable.argtypes = [i32]
         L.gmm_profile_enable.restype = None
         L.gmm_profile_read.argtypes = [P(ctypes.c_char_p), P(ctypes.c_double), P(ctypes.c_long),
@@ -212,3 +214,9 @@ def gmm_profile_read(max_kernels: int = 32) -> dict:
     n_l = (ctypes.c_long * max_kernels)()
     n = lib().gmm_profile_read(names, ms, n_l, max_kernels)
     return {names[i].decode(): (ms[i], n_l[i]) for i in range(min(n, max_kernels))}
+
+
+def gmm_debug_tc_gemm(A, B, C, kdim, n, status, stream=None) -> int:
+    """Test-only: C = A B^T through the tensor-core building blocks."""
+    return int(lib().gmm_debug_tc_gemm(_ptr(A), _ptr(B), _ptr(C), kdim, n, _ptr(status),
+                                       _stream(stream)))
