@@ -59,6 +59,9 @@ enum {
   GMM_FLAG_EMPTY = 8    /* s0 < min_s0: mean and covariance kept */
 };
 
+/* gmm_opts.flags bits. */
+enum { GMM_OPT_CUDA_CORES = 1 };
+
 /* Model parameters, fp32 device arrays (layout above). */
 typedef struct {
   float* pi;
@@ -74,7 +77,9 @@ typedef struct {
  * var_floor: lower bound applied to updated variances (and the diagonal of a
  * full covariance).  min_s0: a component whose responsibility sum s0 is
  * below it keeps its mean and covariance (its weight becomes s0/N).
- * flags: reserved, 0. */
+ * flags: GMM_OPT_CUDA_CORES (bit 0) computes every log-density on CUDA cores
+ * even where the tensor-core screening path applies (diagonal / isotropic
+ * covariance, D = 64 or 128); other bits reserved, 0. */
 typedef struct {
   float ridge_rel;
   float var_floor;
@@ -166,7 +171,8 @@ gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int
  * prepared: output of gmm_prepare for the same D, K, cov.
  * ids:      N*m int32 (device), gamma: N*m float (device), lse: N floats or NULL.
  * m:        1..8, m <= K.
- * ws:       at least 256 bytes (the status word); gmm_workspace_bytes is enough.
+ * ws:       gmm_workspace_bytes(N, D, K, cov, xdtype) bytes (status word and the
+ *           list of points handed from the tensor-core to the CUDA-core path).
  */
 gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
                            const void* prepared, gmm_cov_type cov, int m, int32_t* ids,

@@ -20,6 +20,7 @@ GMM_F32, GMM_F16, GMM_BF16 = 0, 1, 2
 GMM_OK, GMM_ERR_INVALID_ARG, GMM_ERR_UNSUPPORTED, GMM_ERR_NOT_PD = 0, 1, 2, 3
 GMM_ERR_NONFINITE, GMM_ERR_WORKSPACE, GMM_ERR_TIMEOUT, GMM_ERR_CUDA = 4, 5, 6, 7
 GMM_FLAG_RIDGE, GMM_FLAG_NOT_PD, GMM_FLAG_FLOOR, GMM_FLAG_EMPTY = 1, 2, 4, 8
+GMM_OPT_CUDA_CORES = 1
 
 EXPORTS = (
     "gmm_default_opts", "gmm_status_string", "gmm_workspace_bytes", "gmm_prepared_bytes",

@@ -16,6 +16,15 @@ cudaError_t launch_prepare(const gmm_params* p, int D, int K, int cov, float rid
 cudaError_t simt_lse(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                      const void* prepared, float* lse, double* ll_part, int m, int32_t* ids,
                      float* gamma, DeviceStatus* st, cudaStream_t s);
+cudaError_t simt_lse_rows(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                          const void* prepared, float* lse, double* ll_part, int m, int32_t* ids,
+                          float* gamma, DeviceStatus* st, const uint32_t* rows,
+                          const uint32_t* row_count, int grid, cudaStream_t s);
+cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                      const void* prepared, int mode, float* lse, double* ll_part, int m,
+                      int32_t* ids, float* gamma, uint32_t* fb_rows, uint32_t* fb_count,
+                      DeviceStatus* st, cudaStream_t s);
+int tc_screen_grid(int64_t N);
 cudaError_t simt_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                        const void* prepared, const float* lse, int parts, double* part,
                        int accumulate, cudaStream_t s);
@@ -30,6 +39,8 @@ namespace {
 
 constexpr int kLseRows = 128;      // rows per block of the LSE kernel
 constexpr int kTargetCtas = 608;   // 4 x 152 SMs: statistics blocks per launch
+constexpr int kListGrid = 304;     // blocks of the CUDA-core pass over handed-over rows
+constexpr int kMaxScreenGrid = 1024;  // upper bound of tc_screen_grid (SM count)
 constexpr int kMaxK = 1 << 16;
 
 bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
@@ -48,11 +59,15 @@ int stat_parts(int64_t N, int D, int K, int cov) {
 }
 
 struct WsLayout {
-  size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_stage,
-      bytes;
+  size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_fb,
+      off_stage, bytes;
   int parts;
   int64_t lse_rows;
 };
+
+bool use_tc(int D, int cov, const gmm_opts& o) {
+  return tc_eligible(D, cov) && !(o.flags & GMM_OPT_CUDA_CORES);
+}
 
 // rows: rows processed per launch (N, or the chunk size of the host path);
 // stage_bytes: host path staging buffers (0 otherwise).
@@ -63,11 +78,17 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_prep = o;   o = align_up(o + PreparedLayout::make(D, K, cov).bytes);
   W.lse_rows = rows;
   W.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)rows);
-  W.off_llpart = o; o = align_up(o + sizeof(double) * (size_t)((rows + kLseRows - 1) / kLseRows));
+  {
+    // dense LSE blocks, or the tensor-core CTAs followed by the list blocks
+    const size_t dense = (size_t)((rows + kLseRows - 1) / kLseRows);
+    const size_t tcl = (size_t)(kMaxScreenGrid + kListGrid);
+    W.off_llpart = o; o = align_up(o + sizeof(double) * (dense > tcl ? dense : tcl));
+  }
   W.off_ll = o;     o = align_up(o + sizeof(double));
   W.parts = stat_parts(rows, D, K, cov);
   W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)W.parts * K * stat_width(D, cov));
   W.off_flags = o;  o = align_up(o + sizeof(int32_t) * K);
+  W.off_fb = o;     o = align_up(o + sizeof(uint32_t) * (size_t)rows);
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
@@ -136,18 +157,36 @@ struct ProfScope {
 // The E-step and statistics for one block of rows, accumulating into the
 // workspace partials (accumulate = 0 for the first block of an iteration).
 gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int K, int cov,
-                      const WsLayout& W, void* ws, float* lse, int accumulate, cudaStream_t s) {
+                      const WsLayout& W, void* ws, float* lse, int accumulate, bool tc,
+                      cudaStream_t s) {
   DeviceStatus* st = at<DeviceStatus>(ws, W.off_status);
   const void* prep = at<char>(ws, W.off_prep);
   double* llp = at<double>(ws, W.off_llpart);
-  {
+  int64_t nll = (rows + kLseRows - 1) / kLseRows;
+  if (tc) {
+    // screen on the tensor cores; rows whose candidate list overflowed go
+    // through the CUDA-core kernel in row-list mode
+    uint32_t* fb = at<uint32_t>(ws, W.off_fb);
+    GMM_TRY(cudaMemsetAsync(&st->fb_count, 0, sizeof(uint32_t), s));
+    const int g1 = tc_screen_grid(rows);
+    {
+      GMM_PROF("tc_screen_kernel");
+      GMM_TRY(tc_screen(X, xdtype, rows, D, K, cov, prep, 0, lse, llp, 0, nullptr, nullptr, fb,
+                        &st->fb_count, st, s));
+    }
+    {
+      GMM_PROF("lse_rows_kernel");
+      GMM_TRY(simt_lse_rows(X, xdtype, rows, D, K, cov, prep, lse, llp + g1, 0, nullptr, nullptr,
+                            st, fb, &st->fb_count, kListGrid, s));
+    }
+    nll = g1 + kListGrid;
+  } else {
     GMM_PROF("lse_kernel");
     GMM_TRY(simt_lse(X, xdtype, rows, D, K, cov, prep, lse, llp, 0, nullptr, nullptr, st, s));
   }
   {
     GMM_PROF("ll_finalize_kernel");
-    GMM_TRY(launch_ll_finalize(llp, (rows + kLseRows - 1) / kLseRows, at<double>(ws, W.off_ll),
-                               accumulate, s));
+    GMM_TRY(launch_ll_finalize(llp, nll, at<double>(ws, W.off_ll), accumulate, s));
   }
   {
     GMM_PROF("stats_kernel");
@@ -279,7 +318,7 @@ gmm_status gmm_em_step(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
     GMM_TRY(launch_prepare(params, D, K, cov, o.ridge_rel, prep, st, s));
   }
   float* lse = lse_dev ? lse_dev : at<float>(ws, W.off_lse);
-  gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, 0, s);
+  gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, 0, use_tc(D, cov, o), s);
   if (r != GMM_OK) return r;
   {
     GMM_PROF("mstep_kernel");
@@ -336,7 +375,7 @@ gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int
     GMM_TRY(cudaEventRecord(res->copied[b], res->copy));
     GMM_TRY(cudaStreamWaitEvent(s, res->copied[b], 0));
     gmm_status r = estep_rows(stage[b], xdtype, rn, D, K, cov, W, ws, at<float>(ws, W.off_lse),
-                              ci > 0, s);
+                              ci > 0, use_tc(D, cov, o), s);
     if (r != GMM_OK) return r;
     GMM_TRY(cudaEventRecord(res->consumed[b], s));
   }
@@ -363,10 +402,24 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
   if (c != GMM_OK) return c;
   if (!prepared || !ids || !gamma || !ws || m < 1 || m > 8 || m > K) return GMM_ERR_INVALID_ARG;
   if (((uintptr_t)X & 15) || ((uintptr_t)ws & 255)) return GMM_ERR_INVALID_ARG;
-  if (ws_bytes < sizeof(DeviceStatus)) return GMM_ERR_WORKSPACE;
+  const WsLayout W = ws_layout(N, N, D, K, cov, 0);
+  const bool tc = tc_eligible(D, cov);
+  if (ws_bytes < (tc ? W.bytes : sizeof(DeviceStatus))) return GMM_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   DeviceStatus* st = static_cast<DeviceStatus*>(ws);
   GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
+  if (tc) {
+    uint32_t* fb = at<uint32_t>(ws, W.off_fb);
+    {
+      GMM_PROF("tc_screen_kernel");
+      GMM_TRY(tc_screen(X, xdtype, N, D, K, cov, prepared, 1, lse, nullptr, m, ids, gamma, fb,
+                        &st->fb_count, st, s));
+    }
+    GMM_PROF("lse_rows_kernel");
+    GMM_TRY(simt_lse_rows(X, xdtype, N, D, K, cov, prepared, lse, nullptr, m, ids, gamma, st, fb,
+                          &st->fb_count, kListGrid, s));
+    return GMM_OK;
+  }
   GMM_PROF("lse_topm_kernel");
   GMM_TRY(simt_lse(X, xdtype, N, D, K, cov, prepared, lse, nullptr, m, ids, gamma, st, s));
   return GMM_OK;

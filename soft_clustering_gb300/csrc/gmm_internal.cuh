@@ -18,9 +18,10 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a = kAlign) {
 // Status-word bits (first failing condition recorded as a gmm_status value;
 // later conditions only OR into the detail word).
 struct DeviceStatus {
-  int32_t code;     // gmm_status of the first device-side failure (0 = none)
-  int32_t detail;   // OR of (1 << gmm_status) for every failure seen
-  int32_t pad[62];
+  int32_t code;        // gmm_status of the first device-side failure (0 = none)
+  int32_t detail;      // OR of (1 << gmm_status) for every failure seen
+  uint32_t fb_count;   // rows the tensor-core kernel handed to the CUDA-core path
+  int32_t pad[61];
 };
 
 __device__ inline void raise_status(DeviceStatus* st, int code) {
@@ -40,6 +41,14 @@ __host__ __device__ inline int prec_width(int D, int cov) {
   return cov == GMM_COV_FULL ? D * D : (cov == GMM_COV_DIAG ? D : 1);
 }
 
+// Tensor-core screening applies to diagonal / isotropic covariance with
+// D = 64 or 128: the log-density is screened as [x, x^2] . [b1, b2] with
+// b1 = mu / var, b2 = -1 / (2 var) on fp16 tensor cores.
+constexpr int kTcChunk = 128;  // components per screening chunk (MMA N)
+__host__ __device__ inline bool tc_eligible(int D, int cov) {
+  return (cov == GMM_COV_DIAG || cov == GMM_COV_ISO) && (D == 64 || D == 128);
+}
+
 // Prepared-parameter block written by gmm_prepare.
 struct PreparedLayout {
   int D, K, cov;
@@ -47,7 +56,12 @@ struct PreparedLayout {
   size_t off_c;      // float [K]    log pi - log|S|/2 - (D/2) log 2pi  (-inf: excluded)
   size_t off_mu;     // float [K*D]  means
   size_t off_prec;   // float [K*P]  diag: 1/var; iso: 1/var; full: W = L^-1 (lower)
-  size_t off_tc;     // tensor-core operand blocks (see tc kernels); 0 bytes if none
+  // tensor-core screening operands (tc_eligible shapes only):
+  int tc_chunks;     // ceil(K / 128)
+  size_t off_tcB;    // fp16 [chunks][2D/64][128 rows][64]: (b1, b2)/scale as 128-byte
+                     // swizzled K-major tiles, one contiguous image per chunk
+  size_t tcB_chunk_bytes;
+  size_t off_tcT;    // float [chunks][3][128]: scale (power of 2), |(b1,b2)|_2, bias
   size_t tc_bytes;
   size_t bytes;
 
@@ -59,10 +73,21 @@ struct PreparedLayout {
     L.off_c = o;     o = align_up(o + sizeof(float) * K);
     L.off_mu = o;    o = align_up(o + sizeof(float) * (size_t)K * D);
     L.off_prec = o;  o = align_up(o + sizeof(float) * (size_t)K * prec_width(D, cov));
-    L.off_tc = o;
+    L.tc_chunks = 0;
+    L.off_tcB = L.off_tcT = o;
+    L.tcB_chunk_bytes = 0;
     L.tc_bytes = 0;
-    o = align_up(o + L.tc_bytes);
-    L.bytes = o;
+    if (tc_eligible(D, cov)) {
+      L.tc_chunks = (K + kTcChunk - 1) / kTcChunk;
+      o = align_up(o, 1024);
+      L.off_tcB = o;
+      L.tcB_chunk_bytes = (size_t)kTcChunk * 2 * D * 2;
+      o = align_up(o + L.tcB_chunk_bytes * L.tc_chunks);
+      L.off_tcT = o;
+      o = align_up(o + sizeof(float) * 3 * kTcChunk * L.tc_chunks);
+      L.tc_bytes = o - L.off_tcB;
+    }
+    L.bytes = align_up(o);
     return L;
   }
 };

@@ -9,6 +9,7 @@
 #include <math.h>
 
 #include "gmm_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gmm {
 
@@ -153,7 +154,80 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
   }
 }
 
+// Screening operands for the tensor-core kernel (diagonal / isotropic, D = 64
+// or 128), one block per component of the padded range [0, 128 * chunks).
+// Row k of chunk k / 128 holds (b1, b2) = (mu w, -w / 2) divided by a power of
+// two s_k chosen so max |b| / s_k <= 2^14 (no fp16 overflow whatever the
+// variance), rounded to fp16 and stored in the 128-byte swizzled K-major
+// layout the MMA reads.  The trailer keeps s_k, |(b1, b2)|_2 (for the
+// rounding bound) and the screening bias c_k - (1/2) sum_d mu_d^2 w_d (the
+// constant of the expanded form).  Components with bias -inf and padding rows
+// get b = 0 and bias -inf.
+__global__ void prepare_tc_kernel(PreparedLayout L, void* prepared) {
+  __shared__ double red[32];
+  __shared__ double s_max;
+  const int k = blockIdx.x;
+  const int D = L.D, KD = 2 * D;
+  const int chunk = k / kTcChunk, row = k % kTcChunk;
+  unsigned char* img = at<unsigned char>(prepared, L.off_tcB) + (size_t)chunk * L.tcB_chunk_bytes;
+  float* trail = at<float>(prepared, L.off_tcT) + (size_t)chunk * 3 * kTcChunk;
+  const bool live = k < L.K && at<float>(prepared, L.off_c)[k] != -INFINITY;
+  const float* mu = at<float>(prepared, L.off_mu) + (size_t)(live ? k : 0) * D;
+  const float* prec = at<float>(prepared, L.off_prec) +
+                      (size_t)(live ? k : 0) * (L.cov == GMM_COV_DIAG ? D : 1);
+  auto bval = [&](int j) -> double {
+    if (!live) return 0.0;
+    const int d = j < D ? j : j - D;
+    const double w = (double)prec[L.cov == GMM_COV_DIAG ? d : 0];
+    return j < D ? (double)mu[d] * w : -0.5 * w;
+  };
+  double mx = 0.0, n2 = 0.0, q = 0.0;
+  for (int j = threadIdx.x; j < KD; j += blockDim.x) {
+    const double b = bval(j);
+    mx = fmax(mx, fabs(b));
+    n2 += b * b;
+    if (j < D && live) q += (double)mu[j] * b;  // mu^2 w
+  }
+  // block max and sums (fixed order)
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+    q += __shfl_xor_sync(0xffffffffu, q, o);
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __shared__ double s_q;
+  if (lane == 0) { red[wid] = mx; red[8 + wid] = n2; red[16 + wid] = q; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double m = 0.0, s = 0.0, qq = 0.0;
+    for (int i = 0; i < nw; ++i) { m = fmax(m, red[i]); s += red[8 + i]; qq += red[16 + i]; }
+    s_max = m;
+    red[31] = s;
+    s_q = qq;
+  }
+  __syncthreads();
+  const double m = s_max;
+  const double scale = m > 0.0 ? ldexp(1.0, (int)ceil(log2(m)) - 14) : 1.0;
+  for (int j = threadIdx.x; j < KD; j += blockDim.x) {
+    const __half h = __double2half(bval(j) / scale);
+    *reinterpret_cast<__half*>(img + tc::sw128_offset(row, j, kTcChunk)) = h;
+  }
+  if (threadIdx.x == 0) {
+    trail[row] = (float)scale;
+    trail[kTcChunk + row] = (float)sqrt(red[31]);
+    trail[2 * kTcChunk + row] =
+        live ? (float)((double)at<float>(prepared, L.off_c)[k] - 0.5 * s_q) : -INFINITY;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_prepare_tc(int D, int K, int cov, void* prepared, cudaStream_t s) {
+  PreparedLayout L = PreparedLayout::make(D, K, cov);
+  if (!L.tc_chunks) return cudaSuccess;
+  prepare_tc_kernel<<<L.tc_chunks * kTcChunk, 128, 0, s>>>(L, prepared);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prepare(const gmm_params* p, int D, int K, int cov, float ridge_rel,
                            void* prepared, DeviceStatus* st, cudaStream_t s) {
@@ -169,6 +243,9 @@ cudaError_t launch_prepare(const gmm_params* p, int D, int K, int cov, float rid
     int nv = cov == GMM_COV_DIAG ? D : 1;
     prepare_diag_kernel<<<K, 128, 0, s>>>(p->pi, p->mu, p->cov, D, K, nv, ridge_rel, L, prepared,
                                           st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_prepare_tc(D, K, cov, prepared, s);
   }
   return cudaGetLastError();
 }

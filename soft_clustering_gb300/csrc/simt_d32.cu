@@ -6,11 +6,12 @@ namespace gmm {
 template <>
 cudaError_t simt_lse_d<32>(const void* X, int xdtype, int64_t N, int K, int cov,
                           const void* prepared, float* lse, double* ll_part, int m, int32_t* ids,
-                          float* gamma, DeviceStatus* st, cudaStream_t s) {
+                          float* gamma, DeviceStatus* st, const uint32_t* rows,
+                          const uint32_t* row_count, int grid, cudaStream_t s) {
   PreparedLayout L = PreparedLayout::make(32, K, cov);
   return dispatch_cx(cov, xdtype, [&](auto Cc, auto Xc) {
     return simt::run_lse<32, decltype(Cc)::value, decltype(Xc)::value>(
-        X, N, K, prepared, L, lse, ll_part, m, ids, gamma, st, s);
+        X, N, K, prepared, L, lse, ll_part, m, ids, gamma, st, rows, row_count, grid, s);
   });
 }
 

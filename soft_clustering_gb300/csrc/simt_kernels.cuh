@@ -54,28 +54,51 @@ __device__ __forceinline__ void load_row(const void* X, int64_t n, float* x) {
   for (int d = 0; d < D; ++d) x[d] = load_x<XT>(X, (size_t)n * D + d);
 }
 
+// Sum of w_d (x_d - mu_d)^2 over d for diag / iso.  For D >= 64 the order
+// is the one the tensor-core path's warp-cooperative refinement uses: 32
+// partial sums over D/32 consecutive dimensions each (sequential fma), then
+// the xor-butterfly tree of a warp reduction, so every kernel produces the
+// same bits for the same (point, component).  Smaller D: 4 interleaved partial
+// sums combined pairwise.
+template <int D, int COV, typename XF, typename MF, typename WF>
+__device__ __forceinline__ float dist2_diag(XF xf, MF mf, WF wf) {
+  if constexpr (D >= 64) {
+    constexpr int DPL = D / 32;
+    float p[32];
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) {
+        const int d = l * DPL + i;
+        const float t = xf(d) - mf(d);
+        part = fmaf(t * t, wf(d), part);
+      }
+      p[l] = part;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int i = 0; i < o; ++i) p[i] = p[i] + p[i + o];
+    return p[0];
+  } else {
+    float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const float t = xf(d) - mf(d);
+      p[d & 3] = fmaf(t * t, wf(d), p[d & 3]);
+    }
+    return (p[0] + p[2]) + (p[1] + p[3]);
+  }
+}
+
 // log joint of one component for a point held in registers (diag / iso).
-// d^2 = sum_d (x_d - mu_d)^2 w_d is summed in 8 interleaved fp32 partial sums
-// combined pairwise: the rounding error of the sum (the dominant error of the
-// log-density) drops about threefold against one running sum.
 template <int D, int COV>
 __device__ __forceinline__ float logj_diag(const float* x, const float* mu, const float* prec,
                                            float c) {
-  constexpr int NP = D >= 64 ? 8 : 4;
-  float p[NP];
-#pragma unroll
-  for (int i = 0; i < NP; ++i) p[i] = 0.f;
-#pragma unroll
-  for (int d = 0; d < D; ++d) {
-    float t = x[d] - mu[d];
-    float w = COV == GMM_COV_DIAG ? prec[d] : prec[0];
-    p[d % NP] = fmaf(t * t, w, p[d % NP]);
-  }
-#pragma unroll
-  for (int h = NP / 2; h > 0; h /= 2)
-#pragma unroll
-    for (int i = 0; i < h; ++i) p[i] += p[i + h];
-  return c - 0.5f * p[0];
+  const float s = dist2_diag<D, COV>([&](int d) { return x[d]; }, [&](int d) { return mu[d]; },
+                                     [&](int d) { return COV == GMM_COV_DIAG ? prec[d] : prec[0]; });
+  return c - 0.5f * s;
 }
 
 // Full: z = W (x - mu), d^2 = z.z, with W lower triangular.  Each z_i is
@@ -111,7 +134,8 @@ template <int D, int COV, int XT>
 __global__ void __launch_bounds__(kLseThreads)
 lse_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict__ prepared,
            PreparedLayout L, float* __restrict__ lse_out, double* __restrict__ ll_part, int m,
-           int32_t* __restrict__ ids, float* __restrict__ gamma, DeviceStatus* st) {
+           int32_t* __restrict__ ids, float* __restrict__ gamma, DeviceStatus* st,
+           const uint32_t* __restrict__ rows, const uint32_t* __restrict__ row_count) {
   using S = LseShape<D, COV>;
   extern __shared__ float sm[];
   float* s_mu = sm;                      // KC*D
@@ -119,8 +143,15 @@ lse_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict_
   float* s_c = s_prec + S::KC * S::P;    // KC
   __shared__ double red[kLseThreads / 32];
 
-  const int64_t n = (int64_t)blockIdx.x * kLseThreads + threadIdx.x;
-  const bool valid = n < N;
+  // Dense mode: point n = group * 128 + thread.  Row-list mode: the points
+  // rows[0 .. *row_count) (the rows the tensor-core kernel handed over).
+  const int64_t cnt = rows ? (int64_t)*row_count : N;
+  const int64_t ngroups = (cnt + kLseThreads - 1) / kLseThreads;
+  double ll_acc = 0.0;
+  for (int64_t grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
+  const int64_t idx = grp * kLseThreads + threadIdx.x;
+  const bool valid = idx < cnt;
+  const int64_t n = valid ? (rows ? (int64_t)rows[idx] : idx) : 0;
   const float* g_c = at<float>(prepared, L.off_c);
   const float* g_mu = at<float>(prepared, L.off_mu);
   const float* g_prec = at<float>(prepared, L.off_prec);
@@ -182,19 +213,19 @@ lse_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict_
       }
     }
   }
-  double lsev = 0.0;
   if (valid) {
     const float lse = run_m + logf(run_s);
     if (lse_out) lse_out[n] = lse;
     if (!isfinite(lse)) raise_status(st, GMM_ERR_NONFINITE);
-    lsev = (double)lse;
+    ll_acc += (double)lse;
     for (int j = 0; j < m; ++j) {
       ids[n * m + j] = ti[j] == 0x7fffffff ? -1 : ti[j];
       gamma[n * m + j] = tv[j] == -INFINITY ? 0.f : expf(tv[j] - lse);
     }
   }
+  }  // groups
   if (ll_part) {
-    lsev = warp_sum(lsev);
+    double lsev = warp_sum(ll_acc);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lsev;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -289,22 +320,14 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
           }
           l = logj_full<D>(y, s_prec + kk * P, s_c[kk]);
         } else {
-          // same summation order as logj_diag, so both passes agree
-          constexpr int NP = D >= 64 ? 8 : 4;
-          float pp[NP];
-#pragma unroll
-          for (int i = 0; i < NP; ++i) pp[i] = 0.f;
-#pragma unroll 8
-          for (int d = 0; d < D; ++d) {
-            float tt = s_x[r * XS + d] - s_mu[kk * D + d];
-            float w = COV == GMM_COV_DIAG ? s_prec[kk * P + d] : s_prec[kk * P];
-            pp[d % NP] = fmaf(tt * tt, w, pp[d % NP]);
-          }
-#pragma unroll
-          for (int h = NP / 2; h > 0; h /= 2)
-#pragma unroll
-            for (int i = 0; i < h; ++i) pp[i] += pp[i + h];
-          l = s_c[kk] - 0.5f * pp[0];
+          // same summation order as every other log-density evaluation
+          const float* xr = s_x + r * XS;
+          const float* mk = s_mu + kk * D;
+          const float* wk = s_prec + kk * P;
+          const float d2 = dist2_diag<D, COV>(
+              [&](int d) { return xr[d]; }, [&](int d) { return mk[d]; },
+              [&](int d) { return COV == GMM_COV_DIAG ? wk[d] : wk[0]; });
+          l = s_c[kk] - 0.5f * d2;
         }
         g = expf(l - lse[t0r + r]);
       }
@@ -456,16 +479,20 @@ size_t stat_smem() {
   return b;
 }
 
+// grid 0: dense, one block per 128 points.  With a row list, `grid` blocks
+// walk the list.
 template <int D, int COV, int XT>
 cudaError_t run_lse(const void* X, int64_t N, int K, const void* prepared, const PreparedLayout& L,
                     float* lse, double* ll_part, int m, int32_t* ids, float* gamma,
-                    DeviceStatus* st, cudaStream_t s) {
+                    DeviceStatus* st, const uint32_t* rows, const uint32_t* row_count, int grid,
+                    cudaStream_t s) {
   size_t smem = lse_smem<D, COV, XT>();
   auto kern = lse_kernel<D, COV, XT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int64_t blocks = (N + kLseThreads - 1) / kLseThreads;
-  kern<<<(unsigned)blocks, kLseThreads, smem, s>>>(X, N, K, prepared, L, lse, ll_part, m, ids, gamma, st);
+  int64_t blocks = rows ? grid : (N + kLseThreads - 1) / kLseThreads;
+  kern<<<(unsigned)blocks, kLseThreads, smem, s>>>(X, N, K, prepared, L, lse, ll_part, m, ids,
+                                                   gamma, st, rows, row_count);
   return cudaGetLastError();
 }
 
@@ -511,7 +538,8 @@ cudaError_t dispatch_cx(int cov, int xt, Fn&& fn) {
 template <int D>
 cudaError_t simt_lse_d(const void* X, int xdtype, int64_t N, int K, int cov, const void* prepared,
                        float* lse, double* ll_part, int m, int32_t* ids, float* gamma,
-                       DeviceStatus* st, cudaStream_t s);
+                       DeviceStatus* st, const uint32_t* rows, const uint32_t* row_count,
+                       int grid, cudaStream_t s);
 template <int D>
 cudaError_t simt_stats_d(const void* X, int xdtype, int64_t N, int K, int cov,
                          const void* prepared, const float* lse, int parts, double* part,

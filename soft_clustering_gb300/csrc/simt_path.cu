@@ -13,16 +13,24 @@ int simt_stat_chunk(int D, int cov) {
   }
 }
 
+cudaError_t simt_lse_rows(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                          const void* prepared, float* lse, double* ll_part, int m, int32_t* ids,
+                          float* gamma, DeviceStatus* st, const uint32_t* rows,
+                          const uint32_t* row_count, int grid, cudaStream_t s) {
+  switch (D) {
+    case 16: return simt_lse_d<16>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, rows, row_count, grid, s);
+    case 32: return simt_lse_d<32>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, rows, row_count, grid, s);
+    case 64: return simt_lse_d<64>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, rows, row_count, grid, s);
+    case 128: return simt_lse_d<128>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, rows, row_count, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t simt_lse(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                      const void* prepared, float* lse, double* ll_part, int m, int32_t* ids,
                      float* gamma, DeviceStatus* st, cudaStream_t s) {
-  switch (D) {
-    case 16: return simt_lse_d<16>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, s);
-    case 32: return simt_lse_d<32>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, s);
-    case 64: return simt_lse_d<64>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, s);
-    case 128: return simt_lse_d<128>(X, xdtype, N, K, cov, prepared, lse, ll_part, m, ids, gamma, st, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return simt_lse_rows(X, xdtype, N, D, K, cov, prepared, lse, ll_part, m, ids, gamma, st,
+                       nullptr, nullptr, 0, s);
 }
 
 cudaError_t simt_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,

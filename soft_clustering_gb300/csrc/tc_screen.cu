@@ -1,0 +1,534 @@
+// tc_screen.cu - E-step on the tensor cores: screen every point-component
+// pair with one fp16 tcgen05 contraction, then compute the few pairs that
+// matter exactly on CUDA cores.
+//
+// For diagonal / isotropic covariance the log joint density is
+//   l_nk = c_k + sum_d x_d (mu_kd w_kd) + x_d^2 (-w_kd / 2),   w = 1/var,
+// a dense contraction [x, x^2] . [b1, b2] ("low-precision GMM operator"
+// notes, sec. 1.2-1.3; Flash-GMM summary, Method: all-K distances per tile).
+// Its terms are large and cancel (|x.b1| ~ 1e4 against l ~ 1e2 for tight
+// clusters), so fp16 operands with fp32 accumulation give only a screen.
+// Each screened value comes with a rigorous bound on its error,
+//   |l~ - l| <= beta_nk = kappa |[x, x^2]|_2 |[b1, b2]|_2 + margin,
+// from the fp16 rounding of b and x^2 (2^-11 each), of fp32 inputs (2^-11)
+// and fp32 accumulation.  A component is kept when its upper bound l~ + beta
+// reaches within T = 40 nats of the largest lower bound l~ - beta; every
+// kept pair is then evaluated exactly in the centred fp32 form
+// sum_d w_d (x_d - mu_d)^2, and LSE_n, the log-likelihood, top-m and the
+// responsibilities come from those exact values (sec. 3.2, 4.2: fp32 online
+// log-sum-exp).  Components more than 40 nats below the best carry less than
+// 4.3e-18 of a point's responsibility.  A point whose kept list overflowed
+// (more than 32 candidates, with an evicted one still within the window) is
+// handed to the CUDA-core path through a row list.
+//
+// Roles (one CTA per SM, persistent over 128-point tiles in a fixed order):
+//   warps 0-3  epilogue: TMEM lane quarter w -> 32 points; candidates,
+//              exact refinement (warp-cooperative), outputs
+//   warps 4-7  producers: one point row per thread -> [x, x^2] fp16 tile in
+//              shared memory (128-byte swizzled K-major), row norms
+//   warp  8    lane 0 issues bulk copies of the parameter chunks and the
+//              tcgen05.mma instructions; the warp owns the TMEM allocation
+#include <math.h>
+
+#include "gmm_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace gmm {
+namespace {
+
+constexpr int kBM = 128;          // points per tile (MMA M)
+constexpr int kBN = kTcChunk;     // components per chunk (MMA N)
+constexpr int kCS = 32;           // candidates kept per point
+constexpr float kT = 40.f;        // nats
+constexpr float kKappa = 1.5e-3f; // 3 x 2^-11 rounding + accumulation allowance
+constexpr int kThreads = 288;
+constexpr uint32_t kWait = 1u << 22;
+
+enum { MODE_EM = 0, MODE_ASSIGN = 1 };
+
+struct ScreenArgs {
+  const void* X;
+  int64_t N;
+  int K;
+  int m;                 // top-m (assign mode)
+  const void* prepared;
+  PreparedLayout L;
+  float* lse;            // [N] or null
+  double* ll_part;       // [gridDim.x] (EM) or null
+  int32_t* ids;          // [N*m] (assign)
+  float* gamma;          // [N*m] (assign)
+  uint32_t* fb_rows;     // rows handed to the CUDA-core path
+  uint32_t* fb_count;
+  DeviceStatus* st;
+};
+
+template <int D>
+struct Shape {
+  static constexpr int KD = 2 * D;
+  static constexpr int KSTEPS = KD / 16;
+  static constexpr int A_BYTES = kBM * KD * 2;
+  static constexpr int B_BYTES = kBN * KD * 2;
+  static constexpr int T_BYTES = 3 * kBN * 4;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + A_BYTES;          // 2 buffers
+  static constexpr int OFF_T = OFF_B + 2 * B_BYTES;      // 2 trailers
+  static constexpr int OFF_RN = OFF_T + 2 * T_BYTES;     // 2 x 128 row norms
+  static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;   // [kCS][128] float
+  static constexpr int OFF_CK = OFF_CUB + kCS * kBM * 4; // [kCS][128] u16
+  static constexpr int OFF_BAR = OFF_CK + kCS * kBM * 2; // 16 mbarriers
+  static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+  static constexpr int BYTES = OFF_MISC + 64;
+  static constexpr int SMEM = BYTES + 1024;              // base alignment slack
+};
+
+enum Bar {
+  A_FULL = 0, A_EMPTY = 1, B_FULL = 2, B_EMPTY = 4, T_FULL = 6, T_EMPTY = 8, TR_FULL = 10,
+  R_FULL = 12, R_FREE = 14
+};
+
+template <int XT>
+__device__ __forceinline__ void load8(const void* X, size_t elem, float* v) {
+  if constexpr (XT == GMM_F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(X) + elem);
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(X) + elem));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (XT == GMM_F16) {
+        __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+        float2 f = __half22float2(h);
+        v[2 * i] = f.x; v[2 * i + 1] = f.y;
+      } else {
+        __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+        float2 f = __bfloat1622float2(h);
+        v[2 * i] = f.x; v[2 * i + 1] = f.y;
+      }
+    }
+  }
+}
+
+// Bounded wait whose outcome is the same for every lane of the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  const bool ok = tc::mbar_wait(bar, parity, kWait);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool warp_aborted(volatile int* flag) {
+  return __any_sync(0xffffffffu, *flag != 0);
+}
+
+template <int XT>
+__device__ __forceinline__ float load1(const void* X, size_t elem) {
+  return load_x<XT>(X, elem);
+}
+
+template <int D, int XT, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs a) {
+  using S = Shape<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sA = sm + S::OFF_A;
+  unsigned char* sB = sm + S::OFF_B;
+  float* sT = (float*)(sm + S::OFF_T);
+  float* sRN = (float*)(sm + S::OFF_RN);
+  float* sCUB = (float*)(sm + S::OFF_CUB);
+  uint16_t* sCK = (uint16_t*)(sm + S::OFF_CK);
+  uint64_t* bar = (uint64_t*)(sm + S::OFF_BAR);
+  uint32_t* tmem_slot = (uint32_t*)(sm + S::OFF_MISC);
+  volatile int* abort_flag = (volatile int*)(sm + S::OFF_MISC + 4);
+  __shared__ double ll_red[4];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t ntiles = (a.N + kBM - 1) / kBM;
+  const int my_tiles = blockIdx.x < ntiles ? (int)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+  const int nch = a.L.tc_chunks;
+  const bool resident = nch <= 2;  // parameter chunks loaded once and kept
+
+  if (warp == 8) {
+    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(&bar[A_FULL], 4);
+    tc::mbar_init(&bar[A_EMPTY], 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&bar[B_FULL + i], 1);
+      tc::mbar_init(&bar[B_EMPTY + i], 1);
+      tc::mbar_init(&bar[T_FULL + i], 1);
+      tc::mbar_init(&bar[T_EMPTY + i], 4);
+      tc::mbar_init(&bar[TR_FULL + i], 1);
+      tc::mbar_init(&bar[R_FULL + i], 4);
+      tc::mbar_init(&bar[R_FREE + i], 4);
+    }
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&](void) {
+    *abort_flag = 1;
+    raise_status(a.st, GMM_ERR_TIMEOUT);
+  };
+
+  const unsigned char* gB = at<unsigned char>(a.prepared, a.L.off_tcB);
+  const float* gT = at<float>(a.prepared, a.L.off_tcT);
+  const float* g_mu = at<float>(a.prepared, a.L.off_mu);
+  const float* g_prec = at<float>(a.prepared, a.L.off_prec);
+  const float* g_c = at<float>(a.prepared, a.L.off_c);
+  const bool iso = a.L.cov == GMM_COV_ISO;
+
+  if (warp == 8) {
+    // ------------------------------------------------ MMA issue + loads
+    if (lane == 0 && my_tiles > 0) {
+      const int64_t total = (int64_t)my_tiles * nch;
+      auto load_b = [&](int64_t g) {
+        const int buf = (int)(g & 1), c = (int)(g % nch);
+        tc::mbar_arrive_expect_tx(&bar[B_FULL + buf], S::B_BYTES);
+        tc::bulk_g2s(sB + buf * S::B_BYTES, gB + (size_t)c * S::B_BYTES, S::B_BYTES,
+                     &bar[B_FULL + buf]);
+      };
+      if (resident) {
+        for (int c = 0; c < nch; ++c) {
+          tc::mbar_arrive_expect_tx(&bar[B_FULL + c], S::B_BYTES);
+          tc::bulk_g2s(sB + c * S::B_BYTES, gB + (size_t)c * S::B_BYTES, S::B_BYTES,
+                       &bar[B_FULL + c]);
+        }
+      } else {
+        for (int64_t g = 0; g < 2 && g < total; ++g) load_b(g);
+      }
+      const uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
+      bool ok = true;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        if (!tc::mbar_wait(&bar[A_FULL], it & 1, kWait)) { fail(); ok = false; break; }
+        tc::tc_fence_after();
+        for (int j = 0; j < nch; ++j) {
+          const int64_t g = (int64_t)it * nch + j;
+          const int buf = (int)(g & 1);
+          const uint32_t use = (uint32_t)(g >> 1);
+          const int bbuf = resident ? j : buf;
+          if (!tc::mbar_wait(&bar[B_FULL + bbuf], resident ? 0u : (use & 1), kWait) ||
+              !tc::mbar_wait(&bar[T_EMPTY + buf], (use & 1) ^ 1, kWait) || *abort_flag) {
+            fail(); ok = false; break;
+          }
+          tc::tc_fence_after();
+          tc::mbar_arrive_expect_tx(&bar[TR_FULL + buf], S::T_BYTES);
+          tc::bulk_g2s(sT + buf * (S::T_BYTES / 4), gT + (size_t)j * 3 * kBN, S::T_BYTES,
+                       &bar[TR_FULL + buf]);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
+          const unsigned char* bb = sB + bbuf * S::B_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < S::KSTEPS; ++ks) {
+            const int atom = ks >> 2, within = (ks & 3) * 32;
+            const uint64_t da = tc::sdesc_k128(tc::smem_addr(sA + atom * kBM * 128 + within));
+            const uint64_t db = tc::sdesc_k128(tc::smem_addr(bb + atom * kBN * 128 + within));
+            tc::mma_f16(d_tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+          }
+          if (!resident) tc::mma_commit(&bar[B_EMPTY + buf]);
+          tc::mma_commit(&bar[T_FULL + buf]);
+          if (j == nch - 1) tc::mma_commit(&bar[A_EMPTY]);
+          if (!resident && g + 1 < total && g + 1 >= 2) {
+            // refill the other buffer once the MMAs of chunk g-1 are done
+            const int pb = (int)((g + 1) & 1);
+            const uint32_t puse = (uint32_t)((g + 1) >> 1);
+            if (!tc::mbar_wait(&bar[B_EMPTY + pb], (puse - 1) & 1, kWait)) {
+              fail(); ok = false; break;
+            }
+            load_b(g + 1);
+          }
+        }
+      }
+      // drain: the last parameter loads must land before the CTA exits
+      if (!resident && total >= 1) {
+        for (int64_t g = total - 2; g < total; ++g) {
+          if (g < 0) continue;
+          tc::mbar_wait(&bar[B_EMPTY + (int)(g & 1)], (uint32_t)((g >> 1) & 1), kWait);
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------- producers
+    const int p = tid - 128;
+    for (int it = 0; it < my_tiles; ++it) {
+      if (warp_aborted(abort_flag)) break;
+      if (it > 0 && !warp_wait(&bar[A_EMPTY], (it - 1) & 1)) { fail(); break; }
+      if (it >= 2 && !warp_wait(&bar[R_FREE + (it & 1)], ((it >> 1) - 1) & 1)) {
+        fail(); break;
+      }
+      const int64_t tile = blockIdx.x + (int64_t)it * gridDim.x;
+      const int64_t n = tile * kBM + p;
+      float rn2 = 0.f;
+#pragma unroll 4
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        float v[8];
+        if (n < a.N) load8<XT>(a.X, (size_t)n * D + c8 * 8, v);
+        else
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        uint32_t hx[4], hq[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 xx = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+          const __half2 qq = __floats2half2_rn(v[2 * i] * v[2 * i], v[2 * i + 1] * v[2 * i + 1]);
+          const float2 xf = __half22float2(xx), qf = __half22float2(qq);
+          rn2 += xf.x * xf.x + xf.y * xf.y + qf.x * qf.x + qf.y * qf.y;
+          hx[i] = *reinterpret_cast<const uint32_t*>(&xx);
+          hq[i] = *reinterpret_cast<const uint32_t*>(&qq);
+        }
+        *reinterpret_cast<uint4*>(sA + tc::sw128_offset(p, c8 * 8, kBM)) =
+            make_uint4(hx[0], hx[1], hx[2], hx[3]);
+        *reinterpret_cast<uint4*>(sA + tc::sw128_offset(p, D + c8 * 8, kBM)) =
+            make_uint4(hq[0], hq[1], hq[2], hq[3]);
+      }
+      // fp16 subnormal / input rounding floor, so the bound never reaches 0
+      sRN[(it & 1) * kBM + p] = sqrtf(rn2) + 1e-6f * (float)D;
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&bar[A_FULL]);
+        tc::mbar_arrive(&bar[R_FULL + (it & 1)]);
+      }
+    }
+  } else {
+    // -------------------------------------------------------- epilogue
+    const int r = tid;  // row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    double ll_acc = 0.0;
+    for (int it = 0; it < my_tiles; ++it) {
+      if (warp_aborted(abort_flag)) break;
+      const int64_t tile = blockIdx.x + (int64_t)it * gridDim.x;
+      const int64_t n0 = tile * kBM, n = n0 + r;
+      const bool valid = n < a.N;
+      if (!warp_wait(&bar[R_FULL + (it & 1)], (it >> 1) & 1)) { fail(); break; }
+      const float rn = sRN[(it & 1) * kBM + r];
+      float m_lo = -INFINITY, dropped = -INFINITY;
+      float lbm[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) lbm[i] = -INFINITY;
+      int cnt = 0;
+      bool ok = true;
+      for (int j = 0; j < nch; ++j) {
+        const int64_t g = (int64_t)it * nch + j;
+        const int buf = (int)(g & 1);
+        const uint32_t use = (uint32_t)(g >> 1);
+        if (!warp_wait(&bar[T_FULL + buf], use & 1) || !warp_wait(&bar[TR_FULL + buf], use & 1)) {
+          fail(); ok = false; break;
+        }
+        tc::tc_fence_after();
+        const float* tr = sT + buf * (S::T_BYTES / 4);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(tmem_base + lane_base + (uint32_t)(buf * kBN + c0), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int kk = c0 + i;
+            const float lt = fmaf(v[i], tr[kk], tr[2 * kBN + kk]);
+            const float beta = fmaf(kKappa * rn, tr[kBN + kk], 1e-3f + 1e-6f * fabsf(lt));
+            const float lo = lt - beta, hi = lt + beta;
+            m_lo = fmaxf(m_lo, lo);
+            float thr = m_lo - kT;
+            if constexpr (MODE == MODE_ASSIGN) {
+              if (lo > lbm[a.m - 1]) {
+                // keep the m largest lower bounds (descending)
+                float cur = lo;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                  if (t < a.m && cur > lbm[t]) { const float tmp = lbm[t]; lbm[t] = cur; cur = tmp; }
+                }
+              }
+              thr = fminf(thr, lbm[a.m - 1]);
+            }
+            if (hi >= thr && valid) {
+              const int k = j * kBN + kk;
+              if (cnt == kCS) {
+                // full: drop what fell out of the window, then evict the smallest
+                int w = 0;
+                for (int e = 0; e < kCS; ++e) {
+                  const float u = sCUB[e * kBM + r];
+                  if (u >= thr) { sCUB[w * kBM + r] = u; sCK[w * kBM + r] = sCK[e * kBM + r]; ++w; }
+                }
+                cnt = w;
+                if (cnt == kCS) {
+                  int emin = 0;
+                  float umin = sCUB[r];
+                  for (int e = 1; e < kCS; ++e) {
+                    const float u = sCUB[e * kBM + r];
+                    if (u < umin) { umin = u; emin = e; }
+                  }
+                  if (hi > umin) {
+                    dropped = fmaxf(dropped, umin);
+                    sCUB[emin * kBM + r] = hi;
+                    sCK[emin * kBM + r] = (uint16_t)k;
+                  } else {
+                    dropped = fmaxf(dropped, hi);
+                  }
+                  continue;
+                }
+              }
+              sCUB[cnt * kBM + r] = hi;
+              sCK[cnt * kBM + r] = (uint16_t)k;
+              ++cnt;
+            }
+          }
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[R_FREE + (it & 1)]);
+      if (!ok) break;
+      // final window and compaction
+      float thr = m_lo - kT;
+      if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, lbm[a.m - 1]);
+      {
+        int w = 0;
+        for (int e = 0; e < cnt; ++e) {
+          const float u = sCUB[e * kBM + r];
+          if (u >= thr) { sCUB[w * kBM + r] = u; sCK[w * kBM + r] = sCK[e * kBM + r]; ++w; }
+        }
+        cnt = w;
+      }
+      const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
+      // exact refinement, one candidate at a time per warp, lanes over dims
+      constexpr int DPL = D / 32;
+      int maxc = exact ? cnt : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) maxc = max(maxc, __shfl_xor_sync(0xffffffffu, maxc, o));
+      for (int e = 0; e < maxc; ++e) {
+        unsigned mask = __ballot_sync(0xffffffffu, exact && e < cnt);
+        while (mask) {
+          const int b = __ffs(mask) - 1;
+          mask &= mask - 1;
+          const int rb = warp * 32 + b;
+          const int k = sCK[e * kBM + rb];
+          const int64_t nb = n0 + rb;
+          float part = 0.f;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) {
+            const int d = lane * DPL + i;
+            const float xv = load1<XT>(a.X, (size_t)nb * D + d);
+            const float t = xv - __ldg(g_mu + (size_t)k * D + d);
+            const float w = iso ? __ldg(g_prec + k) : __ldg(g_prec + (size_t)k * D + d);
+            part = fmaf(t * t, w, part);
+          }
+          const float sum = warp_sum(part);
+          if (lane == b) sCUB[e * kBM + rb] = __ldg(g_c + k) - 0.5f * sum;
+        }
+      }
+      __syncwarp();
+      if (exact) {
+        float mx = -INFINITY;
+        for (int e = 0; e < cnt; ++e) mx = fmaxf(mx, sCUB[e * kBM + r]);
+        float s = 0.f;
+        for (int e = 0; e < cnt; ++e) s += expf(sCUB[e * kBM + r] - mx);
+        const float lse = mx + logf(s);
+        if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+        if (a.lse) a.lse[n] = lse;
+        if constexpr (MODE == MODE_EM) {
+          ll_acc += (double)lse;
+        } else {
+          // top-m by exact value, ties to the lower component
+          uint32_t taken = 0;
+          for (int t = 0; t < a.m; ++t) {
+            int best = -1, bk = 0x7fffffff;
+            float bv = -INFINITY;
+            for (int e = 0; e < cnt; ++e) {
+              if (taken & (1u << e)) continue;
+              const float v = sCUB[e * kBM + r];
+              const int k = sCK[e * kBM + r];
+              if (best < 0 || v > bv || (v == bv && k < bk)) { best = e; bv = v; bk = k; }
+            }
+            if (best < 0) {
+              a.ids[n * a.m + t] = -1;
+              a.gamma[n * a.m + t] = 0.f;
+              continue;
+            }
+            taken |= 1u << best;
+            a.ids[n * a.m + t] = bk;
+            a.gamma[n * a.m + t] = bv == -INFINITY ? 0.f : expf(bv - lse);
+          }
+        }
+      } else if (valid) {
+        const uint32_t slot = atomicAdd(a.fb_count, 1u);
+        a.fb_rows[slot] = (uint32_t)n;
+      }
+      __syncwarp();
+    }
+    if constexpr (MODE == MODE_EM) {
+      const double s = warp_sum(ll_acc);
+      if (lane == 0) ll_red[warp] = s;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if constexpr (MODE == MODE_EM) {
+    if (tid == 0 && a.ll_part)
+      a.ll_part[blockIdx.x] = ((ll_red[0] + ll_red[1]) + ll_red[2]) + ll_red[3];
+  }
+  if (warp == 8) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, 256);
+  }
+}
+
+template <int D, int XT, int MODE>
+cudaError_t run_screen(const ScreenArgs& args, int grid, cudaStream_t s) {
+  auto kern = tc_screen_kernel<D, XT, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Shape<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, Shape<D>::SMEM, s>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Grid of the screening kernel: one persistent CTA per SM (capped by tiles).
+int tc_screen_grid(int64_t N) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  const int64_t tiles = (N + kBM - 1) / kBM;
+  return (int)(tiles < sms ? tiles : sms);
+}
+
+// mode 0: EM (lse, ll_part); mode 1: assign (top-m).
+cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                      const void* prepared, int mode, float* lse, double* ll_part, int m,
+                      int32_t* ids, float* gamma, uint32_t* fb_rows, uint32_t* fb_count,
+                      DeviceStatus* st, cudaStream_t s) {
+  ScreenArgs a;
+  a.X = X; a.N = N; a.K = K; a.m = m; a.prepared = prepared;
+  a.L = PreparedLayout::make(D, K, cov);
+  a.lse = lse; a.ll_part = ll_part; a.ids = ids; a.gamma = gamma;
+  a.fb_rows = fb_rows; a.fb_count = fb_count; a.st = st;
+  if (!a.L.tc_chunks || N < 1) return cudaErrorInvalidValue;
+  const int grid = tc_screen_grid(N);
+#define GMM_SCREEN(DD, XX)                                                              \
+  return mode == MODE_EM ? run_screen<DD, XX, MODE_EM>(a, grid, s)                      \
+                         : run_screen<DD, XX, MODE_ASSIGN>(a, grid, s)
+  if (D == 128) {
+    if (xdtype == GMM_F16) { GMM_SCREEN(128, GMM_F16); }
+    if (xdtype == GMM_BF16) { GMM_SCREEN(128, GMM_BF16); }
+    GMM_SCREEN(128, GMM_F32);
+  } else {
+    if (xdtype == GMM_F16) { GMM_SCREEN(64, GMM_F16); }
+    if (xdtype == GMM_BF16) { GMM_SCREEN(64, GMM_BF16); }
+    GMM_SCREEN(64, GMM_F32);
+  }
+#undef GMM_SCREEN
+}
+
+}  // namespace gmm

@@ -85,7 +85,7 @@ class Assigner:
         self.ids = torch.empty(N, m, dtype=torch.int32, device=self.device)
         self.gamma = torch.empty(N, m, dtype=torch.float32, device=self.device)
         self.lse = torch.empty(N, dtype=torch.float32, device=self.device)
-        self.ws_bytes = 256
+        self.ws_bytes = gmm_workspace_bytes(N, D, K, cov_type, xdtype)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
 
     def prepare(self, pi, mu, cov, opts=None, stream=None):

@@ -22,10 +22,13 @@ PI_ATOL = 1e-5
 TOP1_MIN = 0.999
 TIE_EPS = 1e-6
 # Trajectories (each side iterating on its own from theta_0) are held to the
-# per-iteration LL bound and to a 10x wider parameter band: a parameter that
-# depends on a few boundary points amplifies last-bit differences of the
-# previous iterate, so the strict bound is a per-step (same input) bound.
+# per-iteration LL bound, and their parameters to a 10x wider band on the
+# components holding at least TRAJ_MIN_S0 points of responsibility: a
+# parameter that depends on a few boundary points amplifies last-bit
+# differences of the previous iterate, so the strict bound is a per-step
+# (same input) bound.
 TRAJ_PARAM_RTOL = 2e-2
+TRAJ_MIN_S0 = 5.0
 
 
 def diagnostics(got, ref):
@@ -49,7 +52,7 @@ def scaled_rel_err(got, ref):
     return np.abs(got - ref) / np.maximum(np.abs(ref), PARAM_FLOOR * scale + 1e-300)
 
 
-def compare_step(gpu, ref, what="", min_s0=None, param_rtol=PARAM_RTOL):
+def compare_step(gpu, ref, what="", min_s0=None, param_rtol=PARAM_RTOL, min_mass=None):
     """gpu/ref: dicts with pi, mu, cov, ll.  Returns a list of failure strings.
     With min_s0 (and ref['s0']), components whose oracle s0 lies within 1e-4
     (relative) of the empty threshold are left out of the mean/covariance
@@ -59,6 +62,8 @@ def compare_step(gpu, ref, what="", min_s0=None, param_rtol=PARAM_RTOL):
     if min_s0 is not None and "s0" in ref:
         s0 = np.asarray(ref["s0"])
         keep = np.abs(s0 - min_s0) > 1e-4 * max(min_s0, 1e-30)
+        if min_mass is not None:
+            keep &= s0 >= min_mass
     ll_err = abs(gpu["ll"] - ref["ll"]) / max(abs(ref["ll"]), 1e-300)
     if not ll_err <= LL_RTOL:
         fails.append("%s LL rel err %.3g (gpu %.10g ref %.10g)" % (what, ll_err, gpu["ll"], ref["ll"]))

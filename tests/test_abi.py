@@ -53,7 +53,7 @@ def test_sizes(lib):
         ws = G.gmm_workspace_bytes(N, D, K, cov, G.GMM_F16)
         assert 0 < ws < N * K * 4 / 4, (N, K, ws)
         ws2 = G.gmm_workspace_bytes(2 * N, D, K, cov, G.GMM_F16)
-        assert ws2 - ws <= 8 * N + 4096  # only O(N) terms grow with N
+        assert ws2 - ws <= 16 * N + 4096  # only O(N) terms grow with N
 
 
 def test_invalid_args_are_synchronous(lib):

@@ -61,7 +61,8 @@ def _run_parity(wl, iters, trajectory=True):
             pi, mu, cov = state.params_numpy()
             got = dict(pi=pi, mu=mu, cov=cov, ll=float(state.loglik.item()))
             fails += parity.compare_step(got, ref, "%s trajectory %d" % (wl.name, t),
-                                         opts["min_s0"], parity.TRAJ_PARAM_RTOL)
+                                         opts["min_s0"], parity.TRAJ_PARAM_RTOL,
+                                         parity.TRAJ_MIN_S0)
             ref_theta = (ref["pi"], ref["mu"], ref["cov"])
     assert not fails, "\n".join(fails[:10])
 
@@ -248,3 +249,28 @@ def test_invalid_workspace_and_alignment():
     st = G.gmm_em_step(X.data_ptr() + 4, wl.dtype, wl.N, wl.D, wl.K, s.pi, s.mu, s.cov,
                        wl.cov_type, s.ws, s.ws_bytes, s.loglik, raise_on_error=False)
     assert st == G.GMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name,n,cov", [("embed_diag", 20_011, datagen.COV_DIAG),
+                                        ("large_diag", 9_003, datagen.COV_DIAG),
+                                        ("large_diag", 9_003, datagen.COV_ISO)])
+def test_tensor_core_path_matches_cuda_core_path(name, n, cov):
+    """The tensor-core screening path and the CUDA-core path agree point by
+    point (LSE_n) and on the updated parameters, at theta_0 (dense candidate
+    lists, many rows handed over) and one iteration later (sparse lists)."""
+    import soft_clustering_gb300 as G
+    wl = _workload(name, n=n, cov_type=cov, K=min(datagen.WORKLOADS[name].K, 512))
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    theta = f32(datagen.init_params(mix, bits))
+    opts = datagen.em_opts(theta)
+    Xd = to_device(bits, wl.dtype)
+    for it in range(2):
+        tc = gpu_step(make_state(wl), Xd, theta, want_lse=True, opts=opts)
+        cc = gpu_step(make_state(wl), Xd, theta, want_lse=True,
+                      opts=dict(opts, flags=G.GMM_OPT_CUDA_CORES))
+        assert tc["status"] == 0 and cc["status"] == 0
+        np.testing.assert_allclose(tc["lse"], cc["lse"], rtol=2e-6, atol=2e-4)
+        fails = parity.compare_step(tc, cc, "%s iter %d tc vs cuda cores" % (name, it))
+        assert not fails, fails
+        theta = f32((cc["pi"], cc["mu"], cc["cov"]))
