@@ -51,7 +51,7 @@ def test_sizes(lib):
                          (200_000_000, 128, 1024, G.GMM_COV_DIAG),
                          (1_000_000, 64, 16, G.GMM_COV_FULL)]:
         ws = G.gmm_workspace_bytes(N, D, K, cov, G.GMM_F16)
-        assert 0 < ws < N * K * 4 / 4, (N, K, ws)
+        assert 0 < ws < N * K * 4 / 2, (N, K, ws)
         ws2 = G.gmm_workspace_bytes(2 * N, D, K, cov, G.GMM_F16)
         assert ws2 - ws <= 16 * N + 4096  # only O(N) terms grow with N
 
