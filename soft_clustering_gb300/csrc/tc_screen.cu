@@ -23,7 +23,7 @@
 //
 // Roles (one CTA per SM, persistent over 128-point tiles in a fixed order):
 //   warps 0-3  epilogue: TMEM lane quarter w -> 32 points; candidates,
-//              exact refinement (warp-cooperative), outputs
+//              exact refinement of each point's own candidates, outputs
 //   warps 4-7  producers: one point row per thread -> [x, x^2] fp16 tile in
 //              shared memory (128-byte swizzled K-major), row norms
 //   warp  8    lane 0 issues bulk copies of the parameter chunks and the
@@ -124,6 +124,117 @@ __device__ __forceinline__ bool warp_aborted(volatile int* flag) {
 template <int XT>
 __device__ __forceinline__ float load1(const void* X, size_t elem) {
   return load_x<XT>(X, elem);
+}
+
+// Keeps lbm[0..m) the m largest values seen (descending); v > lbm[m-1].
+__device__ __forceinline__ void insert_lower_bound(float* lbm, int m, float v) {
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    if (t < m && v > lbm[t]) { const float tmp = lbm[t]; lbm[t] = v; v = tmp; }
+  }
+}
+
+// Full candidate list of row r: drop entries that fell out of the window,
+// then evict the smallest upper bound if the new one is larger.  Returns the
+// new count; *dropped is the largest upper bound ever discarded while still
+// inside the window.
+__device__ __noinline__ int insert_full(float* sCUB, uint16_t* sCK, int r, int k, float hi,
+                                        float thr, float* dropped) {
+  int w = 0;
+  for (int e = 0; e < kCS; ++e) {
+    const float u = sCUB[e * kBM + r];
+    if (u >= thr) { sCUB[w * kBM + r] = u; sCK[w * kBM + r] = sCK[e * kBM + r]; ++w; }
+  }
+  if (w < kCS) {
+    sCUB[w * kBM + r] = hi;
+    sCK[w * kBM + r] = (uint16_t)k;
+    return w + 1;
+  }
+  int emin = 0;
+  float umin = sCUB[r];
+  for (int e = 1; e < kCS; ++e) {
+    const float u = sCUB[e * kBM + r];
+    if (u < umin) { umin = u; emin = e; }
+  }
+  if (hi > umin) {
+    *dropped = fmaxf(*dropped, umin);
+    sCUB[emin * kBM + r] = hi;
+    sCK[emin * kBM + r] = (uint16_t)k;
+  } else {
+    *dropped = fmaxf(*dropped, hi);
+  }
+  return kCS;
+}
+
+// sum_d w_d (x_d - mu_d)^2 for row n of X, in the order of the CUDA-core
+// kernels (32 partial sums over D/32 consecutive dimensions, then the
+// xor-butterfly tree), with vector loads.
+template <int D, int XT>
+__device__ __forceinline__ float exact_d2(const void* X, int64_t n, const float* mu,
+                                          const float* w, bool iso) {
+  constexpr int DPL = D / 32;
+  float p[32];
+  const float wi = iso ? __ldg(w) : 0.f;
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    float xv[DPL], mv[DPL], wv[DPL];
+    const size_t e0 = (size_t)n * D + l * DPL;
+    if constexpr (DPL == 4) {
+      if constexpr (XT == GMM_F32) {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(X) + e0));
+        xv[0] = q.x; xv[1] = q.y; xv[2] = q.z; xv[3] = q.w;
+      } else {
+        const uint2 q = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(X) + e0));
+        const uint32_t u[2] = {q.x, q.y};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float2 f;
+          if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u[h]));
+          else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[h]));
+          xv[2 * h] = f.x; xv[2 * h + 1] = f.y;
+        }
+      }
+      const float4 mq = __ldg(reinterpret_cast<const float4*>(mu + l * 4));
+      mv[0] = mq.x; mv[1] = mq.y; mv[2] = mq.z; mv[3] = mq.w;
+      if (iso) {
+        wv[0] = wv[1] = wv[2] = wv[3] = wi;
+      } else {
+        const float4 wq = __ldg(reinterpret_cast<const float4*>(w + l * 4));
+        wv[0] = wq.x; wv[1] = wq.y; wv[2] = wq.z; wv[3] = wq.w;
+      }
+    } else {
+      if constexpr (XT == GMM_F32) {
+        const float2 q = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(X) + e0));
+        xv[0] = q.x; xv[1] = q.y;
+      } else {
+        const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const uint16_t*>(X) + e0));
+        float2 f;
+        if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u));
+        else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+        xv[0] = f.x; xv[1] = f.y;
+      }
+      const float2 mq = __ldg(reinterpret_cast<const float2*>(mu + l * 2));
+      mv[0] = mq.x; mv[1] = mq.y;
+      if (iso) {
+        wv[0] = wv[1] = wi;
+      } else {
+        const float2 wq = __ldg(reinterpret_cast<const float2*>(w + l * 2));
+        wv[0] = wq.x; wv[1] = wq.y;
+      }
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      const float t = xv[i] - mv[i];
+      part = fmaf(t * t, wv[i], part);
+    }
+    p[l] = part;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < o; ++i) p[i] = p[i] + p[i + o];
+  return p[0];
 }
 
 template <int D, int XT, int MODE>
@@ -307,8 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       const bool valid = n < a.N;
       if (!warp_wait(&bar[R_FULL + (it & 1)], (it >> 1) & 1)) { fail(); break; }
       const float rn = sRN[(it & 1) * kBM + r];
-      float m_lo = -INFINITY, dropped = -INFINITY;
-      float lbm[8];
+      const float rnk = kKappa * rn;
+      float ref = -INFINITY;  // lower bound of the best log joint of this point
+      float dropped = -INFINITY;
+      float lbm[8];           // assign: the m largest lower bounds seen
 #pragma unroll
       for (int i = 0; i < 8; ++i) lbm[i] = -INFINITY;
       int cnt = 0;
@@ -321,60 +434,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           fail(); ok = false; break;
         }
         tc::tc_fence_after();
-        const float* tr = sT + buf * (S::T_BYTES / 4);
+        const float* tsc = sT + buf * (S::T_BYTES / 4);
+        const float* tcn = tsc + kBN;
+        const float* tbias = tsc + 2 * kBN;
+        const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN);
+        // sweep 1: the chunk's best screened value and its lower bound
+        float best = -INFINITY;
+        int bidx = 0;
 #pragma unroll 1
         for (int c0 = 0; c0 < kBN; c0 += 32) {
           float v[32];
-          tc::tmem_ld32(tmem_base + lane_base + (uint32_t)(buf * kBN + c0), v);
+          tc::tmem_ld32(tcol + (uint32_t)c0, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float lt = fmaf(v[i], tsc[c0 + i], tbias[c0 + i]);
+            if (lt > best) { best = lt; bidx = c0 + i; }
+          }
+        }
+        if (best > -INFINITY)
+          ref = fmaxf(ref, best - fmaf(rnk, tcn[bidx], 1e-3f + 1e-6f * fabsf(best)));
+        // sweep 2: every component whose upper bound reaches within T of ref
+        const float thr_t = ref - kT;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(tcol + (uint32_t)c0, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int kk = c0 + i;
-            const float lt = fmaf(v[i], tr[kk], tr[2 * kBN + kk]);
-            const float beta = fmaf(kKappa * rn, tr[kBN + kk], 1e-3f + 1e-6f * fabsf(lt));
-            const float lo = lt - beta, hi = lt + beta;
-            m_lo = fmaxf(m_lo, lo);
-            float thr = m_lo - kT;
+            const float lt = fmaf(v[i], tsc[kk], tbias[kk]);
+            const float beta = fmaf(rnk, tcn[kk], 1e-3f + 1e-6f * fabsf(lt));
+            const float hi = lt + beta;
+            float thr = thr_t;
             if constexpr (MODE == MODE_ASSIGN) {
-              if (lo > lbm[a.m - 1]) {
-                // keep the m largest lower bounds (descending)
-                float cur = lo;
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                  if (t < a.m && cur > lbm[t]) { const float tmp = lbm[t]; lbm[t] = cur; cur = tmp; }
-                }
-              }
+              const float lo = lt - beta;
+              if (lo > lbm[a.m - 1]) insert_lower_bound(lbm, a.m, lo);
               thr = fminf(thr, lbm[a.m - 1]);
             }
             if (hi >= thr && valid) {
               const int k = j * kBN + kk;
-              if (cnt == kCS) {
-                // full: drop what fell out of the window, then evict the smallest
-                int w = 0;
-                for (int e = 0; e < kCS; ++e) {
-                  const float u = sCUB[e * kBM + r];
-                  if (u >= thr) { sCUB[w * kBM + r] = u; sCK[w * kBM + r] = sCK[e * kBM + r]; ++w; }
-                }
-                cnt = w;
-                if (cnt == kCS) {
-                  int emin = 0;
-                  float umin = sCUB[r];
-                  for (int e = 1; e < kCS; ++e) {
-                    const float u = sCUB[e * kBM + r];
-                    if (u < umin) { umin = u; emin = e; }
-                  }
-                  if (hi > umin) {
-                    dropped = fmaxf(dropped, umin);
-                    sCUB[emin * kBM + r] = hi;
-                    sCK[emin * kBM + r] = (uint16_t)k;
-                  } else {
-                    dropped = fmaxf(dropped, hi);
-                  }
-                  continue;
-                }
+              if (cnt < kCS) {
+                sCUB[cnt * kBM + r] = hi;
+                sCK[cnt * kBM + r] = (uint16_t)k;
+                ++cnt;
+              } else {
+                cnt = insert_full(sCUB, sCK, r, k, hi, thr, &dropped);
               }
-              sCUB[cnt * kBM + r] = hi;
-              sCK[cnt * kBM + r] = (uint16_t)k;
-              ++cnt;
             }
           }
         }
@@ -386,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       if (lane == 0) tc::mbar_arrive(&bar[R_FREE + (it & 1)]);
       if (!ok) break;
       // final window and compaction
-      float thr = m_lo - kT;
+      float thr = ref - kT;
       if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, lbm[a.m - 1]);
       {
         int w = 0;
@@ -397,36 +502,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         cnt = w;
       }
       const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
-      // exact refinement, one candidate at a time per warp, lanes over dims
-      constexpr int DPL = D / 32;
-      int maxc = exact ? cnt : 0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) maxc = max(maxc, __shfl_xor_sync(0xffffffffu, maxc, o));
-      for (int e = 0; e < maxc; ++e) {
-        unsigned mask = __ballot_sync(0xffffffffu, exact && e < cnt);
-        while (mask) {
-          const int b = __ffs(mask) - 1;
-          mask &= mask - 1;
-          const int rb = warp * 32 + b;
-          const int k = sCK[e * kBM + rb];
-          const int64_t nb = n0 + rb;
-          float part = 0.f;
-#pragma unroll
-          for (int i = 0; i < DPL; ++i) {
-            const int d = lane * DPL + i;
-            const float xv = load1<XT>(a.X, (size_t)nb * D + d);
-            const float t = xv - __ldg(g_mu + (size_t)k * D + d);
-            const float w = iso ? __ldg(g_prec + k) : __ldg(g_prec + (size_t)k * D + d);
-            part = fmaf(t * t, w, part);
-          }
-          const float sum = warp_sum(part);
-          if (lane == b) sCUB[e * kBM + rb] = __ldg(g_c + k) - 0.5f * sum;
-        }
-      }
-      __syncwarp();
       if (exact) {
+        // exact log joints of the kept components (same arithmetic as the
+        // CUDA-core kernels), then the log-sum-exp over them
         float mx = -INFINITY;
-        for (int e = 0; e < cnt; ++e) mx = fmaxf(mx, sCUB[e * kBM + r]);
+        for (int e = 0; e < cnt; ++e) {
+          const int k = sCK[e * kBM + r];
+          const float d2 = exact_d2<D, XT>(a.X, n, g_mu + (size_t)k * D,
+                                           iso ? g_prec + k : g_prec + (size_t)k * D, iso);
+          const float l = __ldg(g_c + k) - 0.5f * d2;
+          sCUB[e * kBM + r] = l;
+          mx = fmaxf(mx, l);
+        }
         float s = 0.f;
         for (int e = 0; e < cnt; ++e) s += expf(sCUB[e * kBM + r] - mx);
         const float lse = mx + logf(s);
