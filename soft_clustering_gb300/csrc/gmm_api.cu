@@ -22,12 +22,22 @@ cudaError_t simt_lse_rows(const void* X, int xdtype, int64_t N, int D, int K, in
                           const uint32_t* row_count, int grid, cudaStream_t s);
 cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                       const void* prepared, int mode, float* lse, double* ll_part, int m,
-                      int32_t* ids, float* gamma, uint32_t* fb_rows, uint32_t* fb_count,
-                      DeviceStatus* st, cudaStream_t s);
+                      int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
+                      uint32_t* tile_cnt, int rec_cap, DeviceStatus* st, cudaStream_t s);
 int tc_screen_grid(int64_t N);
+cudaError_t fb_compact(const uint32_t* fb_mask, int64_t N, uint32_t* rows, uint32_t* count,
+                       cudaStream_t s);
 cudaError_t simt_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                        const void* prepared, const float* lse, int parts, double* part,
                        int accumulate, cudaStream_t s);
+cudaError_t simt_stats_rows(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                            const void* prepared, const float* lse, int parts, double* part,
+                            int accumulate, const uint32_t* rows, const uint32_t* row_count,
+                            cudaStream_t s);
+int sparse_stats_parts(int D, int K);
+cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
+                         int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
+                         int parts, double* part, int accumulate, cudaStream_t s);
 int simt_stat_chunk(int D, int cov);
 cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
                          const float* centre, const int32_t* prep_flags, float var_floor,
@@ -42,6 +52,11 @@ constexpr int kTargetCtas = 608;   // 4 x 152 SMs: statistics blocks per launch
 constexpr int kListGrid = 304;     // blocks of the CUDA-core pass over handed-over rows
 constexpr int kMaxScreenGrid = 1024;  // upper bound of tc_screen_grid (SM count)
 constexpr int kMaxK = 1 << 16;
+// Tensor-core path: rows per slab (one screening launch; its records are
+// consumed before the next slab) and responsibility records per 128-point
+// tile (8 per point on average; rows past it go through the row list).
+constexpr int64_t kSlabRows = 1 << 21;
+constexpr int kRecCap = 1024;
 
 bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
 size_t esize(int xdtype) { return xdtype == GMM_F32 ? 4 : 2; }
@@ -60,8 +75,10 @@ int stat_parts(int64_t N, int D, int K, int cov) {
 
 struct WsLayout {
   size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_fb,
-      off_stage, bytes;
-  int parts;
+      off_fbm, off_rec, off_tcnt, off_stage, bytes;
+  int parts;          // statistics partials of the CUDA-core path
+  int sp_parts;       // tensor-core path: partials of the record kernel ...
+  int lp_parts;       // ... followed by those of the row-list pass
   int64_t lse_rows;
 };
 
@@ -86,9 +103,24 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   }
   W.off_ll = o;     o = align_up(o + sizeof(double));
   W.parts = stat_parts(rows, D, K, cov);
-  W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)W.parts * K * stat_width(D, cov));
+  W.sp_parts = W.lp_parts = 0;
+  int slots = W.parts;
+  const bool tc = tc_eligible(D, cov);
+  if (tc) {
+    W.sp_parts = sparse_stats_parts(D, K);
+    const int kc = simt_stat_chunk(D, cov);
+    const int chunks = (K + kc - 1) / kc;
+    W.lp_parts = (kListGrid + chunks - 1) / chunks;
+    if (W.sp_parts + W.lp_parts > slots) slots = W.sp_parts + W.lp_parts;
+  }
+  W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)slots * K * stat_width(D, cov));
   W.off_flags = o;  o = align_up(o + sizeof(int32_t) * K);
-  W.off_fb = o;     o = align_up(o + sizeof(uint32_t) * (size_t)rows);
+  const int64_t slab = rows < kSlabRows ? rows : kSlabRows;
+  W.off_fb = o;     o = align_up(o + sizeof(uint32_t) * (size_t)(tc ? slab : rows));
+  const size_t slab_tiles = tc ? (size_t)((slab + 127) / 128) : 0;
+  W.off_fbm = o;    o = align_up(o + sizeof(uint32_t) * 4 * slab_tiles);
+  W.off_rec = o;    o = align_up(o + sizeof(uint2) * slab_tiles * kRecCap);
+  W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * slab_tiles);
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
@@ -162,31 +194,62 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
   DeviceStatus* st = at<DeviceStatus>(ws, W.off_status);
   const void* prep = at<char>(ws, W.off_prep);
   double* llp = at<double>(ws, W.off_llpart);
-  int64_t nll = (rows + kLseRows - 1) / kLseRows;
   if (tc) {
-    // screen on the tensor cores; rows whose candidate list overflowed go
-    // through the CUDA-core kernel in row-list mode
+    // Slabs of kSlabRows rows.  Per slab: screen on the tensor cores (exact
+    // LSE and responsibility records of most rows), the CUDA-core pass over
+    // the rows handed over, the log-likelihood, statistics from the records
+    // and the CUDA-core statistics of the handed-over rows.
     uint32_t* fb = at<uint32_t>(ws, W.off_fb);
-    GMM_TRY(cudaMemsetAsync(&st->fb_count, 0, sizeof(uint32_t), s));
-    const int g1 = tc_screen_grid(rows);
-    {
-      GMM_PROF("tc_screen_kernel");
-      GMM_TRY(tc_screen(X, xdtype, rows, D, K, cov, prep, 0, lse, llp, 0, nullptr, nullptr, fb,
-                        &st->fb_count, st, s));
+    uint32_t* fbm = at<uint32_t>(ws, W.off_fbm);
+    uint2* recs = at<uint2>(ws, W.off_rec);
+    uint32_t* tcnt = at<uint32_t>(ws, W.off_tcnt);
+    double* part = at<double>(ws, W.off_part);
+    double* lpart = part + (size_t)W.sp_parts * K * stat_width(D, cov);
+    for (int64_t r0 = 0; r0 < rows; r0 += kSlabRows) {
+      const int64_t sn = (rows - r0) < kSlabRows ? (rows - r0) : kSlabRows;
+      const void* Xs = (const char*)X + (size_t)r0 * D * esize(xdtype);
+      float* ls = lse + r0;
+      const int acc = accumulate || r0 > 0;
+      const int g1 = tc_screen_grid(sn);
+      {
+        GMM_PROF("tc_screen_kernel");
+        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, ls, llp, 0, nullptr, nullptr, fbm,
+                          recs, tcnt, kRecCap, st, s));
+      }
+      {
+        GMM_PROF("fb_compact_kernel");
+        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, s));
+      }
+      {
+        GMM_PROF("lse_rows_kernel");
+        GMM_TRY(simt_lse_rows(Xs, xdtype, sn, D, K, cov, prep, ls, llp + g1, 0, nullptr,
+                              nullptr, st, fb, &st->fb_count, kListGrid, s));
+      }
+      {
+        GMM_PROF("ll_finalize_kernel");
+        GMM_TRY(launch_ll_finalize(llp, g1 + kListGrid, at<double>(ws, W.off_ll), acc, s));
+      }
+      {
+        GMM_PROF("sparse_stats_kernel");
+        GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, tcnt, recs, kRecCap, W.sp_parts,
+                             part, acc, s));
+      }
+      {
+        GMM_PROF("stats_rows_kernel");
+        GMM_TRY(simt_stats_rows(Xs, xdtype, sn, D, K, cov, prep, ls, W.lp_parts, lpart, acc, fb,
+                                &st->fb_count, s));
+      }
     }
-    {
-      GMM_PROF("lse_rows_kernel");
-      GMM_TRY(simt_lse_rows(X, xdtype, rows, D, K, cov, prep, lse, llp + g1, 0, nullptr, nullptr,
-                            st, fb, &st->fb_count, kListGrid, s));
-    }
-    nll = g1 + kListGrid;
-  } else {
+    return GMM_OK;
+  }
+  {
     GMM_PROF("lse_kernel");
     GMM_TRY(simt_lse(X, xdtype, rows, D, K, cov, prep, lse, llp, 0, nullptr, nullptr, st, s));
   }
   {
     GMM_PROF("ll_finalize_kernel");
-    GMM_TRY(launch_ll_finalize(llp, nll, at<double>(ws, W.off_ll), accumulate, s));
+    GMM_TRY(launch_ll_finalize(llp, (rows + kLseRows - 1) / kLseRows, at<double>(ws, W.off_ll),
+                               accumulate, s));
   }
   {
     GMM_PROF("stats_kernel");
@@ -195,6 +258,9 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
   }
   return GMM_OK;
 }
+
+// Partials the M-step merges for the path taken.
+int mstep_parts(const WsLayout& W, bool tc) { return tc ? W.sp_parts + W.lp_parts : W.parts; }
 
 // Library-owned copy stream and events of the host path (one set per device).
 struct HostPathRes {
@@ -322,7 +388,7 @@ gmm_status gmm_em_step(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
   if (r != GMM_OK) return r;
   {
     GMM_PROF("mstep_kernel");
-    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), W.parts, N, D, K, cov,
+    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), mstep_parts(W, use_tc(D, cov, o)), N, D, K, cov,
                          at<float>(prep, PL.off_mu), at<int32_t>(prep, PL.off_flags), o.var_floor,
                          o.min_s0, params, flags_dev ? flags_dev : at<int32_t>(ws, W.off_flags),
                          s));
@@ -381,7 +447,7 @@ gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int
   }
   {
     GMM_PROF("mstep_kernel");
-    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), W.parts, N, D, K, cov,
+    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), mstep_parts(W, use_tc(D, cov, o)), N, D, K, cov,
                          at<float>(prep, PL.off_mu), at<int32_t>(prep, PL.off_flags), o.var_floor,
                          o.min_s0, params, flags_dev ? flags_dev : at<int32_t>(ws, W.off_flags),
                          s));
@@ -409,15 +475,28 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
   DeviceStatus* st = static_cast<DeviceStatus*>(ws);
   GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
   if (tc) {
+    // slabs of kSlabRows rows: screening, then the row list of the slab
     uint32_t* fb = at<uint32_t>(ws, W.off_fb);
-    {
-      GMM_PROF("tc_screen_kernel");
-      GMM_TRY(tc_screen(X, xdtype, N, D, K, cov, prepared, 1, lse, nullptr, m, ids, gamma, fb,
-                        &st->fb_count, st, s));
+    uint32_t* fbm = at<uint32_t>(ws, W.off_fbm);
+    for (int64_t r0 = 0; r0 < N; r0 += kSlabRows) {
+      const int64_t sn = (N - r0) < kSlabRows ? (N - r0) : kSlabRows;
+      const void* Xs = (const char*)X + (size_t)r0 * D * esize(xdtype);
+      float* ls = lse ? lse + r0 : nullptr;
+      int32_t* is = ids + (size_t)r0 * m;
+      float* gs = gamma + (size_t)r0 * m;
+      {
+        GMM_PROF("tc_screen_kernel");
+        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prepared, 1, ls, nullptr, m, is, gs, fbm,
+                          nullptr, nullptr, 0, st, s));
+      }
+      {
+        GMM_PROF("fb_compact_kernel");
+        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, s));
+      }
+      GMM_PROF("lse_rows_kernel");
+      GMM_TRY(simt_lse_rows(Xs, xdtype, sn, D, K, cov, prepared, ls, nullptr, m, is, gs, st, fb,
+                            &st->fb_count, kListGrid, s));
     }
-    GMM_PROF("lse_rows_kernel");
-    GMM_TRY(simt_lse_rows(X, xdtype, N, D, K, cov, prepared, lse, nullptr, m, ids, gamma, st, fb,
-                          &st->fb_count, kListGrid, s));
     return GMM_OK;
   }
   GMM_PROF("lse_topm_kernel");

@@ -18,11 +18,12 @@ cudaError_t simt_lse_d<32>(const void* X, int xdtype, int64_t N, int K, int cov,
 template <>
 cudaError_t simt_stats_d<32>(const void* X, int xdtype, int64_t N, int K, int cov,
                             const void* prepared, const float* lse, int parts, double* part,
-                            int accumulate, cudaStream_t s) {
+                            int accumulate, const uint32_t* rows,
+                            const uint32_t* row_count, cudaStream_t s) {
   PreparedLayout L = PreparedLayout::make(32, K, cov);
   return dispatch_cx(cov, xdtype, [&](auto Cc, auto Xc) {
     return simt::run_stats<32, decltype(Cc)::value, decltype(Xc)::value>(
-        X, N, K, prepared, L, lse, parts, part, accumulate, s);
+        X, N, K, prepared, L, lse, parts, part, accumulate, rows, row_count, s);
   });
 }
 

@@ -247,7 +247,8 @@ template <int D, int COV, int XT>
 __global__ void __launch_bounds__(kStatThreads)
 stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict__ prepared,
              PreparedLayout L, const float* __restrict__ lse, int64_t rows_per_part,
-             double* __restrict__ part, int accumulate) {
+             double* __restrict__ part, int accumulate, const uint32_t* __restrict__ rows,
+             const uint32_t* __restrict__ row_count) {
   using SS = StatShape<D, COV>;
   constexpr int KC = SS::KC, F = SS::F, SLOTS = SS::SLOTS, T = kStatTile;
   constexpr int P = LseShape<D, COV>::P;
@@ -269,8 +270,15 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
 
   const int k0 = blockIdx.x * KC;
   const int kc = min(KC, K - k0);
+  // Dense mode: points [0, N).  Row-list mode: the points rows[0 .. *row_count),
+  // split evenly over the partitions (the count is only known on the device).
+  const int64_t cnt = rows ? (int64_t)*row_count : N;
+  if (rows) {
+    rows_per_part = (cnt + gridDim.y - 1) / gridDim.y;
+    rows_per_part = (rows_per_part + T - 1) / T * T;
+  }
   const int64_t r0 = (int64_t)blockIdx.y * rows_per_part;
-  const int64_t r1 = min(N, r0 + rows_per_part);
+  const int64_t r1 = min(cnt, r0 + rows_per_part);
 
   for (int i = threadIdx.x; i < kc * D; i += kStatThreads)
     s_mu[i] = at<float>(prepared, L.off_mu)[(size_t)k0 * D + i];
@@ -300,7 +308,8 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
     __syncthreads();
     for (int i = threadIdx.x; i < T * D; i += kStatThreads) {
       int r = i / D, d = i % D;
-      s_x[r * XS + d] = r < tn ? load_x<XT>(X, (size_t)(t0r + r) * D + d) : 0.f;
+      const int64_t src = r < tn ? (rows ? (int64_t)rows[t0r + r] : t0r + r) : 0;
+      s_x[r * XS + d] = r < tn ? load_x<XT>(X, (size_t)src * D + d) : 0.f;
     }
     __syncthreads();
     // responsibilities of this chunk for the tile
@@ -329,7 +338,7 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
               [&](int d) { return COV == GMM_COV_DIAG ? wk[d] : wk[0]; });
           l = s_c[kk] - 0.5f * d2;
         }
-        g = expf(l - lse[t0r + r]);
+        g = expf(l - lse[rows ? (int64_t)rows[t0r + r] : t0r + r]);
       }
       s_g[r * KC + kk] = g;
     }
@@ -499,16 +508,18 @@ cudaError_t run_lse(const void* X, int64_t N, int K, const void* prepared, const
 template <int D, int COV, int XT>
 cudaError_t run_stats(const void* X, int64_t N, int K, const void* prepared,
                       const PreparedLayout& L, const float* lse, int parts, double* part,
-                      int accumulate, cudaStream_t s) {
+                      int accumulate, const uint32_t* rows, const uint32_t* row_count,
+                      cudaStream_t s) {
   using SS = StatShape<D, COV>;
   size_t smem = stat_smem<D, COV, XT>();
   auto kern = stats_kernel<D, COV, XT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int64_t rows = (N + parts - 1) / parts;
-  rows = (rows + kStatTile - 1) / kStatTile * kStatTile;
+  int64_t rpp = (N + parts - 1) / parts;
+  rpp = (rpp + kStatTile - 1) / kStatTile * kStatTile;
   dim3 grid((K + SS::KC - 1) / SS::KC, parts);
-  kern<<<grid, kStatThreads, smem, s>>>(X, N, K, prepared, L, lse, rows, part, accumulate);
+  kern<<<grid, kStatThreads, smem, s>>>(X, N, K, prepared, L, lse, rpp, part, accumulate, rows,
+                                        row_count);
   return cudaGetLastError();
 }
 
@@ -543,6 +554,7 @@ cudaError_t simt_lse_d(const void* X, int xdtype, int64_t N, int K, int cov, con
 template <int D>
 cudaError_t simt_stats_d(const void* X, int xdtype, int64_t N, int K, int cov,
                          const void* prepared, const float* lse, int parts, double* part,
-                         int accumulate, cudaStream_t s);
+                         int accumulate, const uint32_t* rows, const uint32_t* row_count,
+                         cudaStream_t s);
 
 }  // namespace gmm

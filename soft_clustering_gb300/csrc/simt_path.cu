@@ -33,16 +33,25 @@ cudaError_t simt_lse(const void* X, int xdtype, int64_t N, int D, int K, int cov
                        nullptr, nullptr, 0, s);
 }
 
+// With a row list, the points rows[0 .. *row_count) (count read on the device).
+cudaError_t simt_stats_rows(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                            const void* prepared, const float* lse, int parts, double* part,
+                            int accumulate, const uint32_t* rows, const uint32_t* row_count,
+                            cudaStream_t s) {
+  switch (D) {
+    case 16: return simt_stats_d<16>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, rows, row_count, s);
+    case 32: return simt_stats_d<32>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, rows, row_count, s);
+    case 64: return simt_stats_d<64>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, rows, row_count, s);
+    case 128: return simt_stats_d<128>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, rows, row_count, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t simt_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                        const void* prepared, const float* lse, int parts, double* part,
                        int accumulate, cudaStream_t s) {
-  switch (D) {
-    case 16: return simt_stats_d<16>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, s);
-    case 32: return simt_stats_d<32>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, s);
-    case 64: return simt_stats_d<64>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, s);
-    case 128: return simt_stats_d<128>(X, xdtype, N, K, cov, prepared, lse, parts, part, accumulate, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return simt_stats_rows(X, xdtype, N, D, K, cov, prepared, lse, parts, part, accumulate,
+                         nullptr, nullptr, s);
 }
 
 }  // namespace gmm

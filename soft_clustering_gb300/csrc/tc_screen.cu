@@ -19,7 +19,8 @@
 // log-sum-exp).  Components more than 40 nats below the best carry less than
 // 4.3e-18 of a point's responsibility.  A point whose kept list overflowed
 // (more than 32 candidates, with an evicted one still within the window) is
-// handed to the CUDA-core path through a row list.
+// handed to the CUDA-core path: one bit per row, turned into an ascending
+// row list by fb_compact so that the order never depends on timing.
 //
 // Roles (one CTA per SM, persistent over 128-point tiles in a fixed order):
 //   warps 0-3  epilogue: TMEM lane quarter w -> 32 points; candidates,
@@ -57,8 +58,11 @@ struct ScreenArgs {
   double* ll_part;       // [gridDim.x] (EM) or null
   int32_t* ids;          // [N*m] (assign)
   float* gamma;          // [N*m] (assign)
-  uint32_t* fb_rows;     // rows handed to the CUDA-core path
-  uint32_t* fb_count;
+  uint32_t* fb_mask;     // [tiles * 4] bit r % 32 of word n / 32: row n handed to
+                         // the CUDA-core path
+  uint2* recs;           // EM: [tiles][rec_cap] responsibility records
+  uint32_t* tile_cnt;    // EM: [tiles] records written per tile
+  int rec_cap;
   DeviceStatus* st;
 };
 
@@ -75,15 +79,15 @@ struct Shape {
   static constexpr int OFF_RN = OFF_T + 2 * T_BYTES;     // 2 x 128 row norms
   static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;   // [kCS][128] float
   static constexpr int OFF_CK = OFF_CUB + kCS * kBM * 4; // [kCS][128] u16
-  static constexpr int OFF_BAR = OFF_CK + kCS * kBM * 2; // 16 mbarriers
-  static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+  static constexpr int OFF_BAR = OFF_CK + kCS * kBM * 2; // 17 mbarriers (24 slots)
+  static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr int SMEM = BYTES + 1024;              // base alignment slack
 };
 
 enum Bar {
   A_FULL = 0, A_EMPTY = 1, B_FULL = 2, B_EMPTY = 4, T_FULL = 6, T_EMPTY = 8, TR_FULL = 10,
-  R_FULL = 12, R_FREE = 14
+  R_FULL = 12, R_FREE = 14, EPI_SYNC = 16
 };
 
 template <int XT>
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   uint64_t* bar = (uint64_t*)(sm + S::OFF_BAR);
   uint32_t* tmem_slot = (uint32_t*)(sm + S::OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + S::OFF_MISC + 4);
+  int* warp_tot = (int*)(sm + S::OFF_MISC + 16);  // [2][4] record counts per epilogue warp
   __shared__ double ll_red[4];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -275,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       tc::mbar_init(&bar[R_FULL + i], 4);
       tc::mbar_init(&bar[R_FREE + i], 4);
     }
+    tc::mbar_init(&bar[EPI_SYNC], 4);
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
@@ -502,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         cnt = w;
       }
       const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
+      float lse = 0.f;
       if (exact) {
         // exact log joints of the kept components (same arithmetic as the
         // CUDA-core kernels), then the log-sum-exp over them
@@ -516,12 +523,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         }
         float s = 0.f;
         for (int e = 0; e < cnt; ++e) s += expf(sCUB[e * kBM + r] - mx);
-        const float lse = mx + logf(s);
-        if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
-        if (a.lse) a.lse[n] = lse;
-        if constexpr (MODE == MODE_EM) {
+        lse = mx + logf(s);
+      }
+      if constexpr (MODE == MODE_EM) {
+        // responsibility records of this tile, in row order: an exclusive
+        // prefix sum of the rows' candidate counts over the 128 epilogue
+        // threads.  Rows past the record capacity go to the row list.
+        const int my = exact ? cnt : 0;
+        int incl = my;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        int* tot = warp_tot + (it & 1) * 4;
+        if (lane == 31) tot[warp] = incl;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[EPI_SYNC]);
+        if (!warp_wait(&bar[EPI_SYNC], it & 1)) { fail(); break; }
+        int off = incl - my, all = 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int t = tot[w];
+          if (w < warp) off += t;
+          all += t;
+        }
+        const int64_t tl = tile;  // tile index within this launch
+        const bool fits = exact && off + cnt <= a.rec_cap;
+        if (exact && off <= a.rec_cap && off + cnt > a.rec_cap) a.tile_cnt[tl] = (uint32_t)off;
+        if (r == kBM - 1 && all <= a.rec_cap) a.tile_cnt[tl] = (uint32_t)all;
+        if (fits) {
+          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+          if (a.lse) a.lse[n] = lse;
           ll_acc += (double)lse;
-        } else {
+          uint2* out = a.recs + (size_t)tl * a.rec_cap + off;
+          for (int e = 0; e < cnt; ++e) {
+            const uint32_t k = sCK[e * kBM + r];
+            const float g = expf(sCUB[e * kBM + r] - lse);
+            out[e] = make_uint2((k << 7) | (uint32_t)r, __float_as_uint(g));
+          }
+        }
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !fits);
+        if (lane == 0) a.fb_mask[tile * 4 + warp] = fbm;
+      } else {
+        if (exact) {
+          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+          if (a.lse) a.lse[n] = lse;
           // top-m by exact value, ties to the lower component
           uint32_t taken = 0;
           for (int t = 0; t < a.m; ++t) {
@@ -543,9 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
             a.gamma[n * a.m + t] = bv == -INFINITY ? 0.f : expf(bv - lse);
           }
         }
-      } else if (valid) {
-        const uint32_t slot = atomicAdd(a.fb_count, 1u);
-        a.fb_rows[slot] = (uint32_t)n;
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
+        if (lane == 0) a.fb_mask[tile * 4 + warp] = fbm;
       }
       __syncwarp();
     }
@@ -563,6 +609,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   if (warp == 8) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base, 256);
+  }
+}
+
+// Ascending list of the rows whose bit is set in the hand-over bitmap
+// (word w covers rows 32w .. 32w + 31): one block; each thread owns a
+// contiguous range of words, counts, takes its offset from a block-wide
+// exclusive scan and writes its rows in order.
+constexpr int kCompactThreads = 1024;
+__global__ void __launch_bounds__(kCompactThreads)
+fb_compact_kernel(const uint32_t* __restrict__ mask, int64_t N, uint32_t* __restrict__ rows,
+                  uint32_t* __restrict__ count) {
+  __shared__ uint32_t wsum[kCompactThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nwords = (N + 31) / 32;
+  const int64_t per = (nwords + kCompactThreads - 1) / kCompactThreads;
+  const int64_t w0 = min(nwords, (int64_t)tid * per), w1 = min(nwords, w0 + per);
+  auto word = [&](int64_t w) {
+    uint32_t m = mask[w];
+    const int64_t left = N - w * 32;
+    if (left < 32) m &= (1u << left) - 1u;
+    return m;
+  };
+  uint32_t mine = 0;
+  for (int64_t w = w0; w < w1; ++w) mine += __popc(word(w));
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t t = wsum[lane], ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += v;
+    }
+    wsum[lane] = ti - t;  // exclusive prefix of the warp totals
+    if (lane == 31) *count = ti;
+  }
+  __syncthreads();
+  uint32_t pos = wsum[warp] + incl - mine;
+  for (int64_t w = w0; w < w1; ++w) {
+    uint32_t m = word(w);
+    while (m) {
+      const int b = __ffs(m) - 1;
+      m &= m - 1u;
+      rows[pos++] = (uint32_t)(w * 32 + b);
+    }
   }
 }
 
@@ -594,14 +691,16 @@ int tc_screen_grid(int64_t N) {
 // mode 0: EM (lse, ll_part); mode 1: assign (top-m).
 cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                       const void* prepared, int mode, float* lse, double* ll_part, int m,
-                      int32_t* ids, float* gamma, uint32_t* fb_rows, uint32_t* fb_count,
-                      DeviceStatus* st, cudaStream_t s) {
+                      int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
+                      uint32_t* tile_cnt, int rec_cap, DeviceStatus* st, cudaStream_t s) {
   ScreenArgs a;
   a.X = X; a.N = N; a.K = K; a.m = m; a.prepared = prepared;
   a.L = PreparedLayout::make(D, K, cov);
   a.lse = lse; a.ll_part = ll_part; a.ids = ids; a.gamma = gamma;
-  a.fb_rows = fb_rows; a.fb_count = fb_count; a.st = st;
+  a.fb_mask = fb_mask; a.st = st;
+  a.recs = recs; a.tile_cnt = tile_cnt; a.rec_cap = rec_cap;
   if (!a.L.tc_chunks || N < 1) return cudaErrorInvalidValue;
+  if (mode == MODE_EM && (!recs || !tile_cnt || rec_cap < kBM)) return cudaErrorInvalidValue;
   const int grid = tc_screen_grid(N);
 #define GMM_SCREEN(DD, XX)                                                              \
   return mode == MODE_EM ? run_screen<DD, XX, MODE_EM>(a, grid, s)                      \
@@ -616,6 +715,13 @@ cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int co
     GMM_SCREEN(64, GMM_F32);
   }
 #undef GMM_SCREEN
+}
+
+// Rows handed over by the screening launch over N rows -> rows[0 .. *count).
+cudaError_t fb_compact(const uint32_t* fb_mask, int64_t N, uint32_t* rows, uint32_t* count,
+                       cudaStream_t s) {
+  fb_compact_kernel<<<1, kCompactThreads, 0, s>>>(fb_mask, N, rows, count);
+  return cudaGetLastError();
 }
 
 }  // namespace gmm
