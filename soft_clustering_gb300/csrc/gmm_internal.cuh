@@ -45,6 +45,10 @@ __host__ __device__ inline int prec_width(int D, int cov) {
 // D = 64 or 128: the log-density is screened as [x, x^2] . [b1, b2] with
 // b1 = mu / var, b2 = -1 / (2 var) on fp16 tensor cores.
 constexpr int kTcChunk = 128;  // components per screening chunk (MMA N)
+// Per-chunk trailer of the screening operands: scale [128], |(b1, b2)|_2
+// [128], then the bias with its absolute and relative fp32 margin
+// (delta_k = 1e-3 + 1e-6 |bias_k|) taken off [128] and added on [128].
+constexpr int kTcTrail = 4 * kTcChunk;
 __host__ __device__ inline bool tc_eligible(int D, int cov) {
   return (cov == GMM_COV_DIAG || cov == GMM_COV_ISO) && (D == 64 || D == 128);
 }
@@ -61,7 +65,8 @@ struct PreparedLayout {
   size_t off_tcB;    // fp16 [chunks][2D/64][128 rows][64]: (b1, b2)/scale as 128-byte
                      // swizzled K-major tiles, one contiguous image per chunk
   size_t tcB_chunk_bytes;
-  size_t off_tcT;    // float [chunks][3][128]: scale (power of 2), |(b1,b2)|_2, bias
+  size_t off_tcT;    // float [chunks][kTcTrail]: scale (power of 2) [128], |(b1,b2)|_2 [128],
+                     // bias - delta [128], bias + delta [128]
   size_t tc_bytes;
   size_t bytes;
 
@@ -84,7 +89,7 @@ struct PreparedLayout {
       L.tcB_chunk_bytes = (size_t)kTcChunk * 2 * D * 2;
       o = align_up(o + L.tcB_chunk_bytes * L.tc_chunks);
       L.off_tcT = o;
-      o = align_up(o + sizeof(float) * 3 * kTcChunk * L.tc_chunks);
+      o = align_up(o + sizeof(float) * kTcTrail * L.tc_chunks);
       L.tc_bytes = o - L.off_tcB;
     }
     L.bytes = align_up(o);

@@ -170,7 +170,7 @@ __global__ void prepare_tc_kernel(PreparedLayout L, void* prepared) {
   const int D = L.D, KD = 2 * D;
   const int chunk = k / kTcChunk, row = k % kTcChunk;
   unsigned char* img = at<unsigned char>(prepared, L.off_tcB) + (size_t)chunk * L.tcB_chunk_bytes;
-  float* trail = at<float>(prepared, L.off_tcT) + (size_t)chunk * 3 * kTcChunk;
+  float* trail = at<float>(prepared, L.off_tcT) + (size_t)chunk * kTcTrail;
   const bool live = k < L.K && at<float>(prepared, L.off_c)[k] != -INFINITY;
   const float* mu = at<float>(prepared, L.off_mu) + (size_t)(live ? k : 0) * D;
   const float* prec = at<float>(prepared, L.off_prec) +
@@ -215,8 +215,12 @@ __global__ void prepare_tc_kernel(PreparedLayout L, void* prepared) {
   if (threadIdx.x == 0) {
     trail[row] = (float)scale;
     trail[kTcChunk + row] = (float)sqrt(red[31]);
-    trail[2 * kTcChunk + row] =
-        live ? (float)((double)at<float>(prepared, L.off_c)[k] - 0.5 * s_q) : -INFINITY;
+    // bias = c_k - sum mu^2 w / 2, with the margin of the fp32 evaluation
+    // (1e-3 absolute + 1e-6 relative), rounded outwards
+    const double bias = live ? (double)at<float>(prepared, L.off_c)[k] - 0.5 * s_q : 0.0;
+    const double dl = 1e-3 + 1e-6 * fabs(bias);
+    trail[2 * kTcChunk + row] = live ? __double2float_rd(bias - dl) : -INFINITY;
+    trail[3 * kTcChunk + row] = live ? __double2float_ru(bias + dl) : -INFINITY;
   }
 }
 

@@ -8,27 +8,33 @@
 // notes, sec. 1.2-1.3; Flash-GMM summary, Method: all-K distances per tile).
 // Its terms are large and cancel (|x.b1| ~ 1e4 against l ~ 1e2 for tight
 // clusters), so fp16 operands with fp32 accumulation give only a screen.
-// Each screened value comes with a rigorous bound on its error,
-//   |l~ - l| <= beta_nk = kappa |[x, x^2]|_2 |[b1, b2]|_2 + margin,
-// from the fp16 rounding of b and x^2 (2^-11 each), of fp32 inputs (2^-11)
-// and fp32 accumulation.  A component is kept when its upper bound l~ + beta
-// reaches within T = 40 nats of the largest lower bound l~ - beta; every
-// kept pair is then evaluated exactly in the centred fp32 form
-// sum_d w_d (x_d - mu_d)^2, and LSE_n, the log-likelihood, top-m and the
-// responsibilities come from those exact values (sec. 3.2, 4.2: fp32 online
-// log-sum-exp).  Components more than 40 nats below the best carry less than
-// 4.3e-18 of a point's responsibility.  A point whose kept list overflowed
-// (more than 32 candidates, with an evicted one still within the window) is
-// handed to the CUDA-core path: one bit per row, turned into an ascending
-// row list by fb_compact so that the order never depends on timing.
+// Each screened value v (accumulator units; scale s_k, bias_k = c_k -
+// sum mu^2 w / 2) comes with a rigorous bound on its error,
+//   |s v + bias - l| <= kappa |[x, x^2]|_2 |[b1, b2]|_2 + 1e-6 (|s v| + |bias|) + 1e-3,
+// from the fp16 rounding of b and x^2 (2^-11 each), of fp32 inputs (2^-11),
+// fp32 accumulation and the fp32 evaluation of the sum (the relative term;
+// its bias part and the 1e-3 are folded into the prepared bias - delta and
+// bias + delta).  A component is kept when its upper bound reaches within
+// T = 40 nats of the largest lower bound; every kept pair is then evaluated
+// exactly in the centred fp32 form sum_d w_d (x_d - mu_d)^2, and LSE_n, the
+// log-likelihood, top-m and the responsibilities come from those exact
+// values (sec. 3.2, 4.2: fp32 log-sum-exp).  Components more than 40 nats
+// below the best carry less than 4.3e-18 of a point's responsibility.  A
+// point whose kept list overflowed (more than 16 candidates in one half of
+// the columns, with an evicted one still within the window) is handed to
+// the CUDA-core path: one bit per row, turned into an ascending row list by
+// fb_compact so that the order never depends on timing.
 //
 // Roles (one CTA per SM, persistent over 128-point tiles in a fixed order):
-//   warps 0-3  epilogue: TMEM lane quarter w -> 32 points; candidates,
-//              exact refinement of each point's own candidates, outputs
-//   warps 4-7  producers: one point row per thread -> [x, x^2] fp16 tile in
-//              shared memory (128-byte swizzled K-major), row norms
-//   warp  8    lane 0 issues bulk copies of the parameter chunks and the
-//              tcgen05.mma instructions; the warp owns the TMEM allocation
+//   warps 0-7   epilogue: warp w reads TMEM lane quarter w % 4 (32 points)
+//               and column half w / 4 of every chunk; each keeps its own
+//               candidate list, refines it exactly, and the two warps of a
+//               quarter combine their results through shared memory
+//   warps 8-11  producers: one point row per thread -> [x, x^2] fp16 tile in
+//               shared memory (128-byte swizzled K-major), row norms; the
+//               next tile's rows are loaded before the buffer is free
+//   warp  12    lane 0 issues bulk copies of the parameter chunks and the
+//               tcgen05.mma instructions; the warp owns the TMEM allocation
 #include <math.h>
 
 #include "gmm_internal.cuh"
@@ -39,10 +45,15 @@ namespace {
 
 constexpr int kBM = 128;          // points per tile (MMA M)
 constexpr int kBN = kTcChunk;     // components per chunk (MMA N)
-constexpr int kCS = 32;           // candidates kept per point
+constexpr int kHalf = kBN / 2;    // columns of a chunk per epilogue warp
+constexpr int kCSH = 16;          // candidates kept per point and column half
 constexpr float kT = 40.f;        // nats
 constexpr float kKappa = 1.5e-3f; // 3 x 2^-11 rounding + accumulation allowance
-constexpr int kThreads = 288;
+constexpr float kRel = 1e-6f;     // relative margin of the fp32 evaluation
+constexpr int kEpiWarps = 8;
+constexpr int kProdWarp0 = 8;     // warps 8-11
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 13 * 32;
 constexpr uint32_t kWait = 1u << 22;
 
 enum { MODE_EM = 0, MODE_ASSIGN = 1 };
@@ -72,46 +83,58 @@ struct Shape {
   static constexpr int KSTEPS = KD / 16;
   static constexpr int A_BYTES = kBM * KD * 2;
   static constexpr int B_BYTES = kBN * KD * 2;
-  static constexpr int T_BYTES = 3 * kBN * 4;
+  static constexpr int T_BYTES = kTcTrail * 4;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + A_BYTES;          // 2 buffers
-  static constexpr int OFF_T = OFF_B + 2 * B_BYTES;      // 2 trailers
-  static constexpr int OFF_RN = OFF_T + 2 * T_BYTES;     // 2 x 128 row norms
-  static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;   // [kCS][128] float
-  static constexpr int OFF_CK = OFF_CUB + kCS * kBM * 4; // [kCS][128] u16
-  static constexpr int OFF_BAR = OFF_CK + kCS * kBM * 2; // 17 mbarriers (24 slots)
+  static constexpr int OFF_B = OFF_A + A_BYTES;             // 2 buffers
+  static constexpr int OFF_T = OFF_B + 2 * B_BYTES;         // 2 trailers
+  static constexpr int OFF_RN = OFF_T + 2 * T_BYTES;        // 2 x 128 row norms
+  static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;      // [2][kCSH][128] float
+  static constexpr int OFF_CK = OFF_CUB + 2 * kCSH * kBM * 4;  // [2][kCSH][128] u16
+  static constexpr int OFF_X = OFF_CK + 2 * kCSH * kBM * 2;    // half exchange
+  static constexpr int X_BYTES = 4 * 2 * kBM * 4 + 2 * kBM * 2;
+  static constexpr int OFF_BAR = (OFF_X + X_BYTES + 7) / 8 * 8;  // 24 mbarrier slots
   static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
   static constexpr int BYTES = OFF_MISC + 64;
-  static constexpr int SMEM = BYTES + 1024;              // base alignment slack
+  static constexpr int SMEM = BYTES + 1024;                 // base alignment slack
 };
+
+// 227 KB of shared memory per block, with the static part (ll_red)
+static_assert(Shape<128>::SMEM + 8 * kEpiWarps <= 232448, "shared memory");
 
 enum Bar {
   A_FULL = 0, A_EMPTY = 1, B_FULL = 2, B_EMPTY = 4, T_FULL = 6, T_EMPTY = 8, TR_FULL = 10,
-  R_FULL = 12, R_FREE = 14, EPI_SYNC = 16
+  R_FULL = 12, R_FREE = 14, EX_A = 16, EX_B = 17, EX_C = 18
 };
 
+// 8 consecutive stored coordinates as float, from raw 16-byte words.
 template <int XT>
-__device__ __forceinline__ void load8(const void* X, size_t elem, float* v) {
+__device__ __forceinline__ void raw_to_float8(const uint4* w, float* v) {
   if constexpr (XT == GMM_F32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(X) + elem);
-    float4 a = __ldg(p), b = __ldg(p + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    v[0] = __uint_as_float(w[0].x); v[1] = __uint_as_float(w[0].y);
+    v[2] = __uint_as_float(w[0].z); v[3] = __uint_as_float(w[0].w);
+    v[4] = __uint_as_float(w[1].x); v[5] = __uint_as_float(w[1].y);
+    v[6] = __uint_as_float(w[1].z); v[7] = __uint_as_float(w[1].w);
   } else {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(X) + elem));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const uint32_t u[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      if constexpr (XT == GMM_F16) {
-        __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-        float2 f = __half22float2(h);
-        v[2 * i] = f.x; v[2 * i + 1] = f.y;
-      } else {
-        __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-        float2 f = __bfloat1622float2(h);
-        v[2 * i] = f.x; v[2 * i + 1] = f.y;
-      }
+      float2 f;
+      if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+      v[2 * i] = f.x; v[2 * i + 1] = f.y;
     }
+  }
+}
+
+// Raw words of 8 coordinates starting at element `elem` (16-byte aligned).
+template <int XT>
+__device__ __forceinline__ void load_raw8(const void* X, size_t elem, uint4* w) {
+  if constexpr (XT == GMM_F32) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(X) + elem);
+    w[0] = __ldg(p);
+    w[1] = __ldg(p + 1);
+  } else {
+    w[0] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(X) + elem));
   }
 }
 
@@ -125,11 +148,6 @@ __device__ __forceinline__ bool warp_aborted(volatile int* flag) {
   return __any_sync(0xffffffffu, *flag != 0);
 }
 
-template <int XT>
-__device__ __forceinline__ float load1(const void* X, size_t elem) {
-  return load_x<XT>(X, elem);
-}
-
 // Keeps lbm[0..m) the m largest values seen (descending); v > lbm[m-1].
 __device__ __forceinline__ void insert_lower_bound(float* lbm, int m, float v) {
 #pragma unroll
@@ -138,91 +156,106 @@ __device__ __forceinline__ void insert_lower_bound(float* lbm, int m, float v) {
   }
 }
 
-// Full candidate list of row r: drop entries that fell out of the window,
-// then evict the smallest upper bound if the new one is larger.  Returns the
-// new count; *dropped is the largest upper bound ever discarded while still
-// inside the window.
-__device__ __noinline__ int insert_full(float* sCUB, uint16_t* sCK, int r, int k, float hi,
+// Full candidate list of row r (entries cub/ck [e * 128 + r]): drop entries
+// that fell out of the window, then evict the smallest upper bound if the
+// new one is larger.  Returns the new count; *dropped is the largest upper
+// bound ever discarded while still inside the window.
+__device__ __noinline__ int insert_full(float* cub, uint16_t* ck, int r, int k, float hi,
                                         float thr, float* dropped) {
   int w = 0;
-  for (int e = 0; e < kCS; ++e) {
-    const float u = sCUB[e * kBM + r];
-    if (u >= thr) { sCUB[w * kBM + r] = u; sCK[w * kBM + r] = sCK[e * kBM + r]; ++w; }
+  for (int e = 0; e < kCSH; ++e) {
+    const float u = cub[e * kBM + r];
+    if (u >= thr) { cub[w * kBM + r] = u; ck[w * kBM + r] = ck[e * kBM + r]; ++w; }
   }
-  if (w < kCS) {
-    sCUB[w * kBM + r] = hi;
-    sCK[w * kBM + r] = (uint16_t)k;
+  if (w < kCSH) {
+    cub[w * kBM + r] = hi;
+    ck[w * kBM + r] = (uint16_t)k;
     return w + 1;
   }
   int emin = 0;
-  float umin = sCUB[r];
-  for (int e = 1; e < kCS; ++e) {
-    const float u = sCUB[e * kBM + r];
+  float umin = cub[r];
+  for (int e = 1; e < kCSH; ++e) {
+    const float u = cub[e * kBM + r];
     if (u < umin) { umin = u; emin = e; }
   }
   if (hi > umin) {
     *dropped = fmaxf(*dropped, umin);
-    sCUB[emin * kBM + r] = hi;
-    sCK[emin * kBM + r] = (uint16_t)k;
+    cub[emin * kBM + r] = hi;
+    ck[emin * kBM + r] = (uint16_t)k;
   } else {
     *dropped = fmaxf(*dropped, hi);
   }
-  return kCS;
+  return kCSH;
 }
 
-// sum_d w_d (x_d - mu_d)^2 for row n of X, in the order of the CUDA-core
-// kernels (32 partial sums over D/32 consecutive dimensions, then the
-// xor-butterfly tree), with vector loads.
-template <int D, int XT>
-__device__ __forceinline__ float exact_d2(const void* X, int64_t n, const float* mu,
-                                          const float* w, bool iso) {
+constexpr int rev5(int j) {
+  return ((j & 1) << 4) | ((j & 2) << 2) | (j & 4) | ((j & 8) >> 2) | ((j & 16) >> 4);
+}
+
+// Operands of one exact evaluation: row n of X against NC components.
+template <int NC>
+struct D2Args {
+  const void* X;
+  int64_t n;
+  const float* mu[NC];
+  const float* w[NC];   // 1/var (iso: one value)
+  float wi[NC];         // iso: the value
+  bool iso;
+};
+
+// Partial l: sum over dimensions l*D/32 .. (l+1)*D/32 - 1 of w (x - mu)^2,
+// sequential fma from 0.
+template <int D, int XT, int NC>
+__device__ __forceinline__ void d2_leaf(const D2Args<NC>& q, int l, float* out) {
   constexpr int DPL = D / 32;
-  float p[32];
-  const float wi = iso ? __ldg(w) : 0.f;
+  float xv[DPL];
+  const size_t e0 = (size_t)q.n * D + l * DPL;
+  if constexpr (DPL == 4) {
+    if constexpr (XT == GMM_F32) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(q.X) + e0));
+      xv[0] = v.x; xv[1] = v.y; xv[2] = v.z; xv[3] = v.w;
+    } else {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(q.X) + e0));
+      const uint32_t u[2] = {v.x, v.y};
 #pragma unroll
-  for (int l = 0; l < 32; ++l) {
-    float xv[DPL], mv[DPL], wv[DPL];
-    const size_t e0 = (size_t)n * D + l * DPL;
-    if constexpr (DPL == 4) {
-      if constexpr (XT == GMM_F32) {
-        const float4 q = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(X) + e0));
-        xv[0] = q.x; xv[1] = q.y; xv[2] = q.z; xv[3] = q.w;
-      } else {
-        const uint2 q = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(X) + e0));
-        const uint32_t u[2] = {q.x, q.y};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float2 f;
-          if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u[h]));
-          else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[h]));
-          xv[2 * h] = f.x; xv[2 * h + 1] = f.y;
-        }
+      for (int hh = 0; hh < 2; ++hh) {
+        float2 f;
+        if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u[hh]));
+        else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[hh]));
+        xv[2 * hh] = f.x; xv[2 * hh + 1] = f.y;
       }
-      const float4 mq = __ldg(reinterpret_cast<const float4*>(mu + l * 4));
+    }
+  } else {
+    if constexpr (XT == GMM_F32) {
+      const float2 v = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(q.X) + e0));
+      xv[0] = v.x; xv[1] = v.y;
+    } else {
+      const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const uint16_t*>(q.X) + e0));
+      float2 f;
+      if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u));
+      else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+      xv[0] = f.x; xv[1] = f.y;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    float mv[DPL], wv[DPL];
+    if constexpr (DPL == 4) {
+      const float4 mq = __ldg(reinterpret_cast<const float4*>(q.mu[c] + l * 4));
       mv[0] = mq.x; mv[1] = mq.y; mv[2] = mq.z; mv[3] = mq.w;
-      if (iso) {
-        wv[0] = wv[1] = wv[2] = wv[3] = wi;
+      if (q.iso) {
+        wv[0] = wv[1] = wv[2] = wv[3] = q.wi[c];
       } else {
-        const float4 wq = __ldg(reinterpret_cast<const float4*>(w + l * 4));
+        const float4 wq = __ldg(reinterpret_cast<const float4*>(q.w[c] + l * 4));
         wv[0] = wq.x; wv[1] = wq.y; wv[2] = wq.z; wv[3] = wq.w;
       }
     } else {
-      if constexpr (XT == GMM_F32) {
-        const float2 q = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(X) + e0));
-        xv[0] = q.x; xv[1] = q.y;
-      } else {
-        const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const uint16_t*>(X) + e0));
-        float2 f;
-        if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u));
-        else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-        xv[0] = f.x; xv[1] = f.y;
-      }
-      const float2 mq = __ldg(reinterpret_cast<const float2*>(mu + l * 2));
+      const float2 mq = __ldg(reinterpret_cast<const float2*>(q.mu[c] + l * 2));
       mv[0] = mq.x; mv[1] = mq.y;
-      if (iso) {
-        wv[0] = wv[1] = wi;
+      if (q.iso) {
+        wv[0] = wv[1] = q.wi[c];
       } else {
-        const float2 wq = __ldg(reinterpret_cast<const float2*>(w + l * 2));
+        const float2 wq = __ldg(reinterpret_cast<const float2*>(q.w[c] + l * 2));
         wv[0] = wq.x; wv[1] = wq.y;
       }
     }
@@ -232,13 +265,42 @@ __device__ __forceinline__ float exact_d2(const void* X, int64_t n, const float*
       const float t = xv[i] - mv[i];
       part = fmaf(t * t, wv[i], part);
     }
-    p[l] = part;
+    out[c] = part;
   }
+}
+
+// The pairwise tree over the 32 partials: node (LO, SZ) covers in-order
+// leaves LO .. LO+SZ-1, leaf j holding partial rev5(j), so node (0, 2) is
+// p_0 + p_16, (0, 4) is (p_0 + p_16) + (p_8 + p_24), and the root is the
+// tree p_i + p_{i+16}, then + 8, 4, 2, 1 that a warp's xor reduction forms.
+template <int D, int XT, int NC, int LO, int SZ>
+__device__ __forceinline__ void d2_tree(const D2Args<NC>& q, float* out) {
+  if constexpr (SZ == 1) {
+    d2_leaf<D, XT, NC>(q, rev5(LO), out);
+  } else {
+    float lft[NC], rgt[NC];
+    d2_tree<D, XT, NC, LO, SZ / 2>(q, lft);
+    d2_tree<D, XT, NC, LO + SZ / 2, SZ / 2>(q, rgt);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+    for (int c = 0; c < NC; ++c) out[c] = lft[c] + rgt[c];
+  }
+}
+
+// sum_d w_d (x_d - mu_d)^2 of row n against NC components, in the order
+// every log-density evaluation of the library uses: 32 partial sums over
+// D/32 consecutive dimensions (sequential fma), combined by the pairwise
+// tree above.
+template <int D, int XT, int NC>
+__device__ __forceinline__ void exact_d2(const D2Args<NC>& q, float* out) {
+  d2_tree<D, XT, NC, 0, 32>(q, out);
+}
+
+// lbm[i] for a run-time i < 8 without indexing a local array.
+__device__ __forceinline__ float pick8(const float* lbm, int i) {
+  float v = lbm[0];
 #pragma unroll
-    for (int i = 0; i < o; ++i) p[i] = p[i] + p[i + o];
-  return p[0];
+  for (int t = 1; t < 8; ++t) v = i == t ? lbm[t] : v;
+  return v;
 }
 
 template <int D, int XT, int MODE>
@@ -252,11 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   float* sRN = (float*)(sm + S::OFF_RN);
   float* sCUB = (float*)(sm + S::OFF_CUB);
   uint16_t* sCK = (uint16_t*)(sm + S::OFF_CK);
+  float* xref = (float*)(sm + S::OFF_X);  // [2][128] per half: best lower bound
+  float* xlbm = xref + 2 * kBM;           // [2][128] m-th largest lower bound (assign)
+  float* xmx = xlbm + 2 * kBM;            // [2][128] max exact log joint
+  float* xsum = xmx + 2 * kBM;            // [2][128] sum exp(l - max)
+  uint16_t* xcnt = (uint16_t*)(xsum + 2 * kBM);  // [2][128] count, 0xffff: not exact
   uint64_t* bar = (uint64_t*)(sm + S::OFF_BAR);
   uint32_t* tmem_slot = (uint32_t*)(sm + S::OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + S::OFF_MISC + 4);
   int* warp_tot = (int*)(sm + S::OFF_MISC + 16);  // [2][4] record counts per epilogue warp
-  __shared__ double ll_red[4];
+  __shared__ double ll_red[kEpiWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t ntiles = (a.N + kBM - 1) / kBM;
@@ -264,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   const int nch = a.L.tc_chunks;
   const bool resident = nch <= 2;  // parameter chunks loaded once and kept
 
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(tmem_slot, 256);
     tc::tmem_relinquish();
   }
@@ -275,12 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       tc::mbar_init(&bar[B_FULL + i], 1);
       tc::mbar_init(&bar[B_EMPTY + i], 1);
       tc::mbar_init(&bar[T_FULL + i], 1);
-      tc::mbar_init(&bar[T_EMPTY + i], 4);
+      tc::mbar_init(&bar[T_EMPTY + i], kEpiWarps);
       tc::mbar_init(&bar[TR_FULL + i], 1);
       tc::mbar_init(&bar[R_FULL + i], 4);
-      tc::mbar_init(&bar[R_FREE + i], 4);
+      tc::mbar_init(&bar[R_FREE + i], kEpiWarps);
     }
-    tc::mbar_init(&bar[EPI_SYNC], 4);
+    tc::mbar_init(&bar[EX_A], kEpiWarps);
+    tc::mbar_init(&bar[EX_B], kEpiWarps);
+    tc::mbar_init(&bar[EX_C], kEpiWarps);
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
@@ -301,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   const float* g_c = at<float>(a.prepared, a.L.off_c);
   const bool iso = a.L.cov == GMM_COV_ISO;
 
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issue + loads
     if (lane == 0 && my_tiles > 0) {
       const int64_t total = (int64_t)my_tiles * nch;
@@ -336,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           }
           tc::tc_fence_after();
           tc::mbar_arrive_expect_tx(&bar[TR_FULL + buf], S::T_BYTES);
-          tc::bulk_g2s(sT + buf * (S::T_BYTES / 4), gT + (size_t)j * 3 * kBN, S::T_BYTES,
+          tc::bulk_g2s(sT + buf * (S::T_BYTES / 4), gT + (size_t)j * kTcTrail, S::T_BYTES,
                        &bar[TR_FULL + buf]);
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
           const unsigned char* bb = sB + bbuf * S::B_BYTES;
@@ -369,25 +438,44 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         }
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= kProdWarp0) {
     // ------------------------------------------------------- producers
-    const int p = tid - 128;
+    constexpr int G = D / 8;                       // 8-coordinate groups per row
+    constexpr int WPG = XT == GMM_F32 ? 2 : 1;     // 16-byte words per group
+    constexpr int PF = XT == GMM_F32 ? (G > 8 ? 8 : G) : G;  // groups loaded ahead
+    const int p = tid - kProdWarp0 * 32;
     for (int it = 0; it < my_tiles; ++it) {
       if (warp_aborted(abort_flag)) break;
+      const int64_t tile = blockIdx.x + (int64_t)it * gridDim.x;
+      const int64_t n = tile * kBM + p;
+      const bool in = n < a.N;
+      // this tile's row, requested before the buffers are free
+      uint4 pre[PF * WPG];
+#pragma unroll
+      for (int g = 0; g < PF; ++g) {
+        if (in) load_raw8<XT>(a.X, (size_t)n * D + g * 8, pre + g * WPG);
+        else
+#pragma unroll
+          for (int i = 0; i < WPG; ++i) pre[g * WPG + i] = make_uint4(0u, 0u, 0u, 0u);
+      }
       if (it > 0 && !warp_wait(&bar[A_EMPTY], (it - 1) & 1)) { fail(); break; }
       if (it >= 2 && !warp_wait(&bar[R_FREE + (it & 1)], ((it >> 1) - 1) & 1)) {
         fail(); break;
       }
-      const int64_t tile = blockIdx.x + (int64_t)it * gridDim.x;
-      const int64_t n = tile * kBM + p;
       float rn2 = 0.f;
-#pragma unroll 4
-      for (int c8 = 0; c8 < D / 8; ++c8) {
-        float v[8];
-        if (n < a.N) load8<XT>(a.X, (size_t)n * D + c8 * 8, v);
-        else
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = 0.f;
+      for (int c8 = 0; c8 < G; ++c8) {
+        float v[8];
+        if (c8 < PF) {
+          raw_to_float8<XT>(pre + c8 * WPG, v);
+        } else {
+          uint4 w[WPG];
+          if (in) load_raw8<XT>(a.X, (size_t)n * D + c8 * 8, w);
+          else
+#pragma unroll
+            for (int i = 0; i < WPG; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
+          raw_to_float8<XT>(w, v);
+        }
         uint32_t hx[4], hq[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -414,18 +502,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     }
   } else {
     // -------------------------------------------------------- epilogue
-    const int r = tid;  // row within the tile == TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int q = warp & 3, h = warp >> 2;
+    const int r = q * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float* cub = sCUB + h * kCSH * kBM;     // this half's candidate list
+    uint16_t* ck = sCK + h * kCSH * kBM;
     double ll_acc = 0.0;
     for (int it = 0; it < my_tiles; ++it) {
       if (warp_aborted(abort_flag)) break;
       const int64_t tile = blockIdx.x + (int64_t)it * gridDim.x;
-      const int64_t n0 = tile * kBM, n = n0 + r;
+      const int64_t n = tile * kBM + r;
       const bool valid = n < a.N;
       if (!warp_wait(&bar[R_FULL + (it & 1)], (it >> 1) & 1)) { fail(); break; }
       const float rn = sRN[(it & 1) * kBM + r];
       const float rnk = kKappa * rn;
-      float ref = -INFINITY;  // lower bound of the best log joint of this point
+      float ref = -INFINITY;  // lower bound of the best log joint (this half)
       float dropped = -INFINITY;
       float lbm[8];           // assign: the m largest lower bounds seen
 #pragma unroll
@@ -440,51 +531,59 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           fail(); ok = false; break;
         }
         tc::tc_fence_after();
-        const float* tsc = sT + buf * (S::T_BYTES / 4);
+        const float* tsc = sT + buf * (S::T_BYTES / 4) + h * kHalf;
         const float* tcn = tsc + kBN;
-        const float* tbias = tsc + 2 * kBN;
-        const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN);
-        // sweep 1: the chunk's best screened value and its lower bound
+        const float* tbl = tsc + 2 * kBN;   // bias - delta
+        const float* tbh = tsc + 3 * kBN;   // bias + delta
+        const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
+        // sweep 1: the best lower bound of the half-chunk,
+        //   lo = (v - kRel |v|) s + (bias - delta) - rnk |b|
         float best = -INFINITY;
-        int bidx = 0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-          float v[32];
-          tc::tmem_ld32(tcol + (uint32_t)c0, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float lt = fmaf(v[i], tsc[c0 + i], tbias[c0 + i]);
-            if (lt > best) { best = lt; bidx = c0 + i; }
-          }
-        }
-        if (best > -INFINITY)
-          ref = fmaxf(ref, best - fmaf(rnk, tcn[bidx], 1e-3f + 1e-6f * fabsf(best)));
-        // sweep 2: every component whose upper bound reaches within T of ref
-        const float thr_t = ref - kT;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-          float v[32];
-          tc::tmem_ld32(tcol + (uint32_t)c0, v);
+        for (int c0 = 0; c0 < kHalf; c0 += 32) {
+          uint32_t u[32];
+          tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+          tc::tmem_wait32(u);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int kk = c0 + i;
-            const float lt = fmaf(v[i], tsc[kk], tbias[kk]);
-            const float beta = fmaf(rnk, tcn[kk], 1e-3f + 1e-6f * fabsf(lt));
-            const float hi = lt + beta;
-            float thr = thr_t;
+            const float v = __uint_as_float(u[i]);
+            const float lo = fmaf(fmaf(-kRel, fabsf(v), v), tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
+            best = fmaxf(best, lo);
+          }
+        }
+        ref = fmaxf(ref, best);
+        // sweep 2: every component whose upper bound
+        //   hi = (v + kRel |v|) s + (bias + delta) + rnk |b|
+        // reaches the window below ref (or, assign, the m-th lower bound)
+        float thr = ref - kT;
+        if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, pick8(lbm, a.m - 1));
+#pragma unroll 1
+        for (int c0 = 0; c0 < kHalf; c0 += 32) {
+          uint32_t u[32];
+          tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+          tc::tmem_wait32(u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int kk = c0 + i;
+            const float v = __uint_as_float(u[i]);
             if constexpr (MODE == MODE_ASSIGN) {
-              const float lo = lt - beta;
-              if (lo > lbm[a.m - 1]) insert_lower_bound(lbm, a.m, lo);
-              thr = fminf(thr, lbm[a.m - 1]);
+              const float lo = fmaf(fmaf(-kRel, fabsf(v), v), tsc[kk],
+                                    fmaf(-rnk, tcn[kk], tbl[kk]));
+              if (lo > pick8(lbm, a.m - 1)) {
+                insert_lower_bound(lbm, a.m, lo);
+                thr = fminf(ref - kT, pick8(lbm, a.m - 1));
+              }
             }
+            const float hi = fmaf(fmaf(kRel, fabsf(v), v), tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
             if (hi >= thr && valid) {
-              const int k = j * kBN + kk;
-              if (cnt < kCS) {
-                sCUB[cnt * kBM + r] = hi;
-                sCK[cnt * kBM + r] = (uint16_t)k;
+              const int k = j * kBN + h * kHalf + kk;
+              if (cnt < kCSH) {
+                cub[cnt * kBM + r] = hi;
+                ck[cnt * kBM + r] = (uint16_t)k;
                 ++cnt;
               } else {
-                cnt = insert_full(sCUB, sCK, r, k, hi, thr, &dropped);
+                cnt = insert_full(cub, ck, r, k, hi, thr, &dropped);
               }
             }
           }
@@ -496,102 +595,161 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[R_FREE + (it & 1)]);
       if (!ok) break;
-      // final window and compaction
-      float thr = ref - kT;
-      if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, lbm[a.m - 1]);
+
+      // exchange A: the window of the point from both halves
+      xref[h * kBM + r] = ref;
+      if constexpr (MODE == MODE_ASSIGN) xlbm[h * kBM + r] = pick8(lbm, a.m - 1);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
+      if (!warp_wait(&bar[EX_A], it & 1)) { fail(); break; }
+      float thr = fmaxf(xref[r], xref[kBM + r]) - kT;
+      // assign: at least m components have a lower bound >= the larger of
+      // the two halves' m-th largest, so nothing below it can be in the top m
+      if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, fmaxf(xlbm[r], xlbm[kBM + r]));
       {
         int w = 0;
         for (int e = 0; e < cnt; ++e) {
-          const float u = sCUB[e * kBM + r];
-          if (u >= thr) { sCUB[w * kBM + r] = u; sCK[w * kBM + r] = sCK[e * kBM + r]; ++w; }
+          const float u = cub[e * kBM + r];
+          if (u >= thr) { cub[w * kBM + r] = u; ck[w * kBM + r] = ck[e * kBM + r]; ++w; }
         }
         cnt = w;
       }
-      const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
+      const bool mine = valid && isfinite(rn) && !(dropped >= thr);
+      // exact log joints of this half's candidates (same arithmetic as the
+      // CUDA-core kernels), two at a time
+      float mx = -INFINITY, ssum = 0.f;
+      if (mine && cnt > 0) {
+        int e = 0;
+        for (; e + 1 < cnt; e += 2) {
+          const int k0 = ck[e * kBM + r], k1 = ck[(e + 1) * kBM + r];
+          D2Args<2> qa;
+          qa.X = a.X; qa.n = n; qa.iso = iso;
+          qa.mu[0] = g_mu + (size_t)k0 * D;
+          qa.mu[1] = g_mu + (size_t)k1 * D;
+          qa.w[0] = iso ? g_prec + k0 : g_prec + (size_t)k0 * D;
+          qa.w[1] = iso ? g_prec + k1 : g_prec + (size_t)k1 * D;
+          qa.wi[0] = iso ? __ldg(qa.w[0]) : 0.f;
+          qa.wi[1] = iso ? __ldg(qa.w[1]) : 0.f;
+          float d2[2];
+          exact_d2<D, XT, 2>(qa, d2);
+          const float l0 = __ldg(g_c + k0) - 0.5f * d2[0];
+          const float l1 = __ldg(g_c + k1) - 0.5f * d2[1];
+          cub[e * kBM + r] = l0;
+          cub[(e + 1) * kBM + r] = l1;
+          mx = fmaxf(mx, fmaxf(l0, l1));
+        }
+        if (e < cnt) {
+          const int k0 = ck[e * kBM + r];
+          D2Args<1> qa;
+          qa.X = a.X; qa.n = n; qa.iso = iso;
+          qa.mu[0] = g_mu + (size_t)k0 * D;
+          qa.w[0] = iso ? g_prec + k0 : g_prec + (size_t)k0 * D;
+          qa.wi[0] = iso ? __ldg(qa.w[0]) : 0.f;
+          float d2[1];
+          exact_d2<D, XT, 1>(qa, d2);
+          const float l0 = __ldg(g_c + k0) - 0.5f * d2[0];
+          cub[e * kBM + r] = l0;
+          mx = fmaxf(mx, l0);
+        }
+        for (int e2 = 0; e2 < cnt; ++e2) ssum += expf(cub[e2 * kBM + r] - mx);
+      }
+      // exchange B: both halves' partial log-sum-exp
+      xmx[h * kBM + r] = mx;
+      xsum[h * kBM + r] = ssum;
+      xcnt[h * kBM + r] = mine ? (uint16_t)cnt : (uint16_t)0xffff;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[EX_B]);
+      if (!warp_wait(&bar[EX_B], it & 1)) { fail(); break; }
+      const int c0 = xcnt[r], c1 = xcnt[kBM + r];
+      const bool exact = c0 != 0xffff && c1 != 0xffff && c0 + c1 > 0;
       float lse = 0.f;
       if (exact) {
-        // exact log joints of the kept components (same arithmetic as the
-        // CUDA-core kernels), then the log-sum-exp over them
-        float mx = -INFINITY;
-        for (int e = 0; e < cnt; ++e) {
-          const int k = sCK[e * kBM + r];
-          const float d2 = exact_d2<D, XT>(a.X, n, g_mu + (size_t)k * D,
-                                           iso ? g_prec + k : g_prec + (size_t)k * D, iso);
-          const float l = __ldg(g_c + k) - 0.5f * d2;
-          sCUB[e * kBM + r] = l;
-          mx = fmaxf(mx, l);
-        }
-        float s = 0.f;
-        for (int e = 0; e < cnt; ++e) s += expf(sCUB[e * kBM + r] - mx);
-        lse = mx + logf(s);
+        const float m0 = xmx[r], m1 = xmx[kBM + r];
+        const float M = fmaxf(m0, m1);
+        float sum = 0.f;
+        if (c0 > 0 && m0 > -INFINITY) sum += xsum[r] * expf(m0 - M);
+        if (c1 > 0 && m1 > -INFINITY) sum += xsum[kBM + r] * expf(m1 - M);
+        lse = M + logf(sum);
       }
       if constexpr (MODE == MODE_EM) {
-        // responsibility records of this tile, in row order: an exclusive
-        // prefix sum of the rows' candidate counts over the 128 epilogue
-        // threads.  Rows past the record capacity go to the row list.
-        const int my = exact ? cnt : 0;
+        // responsibility records of this tile, in row order (half 0's
+        // components, then half 1's): an exclusive prefix sum of the rows'
+        // counts over the 128 rows.  Rows past the capacity go to the row list.
+        const int my = exact ? c0 + c1 : 0;
         int incl = my;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int v = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += v;
         }
-        int* tot = warp_tot + (it & 1) * 4;
-        if (lane == 31) tot[warp] = incl;
+        int* tot = warp_tot + h * 4;
+        if (lane == 31) tot[q] = incl;
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar[EPI_SYNC]);
-        if (!warp_wait(&bar[EPI_SYNC], it & 1)) { fail(); break; }
+        if (lane == 0) tc::mbar_arrive(&bar[EX_C]);
+        if (!warp_wait(&bar[EX_C], it & 1)) { fail(); break; }
         int off = incl - my, all = 0;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const int t = tot[w];
-          if (w < warp) off += t;
+          if (w < q) off += t;
           all += t;
         }
-        const int64_t tl = tile;  // tile index within this launch
-        const bool fits = exact && off + cnt <= a.rec_cap;
-        if (exact && off <= a.rec_cap && off + cnt > a.rec_cap) a.tile_cnt[tl] = (uint32_t)off;
-        if (r == kBM - 1 && all <= a.rec_cap) a.tile_cnt[tl] = (uint32_t)all;
+        const bool fits = exact && off + my <= a.rec_cap;
+        if (h == 0) {
+          if (exact && off <= a.rec_cap && off + my > a.rec_cap) a.tile_cnt[tile] = (uint32_t)off;
+          if (r == kBM - 1 && all <= a.rec_cap) a.tile_cnt[tile] = (uint32_t)all;
+          if (fits) {
+            if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+            if (a.lse) a.lse[n] = lse;
+            ll_acc += (double)lse;
+          }
+          const unsigned fbm = __ballot_sync(0xffffffffu, valid && !fits);
+          if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
+        }
         if (fits) {
-          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
-          if (a.lse) a.lse[n] = lse;
-          ll_acc += (double)lse;
-          uint2* out = a.recs + (size_t)tl * a.rec_cap + off;
-          for (int e = 0; e < cnt; ++e) {
-            const uint32_t k = sCK[e * kBM + r];
-            const float g = expf(sCUB[e * kBM + r] - lse);
-            out[e] = make_uint2((k << 7) | (uint32_t)r, __float_as_uint(g));
+          const int mc = h == 0 ? c0 : c1;
+          uint2* out = a.recs + (size_t)tile * a.rec_cap + off + (h == 0 ? 0 : c0);
+          for (int e = 0; e < mc; ++e) {
+            const uint32_t k = ck[e * kBM + r];
+            const float gm = expf(cub[e * kBM + r] - lse);
+            out[e] = make_uint2((k << 7) | (uint32_t)r, __float_as_uint(gm));
           }
         }
-        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !fits);
-        if (lane == 0) a.fb_mask[tile * 4 + warp] = fbm;
       } else {
-        if (exact) {
-          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
-          if (a.lse) a.lse[n] = lse;
-          // top-m by exact value, ties to the lower component
-          uint32_t taken = 0;
-          for (int t = 0; t < a.m; ++t) {
-            int best = -1, bk = 0x7fffffff;
-            float bv = -INFINITY;
-            for (int e = 0; e < cnt; ++e) {
-              if (taken & (1u << e)) continue;
-              const float v = sCUB[e * kBM + r];
-              const int k = sCK[e * kBM + r];
-              if (best < 0 || v > bv || (v == bv && k < bk)) { best = e; bv = v; bk = k; }
+        if (h == 0) {
+          if (exact) {
+            if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+            if (a.lse) a.lse[n] = lse;
+            // top-m over both halves' exact values, ties to the lower component
+            uint32_t taken = 0;
+            for (int t = 0; t < a.m; ++t) {
+              int best = -1, bk = 0x7fffffff;
+              float bv = -INFINITY;
+              for (int e = 0; e < c0 + c1; ++e) {
+                if (taken & (1u << e)) continue;
+                const int hh = e < c0 ? 0 : kCSH;
+                const int ee = e < c0 ? e : e - c0;
+                const float v = sCUB[(hh + ee) * kBM + r];
+                const int k = sCK[(hh + ee) * kBM + r];
+                if (best < 0 || v > bv || (v == bv && k < bk)) { best = e; bv = v; bk = k; }
+              }
+              if (best < 0) {
+                a.ids[n * a.m + t] = -1;
+                a.gamma[n * a.m + t] = 0.f;
+                continue;
+              }
+              taken |= 1u << best;
+              a.ids[n * a.m + t] = bk;
+              a.gamma[n * a.m + t] = bv == -INFINITY ? 0.f : expf(bv - lse);
             }
-            if (best < 0) {
-              a.ids[n * a.m + t] = -1;
-              a.gamma[n * a.m + t] = 0.f;
-              continue;
-            }
-            taken |= 1u << best;
-            a.ids[n * a.m + t] = bk;
-            a.gamma[n * a.m + t] = bv == -INFINITY ? 0.f : expf(bv - lse);
           }
+          const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
+          if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
         }
-        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
-        if (lane == 0) a.fb_mask[tile * 4 + warp] = fbm;
+        // half 1's list stays untouched until half 0 has read it
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[EX_C]);
+        if (!warp_wait(&bar[EX_C], it & 1)) { fail(); break; }
       }
       __syncwarp();
     }
@@ -606,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     if (tid == 0 && a.ll_part)
       a.ll_part[blockIdx.x] = ((ll_red[0] + ll_red[1]) + ll_red[2]) + ll_red[3];
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base, 256);
   }
