@@ -188,10 +188,6 @@ __device__ __noinline__ int insert_full(float* cub, uint16_t* ck, int r, int k, 
   return kCSH;
 }
 
-constexpr int rev5(int j) {
-  return ((j & 1) << 4) | ((j & 2) << 2) | (j & 4) | ((j & 8) >> 2) | ((j & 16) >> 4);
-}
-
 // Operands of one exact evaluation: row n of X against NC components.
 template <int NC>
 struct D2Args {
@@ -269,30 +265,23 @@ __device__ __forceinline__ void d2_leaf(const D2Args<NC>& q, int l, float* out) 
   }
 }
 
-// The pairwise tree over the 32 partials: node (LO, SZ) covers in-order
-// leaves LO .. LO+SZ-1, leaf j holding partial rev5(j), so node (0, 2) is
-// p_0 + p_16, (0, 4) is (p_0 + p_16) + (p_8 + p_24), and the root is the
-// tree p_i + p_{i+16}, then + 8, 4, 2, 1 that a warp's xor reduction forms.
-template <int D, int XT, int NC, int LO, int SZ>
-__device__ __forceinline__ void d2_tree(const D2Args<NC>& q, float* out) {
-  if constexpr (SZ == 1) {
-    d2_leaf<D, XT, NC>(q, rev5(LO), out);
-  } else {
-    float lft[NC], rgt[NC];
-    d2_tree<D, XT, NC, LO, SZ / 2>(q, lft);
-    d2_tree<D, XT, NC, LO + SZ / 2, SZ / 2>(q, rgt);
-#pragma unroll
-    for (int c = 0; c < NC; ++c) out[c] = lft[c] + rgt[c];
-  }
-}
-
-// sum_d w_d (x_d - mu_d)^2 of row n against NC components, in the order
-// every log-density evaluation of the library uses: 32 partial sums over
-// D/32 consecutive dimensions (sequential fma), combined by the pairwise
-// tree above.
-template <int D, int XT, int NC>
-__device__ __forceinline__ void exact_d2(const D2Args<NC>& q, float* out) {
-  d2_tree<D, XT, NC, 0, 32>(q, out);
+// Lane l's partial of the exact evaluation of row n against one component:
+// sum over dimensions l*D/32 .. (l+1)*D/32 - 1 of w (x - mu)^2 (sequential
+// fma from 0).  The xor reduction over the warp then combines the partials
+// in the pairwise tree order of every other evaluation (p_i + p_{i+16},
+// then + 8, 4, 2, 1; fp32 addition is commutative, so each lane ends with
+// the same bits).
+template <int D, int XT>
+__device__ __forceinline__ float lane_partial(const void* X, int64_t n, const float* mu,
+                                              const float* w, bool iso, int lane) {
+  D2Args<1> q;
+  q.X = X; q.n = n; q.iso = iso;
+  q.mu[0] = mu;
+  q.w[0] = w;
+  q.wi[0] = iso ? __ldg(w) : 0.f;
+  float out;
+  d2_leaf<D, XT, 1>(q, lane, &out);
+  return out;
 }
 
 // lbm[i] for a run-time i < 8 without indexing a local array.
@@ -315,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   float* sCUB = (float*)(sm + S::OFF_CUB);
   uint16_t* sCK = (uint16_t*)(sm + S::OFF_CK);
   float* xref = (float*)(sm + S::OFF_X);  // [2][128] per half: best lower bound
+  volatile float* xref_v = xref;
   float* xlbm = xref + 2 * kBM;           // [2][128] m-th largest lower bound (assign)
   float* xmx = xlbm + 2 * kBM;            // [2][128] max exact log joint
   float* xsum = xmx + 2 * kBM;            // [2][128] sum exp(l - max)
@@ -322,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   uint64_t* bar = (uint64_t*)(sm + S::OFF_BAR);
   uint32_t* tmem_slot = (uint32_t*)(sm + S::OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + S::OFF_MISC + 4);
-  int* warp_tot = (int*)(sm + S::OFF_MISC + 16);  // [2][4] record counts per epilogue warp
   __shared__ double ll_red[kEpiWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -351,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     tc::mbar_init(&bar[EX_B], kEpiWarps);
     tc::mbar_init(&bar[EX_C], kEpiWarps);
     *abort_flag = 0;
+    for (int i = 0; i < 2 * kBM; ++i) xref[i] = -INFINITY;
     tc::mbar_fence_init();
   }
   tc::tc_fence_before();
@@ -553,6 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           }
         }
         ref = fmaxf(ref, best);
+        // share the bound with the partner warp (the other column half of
+        // the same rows): whatever value is there is a lower bound of this
+        // point's best log joint, from this tile (-inf until published)
+        xref_v[h * kBM + r] = ref;
+        ref = fmaxf(ref, xref_v[(1 - h) * kBM + r]);
         // sweep 2: every component whose upper bound
         //   hi = (v + kRel |v|) s + (bias + delta) + rnk |b|
         // reaches the window below ref (or, assign, the m-th lower bound)
@@ -597,12 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       if (!ok) break;
 
       // exchange A: the window of the point from both halves
-      xref[h * kBM + r] = ref;
+      xref_v[h * kBM + r] = ref;
       if constexpr (MODE == MODE_ASSIGN) xlbm[h * kBM + r] = pick8(lbm, a.m - 1);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
       if (!warp_wait(&bar[EX_A], it & 1)) { fail(); break; }
-      float thr = fmaxf(xref[r], xref[kBM + r]) - kT;
+      float thr = fmaxf(xref_v[r], xref_v[kBM + r]) - kT;
       // assign: at least m components have a lower bound >= the larger of
       // the two halves' m-th largest, so nothing below it can be in the top m
       if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, fmaxf(xlbm[r], xlbm[kBM + r]));
@@ -616,42 +611,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       }
       const bool mine = valid && isfinite(rn) && !(dropped >= thr);
       // exact log joints of this half's candidates (same arithmetic as the
-      // CUDA-core kernels), two at a time
+      // CUDA-core kernels), warp-cooperatively: the warp's (row, candidate)
+      // pairs are numbered by an exclusive scan of the counts and taken four
+      // at a time, lane l computing partial l of each
+      {
+        const int mycnt = mine ? cnt : 0;
+        int incl = mycnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const int excl = incl - mycnt;
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        for (int p0 = 0; p0 < total; p0 += 4) {
+          float part[4];
+          int slot[4], kk4[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int pidx = p0 + t;
+            const bool live = pidx < total;
+            // owner lane of pair pidx: the last lane whose excl <= pidx
+            const int owner = __popc(__ballot_sync(0xffffffffu, excl <= pidx)) - 1;
+            const int e = pidx - __shfl_sync(0xffffffffu, excl, owner);
+            const int rr = q * 32 + owner;
+            const int k = live ? (int)ck[e * kBM + rr] : 0;
+            slot[t] = live ? e * kBM + rr : -1;
+            kk4[t] = k;
+            part[t] = live ? lane_partial<D, XT>(a.X, tile * kBM + rr, g_mu + (size_t)k * D,
+                                                 iso ? g_prec + k : g_prec + (size_t)k * D,
+                                                 iso, lane)
+                           : 0.f;
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) part[t] += __shfl_xor_sync(0xffffffffu, part[t], o);
+          if (lane < 4) {
+            float pv = part[0];
+            int sl = slot[0], k = kk4[0];
+#pragma unroll
+            for (int t = 1; t < 4; ++t)
+              if (lane == t) { pv = part[t]; sl = slot[t]; k = kk4[t]; }
+            if (sl >= 0) cub[sl] = __ldg(g_c + k) - 0.5f * pv;
+          }
+        }
+        __syncwarp();
+      }
       float mx = -INFINITY, ssum = 0.f;
       if (mine && cnt > 0) {
-        int e = 0;
-        for (; e + 1 < cnt; e += 2) {
-          const int k0 = ck[e * kBM + r], k1 = ck[(e + 1) * kBM + r];
-          D2Args<2> qa;
-          qa.X = a.X; qa.n = n; qa.iso = iso;
-          qa.mu[0] = g_mu + (size_t)k0 * D;
-          qa.mu[1] = g_mu + (size_t)k1 * D;
-          qa.w[0] = iso ? g_prec + k0 : g_prec + (size_t)k0 * D;
-          qa.w[1] = iso ? g_prec + k1 : g_prec + (size_t)k1 * D;
-          qa.wi[0] = iso ? __ldg(qa.w[0]) : 0.f;
-          qa.wi[1] = iso ? __ldg(qa.w[1]) : 0.f;
-          float d2[2];
-          exact_d2<D, XT, 2>(qa, d2);
-          const float l0 = __ldg(g_c + k0) - 0.5f * d2[0];
-          const float l1 = __ldg(g_c + k1) - 0.5f * d2[1];
-          cub[e * kBM + r] = l0;
-          cub[(e + 1) * kBM + r] = l1;
-          mx = fmaxf(mx, fmaxf(l0, l1));
-        }
-        if (e < cnt) {
-          const int k0 = ck[e * kBM + r];
-          D2Args<1> qa;
-          qa.X = a.X; qa.n = n; qa.iso = iso;
-          qa.mu[0] = g_mu + (size_t)k0 * D;
-          qa.w[0] = iso ? g_prec + k0 : g_prec + (size_t)k0 * D;
-          qa.wi[0] = iso ? __ldg(qa.w[0]) : 0.f;
-          float d2[1];
-          exact_d2<D, XT, 1>(qa, d2);
-          const float l0 = __ldg(g_c + k0) - 0.5f * d2[0];
-          cub[e * kBM + r] = l0;
-          mx = fmaxf(mx, l0);
-        }
-        for (int e2 = 0; e2 < cnt; ++e2) ssum += expf(cub[e2 * kBM + r] - mx);
+        for (int e = 0; e < cnt; ++e) mx = fmaxf(mx, cub[e * kBM + r]);
+        for (int e = 0; e < cnt; ++e) ssum += expf(cub[e * kBM + r] - mx);
       }
       // exchange B: both halves' partial log-sum-exp
       xmx[h * kBM + r] = mx;
@@ -660,6 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[EX_B]);
       if (!warp_wait(&bar[EX_B], it & 1)) { fail(); break; }
+      // both halves have read this tile's bounds: clear for the next tile
+      xref_v[h * kBM + r] = -INFINITY;
       const int c0 = xcnt[r], c1 = xcnt[kBM + r];
       const bool exact = c0 != 0xffff && c1 != 0xffff && c0 + c1 > 0;
       float lse = 0.f;
@@ -676,24 +688,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         // components, then half 1's): an exclusive prefix sum of the rows'
         // counts over the 128 rows.  Rows past the capacity go to the row list.
         const int my = exact ? c0 + c1 : 0;
-        int incl = my;
+        // every warp reads all 128 rows' counts (lane: rows 4 lane .. 4 lane + 3)
+        int rc[4], tsum = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int rr = lane * 4 + t;
+          const int a0 = xcnt[rr], a1 = xcnt[kBM + rr];
+          rc[t] = (a0 != 0xffff && a1 != 0xffff) ? a0 + a1 : 0;
+          tsum += rc[t];
+        }
+        int incl = tsum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int v = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += v;
         }
-        int* tot = warp_tot + h * 4;
-        if (lane == 31) tot[q] = incl;
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar[EX_C]);
-        if (!warp_wait(&bar[EX_C], it & 1)) { fail(); break; }
-        int off = incl - my, all = 0;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int t = tot[w];
-          if (w < q) off += t;
-          all += t;
-        }
+        const int all = __shfl_sync(0xffffffffu, incl, 31);
+        // exclusive offset of row r = prefix of its group of four + earlier rows in it
+        const int grp = r >> 2;
+        int off = __shfl_sync(0xffffffffu, incl - tsum, grp);
+        const int r0c = __shfl_sync(0xffffffffu, rc[0], grp);
+        const int r1c = __shfl_sync(0xffffffffu, rc[1], grp);
+        const int r2c = __shfl_sync(0xffffffffu, rc[2], grp);
+        const int within = r & 3;
+        off += (within > 0 ? r0c : 0) + (within > 1 ? r1c : 0) + (within > 2 ? r2c : 0);
         const bool fits = exact && off + my <= a.rec_cap;
         if (h == 0) {
           if (exact && off <= a.rec_cap && off + my > a.rec_cap) a.tile_cnt[tile] = (uint32_t)off;
