@@ -34,10 +34,11 @@ cudaError_t simt_stats_rows(const void* X, int xdtype, int64_t N, int D, int K, 
                             const void* prepared, const float* lse, int parts, double* part,
                             int accumulate, const uint32_t* rows, const uint32_t* row_count,
                             cudaStream_t s);
-int sparse_stats_parts(int D, int K);
+size_t sparse_stats_ws_bytes(int64_t rows, int D, int K, int rec_cap);
+bool sparse_stats_supported(int K);
 cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
                          int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
-                         int parts, double* part, int accumulate, cudaStream_t s);
+                         void* sws, double* part, int accumulate, cudaStream_t s);
 int simt_stat_chunk(int D, int cov);
 cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
                          const float* centre, const int32_t* prep_flags, float var_floor,
@@ -75,15 +76,17 @@ int stat_parts(int64_t N, int D, int K, int cov) {
 
 struct WsLayout {
   size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_fb,
-      off_fbm, off_rec, off_tcnt, off_stage, bytes;
+      off_fbm, off_rec, off_tcnt, off_sws, off_stage, bytes;
   int parts;          // statistics partials of the CUDA-core path
-  int sp_parts;       // tensor-core path: partials of the record kernel ...
+  int sp_parts;       // tensor-core path: the records' partial (1) ...
   int lp_parts;       // ... followed by those of the row-list pass
   int64_t lse_rows;
 };
 
-bool use_tc(int D, int cov, const gmm_opts& o) {
-  return tc_eligible(D, cov) && !(o.flags & GMM_OPT_CUDA_CORES);
+// The tensor-core E-step of an EM iteration (screening + statistics from
+// its records).
+bool use_tc(int D, int K, int cov, const gmm_opts& o) {
+  return tc_eligible(D, cov) && sparse_stats_supported(K) && !(o.flags & GMM_OPT_CUDA_CORES);
 }
 
 // rows: rows processed per launch (N, or the chunk size of the host path);
@@ -107,7 +110,7 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   int slots = W.parts;
   const bool tc = tc_eligible(D, cov);
   if (tc) {
-    W.sp_parts = sparse_stats_parts(D, K);
+    W.sp_parts = 1;
     const int kc = simt_stat_chunk(D, cov);
     const int chunks = (K + kc - 1) / kc;
     W.lp_parts = (kListGrid + chunks - 1) / chunks;
@@ -121,6 +124,7 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_fbm = o;    o = align_up(o + sizeof(uint32_t) * 4 * slab_tiles);
   W.off_rec = o;    o = align_up(o + sizeof(uint2) * slab_tiles * kRecCap);
   W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * slab_tiles);
+  W.off_sws = o;    o = align_up(o + (tc ? sparse_stats_ws_bytes(slab, D, K, kRecCap) : 0));
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
@@ -230,9 +234,9 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
         GMM_TRY(launch_ll_finalize(llp, g1 + kListGrid, at<double>(ws, W.off_ll), acc, s));
       }
       {
-        GMM_PROF("sparse_stats_kernel");
-        GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, tcnt, recs, kRecCap, W.sp_parts,
-                             part, acc, s));
+        GMM_PROF("sparse_stats");
+        GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, tcnt, recs, kRecCap,
+                             at<char>(ws, W.off_sws), part, acc, s));
       }
       {
         GMM_PROF("stats_rows_kernel");
@@ -384,11 +388,11 @@ gmm_status gmm_em_step(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
     GMM_TRY(launch_prepare(params, D, K, cov, o.ridge_rel, prep, st, s));
   }
   float* lse = lse_dev ? lse_dev : at<float>(ws, W.off_lse);
-  gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, 0, use_tc(D, cov, o), s);
+  gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, 0, use_tc(D, K, cov, o), s);
   if (r != GMM_OK) return r;
   {
     GMM_PROF("mstep_kernel");
-    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), mstep_parts(W, use_tc(D, cov, o)), N, D, K, cov,
+    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), mstep_parts(W, use_tc(D, K, cov, o)), N, D, K, cov,
                          at<float>(prep, PL.off_mu), at<int32_t>(prep, PL.off_flags), o.var_floor,
                          o.min_s0, params, flags_dev ? flags_dev : at<int32_t>(ws, W.off_flags),
                          s));
@@ -441,13 +445,13 @@ gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int
     GMM_TRY(cudaEventRecord(res->copied[b], res->copy));
     GMM_TRY(cudaStreamWaitEvent(s, res->copied[b], 0));
     gmm_status r = estep_rows(stage[b], xdtype, rn, D, K, cov, W, ws, at<float>(ws, W.off_lse),
-                              ci > 0, use_tc(D, cov, o), s);
+                              ci > 0, use_tc(D, K, cov, o), s);
     if (r != GMM_OK) return r;
     GMM_TRY(cudaEventRecord(res->consumed[b], s));
   }
   {
     GMM_PROF("mstep_kernel");
-    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), mstep_parts(W, use_tc(D, cov, o)), N, D, K, cov,
+    GMM_TRY(launch_mstep(at<double>(ws, W.off_part), mstep_parts(W, use_tc(D, K, cov, o)), N, D, K, cov,
                          at<float>(prep, PL.off_mu), at<int32_t>(prep, PL.off_flags), o.var_floor,
                          o.min_s0, params, flags_dev ? flags_dev : at<int32_t>(ws, W.off_flags),
                          s));

@@ -3,16 +3,23 @@
 //
 // The screening kernel writes, per 128-point tile, the (component, point,
 // gamma) of every pair it evaluated exactly, in point order.  All other
-// pairs carry less than 4.3e-18 of their point's responsibility.  This
-// kernel turns the records into per-block statistics without an N x K
-// matrix: a block owns one slice of 8192 / D components (its accumulators,
-// slice x (1 + 2D) fp32, live in shared memory) and one range of tiles; warp w
-// accumulates the records of the components k with k % 8 == w, in record
-// order, so the sums are the same on every run.  Moments are taken about the
-// component's input mean c_k (y = x - c_k); accumulators are flushed into fp64
-// per-block partials every kFlushTiles tiles, and at the end the second
-// moment is moved to the block's own weighted mean, giving the
-// [S0 | S1 about c | M2 about the block mean] partials the M-step merges.
+// pairs carry less than 4.3e-18 of their point's responsibility.  The
+// statistics come from the records without an N x K matrix, in five steps:
+//   count    records per (component, block of kTPB tiles), in shared memory
+//   scan     exclusive offsets over (component, block), the start of each
+//            component's records and of its chunks of kCH records
+//   scatter  each record to its component's list, in point order (a warp
+//            walks its block's records 32 at a time; __match_any_sync ranks
+//            records of the same component, so the order is fixed)
+//   reduce   one warp per chunk: gathers the chunk's rows of X (eight in
+//            flight), accumulates g, g y, g y^2 with y = x - c_k about the
+//            component's input mean c_k (lane l: dimensions l*D/32 ..
+//            (l+1)*D/32 - 1) and writes the chunk's fp32 sums
+//   merge    one warp per component: adds its chunks in fp64 in order and
+//            writes [S0 | S1 about c | M2 about the mean], the partial the
+//            M-step merges (continuing the partial of an earlier call when
+//            accumulating over slabs or chunks of host data).
+// Every sum is taken in a fixed order, so results are the same on every run.
 #include <math.h>
 
 #include "gmm_internal.cuh"
@@ -20,168 +27,346 @@
 namespace gmm {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kFlushTiles = 16;   // fp32 accumulation span (2048 points)
+constexpr int kTile = 128;       // points per record tile
+constexpr int kTPB = 32;         // tiles per counting / scattering block
+constexpr int kCH = 512;         // records per reduction chunk
+constexpr int kScanThreads = 1024;
 
-// Components per block: 64 for D = 128, 128 for D = 64 (about 100 KB of
-// shared memory, two blocks per SM).
-template <int D>
-constexpr int slice_of() { return 8192 / D; }
+// Shared-memory counters limit the component count of this path.
+constexpr int kMaxSparseK = 16384;
 
-// records: uint2 {(k << 7) | row_in_tile, bits of gamma}.
-template <int D, int XT>
-__global__ void __launch_bounds__(kThreads)
-sparse_stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restrict__ prepared,
-                    PreparedLayout L, const uint32_t* __restrict__ tile_cnt,
-                    const uint2* __restrict__ recs, int rec_cap, int64_t ntiles,
-                    int64_t tiles_per_part, double* __restrict__ part, int accumulate) {
-  constexpr int F = 1 + 2 * D;
-  constexpr int DPL = D / 32;
-  constexpr int kSlice = slice_of<D>();
-  extern __shared__ float sm[];
-  float* acc = sm;                       // [kSlice][F]
-  float* cent = acc + kSlice * F;        // [kSlice][D]
-  uint2* srec = (uint2*)(cent + kSlice * D);  // [rec_cap]
+struct SparseLayout {
+  int64_t ntiles, nb, max_recs, max_chunks;
+  size_t off_counts, off_cstart, off_kstart, off_sorted, off_cpart, bytes;
+  static SparseLayout make(int64_t rows, int D, int K, int rec_cap) {
+    SparseLayout S;
+    S.ntiles = (rows + kTile - 1) / kTile;
+    S.nb = (S.ntiles + kTPB - 1) / kTPB;
+    S.max_recs = S.ntiles * rec_cap;
+    S.max_chunks = (S.max_recs + kCH - 1) / kCH + K;
+    size_t o = 0;
+    S.off_counts = o; o = align_up(o + sizeof(uint32_t) * (size_t)K * S.nb);
+    S.off_cstart = o; o = align_up(o + sizeof(uint32_t) * (size_t)(K + 1));
+    S.off_kstart = o; o = align_up(o + sizeof(uint32_t) * (size_t)(K + 1));
+    S.off_sorted = o; o = align_up(o + sizeof(uint2) * (size_t)S.max_recs);
+    S.off_cpart = o;  o = align_up(o + sizeof(float) * (size_t)S.max_chunks * (1 + 2 * D));
+    S.bytes = o;
+    return S;
+  }
+};
 
-  const int s = blockIdx.x;              // component slice
-  const int64_t p = blockIdx.y;          // tile partition
-  const int k0 = s * kSlice;
-  const int kn = min(kSlice, K - k0);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float* g_mu = at<float>(prepared, L.off_mu);
-  for (int i = tid; i < kSlice * D; i += kThreads)
-    cent[i] = i < kn * D ? g_mu[(size_t)k0 * D + i] : 0.f;
-  for (int i = tid; i < kSlice * F; i += kThreads) acc[i] = 0.f;
-  double* out = part + ((size_t)p * K + k0) * F;
-  if (!accumulate) {
-    for (int i = tid; i < kn * F; i += kThreads) out[i] = 0.0;
-  } else {
-    // continue a partial from an earlier call: back to the second moment
-    // about the centre, S2c = M2 + S1^2 / S0
-    for (int i = tid; i < kn * D; i += kThreads) {
-      double* o = out + (size_t)(i / D) * F;
-      const int d = i % D;
-      if (o[0] > 0.0) o[1 + D + d] += o[1 + d] * o[1 + d] / o[0];
+// count: block b walks tiles [b kTPB, (b+1) kTPB) and counts its records per
+// component in shared memory; column b of counts[k][nb].
+__global__ void __launch_bounds__(256)
+rec_count_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restrict__ recs,
+                 int rec_cap, int64_t ntiles, int K, int64_t nb, uint32_t* __restrict__ counts) {
+  extern __shared__ uint32_t hist[];
+  const int64_t b = blockIdx.x;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) hist[k] = 0u;
+  __syncthreads();
+  const int64_t t1 = min(ntiles, (b + 1) * kTPB);
+  for (int64_t t = b * kTPB; t < t1; ++t) {
+    const uint32_t c = tile_cnt[t];
+    const int cnt = c < (uint32_t)rec_cap ? (int)c : rec_cap;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      const uint32_t k = recs[(size_t)t * rec_cap + i].x >> 7;
+      if (k < (uint32_t)K) atomicAdd(&hist[k], 1u);
     }
   }
   __syncthreads();
+  for (int k = threadIdx.x; k < K; k += blockDim.x) counts[(size_t)k * nb + b] = hist[k];
+}
 
-  const int64_t t0 = p * tiles_per_part;
-  const int64_t t1 = min(ntiles, t0 + tiles_per_part);
-  int since_flush = 0;
-  auto flush = [&]() {
-    __syncthreads();
-    for (int i = tid; i < kn * F; i += kThreads) {
-      out[i] += (double)acc[i];
-      acc[i] = 0.f;
+// Exclusive block-wide prefix of one value per thread (kScanThreads).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t = wsum[lane];
+    uint32_t ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += u;
     }
-    __syncthreads();
-  };
-  for (int64_t t = t0; t < t1; ++t) {
-    const uint32_t tc_n = tile_cnt[t];
-    const int cnt = tc_n < (uint32_t)rec_cap ? (int)tc_n : rec_cap;
-    for (int i = tid; i < cnt; i += kThreads) srec[i] = recs[(size_t)t * rec_cap + i];
-    __syncthreads();
+    wsum[lane] = ti - t;
+    if (lane == 31) *total = ti;
+  }
+  __syncthreads();
+  const uint32_t r = wsum[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// scan: counts[k][b] -> exclusive offsets (in place); cstart[k] = first
+// record of component k (cstart[K] = total); kstart[k] = first chunk of
+// component k (kstart[K] = chunk count).
+__global__ void __launch_bounds__(kScanThreads)
+rec_scan_kernel(uint32_t* __restrict__ counts, int K, int64_t nb, uint32_t* __restrict__ cstart,
+                uint32_t* __restrict__ kstart) {
+  __shared__ uint32_t wsum[kScanThreads / 32];
+  __shared__ uint32_t total;
+  const int64_t n = (int64_t)K * nb;
+  const int64_t per = (n + kScanThreads - 1) / kScanThreads;
+  const int64_t i0 = min(n, (int64_t)threadIdx.x * per), i1 = min(n, i0 + per);
+  uint32_t mine = 0;
+  for (int64_t i = i0; i < i1; ++i) mine += counts[i];
+  uint32_t run = block_excl_scan(mine, wsum, &total);
+  for (int64_t i = i0; i < i1; ++i) {
+    const uint32_t c = counts[i];
+    counts[i] = run;
+    run += c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) cstart[K] = total;
+  for (int k = threadIdx.x; k < K; k += kScanThreads) cstart[k] = counts[(size_t)k * nb];
+  __syncthreads();
+  // chunks per component, then their prefix
+  const int kper = (K + kScanThreads - 1) / kScanThreads;
+  const int k0 = min(K, (int)threadIdx.x * kper), k1 = min(K, k0 + kper);
+  uint32_t nch = 0;
+  for (int k = k0; k < k1; ++k) nch += (cstart[k + 1] - cstart[k] + kCH - 1) / kCH;
+  uint32_t krun = block_excl_scan(nch, wsum, &total);
+  for (int k = k0; k < k1; ++k) {
+    kstart[k] = krun;
+    krun += (cstart[k + 1] - cstart[k] + kCH - 1) / kCH;
+  }
+  if (threadIdx.x == 0) kstart[K] = total;
+}
+
+// scatter: the warp of block b places the block's records, in point order,
+// at their component's offsets: sorted[] = {point index in this call, gamma}.
+__global__ void __launch_bounds__(32)
+rec_scatter_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restrict__ recs,
+                   int rec_cap, int64_t ntiles, int K, int64_t nb,
+                   const uint32_t* __restrict__ offsets, uint2* __restrict__ sorted) {
+  extern __shared__ uint32_t cursor[];
+  const int64_t b = blockIdx.x;
+  const int lane = threadIdx.x;
+  for (int k = lane; k < K; k += 32) cursor[k] = offsets[(size_t)k * nb + b];
+  __syncwarp();
+  const int64_t t1 = min(ntiles, (b + 1) * kTPB);
+  for (int64_t t = b * kTPB; t < t1; ++t) {
+    const uint32_t c = tile_cnt[t];
+    const int cnt = c < (uint32_t)rec_cap ? (int)c : rec_cap;
     for (int base = 0; base < cnt; base += 32) {
       const int i = base + lane;
-      uint2 rec = make_uint2(0u, 0u);
-      bool own = false;
-      if (i < cnt) {
-        rec = srec[i];
-        const int k = (int)(rec.x >> 7);
-        own = (k >= k0) && (k < k0 + kn) && (((k - k0) & 7) == warp);
+      const bool live = i < cnt;
+      uint2 rec = make_uint2(0xffffffffu, 0u);
+      if (live) rec = recs[(size_t)t * rec_cap + i];
+      const uint32_t k = rec.x >> 7;
+      const bool ok = live && k < (uint32_t)K;
+      const unsigned grp = __match_any_sync(0xffffffffu, ok ? k : 0xffffffffu);
+      if (ok) {
+        const uint32_t pos = cursor[k] + __popc(grp & ((1u << lane) - 1u));
+        sorted[pos] = make_uint2((uint32_t)(t * kTile + (rec.x & 127)), rec.y);
       }
-      unsigned mask = __ballot_sync(0xffffffffu, own);
-      while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const uint32_t key = __shfl_sync(0xffffffffu, rec.x, b);
-        const float g = __uint_as_float(__shfl_sync(0xffffffffu, rec.y, b));
-        const int kl = (int)(key >> 7) - k0;
-        const int64_t n = t * 128 + (key & 127);
-        if (n >= N) continue;  // (never written for rows past the end)
-        float* a = acc + kl * F;
-#pragma unroll
-        for (int q = 0; q < DPL; ++q) {
-          const int d = q * 32 + lane;  // lane-interleaved: conflict-free shared memory
-          const float y = load_x<XT>(X, (size_t)n * D + d) - cent[kl * D + d];
-          const float gy = g * y;
-          a[1 + d] += gy;
-          a[1 + D + d] = fmaf(gy, y, a[1 + D + d]);
-        }
-        if (lane == 0) a[0] += g;
-        __syncwarp();
-      }
+      __syncwarp();
+      if (ok && lane == 31 - __clz(grp)) cursor[k] += __popc(grp);
+      __syncwarp();
     }
-    __syncthreads();
-    if (++since_flush == kFlushTiles) {
-      flush();
-      since_flush = 0;
-    }
-  }
-  flush();
-  // second moment about this block's weighted mean: M2 = S2c - S1c^2 / S0
-  for (int i = tid; i < kn * D; i += kThreads) {
-    const int kl = i / D, d = i % D;
-    double* o = out + (size_t)kl * F;
-    const double s0 = o[0];
-    if (s0 > 0.0) o[1 + D + d] = o[1 + D + d] - o[1 + d] * o[1 + d] / s0;
   }
 }
 
-template <int D, int XT>
-cudaError_t run_sparse(const void* X, int64_t N, int K, int cov, const void* prepared,
-                       const uint32_t* tile_cnt, const uint2* recs, int rec_cap, int parts,
-                       double* part, int accumulate, cudaStream_t s) {
-  constexpr int F = 1 + 2 * D;
-  constexpr int kSlice = slice_of<D>();
-  const PreparedLayout L = PreparedLayout::make(D, K, cov);
-  const int64_t ntiles = (N + 127) / 128;
-  const int slices = (K + kSlice - 1) / kSlice;
-  const int64_t tpp = (ntiles + parts - 1) / parts;
-  const size_t smem = sizeof(float) * (size_t)kSlice * (F + D) + sizeof(uint2) * (size_t)rec_cap;
-  auto kern = sparse_stats_kernel<D, XT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(slices, parts);
-  kern<<<grid, kThreads, smem, s>>>(X, N, K, prepared, L, tile_cnt, recs, rec_cap, ntiles, tpp,
-                                    part, accumulate);
-  return cudaGetLastError();
+template <int XT, int D, int DPL>
+__device__ __forceinline__ void global_row(const void* X, int64_t n, int d0, float* v) {
+  const size_t e0 = (size_t)n * D + d0;
+  if constexpr (XT == GMM_F32) {
+    if constexpr (DPL == 4) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(X) + e0));
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+      const float2 q = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(X) + e0));
+      v[0] = q.x; v[1] = q.y;
+    }
+  } else {
+    uint32_t u[DPL / 2];
+    if constexpr (DPL == 4) {
+      const uint2 q = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(X) + e0));
+      u[0] = q.x; u[1] = q.y;
+    } else {
+      u[0] = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const uint16_t*>(X) + e0));
+    }
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) {
+      float2 f;
+      if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+      v[2 * i] = f.x; v[2 * i + 1] = f.y;
+    }
+  }
 }
+
+// reduce: warp-per-chunk, grid-stride over the chunks; chunk sums
+// cpart[c] = [s0 | s1 (D) | s2 (D)] in fp32.
+template <int D, int XT>
+__global__ void __launch_bounds__(256)
+rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ mu,
+                  const uint32_t* __restrict__ cstart, const uint32_t* __restrict__ kstart,
+                  const uint2* __restrict__ sorted, float* __restrict__ cpart) {
+  constexpr int DPL = D / 32, F = 1 + 2 * D, B = 8;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t nchunks = kstart[K];
+  for (int64_t c = gw; c < nchunks; c += nw) {
+    // component of chunk c: the last k with kstart[k] <= c
+    int lo = 0, hi = K - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (kstart[mid] <= (uint32_t)c) lo = mid; else hi = mid - 1;
+    }
+    const int k = lo;
+    const uint32_t r0 = cstart[k] + (uint32_t)(c - kstart[k]) * kCH;
+    const uint32_t r1 = min(cstart[k + 1], r0 + kCH);
+    float cen[DPL], s1[DPL], s2[DPL], s0 = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      cen[i] = __ldg(mu + (size_t)k * D + lane * DPL + i);
+      s1[i] = s2[i] = 0.f;
+    }
+    for (uint32_t r = r0; r < r1; r += B) {
+      const uint2 mine = (lane < B && r + lane < r1) ? sorted[r + lane] : make_uint2(0u, 0u);
+      float x[B][DPL];
+      float g[B];
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        const uint32_t n = __shfl_sync(0xffffffffu, mine.x, u);
+        g[u] = __uint_as_float(__shfl_sync(0xffffffffu, mine.y, u));
+        if (r + u < r1) global_row<XT, D, DPL>(X, n, lane * DPL, x[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        if (r + u >= r1) break;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) {
+          const float y = x[u][i] - cen[i];
+          const float gy = g[u] * y;
+          s1[i] += gy;
+          s2[i] = fmaf(gy, y, s2[i]);
+        }
+        s0 += g[u];
+      }
+    }
+    float* o = cpart + (size_t)c * F;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      o[1 + lane * DPL + i] = s1[i];
+      o[1 + D + lane * DPL + i] = s2[i];
+    }
+    if (lane == 0) o[0] = s0;
+  }
+}
+
+// merge: warp-per-component; partial [S0 | S1 about c | M2 about the mean].
+template <int D>
+__global__ void __launch_bounds__(256)
+rec_merge_kernel(int K, const uint32_t* __restrict__ kstart, const float* __restrict__ cpart,
+                 double* __restrict__ part, int accumulate) {
+  constexpr int F = 1 + 2 * D;
+  const int lane = threadIdx.x & 31;
+  const int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (k >= K) return;
+  double* o = part + (size_t)k * F;
+  const uint32_t c0 = kstart[k], c1 = kstart[k + 1];
+  double s0 = 0.0;
+  for (uint32_t c = c0; c < c1; ++c) s0 += (double)cpart[(size_t)c * F];
+  const double S0o = accumulate ? o[0] : 0.0;
+  const double S0 = S0o + s0;
+  for (int d = lane; d < D; d += 32) {
+    double S1 = 0.0, S2c = 0.0;
+    for (uint32_t c = c0; c < c1; ++c) {
+      S1 += (double)cpart[(size_t)c * F + 1 + d];
+      S2c += (double)cpart[(size_t)c * F + 1 + D + d];
+    }
+    if (accumulate) {
+      // continue the earlier partial: its second moment back about c
+      const double o1 = o[1 + d];
+      S2c += o[1 + D + d] + (S0o > 0.0 ? o1 * o1 / S0o : 0.0);
+      S1 += o1;
+    }
+    o[1 + d] = S1;
+    o[1 + D + d] = S0 > 0.0 ? S2c - S1 * S1 / S0 : 0.0;
+  }
+  __syncwarp();
+  if (lane == 0) o[0] = S0;
+}
+
+int g_sms = 0;
 
 }  // namespace
 
-// Partitions of the tile range so that slices x partitions ~ 2 blocks per SM
-// (304 on 152 SMs).  Depends on D and K only, so that every chunk of a
-// streamed pass accumulates into the same partials.
-int sparse_stats_parts(int D, int K) {
-  const int slice = D == 128 ? slice_of<128>() : slice_of<64>();
-  const int slices = (K + slice - 1) / slice;
-  const int p = (304 + slices - 1) / slices;
-  return p < 1 ? 1 : p;
+// Workspace of sparse_stats for calls of up to `rows` points.
+size_t sparse_stats_ws_bytes(int64_t rows, int D, int K, int rec_cap) {
+  return SparseLayout::make(rows, D, K, rec_cap).bytes;
 }
 
+bool sparse_stats_supported(int K) { return K <= kMaxSparseK; }
+
 // Diagonal / isotropic statistics (the partial layout is the same for both;
-// the isotropic M-step averages the diagonal).  prepared: the block written
-// for this call's parameters (its mean array is the centre c).  accumulate:
-// merge into partials left by an earlier call (chunks of host data).
+// the isotropic M-step averages the diagonal) into ONE partial slot, part.
+// prepared: the block written for this call's parameters (its mean array is
+// the centre c).  accumulate: continue the partial of an earlier call.
+// sws: sparse_stats_ws_bytes(N, D, K, rec_cap) bytes, 256-byte aligned.
 cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
                          int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
-                         int parts, double* part, int accumulate, cudaStream_t s) {
-#define GMM_SPARSE(DD, XX) \
-  return run_sparse<DD, XX>(X, N, K, cov, prepared, tile_cnt, recs, rec_cap, parts, part, accumulate, s)
+                         void* sws, double* part, int accumulate, cudaStream_t s) {
+  if (K > kMaxSparseK || (D != 64 && D != 128)) return cudaErrorInvalidValue;
+  const SparseLayout S = SparseLayout::make(N, D, K, rec_cap);
+  const PreparedLayout L = PreparedLayout::make(D, K, cov);
+  uint32_t* counts = at<uint32_t>(sws, S.off_counts);
+  uint32_t* cstart = at<uint32_t>(sws, S.off_cstart);
+  uint32_t* kstart = at<uint32_t>(sws, S.off_kstart);
+  uint2* sorted = at<uint2>(sws, S.off_sorted);
+  float* cpart = at<float>(sws, S.off_cpart);
+  const size_t hsm = sizeof(uint32_t) * (size_t)K;
+  cudaError_t e;
+  if (hsm > 48 * 1024) {
+    e = cudaFuncSetAttribute(rec_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(rec_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm);
+    if (e != cudaSuccess) return e;
+  }
+  rec_count_kernel<<<(unsigned)S.nb, 256, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K, S.nb,
+                                                    counts);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  rec_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, K, S.nb, cstart, kstart);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  rec_scatter_kernel<<<(unsigned)S.nb, 32, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K, S.nb,
+                                                     counts, sorted);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!g_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 1;
+  }
+  const float* mu = at<float>(prepared, L.off_mu);
+  const unsigned rblocks = (unsigned)g_sms * 8;
+#define GMM_REDUCE(DD, XX) \
+  rec_reduce_kernel<DD, XX><<<rblocks, 256, 0, s>>>(X, K, mu, cstart, kstart, sorted, cpart)
   if (D == 128) {
-    if (xdtype == GMM_F16) { GMM_SPARSE(128, GMM_F16); }
-    if (xdtype == GMM_BF16) { GMM_SPARSE(128, GMM_BF16); }
-    GMM_SPARSE(128, GMM_F32);
+    if (xdtype == GMM_F16) GMM_REDUCE(128, GMM_F16);
+    else if (xdtype == GMM_BF16) GMM_REDUCE(128, GMM_BF16);
+    else GMM_REDUCE(128, GMM_F32);
+  } else {
+    if (xdtype == GMM_F16) GMM_REDUCE(64, GMM_F16);
+    else if (xdtype == GMM_BF16) GMM_REDUCE(64, GMM_BF16);
+    else GMM_REDUCE(64, GMM_F32);
   }
-  if (D == 64) {
-    if (xdtype == GMM_F16) { GMM_SPARSE(64, GMM_F16); }
-    if (xdtype == GMM_BF16) { GMM_SPARSE(64, GMM_BF16); }
-    GMM_SPARSE(64, GMM_F32);
-  }
-#undef GMM_SPARSE
-  return cudaErrorInvalidValue;
+#undef GMM_REDUCE
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const unsigned mblocks = (unsigned)(((int64_t)K * 32 + 255) / 256);
+  if (D == 128) rec_merge_kernel<128><<<mblocks, 256, 0, s>>>(K, kstart, cpart, part, accumulate);
+  else rec_merge_kernel<64><<<mblocks, 256, 0, s>>>(K, kstart, cpart, part, accumulate);
+  return cudaGetLastError();
 }
 
 }  // namespace gmm
