@@ -50,11 +50,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As above, suspending the thread for up to `ns` nanoseconds while the
+// phase is incomplete (it resumes when the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_ns(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete; gives up after
-// max_iter polls (each poll may suspend the thread for a short while).
+// max_iter polls of at most a microsecond each.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
   for (uint32_t i = 0; i < max_iter; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_ns(bar, parity, 1000u)) return true;
   return false;
 }
 

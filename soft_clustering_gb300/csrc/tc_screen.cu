@@ -12,8 +12,9 @@
 // sum mu^2 w / 2) comes with a rigorous bound on its error,
 //   |s v + bias - l| <= kappa |[x, x^2]|_2 |[b1, b2]|_2 + 1e-6 (|s v| + |bias|) + 1e-3,
 // from the fp16 rounding of b and x^2 (2^-11 each), of fp32 inputs (2^-11),
-// fp32 accumulation and the fp32 evaluation of the sum (the relative term;
-// its bias part and the 1e-3 are folded into the prepared bias - delta and
+// fp32 accumulation and the fp32 evaluation of the sum (the relative term:
+// its |s v| part is at most 1e-6 |[x, x^2]| |[b1, b2]| and joins kappa, its
+// bias part and the 1e-3 are folded into the prepared bias - delta and
 // bias + delta).  A component is kept when its upper bound reaches within
 // T = 40 nats of the largest lower bound; every kept pair is then evaluated
 // exactly in the centred fp32 form sum_d w_d (x_d - mu_d)^2, and LSE_n, the
@@ -48,8 +49,10 @@ constexpr int kBN = kTcChunk;     // components per chunk (MMA N)
 constexpr int kHalf = kBN / 2;    // columns of a chunk per epilogue warp
 constexpr int kCSH = 16;          // candidates kept per point and column half
 constexpr float kT = 40.f;        // nats
-constexpr float kKappa = 1.5e-3f; // 3 x 2^-11 rounding + accumulation allowance
-constexpr float kRel = 1e-6f;     // relative margin of the fp32 evaluation
+// Cauchy-Schwarz factor of the screening error: 3 x 2^-11 rounding plus the
+// accumulation allowance (1.5e-3), plus 2e-6 that covers the relative fp32
+// margin 1e-6 |s v| <= 1e-6 |a| |b| of evaluating s v + bias
+constexpr float kKappa = 1.5e-3f + 2e-6f;
 constexpr int kEpiWarps = 8;
 constexpr int kProdWarp0 = 8;     // warps 8-11
 constexpr int kMmaWarp = 12;
@@ -265,23 +268,32 @@ __device__ __forceinline__ void d2_leaf(const D2Args<NC>& q, int l, float* out) 
   }
 }
 
-// Lane l's partial of the exact evaluation of row n against one component:
-// sum over dimensions l*D/32 .. (l+1)*D/32 - 1 of w (x - mu)^2 (sequential
-// fma from 0).  The xor reduction over the warp then combines the partials
-// in the pairwise tree order of every other evaluation (p_i + p_{i+16},
-// then + 8, 4, 2, 1; fp32 addition is commutative, so each lane ends with
-// the same bits).
+// Quarter-warp evaluation of one pair: lane q (0..3) of a group of four
+// computes the partials q, q+4, ..., q+28 of the 32-partial form (partial l
+// = sum over dimensions l*D/32 .. (l+1)*D/32 - 1 of w (x - mu)^2,
+// sequential fma from 0) and combines them in the pairwise tree order
+// (+16, +8, +4 inside the lane; +2, +1 across the group with xor
+// shuffles), so the result has the bits of every other evaluation.
 template <int D, int XT>
-__device__ __forceinline__ float lane_partial(const void* X, int64_t n, const float* mu,
-                                              const float* w, bool iso, int lane) {
-  D2Args<1> q;
-  q.X = X; q.n = n; q.iso = iso;
-  q.mu[0] = mu;
-  q.w[0] = w;
-  q.wi[0] = iso ? __ldg(w) : 0.f;
-  float out;
-  d2_leaf<D, XT, 1>(q, lane, &out);
-  return out;
+__device__ __forceinline__ float group_d2(const void* X, int64_t n, const float* mu,
+                                          const float* w, bool iso, int q) {
+  D2Args<1> a;
+  a.X = X; a.n = n; a.iso = iso;
+  a.mu[0] = mu;
+  a.w[0] = w;
+  a.wi[0] = iso ? __ldg(w) : 0.f;
+  float p[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) d2_leaf<D, XT, 1>(a, q + 4 * m, &p[m]);
+  // +16: p[m] + p[m+4]; +8: + p[m+2]; +4: + p[m+1]
+#pragma unroll
+  for (int m = 0; m < 4; ++m) p[m] = p[m] + p[m + 4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) p[m] = p[m] + p[m + 2];
+  float v = p[0] + p[1];
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v;
 }
 
 // lbm[i] for a run-time i < 8 without indexing a local array.
@@ -527,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         const float* tbh = tsc + 3 * kBN;   // bias + delta
         const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
         // sweep 1: the best lower bound of the half-chunk,
-        //   lo = (v - kRel |v|) s + (bias - delta) - rnk |b|
+        //   lo = s v + (bias - delta) - rnk |b|
         float best = -INFINITY;
 #pragma unroll 1
         for (int c0 = 0; c0 < kHalf; c0 += 32) {
@@ -538,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           for (int i = 0; i < 32; ++i) {
             const int kk = c0 + i;
             const float v = __uint_as_float(u[i]);
-            const float lo = fmaf(fmaf(-kRel, fabsf(v), v), tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
+            const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
             best = fmaxf(best, lo);
           }
         }
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         xref_v[h * kBM + r] = ref;
         ref = fmaxf(ref, xref_v[(1 - h) * kBM + r]);
         // sweep 2: every component whose upper bound
-        //   hi = (v + kRel |v|) s + (bias + delta) + rnk |b|
+        //   hi = s v + (bias + delta) + rnk |b|
         // reaches the window below ref (or, assign, the m-th lower bound)
         float thr = ref - kT;
         if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, pick8(lbm, a.m - 1));
@@ -563,14 +575,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
             const int kk = c0 + i;
             const float v = __uint_as_float(u[i]);
             if constexpr (MODE == MODE_ASSIGN) {
-              const float lo = fmaf(fmaf(-kRel, fabsf(v), v), tsc[kk],
-                                    fmaf(-rnk, tcn[kk], tbl[kk]));
+              const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
               if (lo > pick8(lbm, a.m - 1)) {
                 insert_lower_bound(lbm, a.m, lo);
                 thr = fminf(ref - kT, pick8(lbm, a.m - 1));
               }
             }
-            const float hi = fmaf(fmaf(kRel, fabsf(v), v), tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
+            const float hi = fmaf(v, tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
             if (hi >= thr && valid) {
               const int k = j * kBN + h * kHalf + kk;
               if (cnt < kCSH) {
@@ -611,9 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       }
       const bool mine = valid && isfinite(rn) && !(dropped >= thr);
       // exact log joints of this half's candidates (same arithmetic as the
-      // CUDA-core kernels), warp-cooperatively: the warp's (row, candidate)
-      // pairs are numbered by an exclusive scan of the counts and taken four
-      // at a time, lane l computing partial l of each
+      // CUDA-core kernels): the warp's (row, candidate) pairs are numbered by
+      // an exclusive scan of the counts and taken eight at a time
       {
         const int mycnt = mine ? cnt : 0;
         int incl = mycnt;
@@ -624,37 +634,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         }
         const int excl = incl - mycnt;
         const int total = __shfl_sync(0xffffffffu, incl, 31);
-        for (int p0 = 0; p0 < total; p0 += 4) {
-          float part[4];
-          int slot[4], kk4[4];
+        // eight pairs per round, one per group of four lanes
+        const int grp = lane >> 2, gq = lane & 3;
+        for (int p0 = 0; p0 < total; p0 += 8) {
+          const int pidx = p0 + grp;
+          const bool live = pidx < total;
+          // owner lane of pair pidx: the last lane whose excl <= pidx
+          int owner = 0;
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int pidx = p0 + t;
-            const bool live = pidx < total;
-            // owner lane of pair pidx: the last lane whose excl <= pidx
-            const int owner = __popc(__ballot_sync(0xffffffffu, excl <= pidx)) - 1;
-            const int e = pidx - __shfl_sync(0xffffffffu, excl, owner);
-            const int rr = q * 32 + owner;
-            const int k = live ? (int)ck[e * kBM + rr] : 0;
-            slot[t] = live ? e * kBM + rr : -1;
-            kk4[t] = k;
-            part[t] = live ? lane_partial<D, XT>(a.X, tile * kBM + rr, g_mu + (size_t)k * D,
-                                                 iso ? g_prec + k : g_prec + (size_t)k * D,
-                                                 iso, lane)
-                           : 0.f;
+          for (int st = 16; st > 0; st >>= 1) {
+            const int cand = owner + st;
+            const int ev = __shfl_sync(0xffffffffu, excl, cand & 31);
+            if (cand < 32 && ev <= pidx) owner = cand;
           }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int t = 0; t < 4; ++t) part[t] += __shfl_xor_sync(0xffffffffu, part[t], o);
-          if (lane < 4) {
-            float pv = part[0];
-            int sl = slot[0], k = kk4[0];
-#pragma unroll
-            for (int t = 1; t < 4; ++t)
-              if (lane == t) { pv = part[t]; sl = slot[t]; k = kk4[t]; }
-            if (sl >= 0) cub[sl] = __ldg(g_c + k) - 0.5f * pv;
-          }
+          const int e = pidx - __shfl_sync(0xffffffffu, excl, owner);
+          const int rr = q * 32 + owner;
+          const int k = live ? (int)ck[e * kBM + rr] : 0;
+          // (idle groups evaluate row 0 of the tile, which always exists)
+          const float d2 = group_d2<D, XT>(a.X, tile * kBM + (live ? rr : 0), g_mu + (size_t)k * D,
+                                           iso ? g_prec + k : g_prec + (size_t)k * D, iso, gq);
+          if (live && gq == 0) cub[e * kBM + rr] = __ldg(g_c + k) - 0.5f * d2;
         }
         __syncwarp();
       }
