@@ -21,8 +21,7 @@
 // log-likelihood, top-m and the responsibilities come from those exact
 // values (sec. 3.2, 4.2: fp32 log-sum-exp).  Components more than 40 nats
 // below the best carry less than 4.3e-18 of a point's responsibility.  A
-// point whose kept list overflowed (more than 16 candidates in one half of
-// the columns, with an evicted one still within the window) is handed to
+// point with more than 16 candidates in one half of the columns is handed to
 // the CUDA-core path: one bit per row, turned into an ascending row list by
 // fb_compact so that the order never depends on timing.
 //
@@ -159,38 +158,6 @@ __device__ __forceinline__ void insert_lower_bound(float* lbm, int m, float v) {
   }
 }
 
-// Full candidate list of row r (entries cub/ck [e * 128 + r]): drop entries
-// that fell out of the window, then evict the smallest upper bound if the
-// new one is larger.  Returns the new count; *dropped is the largest upper
-// bound ever discarded while still inside the window.
-__device__ __noinline__ int insert_full(float* cub, uint16_t* ck, int r, int k, float hi,
-                                        float thr, float* dropped) {
-  int w = 0;
-  for (int e = 0; e < kCSH; ++e) {
-    const float u = cub[e * kBM + r];
-    if (u >= thr) { cub[w * kBM + r] = u; ck[w * kBM + r] = ck[e * kBM + r]; ++w; }
-  }
-  if (w < kCSH) {
-    cub[w * kBM + r] = hi;
-    ck[w * kBM + r] = (uint16_t)k;
-    return w + 1;
-  }
-  int emin = 0;
-  float umin = cub[r];
-  for (int e = 1; e < kCSH; ++e) {
-    const float u = cub[e * kBM + r];
-    if (u < umin) { umin = u; emin = e; }
-  }
-  if (hi > umin) {
-    *dropped = fmaxf(*dropped, umin);
-    cub[emin * kBM + r] = hi;
-    ck[emin * kBM + r] = (uint16_t)k;
-  } else {
-    *dropped = fmaxf(*dropped, hi);
-  }
-  return kCSH;
-}
-
 // Operands of one exact evaluation: row n of X against NC components.
 template <int NC>
 struct D2Args {
@@ -316,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   float* sCUB = (float*)(sm + S::OFF_CUB);
   uint16_t* sCK = (uint16_t*)(sm + S::OFF_CK);
   float* xref = (float*)(sm + S::OFF_X);  // [2][128] per half: best lower bound
-  volatile float* xref_v = xref;
   float* xlbm = xref + 2 * kBM;           // [2][128] m-th largest lower bound (assign)
   float* xmx = xlbm + 2 * kBM;            // [2][128] max exact log joint
   float* xsum = xmx + 2 * kBM;            // [2][128] sum exp(l - max)
@@ -352,7 +318,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     tc::mbar_init(&bar[EX_B], kEpiWarps);
     tc::mbar_init(&bar[EX_C], kEpiWarps);
     *abort_flag = 0;
-    for (int i = 0; i < 2 * kBM; ++i) xref[i] = -INFINITY;
     tc::mbar_fence_init();
   }
   tc::tc_fence_before();
@@ -375,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issue + loads
     if (lane == 0 && my_tiles > 0) {
-      const int64_t total = (int64_t)my_tiles * nch;
+      const int64_t total = (int64_t)my_tiles * 2 * nch;  // two passes per tile
       auto load_b = [&](int64_t g) {
         const int buf = (int)(g & 1), c = (int)(g % nch);
         tc::mbar_arrive_expect_tx(&bar[B_FULL + buf], S::B_BYTES);
@@ -396,8 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       for (int it = 0; it < my_tiles && ok; ++it) {
         if (!tc::mbar_wait(&bar[A_FULL], it & 1, kWait)) { fail(); ok = false; break; }
         tc::tc_fence_after();
-        for (int j = 0; j < nch; ++j) {
-          const int64_t g = (int64_t)it * nch + j;
+        for (int gi = 0; gi < 2 * nch; ++gi) {
+          const int j = gi % nch;
+          const int64_t g = (int64_t)it * 2 * nch + gi;
           const int buf = (int)(g & 1);
           const uint32_t use = (uint32_t)(g >> 1);
           const int bbuf = resident ? j : buf;
@@ -420,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           }
           if (!resident) tc::mma_commit(&bar[B_EMPTY + buf]);
           tc::mma_commit(&bar[T_FULL + buf]);
-          if (j == nch - 1) tc::mma_commit(&bar[A_EMPTY]);
+          if (gi == 2 * nch - 1) tc::mma_commit(&bar[A_EMPTY]);
           if (!resident && g + 1 < total && g + 1 >= 2) {
             // refill the other buffer once the MMAs of chunk g-1 are done
             const int pb = (int)((g + 1) & 1);
@@ -507,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     const int q = warp & 3, h = warp >> 2;
     const int r = q * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    float* cub = sCUB + h * kCSH * kBM;     // this half's candidate list
-    uint16_t* ck = sCK + h * kCSH * kBM;
+    float* __restrict__ cub = sCUB + h * kCSH * kBM;     // this half's candidate list
+    uint16_t* __restrict__ ck = sCK + h * kCSH * kBM;
     double ll_acc = 0.0;
     for (int it = 0; it < my_tiles; ++it) {
       if (warp_aborted(abort_flag)) break;
@@ -525,101 +491,94 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       for (int i = 0; i < 8; ++i) lbm[i] = -INFINITY;
       int cnt = 0;
       bool ok = true;
-      for (int j = 0; j < nch; ++j) {
-        const int64_t g = (int64_t)it * nch + j;
-        const int buf = (int)(g & 1);
-        const uint32_t use = (uint32_t)(g >> 1);
-        if (!warp_wait(&bar[T_FULL + buf], use & 1) || !warp_wait(&bar[TR_FULL + buf], use & 1)) {
-          fail(); ok = false; break;
+      float thr = -INFINITY;  // the point's window, fixed after pass 0
+      // pass 0: lower bounds only; pass 1 (a second contraction of the same
+      // tile): candidates against the point's final window
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        if (pass == 1) {
+          // exchange A: the best lower bound (assign: the m-th largest) of
+          // both column halves
+          xref[h * kBM + r] = ref;
+          if constexpr (MODE == MODE_ASSIGN) xlbm[h * kBM + r] = pick8(lbm, a.m - 1);
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
+          if (!warp_wait(&bar[EX_A], it & 1)) { fail(); ok = false; break; }
+          thr = fmaxf(xref[r], xref[kBM + r]) - kT;
+          // assign: at least m components have a lower bound >= the larger
+          // of the two halves' m-th largest, so nothing below it can be in
+          // the top m
+          if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, fmaxf(xlbm[r], xlbm[kBM + r]));
         }
-        tc::tc_fence_after();
-        const float* tsc = sT + buf * (S::T_BYTES / 4) + h * kHalf;
-        const float* tcn = tsc + kBN;
-        const float* tbl = tsc + 2 * kBN;   // bias - delta
-        const float* tbh = tsc + 3 * kBN;   // bias + delta
-        const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
-        // sweep 1: the best lower bound of the half-chunk,
-        //   lo = s v + (bias - delta) - rnk |b|
-        float best = -INFINITY;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kHalf; c0 += 32) {
-          uint32_t u[32];
-          tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
-          tc::tmem_wait32(u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int kk = c0 + i;
-            const float v = __uint_as_float(u[i]);
-            const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
-            best = fmaxf(best, lo);
+        for (int j = 0; j < nch; ++j) {
+          const int64_t g = ((int64_t)it * 2 + pass) * nch + j;
+          const int buf = (int)(g & 1);
+          const uint32_t use = (uint32_t)(g >> 1);
+          if (!warp_wait(&bar[T_FULL + buf], use & 1) ||
+              !warp_wait(&bar[TR_FULL + buf], use & 1)) {
+            fail(); ok = false; break;
           }
-        }
-        ref = fmaxf(ref, best);
-        // share the bound with the partner warp (the other column half of
-        // the same rows): whatever value is there is a lower bound of this
-        // point's best log joint, from this tile (-inf until published)
-        xref_v[h * kBM + r] = ref;
-        ref = fmaxf(ref, xref_v[(1 - h) * kBM + r]);
-        // sweep 2: every component whose upper bound
-        //   hi = s v + (bias + delta) + rnk |b|
-        // reaches the window below ref (or, assign, the m-th lower bound)
-        float thr = ref - kT;
-        if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, pick8(lbm, a.m - 1));
+          tc::tc_fence_after();
+          // (the trailer and the candidate lists never overlap)
+          const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4) + h * kHalf;
+          const float* __restrict__ tcn = tsc + kBN;
+          const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
+          const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
+          const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
+          if (pass == 0) {
+            // the best lower bound of the half-chunk,
+            //   lo = s v + (bias - delta) - rnk |b|
+            float best = -INFINITY;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kHalf; c0 += 32) {
-          uint32_t u[32];
-          tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
-          tc::tmem_wait32(u);
+            for (int c0 = 0; c0 < kHalf; c0 += 32) {
+              uint32_t u[32];
+              tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+              tc::tmem_wait32(u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int kk = c0 + i;
-            const float v = __uint_as_float(u[i]);
-            if constexpr (MODE == MODE_ASSIGN) {
-              const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
-              if (lo > pick8(lbm, a.m - 1)) {
-                insert_lower_bound(lbm, a.m, lo);
-                thr = fminf(ref - kT, pick8(lbm, a.m - 1));
+              for (int i = 0; i < 32; ++i) {
+                const int kk = c0 + i;
+                const float v = __uint_as_float(u[i]);
+                const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
+                best = fmaxf(best, lo);
+                if constexpr (MODE == MODE_ASSIGN) {
+                  if (lo > pick8(lbm, a.m - 1)) insert_lower_bound(lbm, a.m, lo);
+                }
               }
             }
-            const float hi = fmaf(v, tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
-            if (hi >= thr && valid) {
-              const int k = j * kBN + h * kHalf + kk;
-              if (cnt < kCSH) {
-                cub[cnt * kBM + r] = hi;
-                ck[cnt * kBM + r] = (uint16_t)k;
-                ++cnt;
-              } else {
-                cnt = insert_full(cub, ck, r, k, hi, thr, &dropped);
+            ref = fmaxf(ref, best);
+          } else {
+            // every component whose upper bound
+            //   hi = s v + (bias + delta) + rnk |b|
+            // reaches the window
+#pragma unroll 1
+            for (int c0 = 0; c0 < kHalf; c0 += 32) {
+              uint32_t u[32];
+              tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+              tc::tmem_wait32(u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int kk = c0 + i;
+                const float v = __uint_as_float(u[i]);
+                const float hi = fmaf(v, tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
+                if (hi >= thr && valid) {
+                  if (cnt < kCSH) {
+                    cub[cnt * kBM + r] = hi;
+                    ck[cnt * kBM + r] = (uint16_t)(j * kBN + h * kHalf + kk);
+                    ++cnt;
+                  } else {
+                    dropped = hi;  // list full: the row goes to the CUDA-core path
+                  }
+                }
               }
             }
           }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
         }
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[R_FREE + (it & 1)]);
       if (!ok) break;
-
-      // exchange A: the window of the point from both halves
-      xref_v[h * kBM + r] = ref;
-      if constexpr (MODE == MODE_ASSIGN) xlbm[h * kBM + r] = pick8(lbm, a.m - 1);
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
-      if (!warp_wait(&bar[EX_A], it & 1)) { fail(); break; }
-      float thr = fmaxf(xref_v[r], xref_v[kBM + r]) - kT;
-      // assign: at least m components have a lower bound >= the larger of
-      // the two halves' m-th largest, so nothing below it can be in the top m
-      if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, fmaxf(xlbm[r], xlbm[kBM + r]));
-      {
-        int w = 0;
-        for (int e = 0; e < cnt; ++e) {
-          const float u = cub[e * kBM + r];
-          if (u >= thr) { cub[w * kBM + r] = u; ck[w * kBM + r] = ck[e * kBM + r]; ++w; }
-        }
-        cnt = w;
-      }
       const bool mine = valid && isfinite(rn) && !(dropped >= thr);
       // exact log joints of this half's candidates (same arithmetic as the
       // CUDA-core kernels): the warp's (row, candidate) pairs are numbered by
@@ -669,8 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[EX_B]);
       if (!warp_wait(&bar[EX_B], it & 1)) { fail(); break; }
-      // both halves have read this tile's bounds: clear for the next tile
-      xref_v[h * kBM + r] = -INFINITY;
       const int c0 = xcnt[r], c1 = xcnt[kBM + r];
       const bool exact = c0 != 0xffff && c1 != 0xffff && c0 + c1 > 0;
       float lse = 0.f;
