@@ -103,9 +103,12 @@ struct Shape {
 // 227 KB of shared memory per block, with the static part (ll_red)
 static_assert(Shape<128>::SMEM + 8 * kEpiWarps <= 232448, "shared memory");
 
+// TMEM accumulator buffers of 128 columns: four when the parameter chunks
+// (and their trailers) stay resident, else two (streamed with B).
+constexpr int kTmemCols = 512;
 enum Bar {
-  A_FULL = 0, A_EMPTY = 1, B_FULL = 2, B_EMPTY = 4, T_FULL = 6, T_EMPTY = 8, TR_FULL = 10,
-  R_FULL = 12, R_FREE = 14, EX_A = 16, EX_B = 17, EX_C = 18
+  A_FULL = 0, A_EMPTY = 1, B_FULL = 2, B_EMPTY = 4, T_FULL = 6, T_EMPTY = 10, TR_FULL = 14,
+  R_FULL = 16, R_FREE = 18, EX_A = 20, EX_B = 21, EX_C = 22
 };
 
 // 8 consecutive stored coordinates as float, from raw 16-byte words.
@@ -297,9 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   const int my_tiles = blockIdx.x < ntiles ? (int)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
   const int nch = a.L.tc_chunks;
   const bool resident = nch <= 2;  // parameter chunks loaded once and kept
+  const int nbuf = resident ? 4 : 2;
 
   if (warp == kMmaWarp) {
-    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -308,11 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&bar[B_FULL + i], 1);
       tc::mbar_init(&bar[B_EMPTY + i], 1);
-      tc::mbar_init(&bar[T_FULL + i], 1);
-      tc::mbar_init(&bar[T_EMPTY + i], kEpiWarps);
       tc::mbar_init(&bar[TR_FULL + i], 1);
       tc::mbar_init(&bar[R_FULL + i], 4);
       tc::mbar_init(&bar[R_FREE + i], kEpiWarps);
+    }
+    for (int i = 0; i < 4; ++i) {
+      tc::mbar_init(&bar[T_FULL + i], 1);
+      tc::mbar_init(&bar[T_EMPTY + i], kEpiWarps);
     }
     tc::mbar_init(&bar[EX_A], kEpiWarps);
     tc::mbar_init(&bar[EX_B], kEpiWarps);
@@ -352,6 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           tc::mbar_arrive_expect_tx(&bar[B_FULL + c], S::B_BYTES);
           tc::bulk_g2s(sB + c * S::B_BYTES, gB + (size_t)c * S::B_BYTES, S::B_BYTES,
                        &bar[B_FULL + c]);
+          tc::mbar_arrive_expect_tx(&bar[TR_FULL + c], S::T_BYTES);
+          tc::bulk_g2s(sT + c * (S::T_BYTES / 4), gT + (size_t)c * kTcTrail, S::T_BYTES,
+                       &bar[TR_FULL + c]);
         }
       } else {
         for (int64_t g = 0; g < 2 && g < total; ++g) load_b(g);
@@ -364,17 +373,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         for (int gi = 0; gi < 2 * nch; ++gi) {
           const int j = gi % nch;
           const int64_t g = (int64_t)it * 2 * nch + gi;
-          const int buf = (int)(g & 1);
-          const uint32_t use = (uint32_t)(g >> 1);
-          const int bbuf = resident ? j : buf;
-          if (!tc::mbar_wait(&bar[B_FULL + bbuf], resident ? 0u : (use & 1), kWait) ||
+          const int sbuf = (int)(g & 1);               // streamed B / trailer buffer
+          const int buf = (int)(g % nbuf);             // TMEM buffer
+          const uint32_t use = (uint32_t)(g / nbuf);
+          const int bbuf = resident ? j : sbuf;
+          if (!tc::mbar_wait(&bar[B_FULL + bbuf], resident ? 0u : (uint32_t)((g >> 1) & 1), kWait) ||
               !tc::mbar_wait(&bar[T_EMPTY + buf], (use & 1) ^ 1, kWait) || *abort_flag) {
             fail(); ok = false; break;
           }
           tc::tc_fence_after();
-          tc::mbar_arrive_expect_tx(&bar[TR_FULL + buf], S::T_BYTES);
-          tc::bulk_g2s(sT + buf * (S::T_BYTES / 4), gT + (size_t)j * kTcTrail, S::T_BYTES,
-                       &bar[TR_FULL + buf]);
+          if (!resident) {
+            // the trailer buffer of g - 2 is free: its TMEM buffer was released
+            tc::mbar_arrive_expect_tx(&bar[TR_FULL + sbuf], S::T_BYTES);
+            tc::bulk_g2s(sT + sbuf * (S::T_BYTES / 4), gT + (size_t)j * kTcTrail, S::T_BYTES,
+                         &bar[TR_FULL + sbuf]);
+          }
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
           const unsigned char* bb = sB + bbuf * S::B_BYTES;
 #pragma unroll
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
             const uint64_t db = tc::sdesc_k128(tc::smem_addr(bb + atom * kBN * 128 + within));
             tc::mma_f16(d_tmem, da, db, idesc, ks > 0 ? 1u : 0u);
           }
-          if (!resident) tc::mma_commit(&bar[B_EMPTY + buf]);
+          if (!resident) tc::mma_commit(&bar[B_EMPTY + sbuf]);
           tc::mma_commit(&bar[T_FULL + buf]);
           if (gi == 2 * nch - 1) tc::mma_commit(&bar[A_EMPTY]);
           if (!resident && g + 1 < total && g + 1 >= 2) {
@@ -511,15 +524,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         }
         for (int j = 0; j < nch; ++j) {
           const int64_t g = ((int64_t)it * 2 + pass) * nch + j;
-          const int buf = (int)(g & 1);
-          const uint32_t use = (uint32_t)(g >> 1);
+          const int buf = (int)(g % nbuf);
+          const uint32_t use = (uint32_t)(g / nbuf);
+          const int tb = resident ? j : (int)(g & 1);  // trailer buffer
           if (!warp_wait(&bar[T_FULL + buf], use & 1) ||
-              !warp_wait(&bar[TR_FULL + buf], use & 1)) {
+              !warp_wait(&bar[TR_FULL + tb], resident ? 0u : (uint32_t)((g >> 1) & 1))) {
             fail(); ok = false; break;
           }
           tc::tc_fence_after();
           // (the trailer and the candidate lists never overlap)
-          const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4) + h * kHalf;
+          const float* __restrict__ tsc = sT + tb * (S::T_BYTES / 4) + h * kHalf;
           const float* __restrict__ tcn = tsc + kBN;
           const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
           const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
@@ -554,19 +568,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               uint32_t u[32];
               tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
               tc::tmem_wait32(u);
+              // a bit per column in the window (no branch in the sweep), then
+              // the (rare) appends in column order
+              uint32_t pm = 0u;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const int kk = c0 + i;
                 const float v = __uint_as_float(u[i]);
                 const float hi = fmaf(v, tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
-                if (hi >= thr && valid) {
-                  if (cnt < kCSH) {
-                    cub[cnt * kBM + r] = hi;
-                    ck[cnt * kBM + r] = (uint16_t)(j * kBN + h * kHalf + kk);
-                    ++cnt;
-                  } else {
-                    dropped = hi;  // list full: the row goes to the CUDA-core path
-                  }
+                pm |= hi >= thr ? (1u << i) : 0u;
+              }
+              if (!valid) pm = 0u;
+              while (pm) {
+                const int kk = c0 + __ffs(pm) - 1;
+                pm &= pm - 1u;
+                if (cnt < kCSH) {
+                  ck[cnt * kBM + r] = (uint16_t)(j * kBN + h * kHalf + kk);
+                  ++cnt;
+                } else {
+                  dropped = INFINITY;  // list full: the row goes to the CUDA-core path
                 }
               }
             }
@@ -740,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   }
   if (warp == kMmaWarp) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, 256);
+    tc::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
