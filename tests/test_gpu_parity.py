@@ -274,3 +274,66 @@ def test_tensor_core_path_matches_cuda_core_path(name, n, cov):
         fails = parity.compare_step(tc, cc, "%s iter %d tc vs cuda cores" % (name, it))
         assert not fails, fails
         theta = f32((cc["pi"], cc["mu"], cc["cov"]))
+
+
+def test_hand_over_rows_match_oracle():
+    """Rows the tensor-core screen hands over (more than 16 candidates in one
+    column half of a chunk) take the CUDA-core row-list kernels.  24 copies of
+    one component in the first column half force that for every point whose
+    window holds them; the statistics of both routes, merged, still match the
+    oracle."""
+    wl = _workload("embed_diag", n=20000)
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    pi, mu, cov = (np.array(p) for p in f32(datagen.init_params(mix, bits)))
+    mu[1:24] = mu[0]
+    cov[1:24] = cov[0]
+    pi[1:24] = pi[0]
+    pi /= pi.sum()
+    theta = f32((pi, mu, cov))
+    opts = datagen.em_opts(theta)
+    state = make_state(wl)
+    ref = oracle_step(bits, wl.dtype, theta, wl.cov_type, opts=opts)
+    got = gpu_step(state, to_device(bits, wl.dtype), theta, opts=opts)
+    assert got["status"] == 0
+    # rows handed over by the screen (the library's status word: code,
+    # detail, hand-over count)
+    handed = int(state.ws[8:12].cpu().numpy().view(np.uint32)[0])
+    assert 0 < handed < wl.N, handed
+    fails = parity.compare_step(got, ref, "hand-over rows", opts["min_s0"])
+    assert not fails, "\n".join(fails[:10])
+
+
+def test_embed_diag_full_size_sampled():
+    """The bench's own launch configuration (1e7 points, 2M-row slabs): LSE_n
+    of sampled points against the oracle's fp64 log-sum-exp of the same
+    points, the log-likelihood against the sum of the LSE outputs, and the
+    updated weights summing to one."""
+    wl = datagen.WORKLOADS["embed_diag"]
+    mix = datagen.planted(wl)
+    keep, ptrs = datagen.upload_tables(mix, device=torch.device("cuda"))
+    X = torch.empty(wl.N * wl.D, dtype=torch.float16, device="cuda")
+    datagen.device_points(mix, 0, wl.N, X.data_ptr(), torch.cuda.current_stream().cuda_stream,
+                          ptrs)
+    theta = f32(datagen.init_params(mix))
+    opts = datagen.em_opts(theta)
+    state = make_state(wl)
+    lse_before = None
+    for it in range(2):
+        got = gpu_step(state, X, theta, want_lse=True, opts=opts)
+        assert got["status"] == 0
+        rng = np.random.default_rng(11 + it)
+        idx = np.sort(rng.choice(wl.N, 1500, replace=False))
+        # include both slab edges and the last row
+        idx = np.unique(np.concatenate([idx, [0, (1 << 21) - 1, 1 << 21, wl.N - 1]]))
+        sample = datagen.points_at(mix, idx)
+        st, L, _ = oracle.log_joint(sample, *(np.asarray(p, np.float64) for p in theta),
+                                    wl.cov_type, xdtype=wl.dtype)
+        assert st == 0
+        m = L.max(axis=1)
+        ref_lse = m + np.log(np.exp(L - m[:, None]).sum(axis=1))
+        np.testing.assert_allclose(got["lse"][idx], ref_lse, rtol=1e-5, atol=2e-3)
+        assert abs(got["ll"] - got["lse"].sum()) <= 1e-6 * abs(got["ll"]) + 1.0
+        assert abs(got["pi"].sum() - 1.0) < 1e-5
+        theta = f32((got["pi"], got["mu"], got["cov"]))
+    del X, keep
