@@ -6,12 +6,13 @@
 // pairs carry less than 4.3e-18 of their point's responsibility.  The
 // statistics come from the records without an N x K matrix, in five steps:
 //   count    records per (component, block of kTPB tiles), in shared memory
-//   scan     exclusive offsets over (component, block), the start of each
-//            component's records and of its chunks of kCH records
+//   scan     per component (a warp each): its total and the exclusive offsets
+//            of its blocks; then one block: the start of each component's
+//            records and of its chunks of kCH records
 //   scatter  each record to its component's list, in point order (a warp
 //            walks its block's records 32 at a time; __match_any_sync ranks
 //            records of the same component, so the order is fixed)
-//   reduce   one warp per chunk: gathers the chunk's rows of X (eight in
+//   reduce   one warp per chunk: gathers the chunk's rows of X (sixteen in
 //            flight), accumulates g, g y, g y^2 with y = x - c_k about the
 //            component's input mean c_k (lane l: dimensions l*D/32 ..
 //            (l+1)*D/32 - 1) and writes the chunk's fp32 sums
@@ -28,7 +29,7 @@ namespace gmm {
 namespace {
 
 constexpr int kTile = 128;       // points per record tile
-constexpr int kTPB = 32;         // tiles per counting / scattering block
+constexpr int kTPB = 8;          // tiles per counting / scattering block
 constexpr int kCH = 512;         // records per reduction chunk
 constexpr int kScanThreads = 1024;
 
@@ -37,7 +38,7 @@ constexpr int kMaxSparseK = 16384;
 
 struct SparseLayout {
   int64_t ntiles, nb, max_recs, max_chunks;
-  size_t off_counts, off_cstart, off_kstart, off_sorted, off_cpart, bytes;
+  size_t off_counts, off_ktot, off_cstart, off_kstart, off_sorted, off_cpart, bytes;
   static SparseLayout make(int64_t rows, int D, int K, int rec_cap) {
     SparseLayout S;
     S.ntiles = (rows + kTile - 1) / kTile;
@@ -46,6 +47,7 @@ struct SparseLayout {
     S.max_chunks = (S.max_recs + kCH - 1) / kCH + K;
     size_t o = 0;
     S.off_counts = o; o = align_up(o + sizeof(uint32_t) * (size_t)K * S.nb);
+    S.off_ktot = o;   o = align_up(o + sizeof(uint32_t) * (size_t)K);
     S.off_cstart = o; o = align_up(o + sizeof(uint32_t) * (size_t)(K + 1));
     S.off_kstart = o; o = align_up(o + sizeof(uint32_t) * (size_t)(K + 1));
     S.off_sorted = o; o = align_up(o + sizeof(uint2) * (size_t)S.max_recs);
@@ -105,38 +107,56 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
   return r;
 }
 
-// scan: counts[k][b] -> exclusive offsets (in place); cstart[k] = first
-// record of component k (cstart[K] = total); kstart[k] = first chunk of
-// component k (kstart[K] = chunk count).
+// scan, part 1 (one warp per component): counts[k][b] -> offsets of block b
+// within component k (in place, exclusive), ktot[k] = the component's total.
+__global__ void __launch_bounds__(256)
+rec_scan_blocks_kernel(uint32_t* __restrict__ counts, int K, int64_t nb,
+                       uint32_t* __restrict__ ktot) {
+  const int lane = threadIdx.x & 31;
+  const int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (k >= K) return;
+  uint32_t* c = counts + (size_t)k * nb;
+  uint32_t carry = 0;
+  for (int64_t base = 0; base < nb; base += 32) {
+    const int64_t i = base + lane;
+    const uint32_t v = i < nb ? c[i] : 0u;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (i < nb) c[i] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) ktot[k] = carry;
+}
+
+// scan, part 2 (one block): cstart[k] = first record of component k
+// (cstart[K] = total); kstart[k] = first chunk of component k (kstart[K] =
+// chunk count).
 __global__ void __launch_bounds__(kScanThreads)
-rec_scan_kernel(uint32_t* __restrict__ counts, int K, int64_t nb, uint32_t* __restrict__ cstart,
-                uint32_t* __restrict__ kstart) {
+rec_scan_comps_kernel(const uint32_t* __restrict__ ktot, int K, uint32_t* __restrict__ cstart,
+                      uint32_t* __restrict__ kstart) {
   __shared__ uint32_t wsum[kScanThreads / 32];
   __shared__ uint32_t total;
-  const int64_t n = (int64_t)K * nb;
-  const int64_t per = (n + kScanThreads - 1) / kScanThreads;
-  const int64_t i0 = min(n, (int64_t)threadIdx.x * per), i1 = min(n, i0 + per);
-  uint32_t mine = 0;
-  for (int64_t i = i0; i < i1; ++i) mine += counts[i];
-  uint32_t run = block_excl_scan(mine, wsum, &total);
-  for (int64_t i = i0; i < i1; ++i) {
-    const uint32_t c = counts[i];
-    counts[i] = run;
-    run += c;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) cstart[K] = total;
-  for (int k = threadIdx.x; k < K; k += kScanThreads) cstart[k] = counts[(size_t)k * nb];
-  __syncthreads();
-  // chunks per component, then their prefix
   const int kper = (K + kScanThreads - 1) / kScanThreads;
   const int k0 = min(K, (int)threadIdx.x * kper), k1 = min(K, k0 + kper);
-  uint32_t nch = 0;
-  for (int k = k0; k < k1; ++k) nch += (cstart[k + 1] - cstart[k] + kCH - 1) / kCH;
+  uint32_t mine = 0, nch = 0;
+  for (int k = k0; k < k1; ++k) {
+    mine += ktot[k];
+    nch += (ktot[k] + kCH - 1) / kCH;
+  }
+  uint32_t run = block_excl_scan(mine, wsum, &total);
+  for (int k = k0; k < k1; ++k) {
+    cstart[k] = run;
+    run += ktot[k];
+  }
+  if (threadIdx.x == 0) cstart[K] = total;
   uint32_t krun = block_excl_scan(nch, wsum, &total);
   for (int k = k0; k < k1; ++k) {
     kstart[k] = krun;
-    krun += (cstart[k + 1] - cstart[k] + kCH - 1) / kCH;
+    krun += (ktot[k] + kCH - 1) / kCH;
   }
   if (threadIdx.x == 0) kstart[K] = total;
 }
@@ -146,11 +166,12 @@ rec_scan_kernel(uint32_t* __restrict__ counts, int K, int64_t nb, uint32_t* __re
 __global__ void __launch_bounds__(32)
 rec_scatter_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restrict__ recs,
                    int rec_cap, int64_t ntiles, int K, int64_t nb,
-                   const uint32_t* __restrict__ offsets, uint2* __restrict__ sorted) {
+                   const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ cstart,
+                   uint2* __restrict__ sorted) {
   extern __shared__ uint32_t cursor[];
   const int64_t b = blockIdx.x;
   const int lane = threadIdx.x;
-  for (int k = lane; k < K; k += 32) cursor[k] = offsets[(size_t)k * nb + b];
+  for (int k = lane; k < K; k += 32) cursor[k] = cstart[k] + offsets[(size_t)k * nb + b];
   __syncwarp();
   const int64_t t1 = min(ntiles, (b + 1) * kTPB);
   for (int64_t t = b * kTPB; t < t1; ++t) {
@@ -211,7 +232,7 @@ __global__ void __launch_bounds__(256)
 rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ mu,
                   const uint32_t* __restrict__ cstart, const uint32_t* __restrict__ kstart,
                   const uint2* __restrict__ sorted, float* __restrict__ cpart) {
-  constexpr int DPL = D / 32, F = 1 + 2 * D, B = 8;
+  constexpr int DPL = D / 32, F = 1 + 2 * D, B = 16;
   const int lane = threadIdx.x & 31;
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -322,6 +343,7 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
   const SparseLayout S = SparseLayout::make(N, D, K, rec_cap);
   const PreparedLayout L = PreparedLayout::make(D, K, cov);
   uint32_t* counts = at<uint32_t>(sws, S.off_counts);
+  uint32_t* ktot = at<uint32_t>(sws, S.off_ktot);
   uint32_t* cstart = at<uint32_t>(sws, S.off_cstart);
   uint32_t* kstart = at<uint32_t>(sws, S.off_kstart);
   uint2* sorted = at<uint2>(sws, S.off_sorted);
@@ -337,10 +359,13 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
   rec_count_kernel<<<(unsigned)S.nb, 256, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K, S.nb,
                                                     counts);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  rec_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, K, S.nb, cstart, kstart);
+  rec_scan_blocks_kernel<<<(unsigned)(((int64_t)K * 32 + 255) / 256), 256, 0, s>>>(counts, K, S.nb,
+                                                                                  ktot);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  rec_scan_comps_kernel<<<1, kScanThreads, 0, s>>>(ktot, K, cstart, kstart);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   rec_scatter_kernel<<<(unsigned)S.nb, 32, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K, S.nb,
-                                                     counts, sorted);
+                                                     counts, cstart, sorted);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (!g_sms) {
     int dev = 0;
