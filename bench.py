@@ -34,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused EM step N*K pairs/s (1 x GB300)"
+METRIC_ASSIGN = "top-m soft assignment N*K pairs/s (1 x GB300)"
 UNIT = "pairs/s"
 DEFAULT_WORKLOAD = "embed_diag"
 COV_NAMES = {0: "full", 1: "diag", 2: "iso"}
@@ -201,27 +202,38 @@ def dist_info():
     return world, rank, local
 
 
+def oracle_once(wl, mix, bits):
+    """One oracle call on `bits`: an EM iteration from theta_0, or (assignment
+    workloads) top-m against the planted parameters."""
+    import datagen
+    import oracle
+    if wl.m:
+        pi, mu, var = datagen.planted_params_f16(mix)
+        return oracle.topm(bits, pi, mu, var, wl.cov_type, wl.m, xdtype=wl.dtype)
+    theta = datagen.init_params(mix)
+    opts = datagen.em_opts(theta)
+    return oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype, opts=opts)
+
+
 def cpu_sample_run(wl, mix, seconds):
     """The oracle (as it stands) on the first n' points of the workload, one
     EM iteration from theta_0; n' sized for about `seconds` of work.
     Returns (pairs_per_s, n', threads, seconds_taken)."""
     import datagen
     import oracle
-    theta = datagen.init_params(mix)
-    opts = datagen.em_opts(theta)
     # calibrate twice: a tiny run is dominated by thread start-up, so the
     # second run (about a second of work) sets the sample size
     n_cal = min(wl.N, 256)
     for _ in range(2):
         bits = datagen.points(mix, 0, n_cal)
         t0 = time.perf_counter()
-        oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype, opts=opts)
+        oracle_once(wl, mix, bits)
         per_point = max((time.perf_counter() - t0) / n_cal, 1e-9)
         n_cal = int(min(wl.N, max(n_cal, 1.0 / per_point)))
     n = int(min(wl.N, max(n_cal, seconds / per_point)))
     bits = datagen.points(mix, 0, n)
     t0 = time.perf_counter()
-    oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype, opts=opts)
+    oracle_once(wl, mix, bits)
     dt = time.perf_counter() - t0
     return n * wl.K / dt, n, oracle.max_threads(), dt
 
@@ -240,21 +252,32 @@ def run_reference(args, wl):
     per_step_s = max(2.0, min(20.0, 150.0 / max(total_steps, 1)))
     _, n, threads, _ = cpu_sample_run(wl, mix, per_step_s)
     bits = datagen.points(mix, 0, n)
-    theta = datagen.init_params(mix)
-    opts = datagen.em_opts(theta)
-    pi, mu, cov = theta
-    for _ in range(args.warmup):
-        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype, opts=opts)
     times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype, opts=opts)
-        times.append(time.perf_counter() - t0)
-        pi, mu, cov = r["pi"], r["mu"], r["cov"]
+    if wl.m:
+        pi, mu, var = datagen.planted_params_f16(mix)
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.topm(bits, pi, mu, var, wl.cov_type, wl.m, xdtype=wl.dtype)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        what = "one top-%d assignment per step" % wl.m
+    else:
+        theta = datagen.init_params(mix)
+        opts = datagen.em_opts(theta)
+        pi, mu, cov = theta
+        for _ in range(args.warmup):
+            r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype, opts=opts)
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            r = oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype, opts=opts)
+            times.append(time.perf_counter() - t0)
+            pi, mu, cov = r["pi"], r["mu"], r["cov"]
+        what = "one EM iteration per step"
     ms = 1e3 * sum(times) / len(times)
     value = n * wl.K / (ms / 1e3)
-    sample = "first %d of %d points, one EM iteration per step (fp64 oracle)" % (n, wl.N)
-    line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+    sample = "first %d of %d points, %s (fp64 oracle)" % (n, wl.N, what)
+    line = dict(metric=METRIC_ASSIGN if wl.m else METRIC, value=value, unit=UNIT, n_gpus=world,
+                steps=args.steps,
                 warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
                 config=config_dict(wl, extra=dict(sample_points=n)),
@@ -438,6 +461,137 @@ def run_ours(args, wl):
     return 0
 
 
+def run_assign(args, wl):
+    """Top-m soft assignment of every point against the planted parameters
+    (the IVF multi-assignment workload): gmm_assign_topm on device-resident X;
+    e2e copies X in from pinned host memory and the ids / gamma out, every step."""
+    import torch
+    import datagen
+    import soft_clustering_gb300 as G
+    from soft_clustering_gb300 import build as gbuild
+    from soft_clustering_gb300.torch_api import Assigner
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        gbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    G.lib()
+    peaks = measured_peaks()
+    wm = work_model(wl)
+    mix = datagen.planted(wl)
+    keep, ptrs = datagen.upload_tables(mix, device=dev)
+    esz = 4 if wl.dtype == 0 else 2
+    X = torch.empty(wl.N * wl.D * esz, dtype=torch.uint8, device=dev)
+    datagen.device_points(mix, 0, wl.N, X.data_ptr(), torch.cuda.current_stream().cuda_stream,
+                          ptrs)
+    pi, mu, var = datagen.planted_params_f16(mix)
+    a = Assigner(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, wl.m, device=dev)
+    a.prepare(pi, mu, var)
+    for _ in range(args.warmup):
+        a.assign(X)
+    torch.cuda.synchronize()
+    status = a.device_status()
+    if status != 0:
+        log("device status after warm-up:", G.status_string(status))
+
+    G.gmm_profile_reset()
+    G.gmm_profile_enable(True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        a.assign(X)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    G.gmm_profile_enable(False)
+    prof = G.gmm_profile_read()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = a.device_status()
+    value = world * wm["pairs"] / (ms / 1e3)
+    launches = sum(n for (_, n) in prof.values())
+    top = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
+    roof = None
+    if top and top in wm["kernels"] and wm["kernels"][top]["bound"] == "tensor":
+        km = wm["kernels"][top]
+        tot_ms, n_launch = prof[top]
+        avg_s = tot_ms / n_launch / 1e3
+        achieved = km["flops"] / avg_s / 1e12
+        roof = dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=achieved / peaks["bf16_tflops"], traffic=traffic_for(top, wl.name),
+                    kernel=top, avg_launch_ms=tot_ms / n_launch, per_launch=km["unit_note"],
+                    hbm_achieved_gbs=km["bytes"] / avg_s / 1e9,
+                    peak_source="bf16 dense GEMM, %s (fp16 = bf16 rate)" % peaks["source"])
+    # assignment roofline: 4NKD flops (no statistics), one read of X + the outputs
+    out_bytes = wl.N * wl.m * 8 + wl.N * 4
+    step_roof_s = max(wl.N * wl.K * 4 * wl.D / (peaks["bf16_tflops"] * 1e12),
+                      (wm["x_bytes"] + out_bytes) / (peaks["hbm_gbs"] * 1e9))
+
+    e2e = None
+    if not args.no_e2e:
+        host = torch.empty(wl.N * wl.D * esz, dtype=torch.uint8, pin_memory=True)
+        host.copy_(X)
+        ids_h = torch.empty(wl.N, wl.m, dtype=torch.int32, pin_memory=True)
+        gam_h = torch.empty(wl.N, wl.m, dtype=torch.float32, pin_memory=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            X.copy_(host, non_blocking=True)
+            a.assign(X, with_lse=False)
+            ids_h.copy_(a.ids, non_blocking=True)
+            gam_h.copy_(a.gamma, non_blocking=True)
+            torch.cuda.synchronize()
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = dict(value=world * wm["pairs"] / e2e_s, unit=UNIT, h2d_bytes_per_step=wm["x_bytes"],
+                   d2h_bytes_per_step=wl.N * wl.m * 8, ms_per_step=e2e_s * 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, thr, dt = cpu_sample_run(wl, mix, 12.0)
+        cpu = dict(value=v, unit=UNIT, cores=thr, kind="oracle",
+                   sample="first %d of %d points, top-%d assignment, %.1f s" % (n, wl.N, wl.m, dt))
+    if rank == 0:
+        line = dict(
+            metric=METRIC_ASSIGN, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+            warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+            vs_baseline=None, dtype="f32", data="synthetic",
+            config=config_dict(wl, extra=dict(
+                m=wl.m, parallelism="replicas" if world > 1 else "single",
+                device_status=G.status_string(status),
+                step_roofline=dict(flops=wl.N * wl.K * 4 * wl.D,
+                                   bytes=wm["x_bytes"] + out_bytes,
+                                   roofline_ms=step_roof_s * 1e3, frac=step_roof_s * 1e3 / ms),
+                kernels={k: dict(ms_per_launch=v[0] / v[1], launches=v[1])
+                         for k, v in prof.items()})),
+            roofline=roof, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clk)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,10 +608,10 @@ def main(argv=None):
     wl = datagen.WORKLOADS[args.workload]
     if args.n:
         wl = wl.with_n(args.n)
-    if wl.m:
-        raise SystemExit("assignment workloads are benchmarked by bench_assign (not yet)")
     if args.impl == "reference":
         return run_reference(args, wl)
+    if wl.m:
+        return run_assign(args, wl)
     return run_ours(args, wl)
 
 

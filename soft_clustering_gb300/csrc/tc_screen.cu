@@ -502,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       float lbm[8];           // assign: the m largest lower bounds seen
 #pragma unroll
       for (int i = 0; i < 8; ++i) lbm[i] = -INFINITY;
+      float lmth = -INFINITY;  // assign: the m-th largest of them
       int cnt = 0;
       bool ok = true;
       float thr = -INFINITY;  // the point's window, fixed after pass 0
@@ -512,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           // exchange A: the best lower bound (assign: the m-th largest) of
           // both column halves
           xref[h * kBM + r] = ref;
-          if constexpr (MODE == MODE_ASSIGN) xlbm[h * kBM + r] = pick8(lbm, a.m - 1);
+          if constexpr (MODE == MODE_ASSIGN) xlbm[h * kBM + r] = lmth;
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
           if (!warp_wait(&bar[EX_A], it & 1)) { fail(); ok = false; break; }
@@ -554,7 +555,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
                 const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
                 best = fmaxf(best, lo);
                 if constexpr (MODE == MODE_ASSIGN) {
-                  if (lo > pick8(lbm, a.m - 1)) insert_lower_bound(lbm, a.m, lo);
+                  if (lo > lmth) {
+                    insert_lower_bound(lbm, a.m, lo);
+                    lmth = pick8(lbm, a.m - 1);
+                  }
                 }
               }
             }
