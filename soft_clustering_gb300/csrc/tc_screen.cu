@@ -21,20 +21,25 @@
 // log-likelihood, top-m and the responsibilities come from those exact
 // values (sec. 3.2, 4.2: fp32 log-sum-exp).  Components more than 40 nats
 // below the best carry less than 4.3e-18 of a point's responsibility.  A
-// point with more than 16 candidates in one half of the columns is handed to
-// the CUDA-core path: one bit per row, turned into an ascending row list by
+// point whose candidate list overflows (15 entries; per column half when the
+// parameters are streamed) is handed to the CUDA-core path: one bit per row, turned into an ascending row list by
 // fb_compact so that the order never depends on timing.
 //
 // Roles (one CTA per SM, persistent over 128-point tiles in a fixed order):
-//   warps 0-7   epilogue: warp w reads TMEM lane quarter w % 4 (32 points)
-//               and column half w / 4 of every chunk; each keeps its own
-//               candidate list, refines it exactly, and the two warps of a
-//               quarter combine their results through shared memory
+//   warps 0-7   epilogue.  Resident parameters (K <= 256): two groups of four
+//               warps take alternate tiles, warp 4g + q reading TMEM lane
+//               quarter q (32 points) over every column, so one group's
+//               refine and records overlap the other group's sweeps; four
+//               TMEM buffers, two per group.  Streamed parameters: warp w
+//               reads lane quarter w % 4 and column half w / 4 of each chunk,
+//               the two warps of a quarter combining their bounds and partial
+//               log-sum-exp through shared memory (up to 30 candidates a row)
 //   warps 8-11  producers: one point row per thread -> [x, x^2] fp16 tile in
 //               shared memory (128-byte swizzled K-major), row norms; the
 //               next tile's rows are loaded before the buffer is free
-//   warp  12    lane 0 issues bulk copies of the parameter chunks and the
-//               tcgen05.mma instructions; the warp owns the TMEM allocation
+//   warp  12    lane 0 issues bulk copies of the parameter chunks and their
+//               trailers and the tcgen05.mma instructions; the warp owns the
+//               TMEM allocation
 #include <math.h>
 
 #include "gmm_internal.cuh"
@@ -45,8 +50,8 @@ namespace {
 
 constexpr int kBM = 128;          // points per tile (MMA M)
 constexpr int kBN = kTcChunk;     // components per chunk (MMA N)
-constexpr int kHalf = kBN / 2;    // columns of a chunk per epilogue warp
-constexpr int kCSH = 16;          // candidates kept per point and column half
+constexpr int kHalf = kBN / 2;    // columns of a chunk per warp (streamed parameters)
+constexpr int kCS = 15;           // candidates per point list (per column half when streamed)
 constexpr float kT = 40.f;        // nats
 // Cauchy-Schwarz factor of the screening error: 3 x 2^-11 rounding plus the
 // accumulation allowance (1.5e-3), plus 2e-6 that covers the relative fp32
@@ -79,7 +84,12 @@ struct ScreenArgs {
   DeviceStatus* st;
 };
 
-template <int D>
+// GRP: the grouped epilogue (resident parameters, K <= 256): two groups of
+// four warps take alternate tiles, each warp all columns of 32 rows; four
+// TMEM buffers and trailer slots.  Otherwise (parameters streamed with B):
+// eight warps, the two of a lane quarter splitting each chunk's columns; two
+// TMEM buffers and trailer slots.
+template <int D, bool GRP>
 struct Shape {
   static constexpr int KD = 2 * D;
   static constexpr int KSTEPS = KD / 16;
@@ -88,27 +98,31 @@ struct Shape {
   static constexpr int T_BYTES = kTcTrail * 4;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + A_BYTES;             // 2 buffers
-  static constexpr int OFF_T = OFF_B + 2 * B_BYTES;         // 2 trailers
-  static constexpr int OFF_RN = OFF_T + 2 * T_BYTES;        // 2 x 128 row norms
-  static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;      // [2][kCSH][128] float
-  static constexpr int OFF_CK = OFF_CUB + 2 * kCSH * kBM * 4;  // [2][kCSH][128] u16
-  static constexpr int OFF_X = OFF_CK + 2 * kCSH * kBM * 2;    // half exchange
-  static constexpr int X_BYTES = 4 * 2 * kBM * 4 + 2 * kBM * 2;
-  static constexpr int OFF_BAR = (OFF_X + X_BYTES + 7) / 8 * 8;  // 24 mbarrier slots
-  static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
+  static constexpr int NT = GRP ? 4 : 2;                    // trailer slots = TMEM buffers
+  static constexpr int OFF_T = OFF_B + 2 * B_BYTES;
+  static constexpr int OFF_RN = OFF_T + NT * T_BYTES;       // 2 x 128 row norms
+  static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;      // [2][kCS][128] float
+  static constexpr int OFF_CK = OFF_CUB + 2 * kCS * kBM * 4;   // [2][kCS][128] u16
+  static constexpr int OFF_X = OFF_CK + 2 * kCS * kBM * 2;     // exchange between warps
+  // grouped: record counts [2 groups][2][128] u16; streamed: per half best
+  // and m-th lower bound, max and sum of the exact values, counts
+  static constexpr int X_BYTES = GRP ? 2 * 2 * kBM * 2 : 4 * 2 * kBM * 4 + 2 * kBM * 2;
+  static constexpr int OFF_BAR = (OFF_X + X_BYTES + 7) / 8 * 8;  // 26 mbarrier slots
+  static constexpr int OFF_MISC = OFF_BAR + 26 * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr int SMEM = BYTES + 1024;                 // base alignment slack
 };
 
 // 227 KB of shared memory per block, with the static part (ll_red)
-static_assert(Shape<128>::SMEM + 8 * kEpiWarps <= 232448, "shared memory");
+static_assert(Shape<128, true>::SMEM + 8 * kEpiWarps <= 232448, "shared memory");
+static_assert(Shape<128, false>::SMEM + 8 * kEpiWarps <= 232448, "shared memory");
 
-// TMEM accumulator buffers of 128 columns: four when the parameter chunks
-// (and their trailers) stay resident, else two (streamed with B).
+// TMEM accumulator buffers of 128 columns (four allocated; the streamed
+// mode uses two).
 constexpr int kTmemCols = 512;
 enum Bar {
   A_FULL = 0, A_EMPTY = 1, B_FULL = 2, B_EMPTY = 4, T_FULL = 6, T_EMPTY = 10, TR_FULL = 14,
-  R_FULL = 16, R_FREE = 18, EX_A = 20, EX_B = 21, EX_C = 22
+  R_FULL = 18, R_FREE = 20, EXG = 22, EX_A = 22, EX_B = 23, EX_C = 24
 };
 
 // 8 consecutive stored coordinates as float, from raw 16-byte words.
@@ -274,9 +288,9 @@ __device__ __forceinline__ float pick8(const float* lbm, int i) {
   return v;
 }
 
-template <int D, int XT, int MODE>
+template <int D, int XT, int MODE, bool GRP>
 __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs a) {
-  using S = Shape<D>;
+  using S = Shape<D, GRP>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* sA = sm + S::OFF_A;
@@ -290,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   float* xmx = xlbm + 2 * kBM;            // [2][128] max exact log joint
   float* xsum = xmx + 2 * kBM;            // [2][128] sum exp(l - max)
   uint16_t* xcnt = (uint16_t*)(xsum + 2 * kBM);  // [2][128] count, 0xffff: not exact
+  uint16_t* xcg = (uint16_t*)(sm + S::OFF_X);    // grouped: [group][tile parity][128] counts
   uint64_t* bar = (uint64_t*)(sm + S::OFF_BAR);
   uint32_t* tmem_slot = (uint32_t*)(sm + S::OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + S::OFF_MISC + 4);
@@ -299,8 +314,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   const int64_t ntiles = (a.N + kBM - 1) / kBM;
   const int my_tiles = blockIdx.x < ntiles ? (int)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
   const int nch = a.L.tc_chunks;
-  const bool resident = nch <= 2;  // parameter chunks loaded once and kept
-  const int nbuf = resident ? 4 : 2;
+  const bool resident = GRP;  // parameter chunks loaded once and kept (K <= 256)
+  // TMEM buffer (and trailer slot) and its use count for contraction gi
+  // (pass gi / nch, chunk gi % nch) of tile it: grouped, chunk j of the
+  // group's tiles keeps buffer 2g + j, the passes in turn; streamed, the
+  // contractions alternate over two buffers
+  auto tbuf = [&](int it, int gi, int* buf, uint32_t* use) {
+    if constexpr (GRP) {
+      *buf = 2 * (it & 1) + gi % nch;
+      *use = (uint32_t)(2 * (it >> 1) + gi / nch);
+    } else {
+      const int64_t gq = (int64_t)it * 2 * nch + gi;
+      *buf = (int)(gq & 1);
+      *use = (uint32_t)(gq >> 1);
+    }
+  };
 
   if (warp == kMmaWarp) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -309,20 +337,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   if (tid == 0) {
     tc::mbar_init(&bar[A_FULL], 4);
     tc::mbar_init(&bar[A_EMPTY], 1);
+    // arrivals per phase from the epilogue: a group (4 warps) or all 8
+    const uint32_t epi = GRP ? 4u : (uint32_t)kEpiWarps;
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&bar[B_FULL + i], 1);
       tc::mbar_init(&bar[B_EMPTY + i], 1);
-      tc::mbar_init(&bar[TR_FULL + i], 1);
       tc::mbar_init(&bar[R_FULL + i], 4);
-      tc::mbar_init(&bar[R_FREE + i], kEpiWarps);
+      tc::mbar_init(&bar[R_FREE + i], epi);
     }
     for (int i = 0; i < 4; ++i) {
       tc::mbar_init(&bar[T_FULL + i], 1);
-      tc::mbar_init(&bar[T_EMPTY + i], kEpiWarps);
+      tc::mbar_init(&bar[T_EMPTY + i], epi);
+      tc::mbar_init(&bar[TR_FULL + i], 1);
     }
-    tc::mbar_init(&bar[EX_A], kEpiWarps);
-    tc::mbar_init(&bar[EX_B], kEpiWarps);
-    tc::mbar_init(&bar[EX_C], kEpiWarps);
+    if constexpr (GRP) {
+      tc::mbar_init(&bar[EXG], 4);
+      tc::mbar_init(&bar[EXG + 1], 4);
+    } else {
+      tc::mbar_init(&bar[EX_A], kEpiWarps);
+      tc::mbar_init(&bar[EX_B], kEpiWarps);
+      tc::mbar_init(&bar[EX_C], kEpiWarps);
+    }
     *abort_flag = 0;
     tc::mbar_fence_init();
   }
@@ -358,9 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           tc::mbar_arrive_expect_tx(&bar[B_FULL + c], S::B_BYTES);
           tc::bulk_g2s(sB + c * S::B_BYTES, gB + (size_t)c * S::B_BYTES, S::B_BYTES,
                        &bar[B_FULL + c]);
-          tc::mbar_arrive_expect_tx(&bar[TR_FULL + c], S::T_BYTES);
-          tc::bulk_g2s(sT + c * (S::T_BYTES / 4), gT + (size_t)c * kTcTrail, S::T_BYTES,
-                       &bar[TR_FULL + c]);
         }
       } else {
         for (int64_t g = 0; g < 2 && g < total; ++g) load_b(g);
@@ -373,21 +405,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         for (int gi = 0; gi < 2 * nch; ++gi) {
           const int j = gi % nch;
           const int64_t g = (int64_t)it * 2 * nch + gi;
-          const int sbuf = (int)(g & 1);               // streamed B / trailer buffer
-          const int buf = (int)(g % nbuf);             // TMEM buffer
-          const uint32_t use = (uint32_t)(g / nbuf);
+          const int sbuf = (int)(g & 1);               // streamed B buffer
+          int buf;                                     // TMEM buffer and trailer slot
+          uint32_t use;
+          tbuf(it, gi, &buf, &use);
           const int bbuf = resident ? j : sbuf;
           if (!tc::mbar_wait(&bar[B_FULL + bbuf], resident ? 0u : (uint32_t)((g >> 1) & 1), kWait) ||
               !tc::mbar_wait(&bar[T_EMPTY + buf], (use & 1) ^ 1, kWait) || *abort_flag) {
             fail(); ok = false; break;
           }
           tc::tc_fence_after();
-          if (!resident) {
-            // the trailer buffer of g - 2 is free: its TMEM buffer was released
-            tc::mbar_arrive_expect_tx(&bar[TR_FULL + sbuf], S::T_BYTES);
-            tc::bulk_g2s(sT + sbuf * (S::T_BYTES / 4), gT + (size_t)j * kTcTrail, S::T_BYTES,
-                         &bar[TR_FULL + sbuf]);
-          }
+          // the trailer slot of a TMEM buffer is free once the buffer is
+          tc::mbar_arrive_expect_tx(&bar[TR_FULL + buf], S::T_BYTES);
+          tc::bulk_g2s(sT + buf * (S::T_BYTES / 4), gT + (size_t)j * kTcTrail, S::T_BYTES,
+                       &bar[TR_FULL + buf]);
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
           const unsigned char* bb = sB + bbuf * S::B_BYTES;
 #pragma unroll
@@ -472,8 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         *reinterpret_cast<uint4*>(sA + tc::sw128_offset(p, D + c8 * 8, kBM)) =
             make_uint4(hq[0], hq[1], hq[2], hq[3]);
       }
-      // fp16 subnormal / input rounding floor, so the bound never reaches 0
-      sRN[(it & 1) * kBM + p] = sqrtf(rn2) + 1e-6f * (float)D;
+      // the norm (its fp32 sum errs by at most (D + 1) 2^-24 relative) with a
+      // floor: fp16 subnormal rounding of x^2 (and of bf16 x below fp16's
+      // normal range) errs by at most 2^-25 per coordinate, sqrt(2D) 2^-25 |b|
+      // in all, below kappa x 1e-3 |b| for D <= 128
+      sRN[(it & 1) * kBM + p] = sqrtf(rn2) * 1.0001f + 1e-3f;
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -482,12 +516,255 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       }
     }
   } else {
-    // -------------------------------------------------------- epilogue
+    if constexpr (GRP) {
+    // ------------------------------------- epilogue (resident parameters)
+    // group g (warps 4g .. 4g+3) takes tiles g, g+2, ...; warp q of the group
+    // reads TMEM lane quarter q (32 points) over every column
+    const int g = warp >> 2, q = warp & 3;
+    const int r = q * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float* __restrict__ cub = sCUB + g * kCS * kBM;     // this group's candidate lists
+    uint16_t* __restrict__ ck = sCK + g * kCS * kBM;
+    double ll_acc = 0.0;
+    for (int it = g; it < my_tiles; it += 2) {
+      if (warp_aborted(abort_flag)) break;
+      const int s = it >> 1;  // the group's s-th tile
+      const int64_t tile = blockIdx.x + (int64_t)it * gridDim.x;
+      const int64_t n = tile * kBM + r;
+      const bool valid = n < a.N;
+      if (!warp_wait(&bar[R_FULL + g], s & 1)) { fail(); break; }
+      const float rn = sRN[g * kBM + r];
+      const float rnk = kKappa * rn;
+      float ref = -INFINITY;  // lower bound of the best log joint
+      float dropped = -INFINITY;
+      float lbm[8];           // assign: the m largest lower bounds seen
+#pragma unroll
+      for (int i = 0; i < 8; ++i) lbm[i] = -INFINITY;
+      float lmth = -INFINITY;  // assign: the m-th largest of them
+      int cnt = 0;
+      bool ok = true;
+      float thr = -INFINITY;  // the point's window, fixed after pass 0
+      // pass 0: lower bounds only; pass 1 (a second contraction of the same
+      // tile): candidates against the point's final window
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        if (pass == 1) {
+          thr = ref - kT;
+          // assign: m components have a lower bound >= the m-th largest, so
+          // nothing below it can be in the top m
+          if constexpr (MODE == MODE_ASSIGN) thr = fminf(thr, lmth);
+        }
+        for (int j = 0; j < nch; ++j) {
+          int buf;
+          uint32_t use;
+          tbuf(it, pass * nch + j, &buf, &use);
+          if (!warp_wait(&bar[T_FULL + buf], use & 1) ||
+              !warp_wait(&bar[TR_FULL + buf], use & 1)) {
+            fail(); ok = false; break;
+          }
+          tc::tc_fence_after();
+          // (the trailer and the candidate lists never overlap)
+          const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4);
+          const float* __restrict__ tcn = tsc + kBN;
+          const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
+          const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
+          const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN);
+          if (pass == 0) {
+            // the best lower bound of the chunk,
+            //   lo = s v + (bias - delta) - rnk |b|
+            float best = -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+              uint32_t u[32];
+              tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+              tc::tmem_wait32(u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int kk = c0 + i;
+                const float v = __uint_as_float(u[i]);
+                const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
+                best = fmaxf(best, lo);
+                if constexpr (MODE == MODE_ASSIGN) {
+                  if (lo > lmth) {
+                    insert_lower_bound(lbm, a.m, lo);
+                    lmth = pick8(lbm, a.m - 1);
+                  }
+                }
+              }
+            }
+            ref = fmaxf(ref, best);
+          } else {
+            // every component whose upper bound
+            //   hi = s v + (bias + delta) + rnk |b|
+            // reaches the window
+#pragma unroll 1
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+              uint32_t u[32];
+              tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+              tc::tmem_wait32(u);
+              // a bit per column in the window (no branch in the sweep), then
+              // the (rare) appends in column order
+              uint32_t pm = 0u;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int kk = c0 + i;
+                const float v = __uint_as_float(u[i]);
+                const float hi = fmaf(v, tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
+                pm |= hi >= thr ? (1u << i) : 0u;
+              }
+              if (!valid) pm = 0u;
+              while (pm) {
+                const int kk = c0 + __ffs(pm) - 1;
+                pm &= pm - 1u;
+                if (cnt < kCS) {
+                  ck[cnt * kBM + r] = (uint16_t)(j * kBN + kk);
+                  ++cnt;
+                } else {
+                  dropped = INFINITY;  // list full: the row goes to the CUDA-core path
+                }
+              }
+            }
+          }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[R_FREE + g]);
+      if (!ok) break;
+      const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
+      // exact log joints of the candidates (same arithmetic as the CUDA-core
+      // kernels): the warp's (row, candidate) pairs are numbered by an
+      // exclusive scan of the counts and taken eight at a time
+      {
+        const int mycnt = exact ? cnt : 0;
+        int incl = mycnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const int excl = incl - mycnt;
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        // eight pairs per round, one per group of four lanes
+        const int grp = lane >> 2, gq = lane & 3;
+        for (int p0 = 0; p0 < total; p0 += 8) {
+          const int pidx = p0 + grp;
+          const bool live = pidx < total;
+          // owner lane of pair pidx: the last lane whose excl <= pidx
+          int owner = 0;
+#pragma unroll
+          for (int st = 16; st > 0; st >>= 1) {
+            const int cand = owner + st;
+            const int ev = __shfl_sync(0xffffffffu, excl, cand & 31);
+            if (cand < 32 && ev <= pidx) owner = cand;
+          }
+          const int e = pidx - __shfl_sync(0xffffffffu, excl, owner);
+          const int rr = q * 32 + owner;
+          const int k = live ? (int)ck[e * kBM + rr] : 0;
+          // (idle groups evaluate row 0 of the tile, which always exists)
+          const float d2 = group_d2<D, XT>(a.X, tile * kBM + (live ? rr : 0), g_mu + (size_t)k * D,
+                                           iso ? g_prec + k : g_prec + (size_t)k * D, iso, gq);
+          if (live && gq == 0) cub[e * kBM + rr] = __ldg(g_c + k) - 0.5f * d2;
+        }
+        __syncwarp();
+      }
+      float lse = 0.f;
+      if (exact) {
+        float mx = -INFINITY, sum = 0.f;
+        for (int e = 0; e < cnt; ++e) mx = fmaxf(mx, cub[e * kBM + r]);
+        for (int e = 0; e < cnt; ++e) sum += expf(cub[e * kBM + r] - mx);
+        lse = mx + logf(sum);
+      }
+      if constexpr (MODE == MODE_EM) {
+        // responsibility records of this tile, in row order: an exclusive
+        // prefix sum of the rows' counts over the 128 rows (published by the
+        // group's four warps).  Rows past the capacity go to the row list.
+        const int my = exact ? cnt : 0;
+        uint16_t* xg = xcg + (g * 2 + (s & 1)) * kBM;
+        xg[r] = (uint16_t)my;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[EXG + g]);
+        if (!warp_wait(&bar[EXG + g], s & 1)) { fail(); break; }
+        // every warp reads all 128 rows' counts (lane: rows 4 lane .. 4 lane + 3)
+        int rc[4], tsum = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          rc[t] = xg[lane * 4 + t];
+          tsum += rc[t];
+        }
+        int incl = tsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const int all = __shfl_sync(0xffffffffu, incl, 31);
+        // exclusive offset of row r = prefix of its group of four + earlier rows in it
+        const int grp4 = r >> 2;
+        int off = __shfl_sync(0xffffffffu, incl - tsum, grp4);
+        const int r0c = __shfl_sync(0xffffffffu, rc[0], grp4);
+        const int r1c = __shfl_sync(0xffffffffu, rc[1], grp4);
+        const int r2c = __shfl_sync(0xffffffffu, rc[2], grp4);
+        const int within = r & 3;
+        off += (within > 0 ? r0c : 0) + (within > 1 ? r1c : 0) + (within > 2 ? r2c : 0);
+        const bool fits = exact && off + my <= a.rec_cap;
+        if (exact && off <= a.rec_cap && off + my > a.rec_cap) a.tile_cnt[tile] = (uint32_t)off;
+        if (r == kBM - 1 && all <= a.rec_cap) a.tile_cnt[tile] = (uint32_t)all;
+        if (fits) {
+          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+          if (a.lse) a.lse[n] = lse;
+          ll_acc += (double)lse;
+          uint2* out = a.recs + (size_t)tile * a.rec_cap + off;
+          for (int e = 0; e < cnt; ++e) {
+            const uint32_t k = ck[e * kBM + r];
+            const float gm = expf(cub[e * kBM + r] - lse);
+            out[e] = make_uint2((k << 7) | (uint32_t)r, __float_as_uint(gm));
+          }
+        }
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !fits);
+        if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
+      } else {
+        if (exact) {
+          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+          if (a.lse) a.lse[n] = lse;
+          // top-m by exact value, ties to the lower component
+          uint32_t taken = 0;
+          for (int t = 0; t < a.m; ++t) {
+            int best = -1, bk = 0x7fffffff;
+            float bv = -INFINITY;
+            for (int e = 0; e < cnt; ++e) {
+              if (taken & (1u << e)) continue;
+              const float v = cub[e * kBM + r];
+              const int k = ck[e * kBM + r];
+              if (best < 0 || v > bv || (v == bv && k < bk)) { best = e; bv = v; bk = k; }
+            }
+            if (best < 0) {
+              a.ids[n * a.m + t] = -1;
+              a.gamma[n * a.m + t] = 0.f;
+              continue;
+            }
+            taken |= 1u << best;
+            a.ids[n * a.m + t] = bk;
+            a.gamma[n * a.m + t] = bv == -INFINITY ? 0.f : expf(bv - lse);
+          }
+        }
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
+        if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
+      }
+      __syncwarp();
+    }
+    if constexpr (MODE == MODE_EM) {
+      const double sacc = warp_sum(ll_acc);
+      if (lane == 0) ll_red[warp] = sacc;
+    }
+    } else {
+    // ------------------------------------ epilogue (streamed parameters)
     const int q = warp & 3, h = warp >> 2;
     const int r = q * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    float* __restrict__ cub = sCUB + h * kCSH * kBM;     // this half's candidate list
-    uint16_t* __restrict__ ck = sCK + h * kCSH * kBM;
+    float* __restrict__ cub = sCUB + h * kCS * kBM;     // this half's candidate list
+    uint16_t* __restrict__ ck = sCK + h * kCS * kBM;
     double ll_acc = 0.0;
     for (int it = 0; it < my_tiles; ++it) {
       if (warp_aborted(abort_flag)) break;
@@ -525,11 +802,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         }
         for (int j = 0; j < nch; ++j) {
           const int64_t g = ((int64_t)it * 2 + pass) * nch + j;
-          const int buf = (int)(g % nbuf);
-          const uint32_t use = (uint32_t)(g / nbuf);
-          const int tb = resident ? j : (int)(g & 1);  // trailer buffer
+          const int buf = (int)(g & 1);             // TMEM buffer and trailer slot
+          const uint32_t use = (uint32_t)(g >> 1);
+          const int tb = buf;
           if (!warp_wait(&bar[T_FULL + buf], use & 1) ||
-              !warp_wait(&bar[TR_FULL + tb], resident ? 0u : (uint32_t)((g >> 1) & 1))) {
+              !warp_wait(&bar[TR_FULL + tb], use & 1)) {
             fail(); ok = false; break;
           }
           tc::tc_fence_after();
@@ -586,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               while (pm) {
                 const int kk = c0 + __ffs(pm) - 1;
                 pm &= pm - 1u;
-                if (cnt < kCSH) {
+                if (cnt < kCS) {
                   ck[cnt * kBM + r] = (uint16_t)(j * kBN + h * kHalf + kk);
                   ++cnt;
                 } else {
@@ -725,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               float bv = -INFINITY;
               for (int e = 0; e < c0 + c1; ++e) {
                 if (taken & (1u << e)) continue;
-                const int hh = e < c0 ? 0 : kCSH;
+                const int hh = e < c0 ? 0 : kCS;
                 const int ee = e < c0 ? e : e - c0;
                 const float v = sCUB[(hh + ee) * kBM + r];
                 const int k = sCK[(hh + ee) * kBM + r];
@@ -755,12 +1032,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       const double s = warp_sum(ll_acc);
       if (lane == 0) ll_red[warp] = s;
     }
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
   if constexpr (MODE == MODE_EM) {
-    if (tid == 0 && a.ll_part)
-      a.ll_part[blockIdx.x] = ((ll_red[0] + ll_red[1]) + ll_red[2]) + ll_red[3];
+    if (tid == 0 && a.ll_part) {
+      double t = 0.0;
+      for (int w = 0; w < kEpiWarps; ++w) t += ll_red[w];
+      a.ll_part[blockIdx.x] = t;
+    }
   }
   if (warp == kMmaWarp) {
     tc::tc_fence_after();
@@ -821,11 +1102,13 @@ fb_compact_kernel(const uint32_t* __restrict__ mask, int64_t N, uint32_t* __rest
 
 template <int D, int XT, int MODE>
 cudaError_t run_screen(const ScreenArgs& args, int grid, cudaStream_t s) {
-  auto kern = tc_screen_kernel<D, XT, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Shape<D>::SMEM);
+  // resident parameters (at most two chunks): the grouped epilogue
+  const bool grp = args.L.tc_chunks <= 2;
+  auto kern = grp ? tc_screen_kernel<D, XT, MODE, true> : tc_screen_kernel<D, XT, MODE, false>;
+  const int smem = grp ? Shape<D, true>::SMEM : Shape<D, false>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Shape<D>::SMEM, s>>>(args);
+  kern<<<grid, kThreads, smem, s>>>(args);
   return cudaGetLastError();
 }
 
