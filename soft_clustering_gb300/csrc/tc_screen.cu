@@ -317,12 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   const bool resident = GRP;  // parameter chunks loaded once and kept (K <= 256)
   // TMEM buffer (and trailer slot) and its use count for contraction gi
   // (pass gi / nch, chunk gi % nch) of tile it: grouped, chunk j of the
-  // group's tiles keeps buffer 2g + j, the passes in turn; streamed, the
-  // contractions alternate over two buffers
+  // group's tiles keeps buffer 2g + j, contracted once and swept by both
+  // passes; streamed, each pass contracts again and the contractions
+  // alternate over two buffers
+  const int ncontr = GRP ? nch : 2 * nch;  // contractions per tile
   auto tbuf = [&](int it, int gi, int* buf, uint32_t* use) {
     if constexpr (GRP) {
-      *buf = 2 * (it & 1) + gi % nch;
-      *use = (uint32_t)(2 * (it >> 1) + gi / nch);
+      *buf = 2 * (it & 1) + gi % nch;   // one contraction per chunk, swept twice
+      *use = (uint32_t)(it >> 1);
     } else {
       const int64_t gq = (int64_t)it * 2 * nch + gi;
       *buf = (int)(gq & 1);
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issue + loads
     if (lane == 0 && my_tiles > 0) {
-      const int64_t total = (int64_t)my_tiles * 2 * nch;  // two passes per tile
+      const int64_t total = (int64_t)my_tiles * ncontr;
       auto load_b = [&](int64_t g) {
         const int buf = (int)(g & 1), c = (int)(g % nch);
         tc::mbar_arrive_expect_tx(&bar[B_FULL + buf], S::B_BYTES);
@@ -402,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       for (int it = 0; it < my_tiles && ok; ++it) {
         if (!tc::mbar_wait(&bar[A_FULL], it & 1, kWait)) { fail(); ok = false; break; }
         tc::tc_fence_after();
-        for (int gi = 0; gi < 2 * nch; ++gi) {
+        for (int gi = 0; gi < ncontr; ++gi) {
           const int j = gi % nch;
-          const int64_t g = (int64_t)it * 2 * nch + gi;
+          const int64_t g = (int64_t)it * ncontr + gi;
           const int sbuf = (int)(g & 1);               // streamed B buffer
           int buf;                                     // TMEM buffer and trailer slot
           uint32_t use;
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           }
           if (!resident) tc::mma_commit(&bar[B_EMPTY + sbuf]);
           tc::mma_commit(&bar[T_FULL + buf]);
-          if (gi == 2 * nch - 1) tc::mma_commit(&bar[A_EMPTY]);
+          if (gi == ncontr - 1) tc::mma_commit(&bar[A_EMPTY]);
           if (!resident && g + 1 < total && g + 1 >= 2) {
             // refill the other buffer once the MMAs of chunk g-1 are done
             const int pb = (int)((g + 1) & 1);
@@ -544,8 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       int cnt = 0;
       bool ok = true;
       float thr = -INFINITY;  // the point's window, fixed after pass 0
-      // pass 0: lower bounds only; pass 1 (a second contraction of the same
-      // tile): candidates against the point's final window
+      // pass 0: lower bounds only; pass 1 (a second sweep of the same
+      // accumulators): candidates against the point's final window
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) {
           thr = ref - kT;
@@ -556,12 +558,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         for (int j = 0; j < nch; ++j) {
           int buf;
           uint32_t use;
-          tbuf(it, pass * nch + j, &buf, &use);
-          if (!warp_wait(&bar[T_FULL + buf], use & 1) ||
-              !warp_wait(&bar[TR_FULL + buf], use & 1)) {
-            fail(); ok = false; break;
+          tbuf(it, j, &buf, &use);
+          if (pass == 0) {
+            if (!warp_wait(&bar[T_FULL + buf], use & 1) ||
+                !warp_wait(&bar[TR_FULL + buf], use & 1)) {
+              fail(); ok = false; break;
+            }
+            tc::tc_fence_after();
           }
-          tc::tc_fence_after();
           // (the trailer and the candidate lists never overlap)
           const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4);
           const float* __restrict__ tcn = tsc + kBN;
@@ -624,9 +628,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               }
             }
           }
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
+          if (pass == 1) {  // the buffer (and its trailer) is free after the second sweep
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
+          }
         }
       }
       __syncwarp();
