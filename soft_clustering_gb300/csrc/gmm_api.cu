@@ -38,7 +38,7 @@ size_t sparse_stats_ws_bytes(int64_t rows, int D, int K, int rec_cap);
 bool sparse_stats_supported(int K);
 cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
                          int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
-                         void* sws, double* part, int accumulate, cudaStream_t s);
+                         void* sws, double* part, int accumulate, double* ll, cudaStream_t s);
 int simt_stat_chunk(int D, int cov);
 cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
                          const float* centre, const int32_t* prep_flags, float var_floor,
@@ -192,9 +192,12 @@ struct ProfScope {
 
 // The E-step and statistics for one block of rows, accumulating into the
 // workspace partials (accumulate = 0 for the first block of an iteration).
+// lse: LSE_n of the rows (the caller's array, or workspace); want_lse: the
+// caller asked for it (otherwise the screen skips the exact log joint of
+// points with a single candidate).
 gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int K, int cov,
-                      const WsLayout& W, void* ws, float* lse, int accumulate, bool tc,
-                      cudaStream_t s) {
+                      const WsLayout& W, void* ws, float* lse, bool want_lse, int accumulate,
+                      bool tc, cudaStream_t s) {
   DeviceStatus* st = at<DeviceStatus>(ws, W.off_status);
   const void* prep = at<char>(ws, W.off_prep);
   double* llp = at<double>(ws, W.off_llpart);
@@ -217,7 +220,8 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
       const int g1 = tc_screen_grid(sn);
       {
         GMM_PROF("tc_screen_kernel");
-        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, ls, llp, 0, nullptr, nullptr, fbm,
+        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, want_lse ? ls : nullptr, llp, 0,
+                          nullptr, nullptr, fbm,
                           recs, tcnt, kRecCap, st, s));
       }
       {
@@ -236,7 +240,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
       {
         GMM_PROF("sparse_stats");
         GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, tcnt, recs, kRecCap,
-                             at<char>(ws, W.off_sws), part, acc, s));
+                             at<char>(ws, W.off_sws), part, acc, at<double>(ws, W.off_ll), s));
       }
       {
         GMM_PROF("stats_rows_kernel");
@@ -388,7 +392,8 @@ gmm_status gmm_em_step(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
     GMM_TRY(launch_prepare(params, D, K, cov, o.ridge_rel, prep, st, s));
   }
   float* lse = lse_dev ? lse_dev : at<float>(ws, W.off_lse);
-  gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, 0, use_tc(D, K, cov, o), s);
+  gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, lse_dev != nullptr, 0,
+                            use_tc(D, K, cov, o), s);
   if (r != GMM_OK) return r;
   {
     GMM_PROF("mstep_kernel");
@@ -445,7 +450,7 @@ gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int
     GMM_TRY(cudaEventRecord(res->copied[b], res->copy));
     GMM_TRY(cudaStreamWaitEvent(s, res->copied[b], 0));
     gmm_status r = estep_rows(stage[b], xdtype, rn, D, K, cov, W, ws, at<float>(ws, W.off_lse),
-                              ci > 0, use_tc(D, K, cov, o), s);
+                              false, ci > 0, use_tc(D, K, cov, o), s);
     if (r != GMM_OK) return r;
     GMM_TRY(cudaEventRecord(res->consumed[b], s));
   }

@@ -53,6 +53,12 @@ __host__ __device__ inline bool tc_eligible(int D, int cov) {
   return (cov == GMM_COV_DIAG || cov == GMM_COV_ISO) && (D == 64 || D == 128);
 }
 
+// Responsibility records of the tensor-core E-step: uint2 {key, gamma bits},
+// key = flag | (component << 7) | row in the 128-point tile.  The flag marks
+// a point's only candidate (gamma 1, its exact log joint not evaluated).
+constexpr uint32_t kRecSingle = 1u << 31;
+constexpr uint32_t kRecKMask = 0xffffffu;  // component = (key >> 7) & kRecKMask
+
 // Prepared-parameter block written by gmm_prepare.
 struct PreparedLayout {
   int D, K, cov;

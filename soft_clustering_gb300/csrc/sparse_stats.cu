@@ -15,17 +15,25 @@
 //   reduce   one warp per chunk: gathers the chunk's rows of X (sixteen in
 //            flight), accumulates g, g y, g y^2 with y = x - c_k about the
 //            component's input mean c_k (lane l: dimensions l*D/32 ..
-//            (l+1)*D/32 - 1) and writes the chunk's fp32 sums
+//            (l+1)*D/32 - 1), and for the flagged records of points with a
+//            single candidate (g = 1) their count and sum of y^2, and writes
+//            the chunk's fp32 sums
 //   merge    one warp per component: adds its chunks in fp64 in order and
 //            writes [S0 | S1 about c | M2 about the mean], the partial the
 //            M-step merges (continuing the partial of an earlier call when
-//            accumulating over slabs or chunks of host data).
+//            accumulating over slabs or chunks of host data); and the
+//            log-likelihood of its single-candidate points,
+//            n1 c_k - 1/2 sum_d w_kd Q_d (their LSE is their log joint).
 // Every sum is taken in a fixed order, so results are the same on every run.
 #include <math.h>
 
 #include "gmm_internal.cuh"
 
 namespace gmm {
+
+cudaError_t launch_ll_finalize(const double* ll_part, int64_t n, double* out, int accumulate,
+                               cudaStream_t s);
+
 namespace {
 
 constexpr int kTile = 128;       // points per record tile
@@ -38,7 +46,7 @@ constexpr int kMaxSparseK = 16384;
 
 struct SparseLayout {
   int64_t ntiles, nb, max_recs, max_chunks;
-  size_t off_counts, off_ktot, off_cstart, off_kstart, off_sorted, off_cpart, bytes;
+  size_t off_counts, off_ktot, off_cstart, off_kstart, off_sorted, off_cpart, off_llk, bytes;
   static SparseLayout make(int64_t rows, int D, int K, int rec_cap) {
     SparseLayout S;
     S.ntiles = (rows + kTile - 1) / kTile;
@@ -51,7 +59,8 @@ struct SparseLayout {
     S.off_cstart = o; o = align_up(o + sizeof(uint32_t) * (size_t)(K + 1));
     S.off_kstart = o; o = align_up(o + sizeof(uint32_t) * (size_t)(K + 1));
     S.off_sorted = o; o = align_up(o + sizeof(uint2) * (size_t)S.max_recs);
-    S.off_cpart = o;  o = align_up(o + sizeof(float) * (size_t)S.max_chunks * (1 + 2 * D));
+    S.off_cpart = o;  o = align_up(o + sizeof(float) * (size_t)S.max_chunks * (2 + 3 * D));
+    S.off_llk = o;    o = align_up(o + sizeof(double) * (size_t)K);
     S.bytes = o;
     return S;
   }
@@ -71,7 +80,7 @@ rec_count_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restrict_
     const uint32_t c = tile_cnt[t];
     const int cnt = c < (uint32_t)rec_cap ? (int)c : rec_cap;
     for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
-      const uint32_t k = recs[(size_t)t * rec_cap + i].x >> 7;
+      const uint32_t k = (recs[(size_t)t * rec_cap + i].x >> 7) & kRecKMask;
       if (k < (uint32_t)K) atomicAdd(&hist[k], 1u);
     }
   }
@@ -162,7 +171,8 @@ rec_scan_comps_kernel(const uint32_t* __restrict__ ktot, int K, uint32_t* __rest
 }
 
 // scatter: the warp of block b places the block's records, in point order,
-// at their component's offsets: sorted[] = {point index in this call, gamma}.
+// at their component's offsets: sorted[] = {single flag | point index in
+// this call, gamma}.
 __global__ void __launch_bounds__(32)
 rec_scatter_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restrict__ recs,
                    int rec_cap, int64_t ntiles, int K, int64_t nb,
@@ -182,12 +192,13 @@ rec_scatter_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restric
       const bool live = i < cnt;
       uint2 rec = make_uint2(0xffffffffu, 0u);
       if (live) rec = recs[(size_t)t * rec_cap + i];
-      const uint32_t k = rec.x >> 7;
+      const uint32_t k = (rec.x >> 7) & kRecKMask;
       const bool ok = live && k < (uint32_t)K;
       const unsigned grp = __match_any_sync(0xffffffffu, ok ? k : 0xffffffffu);
       if (ok) {
         const uint32_t pos = cursor[k] + __popc(grp & ((1u << lane) - 1u));
-        sorted[pos] = make_uint2((uint32_t)(t * kTile + (rec.x & 127)), rec.y);
+        sorted[pos] = make_uint2((uint32_t)(t * kTile + (rec.x & 127)) | (rec.x & kRecSingle),
+                                 rec.y);
       }
       __syncwarp();
       if (ok && lane == 31 - __clz(grp)) cursor[k] += __popc(grp);
@@ -226,13 +237,14 @@ __device__ __forceinline__ void global_row(const void* X, int64_t n, int d0, flo
 }
 
 // reduce: warp-per-chunk, grid-stride over the chunks; chunk sums
-// cpart[c] = [s0 | s1 (D) | s2 (D)] in fp32.
+// cpart[c] = [s0 | s1 (D) | s2 (D) | n1 | q1 (D)] in fp32 (n1, q1: count
+// and sum of y^2 of the flagged single-candidate records).
 template <int D, int XT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ mu,
                   const uint32_t* __restrict__ cstart, const uint32_t* __restrict__ kstart,
                   const uint2* __restrict__ sorted, float* __restrict__ cpart) {
-  constexpr int DPL = D / 32, F = 1 + 2 * D, B = 16;
+  constexpr int DPL = D / 32, F = 2 + 3 * D, B = 16;
   const int lane = threadIdx.x & 31;
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -247,21 +259,23 @@ rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ m
     const int k = lo;
     const uint32_t r0 = cstart[k] + (uint32_t)(c - kstart[k]) * kCH;
     const uint32_t r1 = min(cstart[k + 1], r0 + kCH);
-    float cen[DPL], s1[DPL], s2[DPL], s0 = 0.f;
+    float cen[DPL], s1[DPL], s2[DPL], q1[DPL], s0 = 0.f, n1 = 0.f;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) {
       cen[i] = __ldg(mu + (size_t)k * D + lane * DPL + i);
-      s1[i] = s2[i] = 0.f;
+      s1[i] = s2[i] = q1[i] = 0.f;
     }
     for (uint32_t r = r0; r < r1; r += B) {
       const uint2 mine = (lane < B && r + lane < r1) ? sorted[r + lane] : make_uint2(0u, 0u);
       float x[B][DPL];
       float g[B];
+      uint32_t single = 0u;  // bit u: record r + u is flagged
 #pragma unroll
       for (int u = 0; u < B; ++u) {
-        const uint32_t n = __shfl_sync(0xffffffffu, mine.x, u);
+        const uint32_t key = __shfl_sync(0xffffffffu, mine.x, u);
         g[u] = __uint_as_float(__shfl_sync(0xffffffffu, mine.y, u));
-        if (r + u < r1) global_row<XT, D, DPL>(X, n, lane * DPL, x[u]);
+        single |= (key & kRecSingle) ? (1u << u) : 0u;
+        if (r + u < r1) global_row<XT, D, DPL>(X, key & ~kRecSingle, lane * DPL, x[u]);
       }
 #pragma unroll
       for (int u = 0; u < B; ++u) {
@@ -272,8 +286,10 @@ rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ m
           const float gy = g[u] * y;
           s1[i] += gy;
           s2[i] = fmaf(gy, y, s2[i]);
+          if (single & (1u << u)) q1[i] = fmaf(y, y, q1[i]);
         }
         s0 += g[u];
+        if (single & (1u << u)) n1 += 1.f;
       }
     }
     float* o = cpart + (size_t)c * F;
@@ -281,32 +297,46 @@ rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ m
     for (int i = 0; i < DPL; ++i) {
       o[1 + lane * DPL + i] = s1[i];
       o[1 + D + lane * DPL + i] = s2[i];
+      o[2 + 2 * D + lane * DPL + i] = q1[i];
     }
-    if (lane == 0) o[0] = s0;
+    if (lane == 0) {
+      o[0] = s0;
+      o[1 + 2 * D] = n1;
+    }
   }
 }
 
-// merge: warp-per-component; partial [S0 | S1 about c | M2 about the mean].
+// merge: warp-per-component; partial [S0 | S1 about c | M2 about the mean],
+// and llk[k] = n1 c_k - 1/2 sum_d w_kd Q_d, the log-likelihood of the
+// component's single-candidate points (each one's LSE is its log joint
+// c_k - 1/2 sum_d w_kd (x_d - c_kd)^2, the centre c_k being the input mean).
 template <int D>
 __global__ void __launch_bounds__(256)
 rec_merge_kernel(int K, const uint32_t* __restrict__ kstart, const float* __restrict__ cpart,
-                 double* __restrict__ part, int accumulate) {
-  constexpr int F = 1 + 2 * D;
+                 const float* __restrict__ bias_c, const float* __restrict__ prec, bool iso,
+                 double* __restrict__ part, double* __restrict__ llk, int accumulate) {
+  constexpr int F = 1 + 2 * D, FC = 2 + 3 * D;
   const int lane = threadIdx.x & 31;
   const int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (k >= K) return;
   double* o = part + (size_t)k * F;
   const uint32_t c0 = kstart[k], c1 = kstart[k + 1];
-  double s0 = 0.0;
-  for (uint32_t c = c0; c < c1; ++c) s0 += (double)cpart[(size_t)c * F];
+  double s0 = 0.0, n1 = 0.0;
+  for (uint32_t c = c0; c < c1; ++c) {
+    s0 += (double)cpart[(size_t)c * FC];
+    n1 += (double)cpart[(size_t)c * FC + 1 + 2 * D];
+  }
   const double S0o = accumulate ? o[0] : 0.0;
   const double S0 = S0o + s0;
+  double wq = 0.0;  // this lane's part of sum_d w_kd Q_d
   for (int d = lane; d < D; d += 32) {
-    double S1 = 0.0, S2c = 0.0;
+    double S1 = 0.0, S2c = 0.0, Q = 0.0;
     for (uint32_t c = c0; c < c1; ++c) {
-      S1 += (double)cpart[(size_t)c * F + 1 + d];
-      S2c += (double)cpart[(size_t)c * F + 1 + D + d];
+      S1 += (double)cpart[(size_t)c * FC + 1 + d];
+      S2c += (double)cpart[(size_t)c * FC + 1 + D + d];
+      Q += (double)cpart[(size_t)c * FC + 2 + 2 * D + d];
     }
+    wq += (double)(iso ? prec[k] : prec[(size_t)k * D + d]) * Q;
     if (accumulate) {
       // continue the earlier partial: its second moment back about c
       const double o1 = o[1 + d];
@@ -316,8 +346,12 @@ rec_merge_kernel(int K, const uint32_t* __restrict__ kstart, const float* __rest
     o[1 + d] = S1;
     o[1 + D + d] = S0 > 0.0 ? S2c - S1 * S1 / S0 : 0.0;
   }
+  wq = warp_sum(wq);
   __syncwarp();
-  if (lane == 0) o[0] = S0;
+  if (lane == 0) {
+    o[0] = S0;
+    llk[k] = n1 > 0.0 ? n1 * (double)bias_c[k] - 0.5 * wq : 0.0;
+  }
 }
 
 int g_sms = 0;
@@ -332,13 +366,14 @@ size_t sparse_stats_ws_bytes(int64_t rows, int D, int K, int rec_cap) {
 bool sparse_stats_supported(int K) { return K <= kMaxSparseK; }
 
 // Diagonal / isotropic statistics (the partial layout is the same for both;
-// the isotropic M-step averages the diagonal) into ONE partial slot, part.
+// the isotropic M-step averages the diagonal) into ONE partial slot, part;
+// adds the log-likelihood of the single-candidate points to *ll.
 // prepared: the block written for this call's parameters (its mean array is
 // the centre c).  accumulate: continue the partial of an earlier call.
 // sws: sparse_stats_ws_bytes(N, D, K, rec_cap) bytes, 256-byte aligned.
 cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
                          int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
-                         void* sws, double* part, int accumulate, cudaStream_t s) {
+                         void* sws, double* part, int accumulate, double* ll, cudaStream_t s) {
   if (K > kMaxSparseK || (D != 64 && D != 128)) return cudaErrorInvalidValue;
   const SparseLayout S = SparseLayout::make(N, D, K, rec_cap);
   const PreparedLayout L = PreparedLayout::make(D, K, cov);
@@ -389,9 +424,19 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
 #undef GMM_REDUCE
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const unsigned mblocks = (unsigned)(((int64_t)K * 32 + 255) / 256);
-  if (D == 128) rec_merge_kernel<128><<<mblocks, 256, 0, s>>>(K, kstart, cpart, part, accumulate);
-  else rec_merge_kernel<64><<<mblocks, 256, 0, s>>>(K, kstart, cpart, part, accumulate);
-  return cudaGetLastError();
+  const float* bias_c = at<float>(prepared, L.off_c);
+  const float* prec = at<float>(prepared, L.off_prec);
+  double* llk = at<double>(sws, S.off_llk);
+  const bool iso = cov == GMM_COV_ISO;
+  if (D == 128)
+    rec_merge_kernel<128><<<mblocks, 256, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
+                                                  accumulate);
+  else
+    rec_merge_kernel<64><<<mblocks, 256, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
+                                                 accumulate);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the single-candidate points' log-likelihood joins the total
+  return launch_ll_finalize(llk, K, ll, 1, s);
 }
 
 }  // namespace gmm

@@ -65,6 +65,7 @@ constexpr uint32_t kWait = 1u << 22;
 
 enum { MODE_EM = 0, MODE_ASSIGN = 1 };
 
+
 struct ScreenArgs {
   const void* X;
   int64_t N;
@@ -72,7 +73,7 @@ struct ScreenArgs {
   int m;                 // top-m (assign mode)
   const void* prepared;
   PreparedLayout L;
-  float* lse;            // [N] or null
+  float* lse;            // [N] or null (null: single-candidate points skip the refine)
   double* ll_part;       // [gridDim.x] (EM) or null
   int32_t* ids;          // [N*m] (assign)
   float* gamma;          // [N*m] (assign)
@@ -639,11 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       if (lane == 0) tc::mbar_arrive(&bar[R_FREE + g]);
       if (!ok) break;
       const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
-      // exact log joints of the candidates (same arithmetic as the CUDA-core
-      // kernels): the warp's (row, candidate) pairs are numbered by an
-      // exclusive scan of the counts and taken eight at a time
+      // a point with a single candidate has gamma = 1 (every other component
+      // lies more than 40 nats below it); unless LSE_n is wanted its exact
+      // log joint is not needed here (the statistics give its
+      // log-likelihood term)
+      const bool single = exact && cnt == 1 && a.lse == nullptr;
+      // exact log joints of the other points' candidates (same arithmetic as
+      // the CUDA-core kernels): the warp's (row, candidate) pairs are
+      // numbered by an exclusive scan of the counts and taken eight at a time
       {
-        const int mycnt = exact ? cnt : 0;
+        const int mycnt = (exact && !single) ? cnt : 0;
         int incl = mycnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -676,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         __syncwarp();
       }
       float lse = 0.f;
-      if (exact) {
+      if (exact && !single) {
         float mx = -INFINITY, sum = 0.f;
         for (int e = 0; e < cnt; ++e) mx = fmaxf(mx, cub[e * kBM + r]);
         for (int e = 0; e < cnt; ++e) sum += expf(cub[e * kBM + r] - mx);
@@ -718,20 +724,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         if (exact && off <= a.rec_cap && off + my > a.rec_cap) a.tile_cnt[tile] = (uint32_t)off;
         if (r == kBM - 1 && all <= a.rec_cap) a.tile_cnt[tile] = (uint32_t)all;
         if (fits) {
-          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
-          if (a.lse) a.lse[n] = lse;
-          ll_acc += (double)lse;
           uint2* out = a.recs + (size_t)tile * a.rec_cap + off;
-          for (int e = 0; e < cnt; ++e) {
-            const uint32_t k = ck[e * kBM + r];
-            const float gm = expf(cub[e * kBM + r] - lse);
-            out[e] = make_uint2((k << 7) | (uint32_t)r, __float_as_uint(gm));
+          if (single) {
+            // flagged record: gamma 1, log-likelihood term from the statistics
+            out[0] = make_uint2(kRecSingle | ((uint32_t)ck[r] << 7) | (uint32_t)r,
+                                __float_as_uint(1.f));
+          } else {
+            if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+            if (a.lse) a.lse[n] = lse;
+            ll_acc += (double)lse;
+            for (int e = 0; e < cnt; ++e) {
+              const uint32_t k = ck[e * kBM + r];
+              const float gm = expf(cub[e * kBM + r] - lse);
+              out[e] = make_uint2((k << 7) | (uint32_t)r, __float_as_uint(gm));
+            }
           }
         }
         const unsigned fbm = __ballot_sync(0xffffffffu, valid && !fits);
         if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
       } else {
-        if (exact) {
+        if (single) {
+          a.ids[n * a.m] = ck[r];
+          a.gamma[n * a.m] = 1.f;
+          for (int t = 1; t < a.m; ++t) {
+            a.ids[n * a.m + t] = -1;
+            a.gamma[n * a.m + t] = 0.f;
+          }
+        } else if (exact) {
           if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
           if (a.lse) a.lse[n] = lse;
           // top-m by exact value, ties to the lower component
