@@ -26,7 +26,8 @@ cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int co
                       uint32_t* tile_cnt, int rec_cap, DeviceStatus* st, cudaStream_t s);
 int tc_screen_grid(int64_t N);
 cudaError_t fb_compact(const uint32_t* fb_mask, int64_t N, uint32_t* rows, uint32_t* count,
-                       cudaStream_t s);
+                       uint32_t* segcnt, cudaStream_t s);
+int fb_compact_segments(int64_t N);
 cudaError_t simt_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                        const void* prepared, const float* lse, int parts, double* part,
                        int accumulate, cudaStream_t s);
@@ -76,7 +77,7 @@ int stat_parts(int64_t N, int D, int K, int cov) {
 
 struct WsLayout {
   size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_fb,
-      off_fbm, off_rec, off_tcnt, off_sws, off_stage, bytes;
+      off_fbm, off_fbseg, off_rec, off_tcnt, off_sws, off_stage, bytes;
   int parts;          // statistics partials of the CUDA-core path
   int sp_parts;       // tensor-core path: the records' partial (1) ...
   int lp_parts;       // ... followed by those of the row-list pass
@@ -122,6 +123,7 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_fb = o;     o = align_up(o + sizeof(uint32_t) * (size_t)(tc ? slab : rows));
   const size_t slab_tiles = tc ? (size_t)((slab + 127) / 128) : 0;
   W.off_fbm = o;    o = align_up(o + sizeof(uint32_t) * 4 * slab_tiles);
+  W.off_fbseg = o;  o = align_up(o + sizeof(uint32_t) * (tc ? fb_compact_segments(slab) : 0));
   W.off_rec = o;    o = align_up(o + sizeof(uint2) * slab_tiles * kRecCap);
   W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * slab_tiles);
   W.off_sws = o;    o = align_up(o + (tc ? sparse_stats_ws_bytes(slab, D, K, kRecCap) : 0));
@@ -226,7 +228,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
       }
       {
         GMM_PROF("fb_compact_kernel");
-        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, s));
+        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
       }
       {
         GMM_PROF("lse_rows_kernel");
@@ -500,7 +502,7 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
       }
       {
         GMM_PROF("fb_compact_kernel");
-        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, s));
+        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
       }
       GMM_PROF("lse_rows_kernel");
       GMM_TRY(simt_lse_rows(Xs, xdtype, sn, D, K, cov, prepared, ls, nullptr, m, is, gs, st, fb,

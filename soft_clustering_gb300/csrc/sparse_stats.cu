@@ -18,7 +18,7 @@
 //            (l+1)*D/32 - 1), and for the flagged records of points with a
 //            single candidate (g = 1) their count and sum of y^2, and writes
 //            the chunk's fp32 sums
-//   merge    one warp per component: adds its chunks in fp64 in order and
+//   merge    one block per component: adds its chunks in fp64 in order and
 //            writes [S0 | S1 about c | M2 about the mean], the partial the
 //            M-step merges (continuing the partial of an earlier call when
 //            accumulating over slabs or chunks of host data); and the
@@ -265,8 +265,11 @@ rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ m
       cen[i] = __ldg(mu + (size_t)k * D + lane * DPL + i);
       s1[i] = s2[i] = q1[i] = 0.f;
     }
+    // the next batch's record is requested before this batch's rows
+    uint2 nxt = (lane < B && r0 + lane < r1) ? sorted[r0 + lane] : make_uint2(0u, 0u);
     for (uint32_t r = r0; r < r1; r += B) {
-      const uint2 mine = (lane < B && r + lane < r1) ? sorted[r + lane] : make_uint2(0u, 0u);
+      const uint2 mine = nxt;
+      if (r + B < r1) nxt = (lane < B && r + B + lane < r1) ? sorted[r + B + lane] : make_uint2(0u, 0u);
       float x[B][DPL];
       float g[B];
       uint32_t single = 0u;  // bit u: record r + u is flagged
@@ -306,51 +309,48 @@ rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ m
   }
 }
 
-// merge: warp-per-component; partial [S0 | S1 about c | M2 about the mean],
-// and llk[k] = n1 c_k - 1/2 sum_d w_kd Q_d, the log-likelihood of the
-// component's single-candidate points (each one's LSE is its log joint
-// c_k - 1/2 sum_d w_kd (x_d - c_kd)^2, the centre c_k being the input mean).
+// merge: one block of D threads per component (thread d: dimension d);
+// partial [S0 | S1 about c | M2 about the mean], and llk[k] = n1 c_k - 1/2
+// sum_d w_kd Q_d, the log-likelihood of the component's single-candidate
+// points (each one's LSE is its log joint c_k - 1/2 sum_d w_kd (x_d -
+// c_kd)^2, the centre c_k being the input mean).
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(D)
 rec_merge_kernel(int K, const uint32_t* __restrict__ kstart, const float* __restrict__ cpart,
                  const float* __restrict__ bias_c, const float* __restrict__ prec, bool iso,
                  double* __restrict__ part, double* __restrict__ llk, int accumulate) {
   constexpr int F = 1 + 2 * D, FC = 2 + 3 * D;
-  const int lane = threadIdx.x & 31;
-  const int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (k >= K) return;
+  __shared__ double red[D / 32];
+  const int k = blockIdx.x, d = threadIdx.x, lane = d & 31;
   double* o = part + (size_t)k * F;
   const uint32_t c0 = kstart[k], c1 = kstart[k + 1];
-  double s0 = 0.0, n1 = 0.0;
+  double s0 = 0.0, n1 = 0.0, S1 = 0.0, S2c = 0.0, Q = 0.0;
   for (uint32_t c = c0; c < c1; ++c) {
-    s0 += (double)cpart[(size_t)c * FC];
-    n1 += (double)cpart[(size_t)c * FC + 1 + 2 * D];
+    const float* cp = cpart + (size_t)c * FC;
+    s0 += (double)cp[0];
+    n1 += (double)cp[1 + 2 * D];
+    S1 += (double)cp[1 + d];
+    S2c += (double)cp[1 + D + d];
+    Q += (double)cp[2 + 2 * D + d];
   }
   const double S0o = accumulate ? o[0] : 0.0;
   const double S0 = S0o + s0;
-  double wq = 0.0;  // this lane's part of sum_d w_kd Q_d
-  for (int d = lane; d < D; d += 32) {
-    double S1 = 0.0, S2c = 0.0, Q = 0.0;
-    for (uint32_t c = c0; c < c1; ++c) {
-      S1 += (double)cpart[(size_t)c * FC + 1 + d];
-      S2c += (double)cpart[(size_t)c * FC + 1 + D + d];
-      Q += (double)cpart[(size_t)c * FC + 2 + 2 * D + d];
-    }
-    wq += (double)(iso ? prec[k] : prec[(size_t)k * D + d]) * Q;
-    if (accumulate) {
-      // continue the earlier partial: its second moment back about c
-      const double o1 = o[1 + d];
-      S2c += o[1 + D + d] + (S0o > 0.0 ? o1 * o1 / S0o : 0.0);
-      S1 += o1;
-    }
-    o[1 + d] = S1;
-    o[1 + D + d] = S0 > 0.0 ? S2c - S1 * S1 / S0 : 0.0;
+  if (accumulate) {
+    // continue the earlier partial: its second moment back about c
+    const double o1 = o[1 + d];
+    S2c += o[1 + D + d] + (S0o > 0.0 ? o1 * o1 / S0o : 0.0);
+    S1 += o1;
   }
-  wq = warp_sum(wq);
-  __syncwarp();
-  if (lane == 0) {
+  const double wq = warp_sum((double)(iso ? prec[k] : prec[(size_t)k * D + d]) * Q);
+  if (lane == 0) red[d >> 5] = wq;
+  __syncthreads();  // every thread has read o[0] (S0o) before it is rewritten
+  o[1 + d] = S1;
+  o[1 + D + d] = S0 > 0.0 ? S2c - S1 * S1 / S0 : 0.0;
+  if (d == 0) {
+    double t = 0.0;
+    for (int w = 0; w < D / 32; ++w) t += red[w];
     o[0] = S0;
-    llk[k] = n1 > 0.0 ? n1 * (double)bias_c[k] - 0.5 * wq : 0.0;
+    llk[k] = n1 > 0.0 ? n1 * (double)bias_c[k] - 0.5 * t : 0.0;
   }
 }
 
@@ -423,17 +423,17 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
   }
 #undef GMM_REDUCE
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const unsigned mblocks = (unsigned)(((int64_t)K * 32 + 255) / 256);
+
   const float* bias_c = at<float>(prepared, L.off_c);
   const float* prec = at<float>(prepared, L.off_prec);
   double* llk = at<double>(sws, S.off_llk);
   const bool iso = cov == GMM_COV_ISO;
   if (D == 128)
-    rec_merge_kernel<128><<<mblocks, 256, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
-                                                  accumulate);
+    rec_merge_kernel<128><<<K, 128, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
+                                            accumulate);
   else
-    rec_merge_kernel<64><<<mblocks, 256, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
-                                                 accumulate);
+    rec_merge_kernel<64><<<K, 64, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
+                                          accumulate);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the single-candidate points' log-likelihood joins the total
   return launch_ll_finalize(llk, K, ll, 1, s);

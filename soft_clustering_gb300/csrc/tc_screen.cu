@@ -1074,27 +1074,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   }
 }
 
-// Ascending list of the rows whose bit is set in the hand-over bitmap
-// (word w covers rows 32w .. 32w + 31): one block; each thread owns a
-// contiguous range of words, counts, takes its offset from a block-wide
-// exclusive scan and writes its rows in order.
-constexpr int kCompactThreads = 1024;
-__global__ void __launch_bounds__(kCompactThreads)
-fb_compact_kernel(const uint32_t* __restrict__ mask, int64_t N, uint32_t* __restrict__ rows,
-                  uint32_t* __restrict__ count) {
-  __shared__ uint32_t wsum[kCompactThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Ascending list of the rows whose bit is set in the hand-over bitmap (word
+// w covers rows 32w .. 32w + 31), in two passes over segments of kSegWords
+// words: count per segment, then each segment's block takes its offset (the
+// sum of the earlier segments' counts), scans its threads' counts (8
+// consecutive words each) and writes its rows in order.
+constexpr int kSegThreads = 256;
+constexpr int kSegWords = kSegThreads * 8;
+
+__device__ __forceinline__ uint32_t fb_word(const uint32_t* mask, int64_t N, int64_t w) {
+  uint32_t m = mask[w];
+  const int64_t left = N - w * 32;
+  if (left < 32) m &= (1u << left) - 1u;
+  return m;
+}
+
+__global__ void __launch_bounds__(kSegThreads)
+fb_count_kernel(const uint32_t* __restrict__ mask, int64_t N, uint32_t* __restrict__ segcnt) {
+  __shared__ uint32_t wsum[kSegThreads / 32];
   const int64_t nwords = (N + 31) / 32;
-  const int64_t per = (nwords + kCompactThreads - 1) / kCompactThreads;
-  const int64_t w0 = min(nwords, (int64_t)tid * per), w1 = min(nwords, w0 + per);
-  auto word = [&](int64_t w) {
-    uint32_t m = mask[w];
-    const int64_t left = N - w * 32;
-    if (left < 32) m &= (1u << left) - 1u;
-    return m;
-  };
-  uint32_t mine = 0;
-  for (int64_t w = w0; w < w1; ++w) mine += __popc(word(w));
+  const int64_t w0 = (int64_t)blockIdx.x * kSegWords + threadIdx.x * 8;
+  uint32_t c = 0;
+  for (int i = 0; i < 8; ++i)
+    if (w0 + i < nwords) c += __popc(fb_word(mask, N, w0 + i));
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int i = 0; i < kSegThreads / 32; ++i) t += wsum[i];
+    segcnt[blockIdx.x] = t;
+  }
+}
+
+__global__ void __launch_bounds__(kSegThreads)
+fb_write_kernel(const uint32_t* __restrict__ mask, int64_t N, const uint32_t* __restrict__ segcnt,
+                uint32_t* __restrict__ rows, uint32_t* __restrict__ count) {
+  __shared__ uint32_t wsum[kSegThreads / 32];
+  __shared__ uint32_t base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    uint32_t b = 0;
+    for (unsigned i = 0; i < blockIdx.x; ++i) b += segcnt[i];
+    base = b;
+  }
+  const int64_t nwords = (N + 31) / 32;
+  const int64_t w0 = (int64_t)blockIdx.x * kSegWords + tid * 8;
+  uint32_t words[8], mine = 0;
+  for (int i = 0; i < 8; ++i) {
+    words[i] = w0 + i < nwords ? fb_word(mask, N, w0 + i) : 0u;
+    mine += __popc(words[i]);
+  }
   uint32_t incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -1103,26 +1133,18 @@ fb_compact_kernel(const uint32_t* __restrict__ mask, int64_t N, uint32_t* __rest
   }
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    uint32_t t = wsum[lane], ti = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, ti, o);
-      if (lane >= o) ti += v;
-    }
-    wsum[lane] = ti - t;  // exclusive prefix of the warp totals
-    if (lane == 31) *count = ti;
-  }
-  __syncthreads();
-  uint32_t pos = wsum[warp] + incl - mine;
-  for (int64_t w = w0; w < w1; ++w) {
-    uint32_t m = word(w);
+  uint32_t before = base;
+  for (int i = 0; i < warp; ++i) before += wsum[i];
+  uint32_t pos = before + incl - mine;
+  for (int i = 0; i < 8; ++i) {
+    uint32_t m = words[i];
     while (m) {
       const int b = __ffs(m) - 1;
       m &= m - 1u;
-      rows[pos++] = (uint32_t)(w * 32 + b);
+      rows[pos++] = (uint32_t)((w0 + i) * 32 + b);
     }
   }
+  if (blockIdx.x == gridDim.x - 1 && tid == kSegThreads - 1) *count = pos;
 }
 
 template <int D, int XT, int MODE>
@@ -1182,9 +1204,16 @@ cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int co
 }
 
 // Rows handed over by the screening launch over N rows -> rows[0 .. *count).
+// segcnt: fb_compact_segments(N) words of scratch.
+int fb_compact_segments(int64_t N) { return (int)(((N + 31) / 32 + kSegWords - 1) / kSegWords); }
+
 cudaError_t fb_compact(const uint32_t* fb_mask, int64_t N, uint32_t* rows, uint32_t* count,
-                       cudaStream_t s) {
-  fb_compact_kernel<<<1, kCompactThreads, 0, s>>>(fb_mask, N, rows, count);
+                       uint32_t* segcnt, cudaStream_t s) {
+  const int nseg = fb_compact_segments(N);
+  fb_count_kernel<<<nseg, kSegThreads, 0, s>>>(fb_mask, N, segcnt);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fb_write_kernel<<<nseg, kSegThreads, 0, s>>>(fb_mask, N, segcnt, rows, count);
   return cudaGetLastError();
 }
 
