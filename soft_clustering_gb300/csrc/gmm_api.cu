@@ -39,7 +39,8 @@ size_t sparse_stats_ws_bytes(int64_t rows, int D, int K, int rec_cap);
 bool sparse_stats_supported(int K);
 cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
                          int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
-                         void* sws, double* part, int accumulate, double* ll, cudaStream_t s);
+                         void* sws, double* part, int accumulate, double* ll, DeviceStatus* st,
+                         cudaStream_t s);
 int simt_stat_chunk(int D, int cov);
 cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
                          const float* centre, const int32_t* prep_flags, float var_floor,
@@ -242,7 +243,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
       {
         GMM_PROF("sparse_stats");
         GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, tcnt, recs, kRecCap,
-                             at<char>(ws, W.off_sws), part, acc, at<double>(ws, W.off_ll), s));
+                             at<char>(ws, W.off_sws), part, acc, at<double>(ws, W.off_ll), st, s));
       }
       {
         GMM_PROF("stats_rows_kernel");

@@ -12,8 +12,9 @@
 //   scatter  each record to its component's list, in point order (a warp
 //            walks its block's records 32 at a time; __match_any_sync ranks
 //            records of the same component, so the order is fixed)
-//   reduce   one warp per chunk: gathers the chunk's rows of X (sixteen in
-//            flight), accumulates g, g y, g y^2 with y = x - c_k about the
+//   reduce   one warp per chunk: gathers the chunk's rows of X into shared
+//            memory by bulk copies (a batch in flight while the previous
+//            one is added up), accumulates g, g y, g y^2 with y = x - c_k about the
 //            component's input mean c_k (lane l: dimensions l*D/32 ..
 //            (l+1)*D/32 - 1), and for the flagged records of points with a
 //            single candidate (g = 1) their count and sum of y^2, and writes
@@ -28,6 +29,7 @@
 #include <math.h>
 
 #include "gmm_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gmm {
 
@@ -207,24 +209,26 @@ rec_scatter_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restric
   }
 }
 
-template <int XT, int D, int DPL>
-__device__ __forceinline__ void global_row(const void* X, int64_t n, int d0, float* v) {
-  const size_t e0 = (size_t)n * D + d0;
+// DPL consecutive coordinates of one row staged in shared memory, as float.
+template <int XT, int DPL>
+__device__ __forceinline__ void staged_row(const unsigned char* row, int d0, float* v) {
   if constexpr (XT == GMM_F32) {
+    const float* p = reinterpret_cast<const float*>(row) + d0;
     if constexpr (DPL == 4) {
-      const float4 q = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(X) + e0));
+      const float4 q = *reinterpret_cast<const float4*>(p);
       v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     } else {
-      const float2 q = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(X) + e0));
+      const float2 q = *reinterpret_cast<const float2*>(p);
       v[0] = q.x; v[1] = q.y;
     }
   } else {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(row) + d0;
     uint32_t u[DPL / 2];
     if constexpr (DPL == 4) {
-      const uint2 q = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(X) + e0));
+      const uint2 q = *reinterpret_cast<const uint2*>(p);
       u[0] = q.x; u[1] = q.y;
     } else {
-      u[0] = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const uint16_t*>(X) + e0));
+      u[0] = *reinterpret_cast<const uint32_t*>(p);
     }
 #pragma unroll
     for (int i = 0; i < DPL / 2; ++i) {
@@ -236,20 +240,49 @@ __device__ __forceinline__ void global_row(const void* X, int64_t n, int d0, flo
   }
 }
 
-// reduce: warp-per-chunk, grid-stride over the chunks; chunk sums
-// cpart[c] = [s0 | s1 (D) | s2 (D) | n1 | q1 (D)] in fp32 (n1, q1: count
-// and sum of y^2 of the flagged single-candidate records).
+constexpr int kReduceThreads = 256;
+constexpr uint32_t kReduceWait = 1u << 22;
+
+// Rows of X per batch and warp (staged twice: this batch and the next).
+template <int XT>
+__host__ __device__ constexpr int reduce_batch() { return XT == GMM_F32 ? 8 : 16; }
+
 template <int D, int XT>
-__global__ void __launch_bounds__(256, 2)
+constexpr size_t reduce_smem() {
+  return (size_t)(kReduceThreads / 32) * 2 * reduce_batch<XT>() * D * (XT == GMM_F32 ? 4 : 2) +
+         (size_t)(kReduceThreads / 32) * 2 * sizeof(uint64_t);
+}
+
+// reduce: warp-per-chunk, grid-stride over the chunks.  Each batch's rows
+// of X arrive in the warp's shared-memory stage by one bulk copy per row
+// (lane u copies row u), double buffered, so the next batch is in flight
+// while this one is accumulated.  Chunk sums cpart[c] = [s0 | s1 (D) | s2 (D)
+// | n1 | q1 (D)] in fp32 (n1, q1: count and sum of y^2 of the flagged
+// single-candidate records).
+template <int D, int XT>
+__global__ void __launch_bounds__(kReduceThreads)
 rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ mu,
                   const uint32_t* __restrict__ cstart, const uint32_t* __restrict__ kstart,
-                  const uint2* __restrict__ sorted, float* __restrict__ cpart) {
-  constexpr int DPL = D / 32, F = 2 + 3 * D, B = 16;
-  const int lane = threadIdx.x & 31;
+                  const uint2* __restrict__ sorted, float* __restrict__ cpart, DeviceStatus* st) {
+  constexpr int DPL = D / 32, F = 2 + 3 * D, B = reduce_batch<XT>();
+  constexpr int ROWB = D * (XT == GMM_F32 ? 4 : 2);
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  unsigned char* stage = smem + (size_t)wib * 2 * B * ROWB;  // [2][B][ROWB]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (size_t)(kReduceThreads / 32) * 2 * B * ROWB) +
+                  2 * wib;
+  if (lane == 0) {
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    tc::mbar_fence_init();
+  }
+  __syncwarp();
+  uint32_t ph = 0u;  // bit b: parity of the next phase of stage buffer b
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t nchunks = kstart[K];
-  for (int64_t c = gw; c < nchunks; c += nw) {
+  bool ok = true;
+  for (int64_t c = gw; c < nchunks && ok; c += nw) {
     // component of chunk c: the last k with kstart[k] <= c
     int lo = 0, hi = K - 1;
     while (lo < hi) {
@@ -265,36 +298,56 @@ rec_reduce_kernel(const void* __restrict__ X, int K, const float* __restrict__ m
       cen[i] = __ldg(mu + (size_t)k * D + lane * DPL + i);
       s1[i] = s2[i] = q1[i] = 0.f;
     }
-    // the next batch's record is requested before this batch's rows
-    uint2 nxt = (lane < B && r0 + lane < r1) ? sorted[r0 + lane] : make_uint2(0u, 0u);
+    // lanes 0 .. B-1 hold the records of the batch at r; lane u copies row u
+    auto issue = [&](uint32_t r, int b, uint2* rec) {
+      const int nb = (int)min((uint32_t)B, r1 - r);
+      *rec = lane < nb ? sorted[r + lane] : make_uint2(0u, 0u);
+      if (lane == 0) tc::mbar_arrive_expect_tx(&bar[b], (uint32_t)(nb * ROWB));
+      __syncwarp();
+      if (lane < nb)
+        tc::bulk_g2s(stage + ((size_t)b * B + lane) * ROWB,
+                     static_cast<const unsigned char*>(X) + (size_t)(rec->x & ~kRecSingle) * ROWB,
+                     ROWB, &bar[b]);
+    };
+    uint2 cur, nxt = make_uint2(0u, 0u);
+    int b = 0;
+    issue(r0, 0, &cur);
     for (uint32_t r = r0; r < r1; r += B) {
-      const uint2 mine = nxt;
-      if (r + B < r1) nxt = (lane < B && r + B + lane < r1) ? sorted[r + B + lane] : make_uint2(0u, 0u);
-      float x[B][DPL];
-      float g[B];
-      uint32_t single = 0u;  // bit u: record r + u is flagged
-#pragma unroll
-      for (int u = 0; u < B; ++u) {
-        const uint32_t key = __shfl_sync(0xffffffffu, mine.x, u);
-        g[u] = __uint_as_float(__shfl_sync(0xffffffffu, mine.y, u));
-        single |= (key & kRecSingle) ? (1u << u) : 0u;
-        if (r + u < r1) global_row<XT, D, DPL>(X, key & ~kRecSingle, lane * DPL, x[u]);
+      // the next batch goes to the other buffer, read in the previous round
+      if (r + B < r1) issue(r + B, b ^ 1, &nxt);
+      const bool got = tc::mbar_wait(&bar[b], (ph >> b) & 1u, kReduceWait);
+      ph ^= 1u << b;
+      if (!__all_sync(0xffffffffu, got)) {
+        // wait (bounded) for the copies still in flight, then stop
+        if (!got) tc::mbar_wait(&bar[b], ((ph >> b) & 1u) ^ 1u, kReduceWait);
+        if (r + B < r1) tc::mbar_wait(&bar[b ^ 1], (ph >> (b ^ 1)) & 1u, kReduceWait);
+        if (lane == 0) raise_status(st, GMM_ERR_TIMEOUT);
+        ok = false;
+        break;
       }
-#pragma unroll
-      for (int u = 0; u < B; ++u) {
-        if (r + u >= r1) break;
+      const int nb = (int)min((uint32_t)B, r1 - r);
+      for (int u = 0; u < nb; ++u) {
+        const uint32_t key = __shfl_sync(0xffffffffu, cur.x, u);
+        const float g = __uint_as_float(__shfl_sync(0xffffffffu, cur.y, u));
+        const bool single = (key & kRecSingle) != 0u;
+        float x[DPL];
+        staged_row<XT, DPL>(stage + ((size_t)b * B + u) * ROWB, lane * DPL, x);
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
-          const float y = x[u][i] - cen[i];
-          const float gy = g[u] * y;
+          const float y = x[i] - cen[i];
+          const float gy = g * y;
           s1[i] += gy;
           s2[i] = fmaf(gy, y, s2[i]);
-          if (single & (1u << u)) q1[i] = fmaf(y, y, q1[i]);
+          if (single) q1[i] = fmaf(y, y, q1[i]);
         }
-        s0 += g[u];
-        if (single & (1u << u)) n1 += 1.f;
+        s0 += g;
+        if (single) n1 += 1.f;
       }
+      __syncwarp();  // every lane has read buffer b before it is refilled
+      cur = nxt;
+      b ^= 1;
     }
+    if (!ok) break;
     float* o = cpart + (size_t)c * F;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) {
@@ -373,7 +426,8 @@ bool sparse_stats_supported(int K) { return K <= kMaxSparseK; }
 // sws: sparse_stats_ws_bytes(N, D, K, rec_cap) bytes, 256-byte aligned.
 cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
                          int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
-                         void* sws, double* part, int accumulate, double* ll, cudaStream_t s) {
+                         void* sws, double* part, int accumulate, double* ll, DeviceStatus* st,
+                         cudaStream_t s) {
   if (K > kMaxSparseK || (D != 64 && D != 128)) return cudaErrorInvalidValue;
   const SparseLayout S = SparseLayout::make(N, D, K, rec_cap);
   const PreparedLayout L = PreparedLayout::make(D, K, cov);
@@ -410,8 +464,15 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
   }
   const float* mu = at<float>(prepared, L.off_mu);
   const unsigned rblocks = (unsigned)g_sms * 8;
-#define GMM_REDUCE(DD, XX) \
-  rec_reduce_kernel<DD, XX><<<rblocks, 256, 0, s>>>(X, K, mu, cstart, kstart, sorted, cpart)
+#define GMM_REDUCE(DD, XX)                                                                    \
+  do {                                                                                        \
+    constexpr size_t sm = reduce_smem<DD, XX>();                                              \
+    e = cudaFuncSetAttribute(rec_reduce_kernel<DD, XX>,                                       \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);           \
+    if (e != cudaSuccess) return e;                                                           \
+    rec_reduce_kernel<DD, XX><<<rblocks, kReduceThreads, sm, s>>>(X, K, mu, cstart, kstart,   \
+                                                                  sorted, cpart, st);         \
+  } while (0)
   if (D == 128) {
     if (xdtype == GMM_F16) GMM_REDUCE(128, GMM_F16);
     else if (xdtype == GMM_BF16) GMM_REDUCE(128, GMM_BF16);
