@@ -136,6 +136,19 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
   return d;
 }
 
+// Descriptor for a K = 16 K-major operand stored without swizzle (layout
+// type 0): 8-row x 16-byte core matrices, the two along K `lbo` = 128 bytes
+// apart (leading byte offset, bits 16-29), consecutive 8-row groups 256 bytes
+// apart (stride byte offset, bits 32-45); version 1 (46-47).
+__device__ __forceinline__ uint64_t sdesc_k16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)(128 >> 4) << 16;
+  d |= (uint64_t)(256 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with fp16 A and B, fp32 accumulator,
 // both operands K-major: D format bits 4-5 = 1 (f32), A/B format bits 7-9 /
 // 10-12 = 0 (f16), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -217,6 +230,12 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int ro
   const int chunk = kin >> 3;       // 16-byte chunk within the row
   const int phys = chunk ^ (row & 7);
   return (uint32_t)(atom * rows * 128 + row * 128 + phys * 16 + (kin & 7) * 2);
+}
+
+// Byte offset of element (row, k), k < 16, of the K = 16 tile that
+// sdesc_k16 describes.
+__host__ __device__ __forceinline__ uint32_t k16_offset(int row, int k) {
+  return (uint32_t)((row >> 3) * 256 + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
 }
 
 }  // namespace tc

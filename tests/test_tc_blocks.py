@@ -19,7 +19,7 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("kdim", [64, 128, 256])
+@pytest.mark.parametrize("kdim", [64, 128, 256, 80, 144, 272])
 @pytest.mark.parametrize("n", [64, 128])
 def test_tc_gemm_exact(kdim, n):
     rng = np.random.default_rng(kdim * 1000 + n)
