@@ -53,6 +53,23 @@ __host__ __device__ inline bool tc_eligible(int D, int cov) {
   return (cov == GMM_COV_DIAG || cov == GMM_COV_ISO) && (D == 64 || D == 128);
 }
 
+// Folded screening operands (up to two chunks, the parameters resident in
+// shared memory): every component of a chunk shares one power-of-two scale
+// S, and one more K = 16 step of the contraction adds the bias and the
+// rigorous error margin, so the accumulator is directly the upper bound
+// hi_k / S.  The extra step's operands:
+//   A row n: [2^10, 1, 2^-10, ru(rn_n 2^-4), 1, 0 ...]
+//   B row k: [b1, b2, b3, ru(u_k 2^4 / S), ru(d_k / S), 0 ...]
+// with bias_k / S = 2^10 b1 + b2 + 2^-10 b3 (fp16 parts), rn_n >= |[x, x^2]|
+// the row norm, u_k = kappa |(b1, b2)_k| + 2^-20 S the margin per unit of
+// row norm and d_k the absolute margin.  Trailer of a folded chunk:
+// u_k [128], d_k [128], then S, 1/S, max u_k, max d_k.
+constexpr int kTcFoldChunks = 2;
+constexpr int kTcExtraK = 16;
+constexpr int kTcExtraBytes = kTcChunk * kTcExtraK * 2;  // one chunk's extra B rows
+enum { kFoldS = 2 * kTcChunk, kFoldInvS, kFoldUMax, kFoldDMax };
+__host__ __device__ inline bool tc_fold(int chunks) { return chunks <= kTcFoldChunks; }
+
 // Responsibility records of the tensor-core E-step: uint2 {key, gamma bits},
 // key = flag | (component << 7) | row in the 128-point tile.  The flag marks
 // a point's only candidate (gamma 1, its exact log joint not evaluated).
@@ -69,10 +86,11 @@ struct PreparedLayout {
   // tensor-core screening operands (tc_eligible shapes only):
   int tc_chunks;     // ceil(K / 128)
   size_t off_tcB;    // fp16 [chunks][2D/64][128 rows][64]: (b1, b2)/scale as 128-byte
-                     // swizzled K-major tiles, one contiguous image per chunk
+                     // swizzled K-major tiles, one contiguous image per chunk; folded:
+                     // followed in each image by the chunk's unswizzled K = 16 extra rows
   size_t tcB_chunk_bytes;
   size_t off_tcT;    // float [chunks][kTcTrail]: scale (power of 2) [128], |(b1,b2)|_2 [128],
-                     // bias - delta [128], bias + delta [128]
+                     // bias - delta [128], bias + delta [128]; folded: see tc_fold
   size_t tc_bytes;
   size_t bytes;
 
@@ -92,7 +110,7 @@ struct PreparedLayout {
       L.tc_chunks = (K + kTcChunk - 1) / kTcChunk;
       o = align_up(o, 1024);
       L.off_tcB = o;
-      L.tcB_chunk_bytes = (size_t)kTcChunk * 2 * D * 2;
+      L.tcB_chunk_bytes = (size_t)kTcChunk * 2 * D * 2 + (tc_fold(L.tc_chunks) ? kTcExtraBytes : 0);
       o = align_up(o + L.tcB_chunk_bytes * L.tc_chunks);
       L.off_tcT = o;
       o = align_up(o + sizeof(float) * kTcTrail * L.tc_chunks);

@@ -154,6 +154,123 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
   }
 }
 
+// fp16 at or above v >= 0 (round up).
+__device__ __forceinline__ __half half_ru(double v) {
+  __half h = __double2half(v);
+  if ((double)__half2float(h) < v) h = __ushort_as_half((unsigned short)(__half_as_ushort(h) + 1));
+  return h;
+}
+
+// Margin of the folded screening per unit of row norm: the fp16 rounding of
+// both operands (3 x 2^-11) and the tensor-core accumulation allowance
+// (3.5e-5 of sum |a b|), with 1e-4 relative for the accumulation error of
+// the margin terms themselves and 2e-6 spare.
+constexpr double kFoldKappa = 1.5e-3 * 1.0001 + 2e-6;
+
+// Folded operands, part 1: one block of 128 threads per chunk, thread t for
+// component k = 128 chunk + t.  Picks the chunk's scale S, a power of two
+// with max |b| / S <= 2^14, |bias| / S <= 2^25 and max d_k / S <= 2^15 (no
+// fp16 overflow in either step), and writes the extra K = 16 row of B, the
+// margins u_k and d_k and the trailer scalars (see tc_fold).  d_k covers the
+// 1e-3 + 1e-6 |bias| gap between the expanded form and the exact fp32
+// log-density, the accumulation allowance on the bias terms (3.6e-5 |bias|)
+// and the residual of the bias split.  Dead and padding components get
+// bias part -inf and zero margins.
+__global__ void __launch_bounds__(kTcChunk) prepare_fold_scale_kernel(PreparedLayout L,
+                                                                      void* prepared) {
+  __shared__ double red[3][kTcChunk / 32];
+  __shared__ double sS;
+  const int chunk = blockIdx.x, t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int k = chunk * kTcChunk + t;
+  const int D = L.D;
+  const bool live = k < L.K && at<float>(prepared, L.off_c)[k] != -INFINITY;
+  const float* mu = at<float>(prepared, L.off_mu) + (size_t)(live ? k : 0) * D;
+  const float* prec = at<float>(prepared, L.off_prec) +
+                      (size_t)(live ? k : 0) * (L.cov == GMM_COV_DIAG ? D : 1);
+  double mx = 0.0, n2 = 0.0, q = 0.0;
+  if (live) {
+    for (int d = 0; d < D; ++d) {
+      const double w = (double)prec[L.cov == GMM_COV_DIAG ? d : 0];
+      const double b1 = (double)mu[d] * w, b2 = -0.5 * w;
+      mx = fmax(mx, fmax(fabs(b1), fabs(b2)));
+      n2 += b1 * b1 + b2 * b2;
+      q += (double)mu[d] * b1;
+    }
+  }
+  const double bias = live ? (double)at<float>(prepared, L.off_c)[k] - 0.5 * q : 0.0;
+  // the d_k bound before the split residual (which is below 1e-7 |bias|)
+  const double dpre = live ? 1.0001 * (1e-3 + 3.72e-5 * fabs(bias)) : 0.0;
+  double m0 = mx, m1 = fabs(bias), m2 = dpre;
+  for (int o = 16; o > 0; o >>= 1) {
+    m0 = fmax(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+    m1 = fmax(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    m2 = fmax(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+  }
+  if (lane == 0) { red[0][wid] = m0; red[1][wid] = m1; red[2][wid] = m2; }
+  __syncthreads();
+  if (t == 0) {
+    double M = 0.0, B = 0.0, Dm = 0.0;
+    for (int i = 0; i < kTcChunk / 32; ++i) {
+      M = fmax(M, red[0][i]); B = fmax(B, red[1][i]); Dm = fmax(Dm, red[2][i]);
+    }
+    int e = -1000;
+    if (M > 0.0) e = max(e, (int)ceil(log2(M)) - 14);
+    if (B > 0.0) e = max(e, (int)ceil(log2(B)) - 25);
+    if (Dm > 0.0) e = max(e, (int)ceil(log2(Dm)) - 15);
+    if (e == -1000) e = 0;
+    sS = ldexp(1.0, e);
+  }
+  __syncthreads();
+  const double S = sS;
+  // bias / S = 2^10 b1 + b2 + 2^-10 b3 (fp16 parts), residual r3
+  __half p1 = __ushort_as_half((unsigned short)0xFC00), p2 = __double2half(0.0), p3 = p2;
+  double r3 = 0.0;
+  if (live) {
+    const double beta = bias / S;
+    p1 = __double2half(beta * 0x1p-10);
+    const double r1 = beta - (double)__half2float(p1) * 0x1p10;
+    p2 = __double2half(r1);
+    const double r2 = r1 - (double)__half2float(p2);
+    p3 = __double2half(r2 * 0x1p10);
+    r3 = r2 - (double)__half2float(p3) * 0x1p-10;
+  }
+  const double u = live ? kFoldKappa * sqrt(n2) + 0x1p-20 * S : 0.0;
+  const double dk = live ? dpre + 1.0001 * 1.01 * fabs(r3) * S : 0.0;
+  unsigned char* img = at<unsigned char>(prepared, L.off_tcB) + (size_t)chunk * L.tcB_chunk_bytes +
+                       (size_t)kTcChunk * 2 * D * 2;
+  const __half zero = __double2half(0.0);
+  for (int e = 0; e < kTcExtraK; ++e) {
+    __half h = zero;
+    if (e == 0) h = p1;
+    else if (e == 1) h = p2;
+    else if (e == 2) h = p3;
+    else if (e == 3 && live) h = half_ru(u * 16.0 / S);
+    else if (e == 4 && live) h = half_ru(dk / S);
+    *reinterpret_cast<__half*>(img + tc::k16_offset(t, e)) = h;
+  }
+  float* trail = at<float>(prepared, L.off_tcT) + (size_t)chunk * kTcTrail;
+  const float uf = __double2float_ru(u), df = __double2float_ru(dk);
+  trail[t] = uf;
+  trail[kTcChunk + t] = df;
+  // chunk maxima of the margins (for the assignment's m-th lower bound)
+  float a0 = uf, a1 = df;
+  for (int o = 16; o > 0; o >>= 1) {
+    a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, o));
+    a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, o));
+  }
+  __syncthreads();
+  if (lane == 0) { red[0][wid] = a0; red[1][wid] = a1; }
+  __syncthreads();
+  if (t == 0) {
+    float U = 0.f, Dm = 0.f;
+    for (int i = 0; i < kTcChunk / 32; ++i) { U = fmaxf(U, (float)red[0][i]); Dm = fmaxf(Dm, (float)red[1][i]); }
+    trail[kFoldS] = (float)S;
+    trail[kFoldInvS] = (float)(1.0 / S);
+    trail[kFoldUMax] = U;
+    trail[kFoldDMax] = Dm;
+  }
+}
+
 // Screening operands for the tensor-core kernel (diagonal / isotropic, D = 64
 // or 128), one block per component of the padded range [0, 128 * chunks).
 // Row k of chunk k / 128 holds (b1, b2) = (mu w, -w / 2) divided by a power of
@@ -162,7 +279,9 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
 // layout the MMA reads.  The trailer keeps s_k, |(b1, b2)|_2 (for the
 // rounding bound) and the screening bias c_k - (1/2) sum_d mu_d^2 w_d (the
 // constant of the expanded form).  Components with bias -inf and padding rows
-// get b = 0 and bias -inf.
+// get b = 0 and bias -inf.  Folded chunks (tc_fold) divide by the chunk's
+// common scale instead, and their trailer comes from
+// prepare_fold_scale_kernel.
 __global__ void prepare_tc_kernel(PreparedLayout L, void* prepared) {
   __shared__ double red[32];
   __shared__ double s_max;
@@ -207,12 +326,15 @@ __global__ void prepare_tc_kernel(PreparedLayout L, void* prepared) {
   }
   __syncthreads();
   const double m = s_max;
-  const double scale = m > 0.0 ? ldexp(1.0, (int)ceil(log2(m)) - 14) : 1.0;
+  // folded: the chunk's common scale (written by prepare_fold_scale_kernel)
+  const bool fold = tc_fold(L.tc_chunks);
+  const double scale = fold ? (double)trail[kFoldS]
+                            : (m > 0.0 ? ldexp(1.0, (int)ceil(log2(m)) - 14) : 1.0);
   for (int j = threadIdx.x; j < KD; j += blockDim.x) {
     const __half h = __double2half(bval(j) / scale);
     *reinterpret_cast<__half*>(img + tc::sw128_offset(row, j, kTcChunk)) = h;
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !fold) {
     trail[row] = (float)scale;
     trail[kTcChunk + row] = (float)sqrt(red[31]);
     // bias = c_k - sum mu^2 w / 2, with the margin of the fp32 evaluation
@@ -229,6 +351,11 @@ __global__ void prepare_tc_kernel(PreparedLayout L, void* prepared) {
 cudaError_t launch_prepare_tc(int D, int K, int cov, void* prepared, cudaStream_t s) {
   PreparedLayout L = PreparedLayout::make(D, K, cov);
   if (!L.tc_chunks) return cudaSuccess;
+  if (tc_fold(L.tc_chunks)) {
+    prepare_fold_scale_kernel<<<L.tc_chunks, kTcChunk, 0, s>>>(L, prepared);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   prepare_tc_kernel<<<L.tc_chunks * kTcChunk, 128, 0, s>>>(L, prepared);
   return cudaGetLastError();
 }

@@ -51,7 +51,8 @@ namespace {
 constexpr int kBM = 128;          // points per tile (MMA M)
 constexpr int kBN = kTcChunk;     // components per chunk (MMA N)
 constexpr int kHalf = kBN / 2;    // columns of a chunk per warp (streamed parameters)
-constexpr int kCS = 15;           // candidates per point list (per column half when streamed)
+constexpr int kCS = 15;           // candidates per list, streamed parameters (per column half)
+constexpr int kCSG = 13;          // candidates per point list, resident parameters
 constexpr float kT = 40.f;        // nats
 // Cauchy-Schwarz factor of the screening error: 3 x 2^-11 rounding plus the
 // accumulation allowance (1.5e-3), plus 2e-6 that covers the relative fp32
@@ -85,26 +86,30 @@ struct ScreenArgs {
   DeviceStatus* st;
 };
 
-// GRP: the grouped epilogue (resident parameters, K <= 256): two groups of
-// four warps take alternate tiles, each warp all columns of 32 rows; four
-// TMEM buffers and trailer slots.  Otherwise (parameters streamed with B):
+// GRP: the grouped epilogue (resident, folded parameters, K <= 256): two
+// groups of four warps take alternate tiles, each warp all columns of 32
+// rows; four TMEM buffers, no trailer in shared memory.  Otherwise (parameters streamed with B):
 // eight warps, the two of a lane quarter splitting each chunk's columns; two
 // TMEM buffers and trailer slots.
 template <int D, bool GRP>
 struct Shape {
   static constexpr int KD = 2 * D;
   static constexpr int KSTEPS = KD / 16;
+  static constexpr int CS = GRP ? kCSG : kCS;              // candidates per list
   static constexpr int A_BYTES = kBM * KD * 2;
-  static constexpr int B_BYTES = kBN * KD * 2;
+  static constexpr int AX_BYTES = GRP ? kBM * kTcExtraK * 2 : 0;  // folded extra step of A
+  static constexpr int B_MAIN = kBN * KD * 2;
+  static constexpr int B_BYTES = B_MAIN + (GRP ? kTcExtraBytes : 0);  // one chunk's image
   static constexpr int T_BYTES = kTcTrail * 4;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + A_BYTES;             // 2 buffers
-  static constexpr int NT = GRP ? 4 : 2;                    // trailer slots = TMEM buffers
+  static constexpr int OFF_AX = OFF_A + A_BYTES;
+  static constexpr int OFF_B = OFF_AX + AX_BYTES;           // 2 buffers
+  static constexpr int NT = GRP ? 0 : 2;                    // trailer slots (folded: none)
   static constexpr int OFF_T = OFF_B + 2 * B_BYTES;
   static constexpr int OFF_RN = OFF_T + NT * T_BYTES;       // 2 x 128 row norms
-  static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;      // [2][kCS][128] float
-  static constexpr int OFF_CK = OFF_CUB + 2 * kCS * kBM * 4;   // [2][kCS][128] u16
-  static constexpr int OFF_X = OFF_CK + 2 * kCS * kBM * 2;     // exchange between warps
+  static constexpr int OFF_CUB = OFF_RN + 2 * kBM * 4;      // [2][CS][128] float
+  static constexpr int OFF_CK = OFF_CUB + 2 * CS * kBM * 4;    // [2][CS][128] u16
+  static constexpr int OFF_X = OFF_CK + 2 * CS * kBM * 2;      // exchange between warps
   // grouped: record counts [2 groups][2][128] u16; streamed: per half best
   // and m-th lower bound, max and sum of the exact values, counts
   static constexpr int X_BYTES = GRP ? 2 * 2 * kBM * 2 : 4 * 2 * kBM * 4 + 2 * kBM * 2;
@@ -174,6 +179,13 @@ __device__ __forceinline__ void insert_lower_bound(float* lbm, int m, float v) {
   for (int t = 0; t < 8; ++t) {
     if (t < m && v > lbm[t]) { const float tmp = lbm[t]; lbm[t] = v; v = tmp; }
   }
+}
+
+// Four consecutive trailer entries of one field (16-byte aligned): one
+// shared load serves four columns.
+__device__ __forceinline__ void ld_trail4(const float* p, float* o) {
+  const float4 q = *reinterpret_cast<const float4*>(p);
+  o[0] = q.x; o[1] = q.y; o[2] = q.z; o[3] = q.w;
 }
 
 // Operands of one exact evaluation: row n of X against NC components.
@@ -388,13 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       auto load_b = [&](int64_t g) {
         const int buf = (int)(g & 1), c = (int)(g % nch);
         tc::mbar_arrive_expect_tx(&bar[B_FULL + buf], S::B_BYTES);
-        tc::bulk_g2s(sB + buf * S::B_BYTES, gB + (size_t)c * S::B_BYTES, S::B_BYTES,
+        tc::bulk_g2s(sB + buf * S::B_BYTES, gB + (size_t)c * a.L.tcB_chunk_bytes, S::B_BYTES,
                      &bar[B_FULL + buf]);
       };
       if (resident) {
         for (int c = 0; c < nch; ++c) {
           tc::mbar_arrive_expect_tx(&bar[B_FULL + c], S::B_BYTES);
-          tc::bulk_g2s(sB + c * S::B_BYTES, gB + (size_t)c * S::B_BYTES, S::B_BYTES,
+          tc::bulk_g2s(sB + c * S::B_BYTES, gB + (size_t)c * a.L.tcB_chunk_bytes, S::B_BYTES,
                        &bar[B_FULL + c]);
         }
       } else {
@@ -418,10 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
             fail(); ok = false; break;
           }
           tc::tc_fence_after();
-          // the trailer slot of a TMEM buffer is free once the buffer is
-          tc::mbar_arrive_expect_tx(&bar[TR_FULL + buf], S::T_BYTES);
-          tc::bulk_g2s(sT + buf * (S::T_BYTES / 4), gT + (size_t)j * kTcTrail, S::T_BYTES,
-                       &bar[TR_FULL + buf]);
+          if constexpr (!GRP) {
+            // the trailer slot of a TMEM buffer is free once the buffer is
+            tc::mbar_arrive_expect_tx(&bar[TR_FULL + buf], S::T_BYTES);
+            tc::bulk_g2s(sT + buf * (S::T_BYTES / 4), gT + (size_t)j * kTcTrail, S::T_BYTES,
+                         &bar[TR_FULL + buf]);
+          }
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
           const unsigned char* bb = sB + bbuf * S::B_BYTES;
 #pragma unroll
@@ -430,6 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
             const uint64_t da = tc::sdesc_k128(tc::smem_addr(sA + atom * kBM * 128 + within));
             const uint64_t db = tc::sdesc_k128(tc::smem_addr(bb + atom * kBN * 128 + within));
             tc::mma_f16(d_tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+          }
+          if constexpr (GRP) {
+            // the folded step: bias and margin (unswizzled K = 16 operands)
+            tc::mma_f16(d_tmem, tc::sdesc_k16(tc::smem_addr(sm + S::OFF_AX)),
+                        tc::sdesc_k16(tc::smem_addr(bb + S::B_MAIN)), idesc, 1u);
           }
           if (!resident) tc::mma_commit(&bar[B_EMPTY + sbuf]);
           tc::mma_commit(&bar[T_FULL + buf]);
@@ -510,7 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       // floor: fp16 subnormal rounding of x^2 (and of bf16 x below fp16's
       // normal range) errs by at most 2^-25 per coordinate, sqrt(2D) 2^-25 |b|
       // in all, below kappa x 1e-3 |b| for D <= 128
-      sRN[(it & 1) * kBM + p] = sqrtf(rn2) * 1.0001f + 1e-3f;
+      const float rn = sqrtf(rn2) * 1.0001f + 1e-3f;
+      sRN[(it & 1) * kBM + p] = rn;
+      if constexpr (GRP) {
+        // the folded step's row: [2^10, 1, 2^-10, ru(rn / 16), 1, 0 ...]
+        const uint32_t h3 = (uint32_t)__half_as_ushort(__float2half_ru(rn * 0.0625f));
+        *reinterpret_cast<uint4*>(sm + S::OFF_AX + tc::k16_offset(p, 0)) =
+            make_uint4(0x3C006400u, 0x1400u | (h3 << 16), 0x3C00u, 0u);
+        *reinterpret_cast<uint4*>(sm + S::OFF_AX + tc::k16_offset(p, 8)) = make_uint4(0u, 0u, 0u, 0u);
+      }
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -526,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     const int g = warp >> 2, q = warp & 3;
     const int r = q * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    float* __restrict__ cub = sCUB + g * kCS * kBM;     // this group's candidate lists
-    uint16_t* __restrict__ ck = sCK + g * kCS * kBM;
+    float* __restrict__ cub = sCUB + g * kCSG * kBM;     // this group's candidate lists
+    uint16_t* __restrict__ ck = sCK + g * kCSG * kBM;
     double ll_acc = 0.0;
     for (int it = g; it < my_tiles; it += 2) {
       if (warp_aborted(abort_flag)) break;
@@ -537,7 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       const bool valid = n < a.N;
       if (!warp_wait(&bar[R_FULL + g], s & 1)) { fail(); break; }
       const float rn = sRN[g * kBM + r];
-      const float rnk = kKappa * rn;
       float ref = -INFINITY;  // lower bound of the best log joint
       float dropped = -INFINITY;
       float lbm[8];           // assign: the m largest lower bounds seen
@@ -561,34 +587,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           uint32_t use;
           tbuf(it, j, &buf, &use);
           if (pass == 0) {
-            if (!warp_wait(&bar[T_FULL + buf], use & 1) ||
-                !warp_wait(&bar[TR_FULL + buf], use & 1)) {
-              fail(); ok = false; break;
-            }
+            if (!warp_wait(&bar[T_FULL + buf], use & 1)) { fail(); ok = false; break; }
             tc::tc_fence_after();
           }
-          // (the trailer and the candidate lists never overlap)
-          const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4);
-          const float* __restrict__ tcn = tsc + kBN;
-          const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
-          const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
+          // the chunk's scale and margins (see tc_fold)
+          const float* __restrict__ gTj = gT + (size_t)j * kTcTrail;
+          const float Sj = __ldg(gTj + kFoldS);
           const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN);
           if (pass == 0) {
-            // the best lower bound of the chunk,
-            //   lo = s v + (bias - delta) - rnk |b|
-            float best = -INFINITY;
-#pragma unroll 1
+            // the accumulators hold hi_k / S.  The largest, its column packed
+            // into the low seven bits (a change below 2^-16 relative), names
+            // a component whose lower bound hi - 2.01 (rn u + d) bounds the
+            // best log joint from below
+            float pk0 = -INFINITY, pk1 = -INFINITY;  // two chains
+            float wmax = 0.f;
+            if constexpr (MODE == MODE_ASSIGN)
+              wmax = 2.01f * fmaf(rn, __ldg(gTj + kFoldUMax), __ldg(gTj + kFoldDMax));
+#pragma unroll
             for (int c0 = 0; c0 < kBN; c0 += 32) {
               uint32_t u[32];
               tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
               tc::tmem_wait32(u);
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                const int kk = c0 + i;
-                const float v = __uint_as_float(u[i]);
-                const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
-                best = fmaxf(best, lo);
+                const float pv = __uint_as_float((u[i] & ~0x7Fu) | (uint32_t)(c0 + i));
+                if (i & 1) pk1 = fmaxf(pk1, pv);
+                else pk0 = fmaxf(pk0, pv);
                 if constexpr (MODE == MODE_ASSIGN) {
+                  // a lower bound with the chunk's largest margin
+                  const float h = Sj * __uint_as_float(u[i]);
+                  const float lo = h - wmax - 1e-6f * fabsf(h);
                   if (lo > lmth) {
                     insert_lower_bound(lbm, a.m, lo);
                     lmth = pick8(lbm, a.m - 1);
@@ -596,11 +624,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
                 }
               }
             }
-            ref = fmaxf(ref, best);
+            const uint32_t pb = __float_as_uint(fmaxf(pk0, pk1));
+            const int kh = (int)(pb & 0x7Fu);
+            const float t0 = __uint_as_float(pb & ~0x7Fu);
+            const float h = Sj * (t0 - fabsf(t0) * 0x1p-15f);
+            const float lo = h - 2.01f * fmaf(rn, __ldg(gTj + kh), __ldg(gTj + kTcChunk + kh)) -
+                             1e-6f * fabsf(h);
+            ref = fmaxf(ref, lo);
           } else {
-            // every component whose upper bound
-            //   hi = s v + (bias + delta) + rnk |b|
-            // reaches the window
+            // every component whose upper bound reaches the window,
+            // hi_k / S >= thr / S (S a power of two)
+            const float tthr = thr * __ldg(gTj + kFoldInvS);
 #pragma unroll 1
             for (int c0 = 0; c0 < kBN; c0 += 32) {
               uint32_t u[32];
@@ -610,17 +644,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               // the (rare) appends in column order
               uint32_t pm = 0u;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int kk = c0 + i;
-                const float v = __uint_as_float(u[i]);
-                const float hi = fmaf(v, tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
-                pm |= hi >= thr ? (1u << i) : 0u;
-              }
+              for (int i = 0; i < 32; ++i) pm |= __uint_as_float(u[i]) >= tthr ? (1u << i) : 0u;
               if (!valid) pm = 0u;
               while (pm) {
                 const int kk = c0 + __ffs(pm) - 1;
                 pm &= pm - 1u;
-                if (cnt < kCS) {
+                if (cnt < kCSG) {
                   ck[cnt * kBM + r] = (uint16_t)(j * kBN + kk);
                   ++cnt;
                 } else {
@@ -629,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               }
             }
           }
-          if (pass == 1) {  // the buffer (and its trailer) is free after the second sweep
+          if (pass == 1) {  // the buffer is free after the second sweep
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
@@ -844,27 +873,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           if (pass == 0) {
             // the best lower bound of the half-chunk,
             //   lo = s v + (bias - delta) - rnk |b|
-            float best = -INFINITY;
+            float best0 = -INFINITY, best1 = -INFINITY;  // two chains
 #pragma unroll 1
             for (int c0 = 0; c0 < kHalf; c0 += 32) {
               uint32_t u[32];
               tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
               tc::tmem_wait32(u);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int kk = c0 + i;
-                const float v = __uint_as_float(u[i]);
-                const float lo = fmaf(v, tsc[kk], fmaf(-rnk, tcn[kk], tbl[kk]));
-                best = fmaxf(best, lo);
-                if constexpr (MODE == MODE_ASSIGN) {
-                  if (lo > lmth) {
-                    insert_lower_bound(lbm, a.m, lo);
-                    lmth = pick8(lbm, a.m - 1);
+              for (int i = 0; i < 32; i += 4) {
+                float sc[4], nb[4], bb[4];
+                ld_trail4(tsc + c0 + i, sc);
+                ld_trail4(tcn + c0 + i, nb);
+                ld_trail4(tbl + c0 + i, bb);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const float v = __uint_as_float(u[i + t]);
+                  const float lo = fmaf(v, sc[t], fmaf(-rnk, nb[t], bb[t]));
+                  if (t & 1) best1 = fmaxf(best1, lo);
+                  else best0 = fmaxf(best0, lo);
+                  if constexpr (MODE == MODE_ASSIGN) {
+                    if (lo > lmth) {
+                      insert_lower_bound(lbm, a.m, lo);
+                      lmth = pick8(lbm, a.m - 1);
+                    }
                   }
                 }
               }
             }
-            ref = fmaxf(ref, best);
+            ref = fmaxf(ref, fmaxf(best0, best1));
           } else {
             // every component whose upper bound
             //   hi = s v + (bias + delta) + rnk |b|
@@ -878,11 +914,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               // the (rare) appends in column order
               uint32_t pm = 0u;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int kk = c0 + i;
-                const float v = __uint_as_float(u[i]);
-                const float hi = fmaf(v, tsc[kk], fmaf(rnk, tcn[kk], tbh[kk]));
-                pm |= hi >= thr ? (1u << i) : 0u;
+              for (int i = 0; i < 32; i += 4) {
+                float sc[4], nb[4], bb[4];
+                ld_trail4(tsc + c0 + i, sc);
+                ld_trail4(tcn + c0 + i, nb);
+                ld_trail4(tbh + c0 + i, bb);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const float v = __uint_as_float(u[i + t]);
+                  const float hi = fmaf(v, sc[t], fmaf(rnk, nb[t], bb[t]));
+                  pm |= hi >= thr ? (1u << (i + t)) : 0u;
+                }
               }
               if (!valid) pm = 0u;
               while (pm) {
@@ -1149,8 +1191,12 @@ fb_write_kernel(const uint32_t* __restrict__ mask, int64_t N, const uint32_t* __
 
 template <int D, int XT, int MODE>
 cudaError_t run_screen(const ScreenArgs& args, int grid, cudaStream_t s) {
-  // resident parameters (at most two chunks): the grouped epilogue
-  const bool grp = args.L.tc_chunks <= 2;
+  // resident, folded parameters (at most two chunks): the grouped epilogue
+  const bool grp = tc_fold(args.L.tc_chunks);
+  // the chunk images in global memory must match the shared-memory layout
+  if ((size_t)(grp ? Shape<D, true>::B_BYTES : Shape<D, false>::B_BYTES) !=
+      args.L.tcB_chunk_bytes)
+    return cudaErrorInvalidValue;
   auto kern = grp ? tc_screen_kernel<D, XT, MODE, true> : tc_screen_kernel<D, XT, MODE, false>;
   const int smem = grp ? Shape<D, true>::SMEM : Shape<D, false>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
