@@ -176,20 +176,6 @@ cudaEvent_t prof_event() {
   return e;
 }
 
-struct ProfScope {
-  const char* name; cudaStream_t s; cudaEvent_t a = nullptr;
-  ProfScope(const char* n, cudaStream_t st) : name(n), s(st) {
-    std::lock_guard<std::mutex> lock(g_prof_mu);
-    if (g_prof_on) { a = prof_event(); cudaEventRecord(a, s); }
-  }
-  ~ProfScope() {
-    if (!a) return;
-    std::lock_guard<std::mutex> lock(g_prof_mu);
-    cudaEvent_t b = prof_event();
-    cudaEventRecord(b, s);
-    g_prof_pending.push_back({name, a, b});
-  }
-};
 
 #define GMM_PROF(name) ProfScope _prof_scope(name, s)
 
@@ -241,7 +227,6 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
         GMM_TRY(launch_ll_finalize(llp, g1 + kListGrid, at<double>(ws, W.off_ll), acc, s));
       }
       {
-        GMM_PROF("sparse_stats");
         GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, tcnt, recs, kRecCap,
                              at<char>(ws, W.off_sws), part, acc, at<double>(ws, W.off_ll), st, s));
       }
@@ -300,6 +285,19 @@ gmm_status host_res(HostPathRes** out) {
 }
 
 }  // namespace
+
+ProfScope::ProfScope(const char* n, cudaStream_t st) : name(n), s(st) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof_on) { a = prof_event(); cudaEventRecord(a, s); }
+}
+
+ProfScope::~ProfScope() {
+  if (!a) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  cudaEvent_t b = prof_event();
+  cudaEventRecord(b, s);
+  g_prof_pending.push_back({name, a, b});
+}
 
 // The statistics partition count the entry points above use, for other
 // translation units that launch the same kernels.

@@ -15,6 +15,19 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a = kAlign) {
   return (v + a - 1) / a * a;
 }
 
+// Profiler scope: when profiling is on (gmm_profile_enable), the launches in
+// its lifetime are bracketed by two CUDA events on `s` and summed under
+// `name` (defined in gmm_api.cu).
+struct ProfScope {
+  const char* name;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  ProfScope(const char* n, cudaStream_t st);
+  ~ProfScope();
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+};
+
 // Status-word bits (first failing condition recorded as a gmm_status value;
 // later conditions only OR into the detail word).
 struct DeviceStatus {

@@ -10,8 +10,9 @@
 //            of its blocks; then one block: the start of each component's
 //            records and of its chunks of kCH records
 //   scatter  each record to its component's list, in point order (a warp
-//            walks its block's records 32 at a time; __match_any_sync ranks
-//            records of the same component, so the order is fixed)
+//            per tile, or per block of tiles for large K, walks the records
+//            32 at a time; __match_any_sync ranks records of the same
+//            component, so the order is fixed)
 //   reduce   one warp per chunk: gathers the chunk's rows of X into shared
 //            memory by bulk copies (a batch in flight while the previous
 //            one is added up), accumulates g, g y, g y^2 with y = x - c_k about the
@@ -118,29 +119,26 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
   return r;
 }
 
-// scan, part 1 (one warp per component): counts[k][b] -> offsets of block b
-// within component k (in place, exclusive), ktot[k] = the component's total.
-__global__ void __launch_bounds__(256)
+// scan, part 1 (one block of kScanThreads per component): counts[k][b] ->
+// offsets of block b within component k (in place, exclusive), ktot[k] =
+// the component's total.
+__global__ void __launch_bounds__(kScanThreads)
 rec_scan_blocks_kernel(uint32_t* __restrict__ counts, int K, int64_t nb,
                        uint32_t* __restrict__ ktot) {
-  const int lane = threadIdx.x & 31;
-  const int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (k >= K) return;
+  __shared__ uint32_t wsum[kScanThreads / 32];
+  __shared__ uint32_t total;
+  const int k = blockIdx.x;
   uint32_t* c = counts + (size_t)k * nb;
   uint32_t carry = 0;
-  for (int64_t base = 0; base < nb; base += 32) {
-    const int64_t i = base + lane;
+  for (int64_t base = 0; base < nb; base += kScanThreads) {
+    const int64_t i = base + threadIdx.x;
     const uint32_t v = i < nb ? c[i] : 0u;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
-    }
-    if (i < nb) c[i] = carry + incl - v;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
+    const uint32_t ex = block_excl_scan(v, wsum, &total);
+    if (i < nb) c[i] = carry + ex;
+    carry += total;
+    __syncthreads();  // total is rewritten by the next round
   }
-  if (lane == 0) ktot[k] = carry;
+  if (threadIdx.x == 0) ktot[k] = carry;
 }
 
 // scan, part 2 (one block): cstart[k] = first record of component k
@@ -210,6 +208,62 @@ rec_scatter_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restric
 }
 
 // DPL consecutive coordinates of one row staged in shared memory, as float.
+// scatter with a warp per tile (K <= kScatterWideK): the block's eight
+// warps first count their tiles' records per component (cnt[w][k]), turn
+// the counts into each tile's starting positions (the block's offset plus
+// the earlier tiles' counts), then place their records as the one-warp
+// kernel does.  The positions are the same as that kernel's.
+constexpr int kScatterWideK = 1024;
+__global__ void __launch_bounds__(32 * kTPB)
+rec_scatter_wide_kernel(const uint32_t* __restrict__ tile_cnt, const uint2* __restrict__ recs,
+                        int rec_cap, int64_t ntiles, int K, int64_t nb,
+                        const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ cstart,
+                        uint2* __restrict__ sorted) {
+  extern __shared__ uint32_t pos[];  // [kTPB][K]
+  const int64_t b = blockIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kTPB * K; i += blockDim.x) pos[i] = 0u;
+  __syncthreads();
+  const int64_t t = b * kTPB + w;
+  int cnt = 0;
+  if (t < ntiles) {
+    const uint32_t c = tile_cnt[t];
+    cnt = c < (uint32_t)rec_cap ? (int)c : rec_cap;
+    for (int i = lane; i < cnt; i += 32) {
+      const uint32_t k = (recs[(size_t)t * rec_cap + i].x >> 7) & kRecKMask;
+      if (k < (uint32_t)K) atomicAdd(&pos[w * K + k], 1u);
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    uint32_t run = cstart[k] + offsets[(size_t)k * nb + b];
+#pragma unroll
+    for (int v = 0; v < kTPB; ++v) {
+      const uint32_t n = pos[v * K + k];
+      pos[v * K + k] = run;
+      run += n;
+    }
+  }
+  __syncthreads();
+  uint32_t* cursor = pos + w * K;
+  for (int base = 0; base < cnt; base += 32) {
+    const int i = base + lane;
+    const bool live = i < cnt;
+    uint2 rec = make_uint2(0xffffffffu, 0u);
+    if (live) rec = recs[(size_t)t * rec_cap + i];
+    const uint32_t k = (rec.x >> 7) & kRecKMask;
+    const bool ok = live && k < (uint32_t)K;
+    const unsigned grp = __match_any_sync(0xffffffffu, ok ? k : 0xffffffffu);
+    if (ok) {
+      const uint32_t at_ = cursor[k] + __popc(grp & ((1u << lane) - 1u));
+      sorted[at_] = make_uint2((uint32_t)(t * kTile + (rec.x & 127)) | (rec.x & kRecSingle), rec.y);
+    }
+    __syncwarp();
+    if (ok && lane == 31 - __clz(grp)) cursor[k] += __popc(grp);
+    __syncwarp();
+  }
+}
+
 template <int XT, int DPL>
 __device__ __forceinline__ void staged_row(const unsigned char* row, int d0, float* v) {
   if constexpr (XT == GMM_F32) {
@@ -377,15 +431,24 @@ rec_merge_kernel(int K, const uint32_t* __restrict__ kstart, const float* __rest
   const int k = blockIdx.x, d = threadIdx.x, lane = d & 31;
   double* o = part + (size_t)k * F;
   const uint32_t c0 = kstart[k], c1 = kstart[k + 1];
-  double s0 = 0.0, n1 = 0.0, S1 = 0.0, S2c = 0.0, Q = 0.0;
+  // the chunk sums are fp32 sums of up to kCH records; adding them up in
+  // fp32 (even and odd chunks apart, then together) keeps their accuracy,
+  // and the FP64 pipe is left for the second moment below
+  float a0[2] = {0.f, 0.f}, an[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f},
+        aq[2] = {0.f, 0.f};
+#pragma unroll 4
   for (uint32_t c = c0; c < c1; ++c) {
     const float* cp = cpart + (size_t)c * FC;
-    s0 += (double)cp[0];
-    n1 += (double)cp[1 + 2 * D];
-    S1 += (double)cp[1 + d];
-    S2c += (double)cp[1 + D + d];
-    Q += (double)cp[2 + 2 * D + d];
+    const int h = (int)((c - c0) & 1u);
+    a0[h] += cp[0];
+    an[h] += cp[1 + 2 * D];
+    a1[h] += cp[1 + d];
+    a2[h] += cp[1 + D + d];
+    aq[h] += cp[2 + 2 * D + d];
   }
+  const double s0 = (double)a0[0] + (double)a0[1], n1 = (double)an[0] + (double)an[1];
+  double S1 = (double)a1[0] + (double)a1[1], S2c = (double)a2[0] + (double)a2[1];
+  const double Q = (double)aq[0] + (double)aq[1];
   const double S0o = accumulate ? o[0] : 0.0;
   const double S0 = S0o + s0;
   if (accumulate) {
@@ -445,17 +508,36 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
     e = cudaFuncSetAttribute(rec_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm);
     if (e != cudaSuccess) return e;
   }
-  rec_count_kernel<<<(unsigned)S.nb, 256, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K, S.nb,
-                                                    counts);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  rec_scan_blocks_kernel<<<(unsigned)(((int64_t)K * 32 + 255) / 256), 256, 0, s>>>(counts, K, S.nb,
-                                                                                  ktot);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  rec_scan_comps_kernel<<<1, kScanThreads, 0, s>>>(ktot, K, cstart, kstart);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  rec_scatter_kernel<<<(unsigned)S.nb, 32, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K, S.nb,
-                                                     counts, cstart, sorted);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    ProfScope p("rec_count_kernel", s);
+    rec_count_kernel<<<(unsigned)S.nb, 256, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K, S.nb,
+                                                      counts);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    ProfScope p("rec_scan_kernels", s);
+    rec_scan_blocks_kernel<<<(unsigned)K, kScanThreads, 0, s>>>(counts, K, S.nb, ktot);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    rec_scan_comps_kernel<<<1, kScanThreads, 0, s>>>(ktot, K, cstart, kstart);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    ProfScope p("rec_scatter_kernel", s);
+    if (K <= kScatterWideK) {
+      const size_t wsm = sizeof(uint32_t) * (size_t)kTPB * K;
+      if (wsm > 48 * 1024) {
+        e = cudaFuncSetAttribute(rec_scatter_wide_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm);
+        if (e != cudaSuccess) return e;
+      }
+      rec_scatter_wide_kernel<<<(unsigned)S.nb, 32 * kTPB, wsm, s>>>(
+          tile_cnt, recs, rec_cap, S.ntiles, K, S.nb, counts, cstart, sorted);
+    } else {
+      rec_scatter_kernel<<<(unsigned)S.nb, 32, hsm, s>>>(tile_cnt, recs, rec_cap, S.ntiles, K,
+                                                         S.nb, counts, cstart, sorted);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (!g_sms) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -473,29 +555,35 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
     rec_reduce_kernel<DD, XX><<<rblocks, kReduceThreads, sm, s>>>(X, K, mu, cstart, kstart,   \
                                                                   sorted, cpart, st);         \
   } while (0)
-  if (D == 128) {
-    if (xdtype == GMM_F16) GMM_REDUCE(128, GMM_F16);
-    else if (xdtype == GMM_BF16) GMM_REDUCE(128, GMM_BF16);
-    else GMM_REDUCE(128, GMM_F32);
-  } else {
-    if (xdtype == GMM_F16) GMM_REDUCE(64, GMM_F16);
-    else if (xdtype == GMM_BF16) GMM_REDUCE(64, GMM_BF16);
-    else GMM_REDUCE(64, GMM_F32);
-  }
+  {
+    ProfScope prof_reduce("rec_reduce_kernel", s);
+    if (D == 128) {
+      if (xdtype == GMM_F16) GMM_REDUCE(128, GMM_F16);
+      else if (xdtype == GMM_BF16) GMM_REDUCE(128, GMM_BF16);
+      else GMM_REDUCE(128, GMM_F32);
+    } else {
+      if (xdtype == GMM_F16) GMM_REDUCE(64, GMM_F16);
+      else if (xdtype == GMM_BF16) GMM_REDUCE(64, GMM_BF16);
+      else GMM_REDUCE(64, GMM_F32);
+    }
 #undef GMM_REDUCE
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 
   const float* bias_c = at<float>(prepared, L.off_c);
   const float* prec = at<float>(prepared, L.off_prec);
   double* llk = at<double>(sws, S.off_llk);
   const bool iso = cov == GMM_COV_ISO;
-  if (D == 128)
-    rec_merge_kernel<128><<<K, 128, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
+  {
+    ProfScope prof_merge("rec_merge_kernel", s);
+    if (D == 128)
+      rec_merge_kernel<128><<<K, 128, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
+                                              accumulate);
+    else
+      rec_merge_kernel<64><<<K, 64, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
                                             accumulate);
-  else
-    rec_merge_kernel<64><<<K, 64, 0, s>>>(K, kstart, cpart, bias_c, prec, iso, part, llk,
-                                          accumulate);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // the single-candidate points' log-likelihood joins the total
   return launch_ll_finalize(llk, K, ll, 1, s);
 }
