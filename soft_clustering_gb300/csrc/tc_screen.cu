@@ -499,6 +499,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       float rn2 = 0.f;
 #pragma unroll
       for (int c8 = 0; c8 < G; ++c8) {
+        if constexpr (XT == GMM_F16) {
+          // fp16 input: x is the operand as stored, and x^2 = RN(x x) is one
+          // packed multiply (fp16 multiplication is correctly rounded, the
+          // same value as rounding the exact fp32 square)
+          const uint32_t w4[4] = {pre[c8].x, pre[c8].y, pre[c8].z, pre[c8].w};
+          uint32_t hq[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 xx = *reinterpret_cast<const __half2*>(&w4[i]);
+            const __half2 qq = __hmul2(xx, xx);
+            const float2 xf = __half22float2(xx), qf = __half22float2(qq);
+            rn2 += xf.x * xf.x + xf.y * xf.y + qf.x * qf.x + qf.y * qf.y;
+            hq[i] = *reinterpret_cast<const uint32_t*>(&qq);
+          }
+          *reinterpret_cast<uint4*>(sA + tc::sw128_offset(p, c8 * 8, kBM)) = pre[c8];
+          *reinterpret_cast<uint4*>(sA + tc::sw128_offset(p, D + c8 * 8, kBM)) =
+              make_uint4(hq[0], hq[1], hq[2], hq[3]);
+          continue;
+        }
         float v[8];
         if (c8 < PF) {
           raw_to_float8<XT>(pre + c8 * WPG, v);
