@@ -492,11 +492,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
 #pragma unroll
           for (int i = 0; i < WPG; ++i) pre[g * WPG + i] = make_uint4(0u, 0u, 0u, 0u);
       }
+      float rn2 = 0.f;
+      if constexpr (XT == GMM_F16) {
+        // fp16 input: the row norm needs only the loaded row, so it is taken
+        // before the wait for the operand buffer (while the previous tile's
+        // contraction runs)
+#pragma unroll
+        for (int c8 = 0; c8 < G; ++c8) {
+          const uint32_t w4[4] = {pre[c8].x, pre[c8].y, pre[c8].z, pre[c8].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 xx = *reinterpret_cast<const __half2*>(&w4[i]);
+            const __half2 qq = __hmul2(xx, xx);
+            const float2 xf = __half22float2(xx), qf = __half22float2(qq);
+            rn2 += xf.x * xf.x + xf.y * xf.y + qf.x * qf.x + qf.y * qf.y;
+          }
+        }
+      }
       if (it > 0 && !warp_wait(&bar[A_EMPTY], (it - 1) & 1)) { fail(); break; }
       if (it >= 2 && !warp_wait(&bar[R_FREE + (it & 1)], ((it >> 1) - 1) & 1)) {
         fail(); break;
       }
-      float rn2 = 0.f;
 #pragma unroll
       for (int c8 = 0; c8 < G; ++c8) {
         if constexpr (XT == GMM_F16) {
@@ -507,10 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           uint32_t hq[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const __half2 xx = *reinterpret_cast<const __half2*>(&w4[i]);
-            const __half2 qq = __hmul2(xx, xx);
-            const float2 xf = __half22float2(xx), qf = __half22float2(qq);
-            rn2 += xf.x * xf.x + xf.y * xf.y + qf.x * qf.x + qf.y * qf.y;
+            const __half2 qq = __hmul2(*reinterpret_cast<const __half2*>(&w4[i]),
+                                       *reinterpret_cast<const __half2*>(&w4[i]));
             hq[i] = *reinterpret_cast<const uint32_t*>(&qq);
           }
           *reinterpret_cast<uint4*>(sA + tc::sw128_offset(p, c8 * 8, kBM)) = pre[c8];
