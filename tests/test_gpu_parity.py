@@ -226,6 +226,59 @@ def test_empty_floor_notpd_flags():
     assert got["status"] == 3 and got["flags"][3] & oracle.FLAG_NOT_PD
 
 
+def test_folded_screen_wide_scales():
+    """Resident, folded screening operands (two chunks of components, the
+    second ragged) under variances four decades apart, so that the chunk's
+    common scale leaves small operands subnormal; with a dead component
+    (pi = 0) and one far from every point.  The same step as the oracle,
+    with and without LSE_n."""
+    rng = np.random.default_rng(23)
+    N, D, K = 3001, 128, 200
+    centres = rng.standard_normal((K, D)) * 0.3
+    sd = (np.exp(rng.uniform(np.log(0.05), np.log(1.0), (K, 1))) *
+          np.exp(rng.uniform(-0.3, 0.3, (K, D))))
+    lab = rng.integers(0, K, N)
+    X = (centres[lab] + rng.standard_normal((N, D)) * sd[lab]).astype(np.float16)
+    bits = X.view(np.uint16)
+    pi = rng.dirichlet(np.full(K, 1.0))
+    pi[7] = 0.0
+    pi = (pi / pi.sum()).astype(np.float32)
+    mu = (centres + 0.1 * sd * rng.standard_normal((K, D))).astype(np.float32)
+    mu[13] = 300.0   # sets chunk 0's common scale: its other operands shrink
+    var = (sd ** 2 * rng.uniform(0.8, 1.25, (K, D))).astype(np.float32)
+    var[13] = 1.0
+    opts = dict(var_floor=1e-8, min_s0=0.5)
+    wl = datagen.Workload("folded", 0, N, D, K, datagen.F16, datagen.COV_DIAG, 1, 0, {})
+    ref = oracle_step(bits, datagen.F16, (pi, mu, var), wl.cov_type, opts=opts, want_lse=True)
+    s = make_state(wl)
+    Xd = to_device(bits, datagen.F16)
+    for want_lse in (False, True):
+        got = gpu_step(s, Xd, (pi, mu, var), want_lse=want_lse, opts=opts)
+        assert got["status"] == 0, got["status"]
+        # the screen keeps most rows (the rest take the CUDA-core row list)
+        handed = int(s.ws[8:12].cpu().numpy().view(np.uint32)[0])
+        assert handed < N // 3, handed
+        fails = parity.compare_step(got, ref, "folded lse=%d" % want_lse, opts["min_s0"])
+        assert not fails, "\n".join(fails[:10])
+        if want_lse:
+            assert np.abs(got["lse"] - ref["lse"]).max() <= 1e-4 * np.abs(ref["lse"]).max()
+    # the same operands in assignment mode (top-4 on the folded screen)
+    m = 4
+    st, ids_ref, gam_ref, lse_ref = oracle.topm(bits, pi, mu, var, wl.cov_type, m,
+                                                xdtype=datagen.F16)
+    assert st == 0
+    from soft_clustering_gb300.torch_api import Assigner
+    a = Assigner(N, D, K, wl.cov_type, datagen.F16, m)
+    a.prepare(pi, mu, var)
+    a.assign(Xd)
+    assert a.device_status() == 0
+    ids = a.ids.cpu().numpy()
+    agree, kept = parity.top1_agreement(ids, ids_ref, gam_ref)
+    assert agree >= parity.TOP1_MIN, (agree, kept)
+    lse = a.lse.cpu().numpy().astype(np.float64)
+    assert np.abs(lse - lse_ref).max() <= 1e-4 * np.abs(lse_ref).max()
+
+
 def test_nonfinite_input_reported():
     N, D, K = 300, 16, 2
     X = np.random.default_rng(1).standard_normal((N, D)).astype(np.float32)
@@ -277,8 +330,8 @@ def test_tensor_core_path_matches_cuda_core_path(name, n, cov):
 
 
 def test_hand_over_rows_match_oracle():
-    """Rows the tensor-core screen hands over (more than 16 candidates in one
-    column half of a chunk) take the CUDA-core row-list kernels.  24 copies of
+    """Rows the tensor-core screen hands over (more candidates than a row's
+    list holds) take the CUDA-core row-list kernels.  24 copies of
     one component in the first column half force that for every point whose
     window holds them; the statistics of both routes, merged, still match the
     oracle."""
