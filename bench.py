@@ -414,7 +414,10 @@ def run_ours(args, wl):
         ll_host = torch.zeros(1, dtype=torch.float64, pin_memory=True)
         del X
         torch.cuda.empty_cache()
-        st2.step_host(host, loglik_host=ll_host)
+        # the same EM iterations as the device-timed loop: W untimed steps
+        # from theta_0, then the K timed ones
+        for _ in range(max(1, args.warmup)):
+            st2.step_host(host, loglik_host=ll_host)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(args.steps):
