@@ -167,63 +167,81 @@ __device__ __forceinline__ __half half_ru(double v) {
 // the margin terms themselves and 2e-6 spare.
 constexpr double kFoldKappa = 1.5e-3 * 1.0001 + 2e-6;
 
-// Folded operands, part 1: one block of 1024 threads per chunk; warp w sums
-// the norms of components 4w .. 4w + 3 (lanes over the coordinates), then
-// thread t < 128 finishes component k = 128 chunk + t.  Picks the chunk's
-// scale S, a power of two with max |b| / S <= 2^14, |bias| / S <= 2^25 and
-// max d_k / S <= 2^15 (no fp16 overflow in either step), and writes the
-// extra K = 16 row of B, the margins u_k and d_k and the trailer scalars
-// (see tc_fold).  d_k covers the 1e-3 + 1e-6 |bias| gap between the
-// expanded form and the exact fp32 log-density, the accumulation allowance
-// on the bias terms (3.6e-5 |bias|) and the residual of the bias split.
-// Dead and padding components get bias part -inf and zero margins.
-constexpr int kFoldThreads = 1024;
-__global__ void __launch_bounds__(kFoldThreads) prepare_fold_scale_kernel(PreparedLayout L,
-                                                                          void* prepared) {
-  __shared__ double s_mx[kTcChunk], s_n2[kTcChunk], s_q[kTcChunk];
+// Folded operands, part 0: one block of 128 threads per component of the
+// padded range: max |b|, |b|^2 and sum mu^2 w in fp64, staged (3 doubles per
+// component) in the chunk's extra-row region, which part 1 overwrites.
+__global__ void __launch_bounds__(kTcChunk) prepare_fold_sums_kernel(PreparedLayout L,
+                                                                     void* prepared) {
+  __shared__ double red[3][kTcChunk / 32];
+  const int k = blockIdx.x, chunk = k / kTcChunk, row = k % kTcChunk;
+  const int D = L.D, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const bool live = k < L.K && at<float>(prepared, L.off_c)[k] != -INFINITY;
+  double mx = 0.0, n2 = 0.0, q = 0.0;
+  if (live) {
+    const float* mu = at<float>(prepared, L.off_mu) + (size_t)k * D;
+    const float* prec = at<float>(prepared, L.off_prec) + (size_t)k * (L.cov == GMM_COV_DIAG ? D : 1);
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      const double w = (double)prec[L.cov == GMM_COV_DIAG ? d : 0];
+      const double b1 = (double)mu[d] * w, b2 = -0.5 * w;
+      mx = fmax(mx, fmax(fabs(b1), fabs(b2)));
+      n2 += b1 * b1 + b2 * b2;
+      q += (double)mu[d] * b1;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+    q += __shfl_xor_sync(0xffffffffu, q, o);
+  }
+  if (lane == 0) { red[0][wid] = mx; red[1][wid] = n2; red[2][wid] = q; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double m = 0.0, a2 = 0.0, qq = 0.0;
+    for (int i = 0; i < kTcChunk / 32; ++i) { m = fmax(m, red[0][i]); a2 += red[1][i]; qq += red[2][i]; }
+    double* stage = reinterpret_cast<double*>(at<unsigned char>(prepared, L.off_tcB) +
+                                              (size_t)chunk * L.tcB_chunk_bytes +
+                                              (size_t)kTcChunk * 2 * D * 2) + 3 * row;
+    stage[0] = m;
+    stage[1] = a2;
+    stage[2] = qq;
+  }
+}
+
+// Folded operands, part 1: one block of 128 threads per chunk, thread t for
+// component k = 128 chunk + t, from the sums part 0 staged.  Picks the
+// chunk's scale S, a power of two with max |b| / S <= 2^14, |bias| / S <=
+// 2^25 and max d_k / S <= 2^15 (no fp16 overflow in either step), and writes
+// the extra K = 16 row of B, the margins u_k and d_k and the trailer scalars
+// (see tc_fold).  d_k covers the 1e-3 + 1e-6 |bias| gap between the expanded
+// form and the exact fp32 log-density, the accumulation allowance on the bias
+// terms (3.6e-5 |bias|) and the residual of the bias split.  Dead and padding
+// components get bias part -inf and zero margins.
+__global__ void __launch_bounds__(kTcChunk) prepare_fold_scale_kernel(PreparedLayout L,
+                                                                      void* prepared) {
   __shared__ double red[3][kTcChunk / 32];
   __shared__ double sS;
   const int chunk = blockIdx.x, t = threadIdx.x, lane = t & 31, wid = t >> 5;
   const int D = L.D;
   const float* cvec = at<float>(prepared, L.off_c);
-  // per-component sums, a warp per component
-  for (int c = wid; c < kTcChunk; c += kFoldThreads / 32) {
-    const int k = chunk * kTcChunk + c;
-    const bool live = k < L.K && cvec[k] != -INFINITY;
-    double mx = 0.0, n2 = 0.0, q = 0.0;
-    if (live) {
-      const float* mu = at<float>(prepared, L.off_mu) + (size_t)k * D;
-      const float* prec = at<float>(prepared, L.off_prec) + (size_t)k * (L.cov == GMM_COV_DIAG ? D : 1);
-      for (int d = lane; d < D; d += 32) {
-        const double w = (double)prec[L.cov == GMM_COV_DIAG ? d : 0];
-        const double b1 = (double)mu[d] * w, b2 = -0.5 * w;
-        mx = fmax(mx, fmax(fabs(b1), fabs(b2)));
-        n2 += b1 * b1 + b2 * b2;
-        q += (double)mu[d] * b1;
-      }
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      n2 += __shfl_xor_sync(0xffffffffu, n2, o);
-      q += __shfl_xor_sync(0xffffffffu, q, o);
-    }
-    if (lane == 0) { s_mx[c] = mx; s_n2[c] = n2; s_q[c] = q; }
-  }
-  __syncthreads();
-  if (t >= kTcChunk) return;
+  const double* stage = reinterpret_cast<const double*>(
+      at<unsigned char>(prepared, L.off_tcB) + (size_t)chunk * L.tcB_chunk_bytes +
+      (size_t)kTcChunk * 2 * D * 2);
+  const double s_mx = stage[3 * t], s_n2 = stage[3 * t + 1], s_q = stage[3 * t + 2];
+  __syncthreads();  // every thread has read its sums before the region is rewritten
+
   const int k = chunk * kTcChunk + t;
   const bool live = k < L.K && cvec[k] != -INFINITY;
-  const double bias = live ? (double)cvec[k] - 0.5 * s_q[t] : 0.0;
+  const double bias = live ? (double)cvec[k] - 0.5 * s_q : 0.0;
   // the d_k bound before the split residual (which is below 1e-7 |bias|)
   const double dpre = live ? 1.0001 * (1e-3 + 3.72e-5 * fabs(bias)) : 0.0;
-  double m0 = s_mx[t], m1 = fabs(bias), m2 = dpre;
+  double m0 = s_mx, m1 = fabs(bias), m2 = dpre;
   for (int o = 16; o > 0; o >>= 1) {
     m0 = fmax(m0, __shfl_xor_sync(0xffffffffu, m0, o));
     m1 = fmax(m1, __shfl_xor_sync(0xffffffffu, m1, o));
     m2 = fmax(m2, __shfl_xor_sync(0xffffffffu, m2, o));
   }
   if (lane == 0) { red[0][wid] = m0; red[1][wid] = m1; red[2][wid] = m2; }
-  asm volatile("bar.sync 1, %0;" ::"r"(kTcChunk));  // the first 128 threads only
+  __syncthreads();
   if (t == 0) {
     double M = 0.0, B = 0.0, Dm = 0.0;
     for (int i = 0; i < kTcChunk / 32; ++i) {
@@ -236,7 +254,7 @@ __global__ void __launch_bounds__(kFoldThreads) prepare_fold_scale_kernel(Prepar
     if (e == -1000) e = 0;
     sS = ldexp(1.0, e);
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(kTcChunk));
+  __syncthreads();
   const double S = sS;
   // bias / S = 2^10 b1 + b2 + 2^-10 b3 (fp16 parts), residual r3
   __half p1 = __ushort_as_half((unsigned short)0xFC00), p2 = __double2half(0.0), p3 = p2;
@@ -250,7 +268,7 @@ __global__ void __launch_bounds__(kFoldThreads) prepare_fold_scale_kernel(Prepar
     p3 = __double2half(r2 * 0x1p10);
     r3 = r2 - (double)__half2float(p3) * 0x1p-10;
   }
-  const double u = live ? kFoldKappa * sqrt(s_n2[t]) + 0x1p-20 * S : 0.0;
+  const double u = live ? kFoldKappa * sqrt(s_n2) + 0x1p-20 * S : 0.0;
   const double dk = live ? dpre + 1.0001 * 1.01 * fabs(r3) * S : 0.0;
   unsigned char* img = at<unsigned char>(prepared, L.off_tcB) + (size_t)chunk * L.tcB_chunk_bytes +
                        (size_t)kTcChunk * 2 * D * 2;
@@ -274,9 +292,9 @@ __global__ void __launch_bounds__(kFoldThreads) prepare_fold_scale_kernel(Prepar
     a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, o));
     a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, o));
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(kTcChunk));  // red is read above before reuse
+  __syncthreads();  // red is read above before reuse
   if (lane == 0) { red[0][wid] = a0; red[1][wid] = a1; }
-  asm volatile("bar.sync 1, %0;" ::"r"(kTcChunk));
+  __syncthreads();
   if (t == 0) {
     float U = 0.f, Dm = 0.f;
     for (int i = 0; i < kTcChunk / 32; ++i) { U = fmaxf(U, (float)red[0][i]); Dm = fmaxf(Dm, (float)red[1][i]); }
@@ -368,7 +386,10 @@ cudaError_t launch_prepare_tc(int D, int K, int cov, void* prepared, cudaStream_
   PreparedLayout L = PreparedLayout::make(D, K, cov);
   if (!L.tc_chunks) return cudaSuccess;
   if (tc_fold(L.tc_chunks)) {
-    prepare_fold_scale_kernel<<<L.tc_chunks, kFoldThreads, 0, s>>>(L, prepared);
+    prepare_fold_sums_kernel<<<L.tc_chunks * kTcChunk, kTcChunk, 0, s>>>(L, prepared);
+    cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+    prepare_fold_scale_kernel<<<L.tc_chunks, kTcChunk, 0, s>>>(L, prepared);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
