@@ -274,11 +274,22 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   // split evenly over the partitions (the count is only known on the device).
   const int64_t cnt = rows ? (int64_t)*row_count : N;
   if (rows) {
+    // at least four tiles per partition: with few handed-over rows most
+    // partitions get none, and leave their partial as it is (accumulating)
+    // or only zero it (the first block of rows)
     rows_per_part = (cnt + gridDim.y - 1) / gridDim.y;
     rows_per_part = (rows_per_part + T - 1) / T * T;
+    if (rows_per_part < 4 * T) rows_per_part = 4 * T;
   }
   const int64_t r0 = (int64_t)blockIdx.y * rows_per_part;
   const int64_t r1 = min(cnt, r0 + rows_per_part);
+  if (rows && r0 >= cnt) {
+    if (!accumulate) {
+      double* out = part + (size_t)blockIdx.y * K * F;
+      for (int f = threadIdx.x; f < kc * F; f += kStatThreads) out[(size_t)k0 * F + f] = 0.0;
+    }
+    return;
+  }
 
   for (int i = threadIdx.x; i < kc * D; i += kStatThreads)
     s_mu[i] = at<float>(prepared, L.off_mu)[(size_t)k0 * D + i];
