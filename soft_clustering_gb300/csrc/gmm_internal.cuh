@@ -103,7 +103,8 @@ struct PreparedLayout {
                      // followed in each image by the chunk's unswizzled K = 16 extra rows
   size_t tcB_chunk_bytes;
   size_t off_tcT;    // float [chunks][kTcTrail]: scale (power of 2) [128], |(b1,b2)|_2 [128],
-                     // bias - delta [128], bias + delta [128]; folded: see tc_fold
+                     // bias - delta [128], bias + delta [128] (the scale is the chunk's, common to its
+                     // components); folded: see tc_fold
   size_t tc_bytes;
   size_t bytes;
 

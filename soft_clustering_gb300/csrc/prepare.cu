@@ -305,6 +305,39 @@ __global__ void __launch_bounds__(kTcChunk) prepare_fold_scale_kernel(PreparedLa
   }
 }
 
+// Streamed chunks (more than kTcFoldChunks): one block of 128 threads per
+// chunk picks the chunk's common scale S, the smallest power of two with
+// max |b| / S <= 2^14 over its components (fp32 maxima: a relative error
+// of 2^-23 cannot overflow fp16), and writes it to every scale slot of the
+// chunk's trailer.
+__global__ void __launch_bounds__(kTcChunk) prepare_stream_scale_kernel(PreparedLayout L,
+                                                                        void* prepared) {
+  __shared__ float red[kTcChunk / 32];
+  __shared__ float sS;
+  const int chunk = blockIdx.x, t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int k = chunk * kTcChunk + t, D = L.D;
+  const bool live = k < L.K && at<float>(prepared, L.off_c)[k] != -INFINITY;
+  float mx = 0.f;
+  if (live) {
+    const float* mu = at<float>(prepared, L.off_mu) + (size_t)k * D;
+    const float* prec = at<float>(prepared, L.off_prec) + (size_t)k * (L.cov == GMM_COV_DIAG ? D : 1);
+    for (int d = 0; d < D; ++d) {
+      const float w = prec[L.cov == GMM_COV_DIAG ? d : 0];
+      mx = fmaxf(mx, fmaxf(fabsf(mu[d] * w), 0.5f * fabsf(w)));
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[wid] = mx;
+  __syncthreads();
+  if (t == 0) {
+    float M = 0.f;
+    for (int i = 0; i < kTcChunk / 32; ++i) M = fmaxf(M, red[i]);
+    sS = M > 0.f ? ldexpf(1.f, (int)ceilf(log2f(M)) - 14) : 1.f;
+  }
+  __syncthreads();
+  at<float>(prepared, L.off_tcT)[(size_t)chunk * kTcTrail + t] = sS;
+}
+
 // Screening operands for the tensor-core kernel (diagonal / isotropic, D = 64
 // or 128), one block per component of the padded range [0, 128 * chunks).
 // Row k of chunk k / 128 holds (b1, b2) = (mu w, -w / 2) divided by a power of
@@ -359,18 +392,21 @@ __global__ void prepare_tc_kernel(PreparedLayout L, void* prepared) {
     s_q = qq;
   }
   __syncthreads();
-  const double m = s_max;
   // folded: the chunk's common scale (written by prepare_fold_scale_kernel)
+  // the chunk's common scale (written by prepare_fold_scale_kernel or
+  // prepare_stream_scale_kernel)
   const bool fold = tc_fold(L.tc_chunks);
-  const double scale = fold ? (double)trail[kFoldS]
-                            : (m > 0.0 ? ldexp(1.0, (int)ceil(log2(m)) - 14) : 1.0);
+  const double scale = fold ? (double)trail[kFoldS] : (double)trail[row];
   for (int j = threadIdx.x; j < KD; j += blockDim.x) {
     const __half h = __double2half(bval(j) / scale);
     *reinterpret_cast<__half*>(img + tc::sw128_offset(row, j, kTcChunk)) = h;
   }
   if (threadIdx.x == 0 && !fold) {
     trail[row] = (float)scale;
-    trail[kTcChunk + row] = (float)sqrt(red[31]);
+    // |(b1, b2)| plus a floor for the operands that the common scale leaves
+    // fp16-subnormal (2^-25 S each, at most 2^-21 S |a| in all, which
+    // kappa |a| (2^-20 S / 1.5e-3) covers)
+    trail[kTcChunk + row] = __double2float_ru(sqrt(red[31]) + 0x1p-20 * scale / 1.5e-3);
     // bias = c_k - sum mu^2 w / 2, with the margin of the fp32 evaluation
     // (1e-3 absolute + 1e-6 relative), rounded outwards
     const double bias = live ? (double)at<float>(prepared, L.off_c)[k] - 0.5 * s_q : 0.0;
@@ -390,6 +426,10 @@ cudaError_t launch_prepare_tc(int D, int K, int cov, void* prepared, cudaStream_
     cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
     prepare_fold_scale_kernel<<<L.tc_chunks, kTcChunk, 0, s>>>(L, prepared);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else {
+    prepare_stream_scale_kernel<<<L.tc_chunks, kTcChunk, 0, s>>>(L, prepared);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -902,6 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           const float* __restrict__ tcn = tsc + kBN;
           const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
           const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
+          const float Sj = tsc[0];  // the chunk's common scale (every slot holds it)
           const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
           if (pass == 0) {
             // the best lower bound of the half-chunk,
@@ -914,14 +915,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               tc::tmem_wait32(u);
 #pragma unroll
               for (int i = 0; i < 32; i += 4) {
-                float sc[4], nb[4], bb[4];
-                ld_trail4(tsc + c0 + i, sc);
+                float nb[4], bb[4];
                 ld_trail4(tcn + c0 + i, nb);
                 ld_trail4(tbl + c0 + i, bb);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                   const float v = __uint_as_float(u[i + t]);
-                  const float lo = fmaf(v, sc[t], fmaf(-rnk, nb[t], bb[t]));
+                  const float lo = fmaf(v, Sj, fmaf(-rnk, nb[t], bb[t]));
                   if (t & 1) best1 = fmaxf(best1, lo);
                   else best0 = fmaxf(best0, lo);
                   if constexpr (MODE == MODE_ASSIGN) {
@@ -948,14 +948,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               uint32_t pm = 0u;
 #pragma unroll
               for (int i = 0; i < 32; i += 4) {
-                float sc[4], nb[4], bb[4];
-                ld_trail4(tsc + c0 + i, sc);
+                float nb[4], bb[4];
                 ld_trail4(tcn + c0 + i, nb);
                 ld_trail4(tbh + c0 + i, bb);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                   const float v = __uint_as_float(u[i + t]);
-                  const float hi = fmaf(v, sc[t], fmaf(rnk, nb[t], bb[t]));
+                  const float hi = fmaf(v, Sj, fmaf(rnk, nb[t], bb[t]));
                   pm |= hi >= thr ? (1u << (i + t)) : 0u;
                 }
               }
