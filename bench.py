@@ -180,18 +180,21 @@ def traffic_for(kernel, workload):
     rec = d.get(kernel, {}).get(workload)
     if not rec:
         return None
-    if rec.get("src_sha") != source_sha():
+    if rec.get("src_sha") != source_sha(rec.get("sources")):
         return None
     return rec.get("bytes_per_launch")
 
 
-def source_sha():
+def source_sha(files=None):
+    """Hash of the library sources `files` (names under csrc/; all of them
+    when None): a capture stays valid while the kernel's own sources do."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "soft_clustering_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+    names = sorted(files) if files else sorted(
+        fn for fn in os.listdir(csrc) if fn.endswith((".cu", ".cuh", ".h")))
+    for fn in names:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 

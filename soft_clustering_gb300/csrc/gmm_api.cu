@@ -161,6 +161,7 @@ gmm_status cuda_status(cudaError_t e) {
 struct ProfRec {
   const char* name;
   cudaEvent_t a, b;
+  int kernels;
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
@@ -178,6 +179,7 @@ cudaEvent_t prof_event() {
 
 
 #define GMM_PROF(name) ProfScope _prof_scope(name, s)
+#define GMM_PROFN(name, n) ProfScope _prof_scope(name, s, n)
 
 // The E-step and statistics for one block of rows, accumulating into the
 // workspace partials (accumulate = 0 for the first block of an iteration).
@@ -214,7 +216,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
                           recs, tcnt, kRecCap, st, s));
       }
       {
-        GMM_PROF("fb_compact_kernel");
+        GMM_PROFN("fb_compact_kernel", 2);
         GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
       }
       {
@@ -286,7 +288,8 @@ gmm_status host_res(HostPathRes** out) {
 
 }  // namespace
 
-ProfScope::ProfScope(const char* n, cudaStream_t st) : name(n), s(st) {
+ProfScope::ProfScope(const char* n, cudaStream_t st, int nkernels)
+    : name(n), s(st), kernels(nkernels) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (g_prof_on) { a = prof_event(); cudaEventRecord(a, s); }
 }
@@ -296,7 +299,7 @@ ProfScope::~ProfScope() {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   cudaEvent_t b = prof_event();
   cudaEventRecord(b, s);
-  g_prof_pending.push_back({name, a, b});
+  g_prof_pending.push_back({name, a, b, kernels});
 }
 
 // The statistics partition count the entry points above use, for other
@@ -360,7 +363,7 @@ gmm_status gmm_prepare(const gmm_params* p, int D, int K, gmm_cov_type cov, cons
   gmm_opts o = opts ? *opts : gmm_default_opts();
   cudaStream_t s = (cudaStream_t)stream;
   {
-    GMM_PROF("prepare_kernel");
+    GMM_PROFN("prepare_kernel", 1 + (tc_eligible(D, cov) ? 3 : 0));
     GMM_TRY(launch_prepare(p, D, K, cov, o.ridge_rel, prepared, nullptr, s));
   }
   if (flags_dev) {
@@ -389,7 +392,7 @@ gmm_status gmm_em_step(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
   PreparedLayout PL = PreparedLayout::make(D, K, cov);
   GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
   {
-    GMM_PROF("prepare_kernel");
+    GMM_PROFN("prepare_kernel", 1 + (tc_eligible(D, cov) ? 3 : 0));
     GMM_TRY(launch_prepare(params, D, K, cov, o.ridge_rel, prep, st, s));
   }
   float* lse = lse_dev ? lse_dev : at<float>(ws, W.off_lse);
@@ -432,7 +435,7 @@ gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int
   char* stage[2] = {at<char>(ws, W.off_stage), at<char>(ws, W.off_stage + stage_one)};
   GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
   {
-    GMM_PROF("prepare_kernel");
+    GMM_PROFN("prepare_kernel", 1 + (tc_eligible(D, cov) ? 3 : 0));
     GMM_TRY(launch_prepare(params, D, K, cov, o.ridge_rel, prep, st, s));
   }
   // The copy stream may start only after earlier work on `s` that used the
@@ -500,7 +503,7 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
                           nullptr, nullptr, 0, st, s));
       }
       {
-        GMM_PROF("fb_compact_kernel");
+        GMM_PROFN("fb_compact_kernel", 2);
         GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
       }
       GMM_PROF("lse_rows_kernel");
@@ -530,7 +533,7 @@ int gmm_profile_read(const char** names, double* ms_total, long* launches, int m
       if (strcmp(g_prof_sum[i].name, r.name) == 0) break;
     if (i == g_prof_sum.size()) g_prof_sum.push_back({r.name, 0.0, 0});
     g_prof_sum[i].ms += ms;
-    g_prof_sum[i].launches += 1;
+    g_prof_sum[i].launches += r.kernels;
     g_prof_pool.push_back(r.a);
     g_prof_pool.push_back(r.b);
   }

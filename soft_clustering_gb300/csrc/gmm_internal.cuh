@@ -16,13 +16,14 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a = kAlign) {
 }
 
 // Profiler scope: when profiling is on (gmm_profile_enable), the launches in
-// its lifetime are bracketed by two CUDA events on `s` and summed under
-// `name` (defined in gmm_api.cu).
+// its lifetime (`kernels` of them) are bracketed by two CUDA events on `s`
+// and summed under `name` (defined in gmm_api.cu).
 struct ProfScope {
   const char* name;
   cudaStream_t s;
+  int kernels;
   cudaEvent_t a = nullptr;
-  ProfScope(const char* n, cudaStream_t st);
+  ProfScope(const char* n, cudaStream_t st, int nkernels = 1);
   ~ProfScope();
   ProfScope(const ProfScope&) = delete;
   ProfScope& operator=(const ProfScope&) = delete;

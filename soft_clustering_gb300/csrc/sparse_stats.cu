@@ -515,7 +515,7 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
-    ProfScope p("rec_scan_kernels", s);
+    ProfScope p("rec_scan_kernels", s, 2);
     rec_scan_blocks_kernel<<<(unsigned)K, kScanThreads, 0, s>>>(counts, K, S.nb, ktot);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     rec_scan_comps_kernel<<<1, kScanThreads, 0, s>>>(ktot, K, cstart, kstart);
@@ -585,6 +585,7 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // the single-candidate points' log-likelihood joins the total
+  ProfScope prof_ll("ll_finalize_kernel", s);
   return launch_ll_finalize(llk, K, ll, 1, s);
 }
 
