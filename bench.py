@@ -205,6 +205,25 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(x, device=None):
+    """The largest x over the ranks of the default process group (x itself
+    without one): every rank's step time or end-to-end time, so the job's
+    rate is set by its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, seconds):
+    """Whole-job throughput: the units every replica processed, over the
+    slowest replica's time."""
+    return world * units_per_rank / seconds
+
+
 def oracle_once(wl, mix, bits):
     """One oracle call on `bits`: an EM iteration from theta_0, or (assignment
     workloads) top-m against the planted parameters."""
@@ -364,14 +383,10 @@ def run_ours(args, wl):
     clk = clocks.stop()
     G.gmm_profile_enable(False)
     prof = G.gmm_profile_read()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
     status = st.device_status()
     ll = float(st.loglik.item())
-    value = world * wm["pairs"] / (ms / 1e3)
+    value = job_rate(world, wm["pairs"], ms / 1e3)
     launches = sum(n for (_, n) in prof.values())
 
     # dominant kernel roofline, measured live in the timed region
@@ -425,12 +440,8 @@ def run_ours(args, wl):
         t0 = time.perf_counter()
         for _ in range(args.steps):
             st2.step_host(host, loglik_host=ll_host)
-        e2e_s = (time.perf_counter() - t0) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = dict(value=world * wm["pairs"] / e2e_s, unit=UNIT,
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, dev)
+        e2e = dict(value=job_rate(world, wm["pairs"], e2e_s), unit=UNIT,
                    h2d_bytes_per_step=wm["x_bytes"], d2h_bytes_per_step=8,
                    ms_per_step=e2e_s * 1e3, chunk_rows=chunk)
 
@@ -526,13 +537,9 @@ def run_assign(args, wl):
     clk = clocks.stop()
     G.gmm_profile_enable(False)
     prof = G.gmm_profile_read()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
     status = a.device_status()
-    value = world * wm["pairs"] / (ms / 1e3)
+    value = job_rate(world, wm["pairs"], ms / 1e3)
     launches = sum(n for (_, n) in prof.values())
     top = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
     roof = None
@@ -565,12 +572,8 @@ def run_assign(args, wl):
             ids_h.copy_(a.ids, non_blocking=True)
             gam_h.copy_(a.gamma, non_blocking=True)
             torch.cuda.synchronize()
-        e2e_s = (time.perf_counter() - t0) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = dict(value=world * wm["pairs"] / e2e_s, unit=UNIT, h2d_bytes_per_step=wm["x_bytes"],
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, dev)
+        e2e = dict(value=job_rate(world, wm["pairs"], e2e_s), unit=UNIT, h2d_bytes_per_step=wm["x_bytes"],
                    d2h_bytes_per_step=wl.N * wl.m * 8, ms_per_step=e2e_s * 1e3)
 
     cpu = None
