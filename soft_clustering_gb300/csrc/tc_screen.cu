@@ -597,6 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       const bool valid = n < a.N;
       if (!warp_wait(&bar[R_FULL + g], s & 1)) { fail(); break; }
       const float rn = sRN[g * kBM + r];
+      // the slot holds only the row norms: hand it back at once, so that the
+      // producers' next write of it never waits for this tile's sweeps
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[R_FREE + g]);
       float ref = -INFINITY;  // lower bound of the best log joint
       float dropped = -INFINITY;
       float lbm[8];           // assign: the m largest lower bounds seen
@@ -699,7 +703,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         }
       }
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar[R_FREE + g]);
       if (!ok) break;
       const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
       // a point with a single candidate has gamma = 1 (every other component
