@@ -224,17 +224,25 @@ def job_rate(world, units_per_rank, seconds):
     return world * units_per_rank / seconds
 
 
-def oracle_once(wl, mix, bits):
-    """One oracle call on `bits`: an EM iteration from theta_0, or (assignment
-    workloads) top-m against the planted parameters."""
+def oracle_params(wl, mix):
+    """The parameters the oracle runs from: theta_0 and the EM options, or
+    (assignment workloads) the planted parameters."""
     import datagen
-    import oracle
     if wl.m:
-        pi, mu, var = datagen.planted_params_f16(mix)
-        return oracle.topm(bits, pi, mu, var, wl.cov_type, wl.m, xdtype=wl.dtype)
+        return datagen.planted_params_f16(mix), None
     theta = datagen.init_params(mix)
-    opts = datagen.em_opts(theta)
-    return oracle.em_step(bits, *theta, wl.cov_type, xdtype=wl.dtype, opts=opts)
+    return theta, datagen.em_opts(theta)
+
+
+def oracle_once(wl, params, bits):
+    """One oracle call on `bits`: an EM iteration from theta_0, or (assignment
+    workloads) top-m against the planted parameters (`params` from
+    oracle_params, made outside the timed call)."""
+    import oracle
+    (pi, mu, cov), opts = params
+    if wl.m:
+        return oracle.topm(bits, pi, mu, cov, wl.cov_type, wl.m, xdtype=wl.dtype)
+    return oracle.em_step(bits, pi, mu, cov, wl.cov_type, xdtype=wl.dtype, opts=opts)
 
 
 def cpu_sample_run(wl, mix, seconds):
@@ -243,19 +251,24 @@ def cpu_sample_run(wl, mix, seconds):
     Returns (pairs_per_s, n', threads, seconds_taken)."""
     import datagen
     import oracle
-    # calibrate twice: a tiny run is dominated by thread start-up, so the
-    # second run (about a second of work) sets the sample size
-    n_cal = min(wl.N, 256)
-    for _ in range(2):
+    params = oracle_params(wl, mix)
+    # calibrate on growing samples until one takes a second or more: small
+    # samples leave most threads idle (the oracle parallelises over blocks
+    # of points), so their time per point overstates a large sample's
+    n_cal = min(wl.N, 16384)
+    while True:
         bits = datagen.points(mix, 0, n_cal)
         t0 = time.perf_counter()
-        oracle_once(wl, mix, bits)
-        per_point = max((time.perf_counter() - t0) / n_cal, 1e-9)
-        n_cal = int(min(wl.N, max(n_cal, 1.0 / per_point)))
+        oracle_once(wl, params, bits)
+        dt = time.perf_counter() - t0
+        per_point = max(dt / n_cal, 1e-9)
+        if dt >= 1.0 or n_cal >= wl.N:
+            break
+        n_cal = int(min(wl.N, max(2 * n_cal, 1.5 / per_point)))
     n = int(min(wl.N, max(n_cal, seconds / per_point)))
     bits = datagen.points(mix, 0, n)
     t0 = time.perf_counter()
-    oracle_once(wl, mix, bits)
+    oracle_once(wl, params, bits)
     dt = time.perf_counter() - t0
     return n * wl.K / dt, n, oracle.max_threads(), dt
 
