@@ -71,3 +71,22 @@ def test_invalid_args_are_synchronous(lib):
     assert st == G.GMM_ERR_INVALID_ARG  # m > 8
     st = lib.gmm_prepare(None, 64, 4, G.GMM_COV_DIAG, None, None, None, None)
     assert st == G.GMM_ERR_INVALID_ARG
+
+
+def test_empty_and_degenerate_sizes_are_rejected(lib):
+    """N = 0 (no points), K = 0 (no components) and D = 0 are argument errors,
+    returned before anything is queued; the size queries answer 0."""
+    p = G.make_params(16, 16, 16)
+    o = G.gmm_default_opts()
+    for N, D, K in [(0, 64, 4), (-1, 64, 4), (100, 64, 0), (100, 0, 4)]:
+        st = lib.gmm_em_step(16, G.GMM_F16, N, D, K, ctypes.byref(p), G.GMM_COV_DIAG,
+                             ctypes.byref(o), 256, 1 << 20, 16, None, None, None)
+        assert st == G.GMM_ERR_INVALID_ARG, (N, D, K, st)
+        st = lib.gmm_assign_topm(16, G.GMM_F16, N, D, K, 256, G.GMM_COV_DIAG, 1, 16, 16, None,
+                                 256, 1 << 20, None)
+        assert st == G.GMM_ERR_INVALID_ARG, (N, D, K, st)
+        st = lib.gmm_em_step_noalloc(16, G.GMM_F16, N, D, K, ctypes.byref(p), G.GMM_COV_DIAG,
+                                     ctypes.byref(o), 16, 16, None, None)
+        assert st == G.GMM_ERR_INVALID_ARG, (N, D, K, st)
+        assert G.gmm_workspace_bytes(N, D, K, G.GMM_COV_DIAG, G.GMM_F16) == 0
+    assert G.gmm_prepared_bytes(64, 0, G.GMM_COV_DIAG) == 0

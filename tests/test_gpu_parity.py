@@ -198,6 +198,36 @@ def test_edge_cases_small():
         assert (got["flags"] == ref["flags"]).all(), (got["flags"], ref["flags"])
 
 
+@pytest.mark.parametrize("D,xdtype,cov", [(128, datagen.F16, datagen.COV_DIAG),
+                                          (64, datagen.BF16, datagen.COV_ISO)])
+def test_tensor_core_edge_cases(D, xdtype, cov):
+    """The tensor-core path at degenerate sizes: one point (one tile, 127 rows
+    past the end), a partial tile, exactly one full tile, one row past it,
+    and K from 1 (one chunk, 127 padding columns) to two full folded chunks.
+    Against the oracle, with and without LSE_n."""
+    for N, K in [(1, 1), (1, 5), (7, 3), (128, 256), (129, 200)]:
+        wl = datagen.Workload("tc_edge", 300 + N + K + D, N, D, K, xdtype, cov, 1,
+                              datagen.MIX_DIAG, dict(mean_sd=1.0, sd_mode=0, lo=0.5, hi=1.0,
+                                                     alpha=1.0))
+        mix = datagen.planted(wl)
+        bits = datagen.points(mix, 0, N)
+        pi = np.full(K, 1.0 / K, dtype=np.float32)
+        mu = mix.mu.astype(np.float32) * 0.5
+        var = np.ones((K, D) if cov == datagen.COV_DIAG else (K,), dtype=np.float32)
+        opts = dict(var_floor=1e-6, min_s0=0.5)
+        ref = oracle_step(bits, wl.dtype, (pi, mu, var), wl.cov_type, opts=opts, want_lse=True)
+        assert ref["status"] == 0
+        Xd = to_device(bits, wl.dtype)
+        for want_lse in (False, True):
+            got = gpu_step(make_state(wl), Xd, (pi, mu, var), want_lse=want_lse, opts=opts)
+            assert got["status"] == 0, (N, K, got["status"])
+            fails = parity.compare_step(got, ref, "N=%d K=%d lse=%d" % (N, K, want_lse), 0.5)
+            assert not fails, fails
+            assert (got["flags"] == ref["flags"]).all(), (got["flags"], ref["flags"])
+            if want_lse:
+                np.testing.assert_allclose(got["lse"], ref["lse"], rtol=1e-5, atol=1e-3)
+
+
 def test_empty_floor_notpd_flags():
     """Empty component (mean far away), variance floor, and a covariance that
     is not positive definite: same flags and parameters as the oracle."""
