@@ -253,6 +253,7 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   constexpr int KC = SS::KC, F = SS::F, SLOTS = SS::SLOTS, T = kStatTile;
   constexpr int P = LseShape<D, COV>::P;
   constexpr int XS = D + 1;  // padded row of the x tile
+  constexpr int YS = D + 1;  // padded row of the y tile (full): a warp's rows in different banks
   extern __shared__ double smd[];
   double* s_r0 = smd;                 // KC     running S0 of this block
   double* s_r1 = s_r0 + KC;           // KC*D   running S1 of this block
@@ -265,8 +266,8 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
   float* s_c = s_prec + KC * P;       // KC
   float* s_t0 = s_c + KC;             // KC     tile sums
   float* s_t1 = s_t0 + KC;            // KC*D
-  float* s_y = s_t1 + KC * D;         // full only: T*KC*D   (y = x - c)
-  short* s_pair = (short*)(s_y + (COV == GMM_COV_FULL ? T * KC * D : 0));
+  float* s_y = s_t1 + KC * D;         // full only: T*KC*YS  (y = x - c)
+  short* s_pair = (short*)(s_y + (COV == GMM_COV_FULL ? T * KC * YS : 0));
 
   const int k0 = blockIdx.x * KC;
   const int kc = min(KC, K - k0);
@@ -336,7 +337,7 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
 #pragma unroll
           for (int d = 0; d < D; ++d) {
             y[d] = s_x[r * XS + d] - s_mu[kk * D + d];
-            s_y[(r * KC + kk) * D + d] = y[d];
+            s_y[(r * KC + kk) * YS + d] = y[d];
           }
           l = logj_full<D>(y, s_prec + kk * P, s_c[kk]);
         } else {
@@ -371,7 +372,7 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
       } else {
         const int d = feat - 1;
         if constexpr (COV == GMM_COV_FULL) {
-          for (int r = 0; r < tn; ++r) acc = fmaf(s_g[r * KC + kk], s_y[(r * KC + kk) * D + d], acc);
+          for (int r = 0; r < tn; ++r) acc = fmaf(s_g[r * KC + kk], s_y[(r * KC + kk) * YS + d], acc);
         } else {
           const float c_d = s_mu[kk * D + d];
           for (int r = 0; r < tn; ++r) acc = fmaf(s_g[r * KC + kk], s_x[r * XS + d] - c_d, acc);
@@ -402,7 +403,7 @@ stats_kernel(const void* __restrict__ X, int64_t N, int K, const void* __restric
       float m2 = 0.f;
       if constexpr (COV == GMM_COV_FULL) {
         for (int r = 0; r < tn; ++r) {
-          const float* y = s_y + (r * KC + kk) * D;
+          const float* y = s_y + (r * KC + kk) * YS;
           m2 = fmaf(s_g[r * KC + kk], (y[a] - ma) * (y[b] - mb), m2);
         }
       } else {
@@ -493,7 +494,7 @@ size_t stat_smem() {
   size_t b = sizeof(double) * (size_t)SS::KC * (2 * D + 2);
   size_t f = (size_t)kStatTile * (D + 1) + kStatTile * SS::KC + SS::KC * D + SS::KC * P + SS::KC +
              SS::KC + SS::KC * D;
-  if (COV == GMM_COV_FULL) f += (size_t)kStatTile * SS::KC * D;
+  if (COV == GMM_COV_FULL) f += (size_t)kStatTile * SS::KC * (D + 1);
   b += f * sizeof(float);
   if (COV == GMM_COV_FULL) b += sizeof(short) * 2 * (D * (D + 1) / 2);
   return b;
