@@ -72,6 +72,24 @@ class GMMState:
     def device_status(self, stream=None):
         return gmm_last_device_status(self.ws, stream)
 
+    def save_checkpoint(self, path, iteration, ll_history=()):
+        """Write the parameters (fp32, bit for bit), the iteration count and the
+        log-likelihood history; waits for the device work queued so far."""
+        from . import checkpoint
+        checkpoint.save(path, self.pi.cpu().numpy(), self.mu.cpu().numpy(),
+                        self.cov.cpu().numpy(), self.cov_type, iteration, ll_history)
+
+    def load_checkpoint(self, path):
+        """Set the parameters from a checkpoint of this shape; returns
+        (iteration, ll_history)."""
+        from . import checkpoint
+        c = checkpoint.load(path)
+        if (c["D"], c["K"], c["cov_type"]) != (self.D, self.K, self.cov_type):
+            raise ValueError("checkpoint is for D=%d K=%d cov=%d, state is D=%d K=%d cov=%d"
+                             % (c["D"], c["K"], c["cov_type"], self.D, self.K, self.cov_type))
+        self.set_params(c["pi"], c["mu"], c["cov"])
+        return c["iteration"], c["ll_history"]
+
 
 class Assigner:
     """Prepared parameters + outputs for top-m assignment of N points."""
