@@ -96,3 +96,38 @@ def top1_agreement(ids_gpu, ids_ref, gamma_ref):
         return 1.0, 0
     agree = (ids_gpu[keep, 0] == ids_ref[keep, 0]).mean()
     return float(agree), int(keep.sum())
+
+
+def replay_bundle(wl, bits, theta, fails, directory=None):
+    """What reproduces a failed parity case (the ops-debug page, sec. 5.3):
+    workload, seed, sizes and recipe, the SHA-256 of the input bits and of
+    each parameter array as fp32, and the failures, as one JSON file in
+    `directory` (else $GMM_REPLAY_DIR, else the temporary directory).
+    Returns its path, or None if it could not be written: the failure itself
+    is reported either way."""
+    try:
+        import hashlib
+        import json
+        import os
+        import tempfile
+        import time
+        d = directory or os.environ.get("GMM_REPLAY_DIR") or tempfile.gettempdir()
+        os.makedirs(d, exist_ok=True)
+
+        def sha(a):
+            return hashlib.sha256(np.ascontiguousarray(a).tobytes()).hexdigest()
+
+        rec = dict(workload=wl.name, seed=int(wl.seed), N=int(wl.N), D=int(wl.D), K=int(wl.K),
+                   x_dtype=int(wl.dtype), cov_type=int(wl.cov_type), kind=int(wl.kind),
+                   recipe={k: float(v) for k, v in dict(wl.recipe).items()},
+                   x_sha256=sha(bits),
+                   params_sha256=[sha(np.asarray(p, dtype=np.float32)) for p in theta],
+                   failures=[str(f) for f in list(fails)[:50]])
+        path = os.path.join(d, "gmm_replay_%s_s%d_n%d_%d.json"
+                            % (wl.name, wl.seed, wl.N, int(time.time() * 1e3)))
+        with open(path, "w") as f:
+            json.dump(rec, f, indent=1)
+        return path
+    except Exception:
+        return None
+

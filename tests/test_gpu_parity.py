@@ -64,6 +64,9 @@ def _run_parity(wl, iters, trajectory=True):
                                          opts["min_s0"], parity.TRAJ_PARAM_RTOL,
                                          parity.TRAJ_MIN_S0)
             ref_theta = (ref["pi"], ref["mu"], ref["cov"])
+    if fails:
+        bundle = parity.replay_bundle(wl, bits, theta0, fails)
+        fails.insert(0, "replay bundle: %s" % bundle)
     assert not fails, "\n".join(fails[:10])
 
 
