@@ -72,6 +72,15 @@ class GMMState:
     def device_status(self, stream=None):
         return gmm_last_device_status(self.ws, stream)
 
+    def fit(self, X, max_iters, tol=0.0, log=None):
+        """EM on device-resident X from the current parameters until the
+        log-likelihood's relative rise is at most tol, or max_iters steps;
+        reads the log-likelihood and the component flags after each step.
+        Returns the dict of em_loop.run_em (history, convergence, records)."""
+        from . import em_loop
+        return em_loop.run_em(lambda: self.step(X), lambda: self.loglik.item(), max_iters, tol,
+                              read_flags=lambda: self.flags.cpu().numpy(), log=log)
+
     def save_checkpoint(self, path, iteration, ll_history=()):
         """Write the parameters (fp32, bit for bit), the iteration count and the
         log-likelihood history; waits for the device work queued so far."""
