@@ -90,3 +90,16 @@ def test_empty_and_degenerate_sizes_are_rejected(lib):
         assert st == G.GMM_ERR_INVALID_ARG, (N, D, K, st)
         assert G.gmm_workspace_bytes(N, D, K, G.GMM_COV_DIAG, G.GMM_F16) == 0
     assert G.gmm_prepared_bytes(64, 0, G.GMM_COV_DIAG) == 0
+
+
+def test_host_streaming_workspace_is_bounded_by_the_chunk(lib):
+    """gmm_em_step_host keeps only a chunk of rows on the device: its
+    workspace does not grow with N, so a data set need not fit in HBM."""
+    for D, K, cov in [(128, 1024, G.GMM_COV_DIAG), (64, 16, G.GMM_COV_FULL)]:
+        chunk = 1 << 20
+        small = G.gmm_workspace_bytes_host(chunk, D, K, cov, G.GMM_BF16, chunk)
+        huge = G.gmm_workspace_bytes_host(10 ** 10, D, K, cov, G.GMM_BF16, chunk)  # 2.5 TB of X at D=128
+        assert 0 < small == huge, (small, huge)
+        assert huge < 10 ** 10 * D * 2 / 1000
+        assert G.gmm_workspace_bytes_host(10 ** 10, D, K, cov, G.GMM_BF16, 2 * chunk) > huge
+
