@@ -66,3 +66,31 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     with contextlib.redirect_stdout(buf):
         rc = bench.run_reference(args, datagen.WORKLOADS["tiny_diag"])
     assert rc == 0 and buf.getvalue() == ""
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch):
+    """Rank 0 of the reference arm prints one JSON line with the bench's keys,
+    the oracle's own throughput as value, cpu_baseline and e2e."""
+    import json
+    import datagen
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    # a small sample instead of the ~seconds-long calibration
+    monkeypatch.setattr(bench, "cpu_sample_run", lambda wl, mix, s: (1.0, 512, 1, 0.01))
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.run_reference(argparse.Namespace(steps=2, warmup=1),
+                                 datagen.WORKLOADS["tiny_diag"])
+    assert rc == 0
+    lines = buf.getvalue().strip().splitlines()
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "impl",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and "512" in d["cpu_baseline"]["sample"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny_diag"
