@@ -1,9 +1,9 @@
-"""The multi-rank side of bench.py, on CPU: two gloo ranks.
+"""The host side of bench.py, on CPU: two gloo ranks, and the reference arm.
 
 Under torchrun every rank runs an independent replica of the workload; the
 job's step time is the largest over the ranks and its rate counts the units
 of every replica.  The reference arm runs on rank 0 alone; the other ranks
-leave without work or output.
+leave without work or output, and rank 0 prints the contract's JSON line.
 """
 import argparse
 import contextlib
