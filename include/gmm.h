@@ -134,6 +134,12 @@ gmm_status gmm_prepare(const gmm_params* p, int D, int K, gmm_cov_type cov, cons
  *      fp64 ([LP] sec. 3.1, "M-step kernel": block-partial then global).
  *   M: pi' = s0/N, mu' = s1/s0, Sigma' = s2/s0 - mu' mu'^T (iso: mean of the
  *      diagonal), floored at var_floor; empty rule with min_s0.
+ *   Where the tensor-core path applies (diagonal / isotropic covariance,
+ *   D = 64 or 128), every pair is screened with a rigorous error bound and
+ *   the pairs within 40 nats of the point's best log joint are evaluated
+ *   exactly in fp32; LSE_n and the statistics use those, and every other pair
+ *   carries less than 4.3e-18 of its point's responsibility.  Points with more
+ *   candidates than a list holds take the CUDA-core path, which uses all K.
  * params:     in: the current parameters; out: updated in place (stream order).
  * loglik_dev: one double, written with sum_n LSE_n at the INPUT parameters.
  * lse_dev:    optional N floats, LSE_n at the input parameters (NULL: skipped).
