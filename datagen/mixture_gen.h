@@ -111,7 +111,8 @@ GEN_HD double gen_ln(double s) {
   p = p * t2 + 1.0 / 3.0;
   p = p * t2 + 1.0;
   double lnm = 2.0 * t * p;
-  /* ln 2 split so that e * LN2_HI is exact for |e| < 2^11. */
+  /* ln 2 split so that e * LN2_HI is exact for |e| < 2^11 (the two-part
+   * constant of Sun Microsystems' freely distributed fdlibm, e_log.c). */
   const double LN2_HI = 6.93147180369123816490e-01;
   const double LN2_LO = 1.90821492927058770002e-10;
   double ed = (double)e;

@@ -128,11 +128,15 @@ gmm_status gmm_prepare(const gmm_params* p, int D, int K, gmm_cov_type cov, cons
  *   E: l_nk = log pi_k + log N(x_n | mu_k, Sigma_k); LSE_n = log sum_k exp(l_nk)
  *      taken in fp32 with the running maximum subtracted ([LP] sec. 3.2, 4.2);
  *      g_nk = exp(l_nk - LSE_n) ([LP] sec. 1.1) - never written to memory.
- *   statistics: s0_k = sum_n g_nk, s1_k = sum_n g_nk x_n,
- *      s2_k = sum_n g_nk x_n x_n^T (diagonal only for diag / iso) ([FG]),
- *      accumulated per thread block in fp32 and reduced in a fixed order in
- *      fp64 ([LP] sec. 3.1, "M-step kernel": block-partial then global).
- *   M: pi' = s0/N, mu' = s1/s0, Sigma' = s2/s0 - mu' mu'^T (iso: mean of the
+ *   statistics: s0_k = sum_n g_nk, the first moment about the input mean
+ *      c_k = mu_k, and the second moment M2_k = sum_n g_nk (x_n - mu'_k)
+ *      (x_n - mu'_k)^T about the updated mean (diagonal only for diag / iso)
+ *      ([FG] Method: online s0, s1, s2), accumulated in fp32 per block of
+ *      points and merged in a fixed order in fp64 with the pairwise update of
+ *      Chan, Golub and LeVeque ([LP] sec. 3.1, "M-step kernel": block
+ *      partials, then a global reduction).
+ *   M: pi' = s0/N, mu' = c + s1/s0, Sigma' = M2/s0 (the same value as
+ *      s2/s0 - mu' mu'^T without its cancellation; iso: mean of the
  *      diagonal), floored at var_floor; empty rule with min_s0.
  *   Where the tensor-core path applies (diagonal / isotropic covariance,
  *   D = 64 or 128), every pair is screened with a rigorous error bound and
@@ -184,6 +188,29 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
                            const void* prepared, gmm_cov_type cov, int m, int32_t* ids,
                            float* gamma, float* lse, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * gmm_ivf_lists - inverted lists of an IVF index with soft multi-assignment,
+ * from the output of gmm_assign_topm ([FG] "Core insight", second point, and
+ * "Experiments / key findings": a vector near a cluster boundary is stored in
+ * the lists of several high-responsibility clusters).  Entry t of point n
+ * (component ids[n*m + t], responsibility gamma[n*m + t]) joins that
+ * component's list when t == 0 (the point's best component; every point is
+ * indexed at least once) or gamma >= gamma_min.  Entries with an id outside
+ * [0, K) are skipped.  Within each list the points are in ascending order;
+ * the lists are bit-for-bit the same on every run.
+ * ids, gamma:  N*m (device), as gmm_assign_topm writes them.
+ * offsets:     K+1 int64 (device, written): list k is entries
+ *              offsets[k] .. offsets[k+1]-1; offsets[K] = entries in all.
+ * list_pts:    point indices (int32, device, written), list_gamma: their
+ *              gamma (device, written); room for N*m entries each.
+ * ws:          gmm_ivf_lists_ws_bytes(N, m, K) bytes (about 4*K*N/8192).
+ * N <= 2^31 - 1, 1 <= m <= 8, 1 <= K <= 65536; gamma_min not NaN.
+ */
+size_t gmm_ivf_lists_ws_bytes(int64_t N, int m, int K);
+gmm_status gmm_ivf_lists(const int32_t* ids, const float* gamma, int64_t N, int m, int K,
+                         float gamma_min, int64_t* offsets, int32_t* list_pts, float* list_gamma,
+                         void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream` and returns the device status word of `ws`: the
  * first device-side failure of the most recent gmm_em_step, gmm_em_step_host
  * or gmm_assign_topm call on that workspace (each call resets the word), or
@@ -198,24 +225,30 @@ gmm_status gmm_last_device_status(void* ws, void* stream);
  * cudaMalloc after start-up - and so cannot provide the `ws` workspace that
  * gmm_em_step needs.
  *
- * Same arithmetic and outputs as gmm_em_step (same kernels, same reduction
- * order).  X, params, loglik_dev, lse_dev (N floats, required here) and
- * flags_dev (optional) are the caller's device buffers.  All other scratch
- * lives in one 64 MiB array built into the library's device image: every
- * GPU that loads the library holds it until the process exits, and nothing
- * is allocated by this call.  The scratch needed is about
- * N/16 + 8*P*K*F + 4*K*(D+2) + prepared-parameter bytes (P statistics blocks,
- * F = 1+2D, or 1+D+D(D+1)/2 for full covariance); sizes that need more than
- * 64 MiB are rejected with GMM_ERR_WORKSPACE (and a message on stderr)
- * before anything is queued.
+ * It always takes the CUDA-core kernels (the path gmm_em_step takes with
+ * GMM_OPT_CUDA_CORES), whatever the shape, and ignores opts->flags: its
+ * results match gmm_em_step's within the parity tolerances of this library,
+ * not bit for bit where gmm_em_step takes the tensor-core path, and it runs
+ * at the CUDA-core path's speed (on 10M x 128 points with K = 256 about 170
+ * times slower than gmm_em_step's tensor-core path).  X, params,
+ * loglik_dev, lse_dev (N floats, required here) and flags_dev (optional) are
+ * the caller's device buffers.  All other scratch lives in one 64 MiB array
+ * built into the library's device image: every GPU that loads the library
+ * holds it until the process exits, and nothing is allocated by this call.
+ * The scratch needed is about N/16 + 8*P*K*F + 4*K*(D+2) + prepared-parameter
+ * bytes (P statistics blocks, F = 1+2D, or 1+D+D(D+1)/2 for full
+ * covariance); sizes that need more than 64 MiB are rejected with
+ * GMM_ERR_WORKSPACE (and a message on stderr) before anything is queued.
  *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, once per device, with that device current); make
- * that first call before any stream capture.  Every call shares the one
- * array, so calls that overlap on the GPU (other streams, other host
- * threads) race: serialise them.  The call synchronises `stream` and
- * returns the first device-side condition of this call (GMM_ERR_NOT_PD,
- * GMM_ERR_NONFINITE) or GMM_OK.
+ * (cudaGetSymbolAddress, once per device, with that device current) and
+ * keeps it for the life of the process, so the library must not be used
+ * across a cudaDeviceReset of that device; make that first call before any
+ * stream capture.  Every call shares the one array, so calls that overlap
+ * on the GPU (other streams, other host threads) race: serialise them.  The
+ * call synchronises `stream` before it returns, and returns the first
+ * device-side condition of this call (GMM_ERR_NOT_PD, GMM_ERR_NONFINITE) or
+ * GMM_OK.
  */
 gmm_status gmm_em_step_noalloc(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
                                gmm_params* params, gmm_cov_type cov, const gmm_opts* opts,

@@ -165,3 +165,29 @@ def fit(X, pi, mu, cov, cov_type, iters, xdtype=None, opts=None):
         out.append(r)
         pi, mu, cov = r["pi"], r["mu"], r["cov"]
     return out
+
+
+def ivf_lists(ids, gamma, K, gamma_min):
+    """Inverted lists of an IVF index with soft multi-assignment, straight
+    from the definition: walking the points in order, entry t of point n
+    joins the list of component ids[n, t] when t == 0 or gamma[n, t] >=
+    gamma_min (compared in float32, the type of both), ids outside [0, K)
+    skipped (Flash-GMM summary, "Core insight": boundary vectors go to
+    several high-responsibility clusters).  Returns (offsets [K+1] int64,
+    point indices int32, gamma float32), each list in point order."""
+    ids = np.asarray(ids)
+    g = np.asarray(gamma, dtype=np.float32)
+    N, m = ids.shape
+    lists = [[] for _ in range(K)]
+    gmin = np.float32(gamma_min)
+    for n in range(N):
+        for t in range(m):
+            k = int(ids[n, t])
+            if 0 <= k < K and (t == 0 or g[n, t] >= gmin):
+                lists[k].append((n, g[n, t]))
+    offsets = np.zeros(K + 1, dtype=np.int64)
+    for k in range(K):
+        offsets[k + 1] = offsets[k] + len(lists[k])
+    pts = np.array([n for L in lists for (n, _) in L], dtype=np.int32)
+    gam = np.array([v for L in lists for (_, v) in L], dtype=np.float32)
+    return offsets, pts, gam

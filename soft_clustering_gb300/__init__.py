@@ -26,7 +26,8 @@ EXPORTS = (
     "gmm_default_opts", "gmm_status_string", "gmm_workspace_bytes", "gmm_prepared_bytes",
     "gmm_prepare", "gmm_em_step", "gmm_workspace_bytes_host", "gmm_em_step_host",
     "gmm_assign_topm", "gmm_last_device_status", "gmm_profile_enable", "gmm_profile_read",
-    "gmm_profile_reset", "gmm_em_step_noalloc", "gmm_debug_tc_gemm",
+    "gmm_profile_reset", "gmm_em_step_noalloc", "gmm_debug_tc_gemm", "gmm_ivf_lists_ws_bytes",
+    "gmm_ivf_lists",
 )
 
 
@@ -78,6 +79,9 @@ def lib():
                                           P(gmm_opts), vp, vp, vp, vp]
         L.gmm_debug_tc_gemm.argtypes = [vp, vp, vp, i32, i32, vp, vp]
         L.gmm_debug_tc_gemm.restype = i32
+        L.gmm_ivf_lists_ws_bytes.argtypes = [i64, i32, i32]
+        L.gmm_ivf_lists_ws_bytes.restype = sz
+        L.gmm_ivf_lists.argtypes = [vp, vp, i64, i32, i32, ctypes.c_float, vp, vp, vp, vp, sz, vp]
         L.gmm_profile_enable.argtypes = [i32]
         L.gmm_profile_enable.restype = None
         L.gmm_profile_read.argtypes = [P(ctypes.c_char_p), P(ctypes.c_double), P(ctypes.c_long),
@@ -85,7 +89,7 @@ def lib():
         L.gmm_profile_read.restype = i32
         L.gmm_profile_reset.restype = None
         for f in ("gmm_prepare", "gmm_em_step", "gmm_em_step_host", "gmm_assign_topm",
-                  "gmm_last_device_status", "gmm_em_step_noalloc"):
+                  "gmm_last_device_status", "gmm_em_step_noalloc", "gmm_ivf_lists"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -194,6 +198,17 @@ def gmm_em_step_noalloc(X, xdtype, N, D, K, pi, mu, cov, cov_type, loglik, lse, 
                                    ctypes.byref(o), _ptr(loglik), _ptr(lse), _ptr(flags),
                                    _stream(stream))
     return _check(st, "gmm_em_step_noalloc", raise_on_error)
+
+
+def gmm_ivf_lists_ws_bytes(N, m, K) -> int:
+    return int(lib().gmm_ivf_lists_ws_bytes(N, m, K))
+
+
+def gmm_ivf_lists(ids, gamma, N, m, K, gamma_min, offsets, list_pts, list_gamma, ws, ws_bytes,
+                  stream=None, raise_on_error=True):
+    st = lib().gmm_ivf_lists(_ptr(ids), _ptr(gamma), N, m, K, float(gamma_min), _ptr(offsets),
+                             _ptr(list_pts), _ptr(list_gamma), _ptr(ws), ws_bytes, _stream(stream))
+    return _check(st, "gmm_ivf_lists", raise_on_error)
 
 
 def gmm_last_device_status(ws, stream=None) -> int:

@@ -50,11 +50,9 @@ cudaError_t launch_ll_finalize(const double* ll_part, int64_t n, double* out, in
 
 namespace {
 
-constexpr int kLseRows = 128;      // rows per block of the LSE kernel
 constexpr int kTargetCtas = 608;   // 4 x 152 SMs: statistics blocks per launch
 constexpr int kListGrid = 304;     // blocks of the CUDA-core pass over handed-over rows
 constexpr int kMaxScreenGrid = 1024;  // upper bound of tc_screen_grid (SM count)
-constexpr int kMaxK = 1 << 16;
 // Tensor-core path: rows per slab (one screening launch; its records are
 // consumed before the next slab) and responsibility records per 128-point
 // tile (8 per point on average; rows past it go through the row list).

@@ -11,6 +11,11 @@
 namespace gmm {
 
 constexpr size_t kAlign = 256;
+// Rows per block of the CUDA-core log-sum-exp kernel (one log-likelihood
+// partial each) and the largest component count the entry points accept;
+// every translation unit that sizes scratch for those kernels uses these.
+constexpr int kLseRows = 128;
+constexpr int kMaxK = 1 << 16;
 __host__ __device__ inline size_t align_up(size_t v, size_t a = kAlign) {
   return (v + a - 1) / a * a;
 }

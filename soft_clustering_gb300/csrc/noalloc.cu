@@ -69,7 +69,7 @@ ScratchLayout scratch_layout(int64_t N, int D, int K, int cov) {
   size_t o = 0;
   L.off_status = o; o = align_up(o + sizeof(DeviceStatus));
   L.off_prep = o;   o = align_up(o + PreparedLayout::make(D, K, cov).bytes);
-  L.off_llpart = o; o = align_up(o + sizeof(double) * (size_t)((N + 127) / 128));
+  L.off_llpart = o; o = align_up(o + sizeof(double) * (size_t)((N + kLseRows - 1) / kLseRows));
   L.off_ll = o;     o = align_up(o + sizeof(double));
   L.parts = stat_parts_for(N, D, K, cov);
   L.off_part = o;   o = align_up(o + sizeof(double) * (size_t)L.parts * K * stat_width(D, cov));
@@ -93,7 +93,7 @@ extern "C" gmm_status gmm_em_step_noalloc(const void* X, gmm_dtype xdtype, int64
                                           int K, gmm_params* params, gmm_cov_type cov,
                                           const gmm_opts* opts, double* loglik_dev,
                                           float* lse_dev, int32_t* flags_dev, void* stream) {
-  if (!X || N < 1 || K < 1 || K > (1 << 16) || xdtype < GMM_F32 || xdtype > GMM_BF16 ||
+  if (!X || N < 1 || K < 1 || K > kMaxK || xdtype < GMM_F32 || xdtype > GMM_BF16 ||
       cov < GMM_COV_FULL || cov > GMM_COV_ISO)
     return GMM_ERR_INVALID_ARG;
   if (!(D == 16 || D == 32 || D == 64 || D == 128)) return D > 0 ? GMM_ERR_UNSUPPORTED : GMM_ERR_INVALID_ARG;
@@ -126,7 +126,7 @@ extern "C" gmm_status gmm_em_step_noalloc(const void* X, gmm_dtype xdtype, int64
   if ((r = cuda_fail(simt_lse(X, xdtype, N, D, K, cov, prep, lse_dev, llp, 0, nullptr, nullptr,
                               st, s))) != GMM_OK)
     return r;
-  if ((r = cuda_fail(launch_ll_finalize(llp, (N + 127) / 128, ll, 0, s))) != GMM_OK) return r;
+  if ((r = cuda_fail(launch_ll_finalize(llp, (N + kLseRows - 1) / kLseRows, ll, 0, s))) != GMM_OK) return r;
   if ((r = cuda_fail(simt_stats(X, xdtype, N, D, K, cov, prep, lse_dev, L.parts, part, 0, s))) !=
       GMM_OK)
     return r;

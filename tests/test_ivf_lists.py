@@ -1,0 +1,149 @@
+"""Inverted lists for IVF multi-assignment (gmm_ivf_lists).
+
+CPU: the list builder the GPU kernel is checked against, pinned to a
+hand-derived example.  GPU: the kernel against that builder, bit for bit
+(offsets, point order, gamma bits), on inputs from the oracle's top-m and on
+random top-m tables that cover ragged sizes, skipped ids, thresholds that
+keep everything or only the best component, and K past the shared-memory
+cursor limit; then end to end from gmm_assign_topm.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "ivf_lists_small.json")
+
+
+def test_builder_golden():
+    g = json.load(open(GOLDEN))
+    ids = np.array(g["ids"], dtype=np.int32)
+    gam = np.array(g["gamma"], dtype=np.float32)
+    for c in g["cases"]:
+        off, pts, lg = oracle.ivf_lists(ids, gam, g["K"], c["gamma_min"])
+        assert off.tolist() == c["offsets"]
+        assert pts.tolist() == c["pts"]
+        assert np.array_equal(lg, np.array(c["gamma"], dtype=np.float32))
+
+
+def test_builder_invariants():
+    """Every list ascending; each point's best component holds it; entry
+    count equals the rank-0 entries plus the ranks >= 1 at or above the
+    threshold."""
+    rng = np.random.default_rng(3)
+    N, m, K = 500, 3, 17
+    ids = np.stack([rng.permutation(K)[:m] for _ in range(N)]).astype(np.int32)
+    gam = rng.dirichlet(np.ones(m), N).astype(np.float32)
+    off, pts, lg = oracle.ivf_lists(ids, gam, K, 0.2)
+    for k in range(K):
+        seg = pts[off[k]:off[k + 1]]
+        assert (np.diff(seg) > 0).all()
+    for n in range(N):
+        k = ids[n, 0]
+        assert n in set(pts[off[k]:off[k + 1]].tolist())
+    assert off[-1] == N + int((gam[:, 1:] >= np.float32(0.2)).sum())
+
+
+def _gpu_lists(ids, gam, K, gmin):
+    import torch
+    import soft_clustering_gb300 as G
+    N, m = ids.shape
+    dev = torch.device("cuda")
+    ids_d = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).to(dev)
+    gam_d = torch.from_numpy(np.ascontiguousarray(gam, dtype=np.float32)).to(dev)
+    off = torch.empty(K + 1, dtype=torch.int64, device=dev)
+    pts = torch.full((N * m,), -7, dtype=torch.int32, device=dev)
+    lg = torch.empty(N * m, dtype=torch.float32, device=dev)
+    wsb = G.gmm_ivf_lists_ws_bytes(N, m, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    G.gmm_ivf_lists(ids_d, gam_d, N, m, K, gmin, off, pts, lg, ws, wsb)
+    torch.cuda.synchronize()
+    o = off.cpu().numpy()
+    tot = int(o[-1])
+    return o, pts.cpu().numpy()[:tot], lg.cpu().numpy()[:tot]
+
+
+def _same(got, ref, what):
+    o, p, g = got
+    ro, rp, rg = ref
+    assert np.array_equal(o, ro), (what, "offsets")
+    assert np.array_equal(p, rp), (what, "points")
+    assert np.array_equal(g.view(np.uint32), rg.view(np.uint32)), (what, "gamma bits")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N,m,K,gmin", [(1, 1, 1, 0.0), (7, 2, 3, 0.5), (8192, 4, 64, 0.05),
+                                        (8192 * 3 + 17, 4, 4096, 0.01), (20001, 3, 20000, 0.1),
+                                        (5000, 8, 300, 2.0), (3000, 4, 50, -1.0)])
+def test_kernel_matches_builder_random(N, m, K, gmin):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from soft_clustering_gb300 import build
+    build.build()
+    rng = np.random.default_rng(N + 31 * m + K)
+    m_eff = min(m, K)
+    ids = np.full((N, m), -1, dtype=np.int32)
+    for n in range(N):
+        ids[n, :m_eff] = rng.choice(K, m_eff, replace=False)
+    gam = np.sort(rng.dirichlet(np.ones(m), N).astype(np.float32), axis=1)[:, ::-1].copy()
+    # some skipped ids and some gammas exactly at the threshold
+    ids[rng.random((N, m)) < 0.02] = -1
+    gam[rng.random((N, m)) < 0.02] = np.float32(gmin)
+    _same(_gpu_lists(ids, gam, K, gmin), oracle.ivf_lists(ids, gam, K, gmin),
+          "N=%d m=%d K=%d" % (N, m, K))
+
+
+@pytest.mark.gpu
+def test_kernel_from_oracle_topm_and_end_to_end():
+    """Lists from the oracle's top-4 (fp32) match the builder bit for bit;
+    lists from the library's own assignment match the builder applied to the
+    library's ids and gamma, and their memberships agree with the oracle's
+    except where a gamma lies within 2e-4 of the threshold or ranks tie."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from soft_clustering_gb300 import build
+    from soft_clustering_gb300.torch_api import Assigner
+    build.build()
+    wl = datagen.WORKLOADS["ivf_assign"].with_n(12_000 + 7)
+    mix = datagen.planted(wl)
+    bits = datagen.points(mix, 0, wl.N)
+    pi, mu, var = datagen.planted_params_f16(mix)
+    st, ids_ref, gam_ref, _ = oracle.topm(bits, pi, mu, var, wl.cov_type, wl.m, xdtype=wl.dtype)
+    assert st == 0
+    gmin = 0.05
+    gam32 = gam_ref.astype(np.float32)
+    ref = oracle.ivf_lists(ids_ref, gam32, wl.K, gmin)
+    _same(_gpu_lists(ids_ref, gam32, wl.K, gmin), ref, "oracle top-m")
+    from gpu_util import to_device
+    a = Assigner(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, wl.m)
+    a.prepare(pi, mu, var)
+    a.assign(to_device(bits, wl.dtype))
+    assert a.device_status() == 0
+    off, pts, lg = (t.cpu().numpy() for t in a.inverted_lists(gmin))
+    ids_g = a.ids.cpu().numpy()
+    gam_g = a.gamma.cpu().numpy()
+    own = oracle.ivf_lists(ids_g, gam_g, wl.K, gmin)
+    _same((off, pts[:off[-1]], lg[:off[-1]]), own, "library top-m")
+    # membership sets against the oracle's, away from the threshold and ties
+    def members(ids, gam):
+        s = set()
+        for n in range(ids.shape[0]):
+            for t in range(ids.shape[1]):
+                if ids[n, t] >= 0 and (t == 0 or gam[n, t] >= gmin):
+                    s.add((n, int(ids[n, t])))
+        return s
+    near = np.abs(gam_ref - gmin) < 2e-4
+    tied = np.zeros_like(near)
+    tied[:, :-1] |= (gam_ref[:, :-1] - gam_ref[:, 1:]) < 1e-6
+    tied[:, 1:] |= (gam_ref[:, :-1] - gam_ref[:, 1:]) < 1e-6
+    skip = set(np.nonzero((near | tied).any(axis=1))[0].tolist())
+    a_ = {p for p in members(ids_g, gam_g) if p[0] not in skip}
+    b_ = {p for p in members(ids_ref, gam_ref) if p[0] not in skip}
+    assert a_ == b_, (len(a_ ^ b_), sorted(a_ ^ b_)[:5])
+    assert len(skip) < wl.N // 20

@@ -3,10 +3,11 @@ memory (a plugin given only its input and output buffers, code running
 inside another framework's memory budget).  Its scratch is a fixed array
 inside the library, so the call needs no workspace.
 
-Checked through the C ABI against gmm_em_step on the same inputs, on two
-calls in a row (two EM iterations, so the second call finds the shared
-scratch holding the first call's contents), within the parity tolerances
-the other GPU tests use.  This file is collected last on purpose.
+Checked through the C ABI on two calls in a row (two EM iterations, so the
+second call finds the shared scratch holding the first call's contents):
+against gmm_em_step on the same inputs, and each call against the fp64
+oracle's step from that call's own input parameters, within the parity
+tolerances the other GPU tests use.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -15,7 +16,7 @@ import torch
 import datagen
 import parity
 import soft_clustering_gb300 as G
-from gpu_util import f32, make_state, set_opts, to_device
+from gpu_util import f32, make_state, oracle_step, set_opts, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +64,11 @@ def test_noalloc_matches_workspace_entry_point(name, n):
         st, got = _noalloc_step(wl, Xd, params, opts)
         assert st == G.GMM_OK, G.status_string(st)
         fails = parity.compare_step(got, ref, "%s noalloc call %d" % (name, call))
+        assert not fails, fails
+        orc = oracle_step(bits, wl.dtype, params, wl.cov_type, opts=opts)
+        assert orc["status"] == 0
+        fails = parity.compare_step(got, orc, "%s noalloc call %d vs oracle" % (name, call),
+                                    opts["min_s0"])
         assert not fails, fails
         np.testing.assert_allclose(got["lse"], lse_ref.cpu().numpy(), rtol=1e-6)
         assert (got["flags"] == ref_state.flags.cpu().numpy()).all()
