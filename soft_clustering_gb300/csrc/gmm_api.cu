@@ -21,8 +21,8 @@ cudaError_t simt_lse_rows(const void* X, int xdtype, int64_t N, int D, int K, in
                           float* gamma, DeviceStatus* st, const uint32_t* rows,
                           const uint32_t* row_count, int grid, cudaStream_t s);
 cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
-                      const void* prepared, int mode, float* lse, double* ll_part, int m,
-                      int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
+                      const void* prepared, int mode, float* lse, int want_lse, double* ll_part,
+                      int m, int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
                       uint32_t* tile_cnt, int rec_cap, DeviceStatus* st, cudaStream_t s);
 int tc_screen_grid(int64_t N);
 cudaError_t fb_compact(const uint32_t* fb_mask, int64_t N, uint32_t* rows, uint32_t* count,
@@ -35,12 +35,12 @@ cudaError_t simt_stats_rows(const void* X, int xdtype, int64_t N, int D, int K, 
                             const void* prepared, const float* lse, int parts, double* part,
                             int accumulate, const uint32_t* rows, const uint32_t* row_count,
                             cudaStream_t s);
-size_t sparse_stats_ws_bytes(int64_t rows, int D, int K, int rec_cap);
-bool sparse_stats_supported(int K);
-cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
-                         int cov, const uint32_t* tile_cnt, const uint2* recs, int rec_cap,
-                         void* sws, double* part, int accumulate, double* ll, DeviceStatus* st,
-                         cudaStream_t s);
+int chunk_stats_blocks(int D, int K);
+int chunk_stats_parts(int D, int K);
+cudaError_t chunk_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,
+                        const void* prepared, const float* lse, const uint2* recs,
+                        const uint32_t* tile_cnt, int rec_cap, double* part, int accumulate,
+                        double* ll_part, cudaStream_t s);
 int simt_stat_chunk(int D, int cov);
 cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
                          const float* centre, const int32_t* prep_flags, float var_floor,
@@ -53,11 +53,14 @@ namespace {
 constexpr int kTargetCtas = 608;   // 4 x 152 SMs: statistics blocks per launch
 constexpr int kListGrid = 304;     // blocks of the CUDA-core pass over handed-over rows
 constexpr int kMaxScreenGrid = 1024;  // upper bound of tc_screen_grid (SM count)
-// Tensor-core path: rows per slab (one screening launch; its records are
-// consumed before the next slab) and responsibility records per 128-point
-// tile (8 per point on average; rows past it go through the row list).
-constexpr int64_t kSlabRows = 1 << 21;
-constexpr int kRecCap = 1024;
+// Tensor-core path: records {key, exact log joint} per 128-point tile (a
+// tile past it is taken densely by the statistics) and rows per slab (one
+// screening launch; its records are consumed before the next slab), so the
+// record buffer stays at 1 GiB: 128 records a point on average for K <= 128,
+// 256 beyond (the early EM iterations keep about a hundred candidates a
+// point on the 128-dimensional workloads).
+int rec_cap_for(int K) { return K <= 128 ? 16384 : 32768; }
+int64_t slab_rows_for(int K) { return K <= 128 ? (int64_t)1 << 20 : (int64_t)1 << 19; }
 
 bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
 size_t esize(int xdtype) { return xdtype == GMM_F32 ? 4 : 2; }
@@ -76,17 +79,18 @@ int stat_parts(int64_t N, int D, int K, int cov) {
 
 struct WsLayout {
   size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_fb,
-      off_fbm, off_fbseg, off_rec, off_tcnt, off_sws, off_stage, bytes;
+      off_fbm, off_fbseg, off_rec, off_tcnt, off_stage, bytes;
   int parts;          // statistics partials of the CUDA-core path
-  int sp_parts;       // tensor-core path: the records' partial (1) ...
-  int lp_parts;       // ... followed by those of the row-list pass
+  int sp_parts;       // tensor-core path: the partitions of the statistics blocks
+  int cs_blocks;      // statistics blocks per slab (log-likelihood partials)
   int64_t lse_rows;
 };
 
 // The tensor-core E-step of an EM iteration (screening + statistics from
 // its records).
 bool use_tc(int D, int K, int cov, const gmm_opts& o) {
-  return tc_eligible(D, cov) && sparse_stats_supported(K) && !(o.flags & GMM_OPT_CUDA_CORES);
+  (void)K;
+  return tc_eligible(D, cov) && !(o.flags & GMM_OPT_CUDA_CORES);
 }
 
 // rows: rows processed per launch (N, or the chunk size of the host path);
@@ -98,34 +102,33 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_prep = o;   o = align_up(o + PreparedLayout::make(D, K, cov).bytes);
   W.lse_rows = rows;
   W.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)rows);
+  const bool tc = tc_eligible(D, cov);
+  W.cs_blocks = tc ? chunk_stats_blocks(D, K) * chunk_stats_parts(D, K) : 0;
   {
     // dense LSE blocks, or the tensor-core CTAs followed by the list blocks
+    // and the statistics blocks
     const size_t dense = (size_t)((rows + kLseRows - 1) / kLseRows);
-    const size_t tcl = (size_t)(kMaxScreenGrid + kListGrid);
+    const size_t tcl = (size_t)(kMaxScreenGrid + kListGrid) + (size_t)W.cs_blocks;
     W.off_llpart = o; o = align_up(o + sizeof(double) * (dense > tcl ? dense : tcl));
   }
   W.off_ll = o;     o = align_up(o + sizeof(double));
   W.parts = stat_parts(rows, D, K, cov);
-  W.sp_parts = W.lp_parts = 0;
+  W.sp_parts = 0;
   int slots = W.parts;
-  const bool tc = tc_eligible(D, cov);
   if (tc) {
-    W.sp_parts = 1;
-    const int kc = simt_stat_chunk(D, cov);
-    const int chunks = (K + kc - 1) / kc;
-    W.lp_parts = (kListGrid + chunks - 1) / chunks;
-    if (W.sp_parts + W.lp_parts > slots) slots = W.sp_parts + W.lp_parts;
+    W.sp_parts = chunk_stats_parts(D, K);
+    if (W.sp_parts > slots) slots = W.sp_parts;
   }
   W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)slots * K * stat_width(D, cov));
   W.off_flags = o;  o = align_up(o + sizeof(int32_t) * K);
-  const int64_t slab = rows < kSlabRows ? rows : kSlabRows;
+  const int64_t slab_max = slab_rows_for(K);
+  const int64_t slab = rows < slab_max ? rows : slab_max;
   W.off_fb = o;     o = align_up(o + sizeof(uint32_t) * (size_t)(tc ? slab : rows));
   const size_t slab_tiles = tc ? (size_t)((slab + 127) / 128) : 0;
   W.off_fbm = o;    o = align_up(o + sizeof(uint32_t) * 4 * slab_tiles);
   W.off_fbseg = o;  o = align_up(o + sizeof(uint32_t) * (tc ? fb_compact_segments(slab) : 0));
-  W.off_rec = o;    o = align_up(o + sizeof(uint2) * slab_tiles * kRecCap);
+  W.off_rec = o;    o = align_up(o + sizeof(uint2) * slab_tiles * (size_t)rec_cap_for(K));
   W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * slab_tiles);
-  W.off_sws = o;    o = align_up(o + (tc ? sparse_stats_ws_bytes(slab, D, K, kRecCap) : 0));
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
@@ -191,49 +194,34 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
   const void* prep = at<char>(ws, W.off_prep);
   double* llp = at<double>(ws, W.off_llpart);
   if (tc) {
-    // Slabs of kSlabRows rows.  Per slab: screen on the tensor cores (exact
-    // LSE and responsibility records of most rows), the CUDA-core pass over
-    // the rows handed over, the log-likelihood, statistics from the records
-    // and the CUDA-core statistics of the handed-over rows.
-    uint32_t* fb = at<uint32_t>(ws, W.off_fb);
+    // Slabs of rows.  Per slab: screen on the tensor cores (exact LSE_n of
+    // every point and records of its candidates), statistics from the
+    // records, the log-likelihood.
     uint32_t* fbm = at<uint32_t>(ws, W.off_fbm);
     uint2* recs = at<uint2>(ws, W.off_rec);
     uint32_t* tcnt = at<uint32_t>(ws, W.off_tcnt);
     double* part = at<double>(ws, W.off_part);
-    double* lpart = part + (size_t)W.sp_parts * K * stat_width(D, cov);
-    for (int64_t r0 = 0; r0 < rows; r0 += kSlabRows) {
-      const int64_t sn = (rows - r0) < kSlabRows ? (rows - r0) : kSlabRows;
+    const int64_t slab_rows = slab_rows_for(K);
+    const int rec_cap = rec_cap_for(K);
+    for (int64_t r0 = 0; r0 < rows; r0 += slab_rows) {
+      const int64_t sn = (rows - r0) < slab_rows ? (rows - r0) : slab_rows;
       const void* Xs = (const char*)X + (size_t)r0 * D * esize(xdtype);
       float* ls = lse + r0;
       const int acc = accumulate || r0 > 0;
       const int g1 = tc_screen_grid(sn);
       {
         GMM_PROF("tc_screen_kernel");
-        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, want_lse ? ls : nullptr, llp, 0,
-                          nullptr, nullptr, fbm,
-                          recs, tcnt, kRecCap, st, s));
+        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, ls, want_lse ? 1 : 0, llp, 0,
+                          nullptr, nullptr, fbm, recs, tcnt, rec_cap, st, s));
       }
       {
-        GMM_PROFN("fb_compact_kernel", 2);
-        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
-      }
-      {
-        GMM_PROF("lse_rows_kernel");
-        GMM_TRY(simt_lse_rows(Xs, xdtype, sn, D, K, cov, prep, ls, llp + g1, 0, nullptr,
-                              nullptr, st, fb, &st->fb_count, kListGrid, s));
+        GMM_PROF("chunk_stats_kernel");
+        GMM_TRY(chunk_stats(Xs, xdtype, sn, D, K, cov, prep, ls, recs, tcnt, rec_cap, part, acc,
+                            llp + g1, s));
       }
       {
         GMM_PROF("ll_finalize_kernel");
-        GMM_TRY(launch_ll_finalize(llp, g1 + kListGrid, at<double>(ws, W.off_ll), acc, s));
-      }
-      {
-        GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, tcnt, recs, kRecCap,
-                             at<char>(ws, W.off_sws), part, acc, at<double>(ws, W.off_ll), st, s));
-      }
-      {
-        GMM_PROF("stats_rows_kernel");
-        GMM_TRY(simt_stats_rows(Xs, xdtype, sn, D, K, cov, prep, ls, W.lp_parts, lpart, acc, fb,
-                                &st->fb_count, s));
+        GMM_TRY(launch_ll_finalize(llp, g1 + W.cs_blocks, at<double>(ws, W.off_ll), acc, s));
       }
     }
     return GMM_OK;
@@ -256,7 +244,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
 }
 
 // Partials the M-step merges for the path taken.
-int mstep_parts(const WsLayout& W, bool tc) { return tc ? W.sp_parts + W.lp_parts : W.parts; }
+int mstep_parts(const WsLayout& W, bool tc) { return tc ? W.sp_parts : W.parts; }
 
 // Library-owned copy stream and events of the host path (one set per device).
 struct HostPathRes {
@@ -486,18 +474,19 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
   DeviceStatus* st = static_cast<DeviceStatus*>(ws);
   GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
   if (tc) {
-    // slabs of kSlabRows rows: screening, then the row list of the slab
+    // slabs of rows: screening, then the row list of the slab
     uint32_t* fb = at<uint32_t>(ws, W.off_fb);
     uint32_t* fbm = at<uint32_t>(ws, W.off_fbm);
-    for (int64_t r0 = 0; r0 < N; r0 += kSlabRows) {
-      const int64_t sn = (N - r0) < kSlabRows ? (N - r0) : kSlabRows;
+    const int64_t slab_rows = slab_rows_for(K);
+    for (int64_t r0 = 0; r0 < N; r0 += slab_rows) {
+      const int64_t sn = (N - r0) < slab_rows ? (N - r0) : slab_rows;
       const void* Xs = (const char*)X + (size_t)r0 * D * esize(xdtype);
       float* ls = lse ? lse + r0 : nullptr;
       int32_t* is = ids + (size_t)r0 * m;
       float* gs = gamma + (size_t)r0 * m;
       {
         GMM_PROF("tc_screen_kernel");
-        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prepared, 1, ls, nullptr, m, is, gs, fbm,
+        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prepared, 1, ls, 0, nullptr, m, is, gs, fbm,
                           nullptr, nullptr, 0, st, s));
       }
       {

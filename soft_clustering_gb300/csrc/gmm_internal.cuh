@@ -89,9 +89,9 @@ constexpr int kTcExtraBytes = kTcChunk * kTcExtraK * 2;  // one chunk's extra B 
 enum { kFoldS = 2 * kTcChunk, kFoldInvS, kFoldUMax, kFoldDMax };
 __host__ __device__ inline bool tc_fold(int chunks) { return chunks <= kTcFoldChunks; }
 
-// Responsibility records of the tensor-core E-step: uint2 {key, gamma bits},
-// key = flag | (component << 7) | row in the 128-point tile.  The flag marks
-// a point's only candidate (gamma 1, its exact log joint not evaluated).
+// Records of the tensor-core E-step: uint2 {key, bits of the exact fp32 log
+// joint}, key = flag | (component << 7) | row in the 128-point tile.  The
+// flag marks a point's only candidate (gamma 1, its log joint not evaluated).
 constexpr uint32_t kRecSingle = 1u << 31;
 constexpr uint32_t kRecKMask = 0xffffffu;  // component = (key >> 7) & kRecKMask
 

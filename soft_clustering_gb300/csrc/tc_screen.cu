@@ -40,6 +40,7 @@
 //   warp  12    lane 0 issues bulk copies of the parameter chunks and their
 //               trailers and the tcgen05.mma instructions; the warp owns the
 //               TMEM allocation
+#include <float.h>
 #include <math.h>
 
 #include "gmm_internal.cuh"
@@ -74,14 +75,16 @@ struct ScreenArgs {
   int m;                 // top-m (assign mode)
   const void* prepared;
   PreparedLayout L;
-  float* lse;            // [N] or null (null: single-candidate points skip the refine)
+  float* lse;            // [N] or null (assign mode: null skips the output)
+  int want_lse;          // EM: LSE_n of every point is wanted (else a point with a single
+                         // candidate keeps gamma 1 without its exact log joint)
   double* ll_part;       // [gridDim.x] (EM) or null
   int32_t* ids;          // [N*m] (assign)
   float* gamma;          // [N*m] (assign)
-  uint32_t* fb_mask;     // [tiles * 4] bit r % 32 of word n / 32: row n handed to
-                         // the CUDA-core path
-  uint2* recs;           // EM: [tiles][rec_cap] responsibility records
-  uint32_t* tile_cnt;    // EM: [tiles] records written per tile
+  uint32_t* fb_mask;     // assign: [tiles * 4] bit r % 32 of word n / 32: row n
+                         // handed to the CUDA-core path
+  uint2* recs;           // EM: [tiles][rec_cap] records {key, exact log joint}
+  uint32_t* tile_cnt;    // EM: [tiles] records of the tile (> rec_cap: they did not fit)
   int rec_cap;
   DeviceStatus* st;
 };
@@ -301,6 +304,85 @@ __device__ __forceinline__ float pick8(const float* lbm, int i) {
   return v;
 }
 
+// Exact log joints of the warp's candidate lists (same arithmetic as the
+// CUDA-core kernels): the warp's (row, candidate) pairs are numbered by an
+// exclusive scan of the per-lane counts and taken eight at a time, four lanes
+// per pair; cub[e][row] receives l of candidate e.
+template <int D, int XT>
+__device__ __forceinline__ void refine_lists(const void* X, int64_t tile, int q, int lane,
+                                             int mycnt, float* cub, const uint16_t* ck,
+                                             const float* g_mu, const float* g_prec,
+                                             const float* g_c, bool iso) {
+  __syncwarp();  // every lane's list entries are written
+  int incl = mycnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - mycnt;
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  const int grp = lane >> 2, gq = lane & 3;
+  for (int p0 = 0; p0 < total; p0 += 8) {
+    const int pidx = p0 + grp;
+    const bool live = pidx < total;
+    // owner lane of pair pidx: the last lane whose excl <= pidx
+    int owner = 0;
+#pragma unroll
+    for (int st = 16; st > 0; st >>= 1) {
+      const int cand = owner + st;
+      const int ev = __shfl_sync(0xffffffffu, excl, cand & 31);
+      if (cand < 32 && ev <= pidx) owner = cand;
+    }
+    const int e = pidx - __shfl_sync(0xffffffffu, excl, owner);
+    const int rr = q * 32 + owner;
+    const int k = live ? (int)ck[e * kBM + rr] : 0;
+    // (idle groups evaluate row 0 of the tile, which always exists)
+    const float d2 = group_d2<D, XT>(X, tile * kBM + (live ? rr : 0), g_mu + (size_t)k * D,
+                                     iso ? g_prec + k : g_prec + (size_t)k * D, iso, gq);
+    if (live && gq == 0) cub[e * kBM + rr] = __ldg(g_c + k) - 0.5f * d2;
+  }
+  __syncwarp();
+}
+
+// Folds this row's cnt exact values into its running log-sum-exp (mx, sum).
+__device__ __forceinline__ void fold_lse(const float* cub, int r, int cnt, float* mx, float* sum) {
+  float lmx = -INFINITY;
+  for (int e = 0; e < cnt; ++e) lmx = fmaxf(lmx, cub[e * kBM + r]);
+  if (lmx == -INFINITY) return;
+  const float nm = fmaxf(*mx, lmx);
+  float s = *mx == -INFINITY ? 0.f : *sum * expf(*mx - nm);
+  for (int e = 0; e < cnt; ++e) s += expf(cub[e * kBM + r] - nm);
+  *mx = nm;
+  *sum = s;
+}
+
+// Writes this row's cnt records {(k << 7) | row, l} to the tile's buffer at
+// positions taken from the tile's shared-memory cursor (one atomic per warp;
+// the order inside the buffer does not matter).  Positions past rec_cap are
+// not written; the tile's count then tells the statistics to take it densely.
+__device__ __forceinline__ void emit_records(int lane, int r, int cnt, const float* cub,
+                                             const uint16_t* ck, uint32_t* cursor, uint2* out,
+                                             int rec_cap, bool single) {
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  uint32_t base = 0;
+  if (lane == 0 && total > 0) base = atomicAdd(cursor, (uint32_t)total);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  const uint32_t p0 = base + (uint32_t)(incl - cnt);
+  for (int e = 0; e < cnt; ++e) {
+    if (p0 + e < (uint32_t)rec_cap) {
+      const uint32_t key = (single ? kRecSingle : 0u) | ((uint32_t)ck[e * kBM + r] << 7) | (uint32_t)r;
+      out[p0 + e] = make_uint2(key, single ? 0u : __float_as_uint(cub[e * kBM + r]));
+    }
+  }
+}
+
 template <int D, int XT, int MODE, bool GRP>
 __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs a) {
   using S = Shape<D, GRP>;
@@ -321,6 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   uint64_t* bar = (uint64_t*)(sm + S::OFF_BAR);
   uint32_t* tmem_slot = (uint32_t*)(sm + S::OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + S::OFF_MISC + 4);
+  // EM: record cursors, one per tile in flight, used round robin over three
+  // (grouped: three per group)
+  uint32_t* cursors = (uint32_t*)(sm + S::OFF_MISC + 16);
   __shared__ double ll_red[kEpiWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -333,13 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   // group's tiles keeps buffer 2g + j, contracted once and swept by both
   // passes; streamed, each pass contracts again and the contractions
   // alternate over two buffers
-  const int ncontr = GRP ? nch : 2 * nch;  // contractions per tile
+  // streamed parameters, EM: one contraction per chunk, swept once against a
+  // running window; assignment: contracted twice (bounds, then candidates)
+  const int ncontr = (GRP || MODE == MODE_EM) ? nch : 2 * nch;  // contractions per tile
   auto tbuf = [&](int it, int gi, int* buf, uint32_t* use) {
     if constexpr (GRP) {
       *buf = 2 * (it & 1) + gi % nch;   // one contraction per chunk, swept twice
       *use = (uint32_t)(it >> 1);
     } else {
-      const int64_t gq = (int64_t)it * 2 * nch + gi;
+      const int64_t gq = (int64_t)it * ncontr + gi;
       *buf = (int)(gq & 1);
       *use = (uint32_t)(gq >> 1);
     }
@@ -374,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       tc::mbar_init(&bar[EX_C], kEpiWarps);
     }
     *abort_flag = 0;
+    for (int i = 0; i < 6; ++i) cursors[i] = 0u;
     tc::mbar_fence_init();
   }
   tc::tc_fence_before();
@@ -610,6 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       int cnt = 0;
       bool ok = true;
       float thr = -INFINITY;  // the point's window, fixed after pass 0
+      // EM: running log-sum-exp of the candidates refined so far, records
+      // written by flushes of a full list, and the tile's record cursor
+      float mx = -INFINITY, ssum = 0.f;
+      int nrec = 0;
+      bool flushed = false;
+      uint32_t* cur = cursors + g * 3 + s % 3;
       // pass 0: lower bounds only; pass 1 (a second sweep of the same
       // accumulators): candidates against the point's final window
       for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -683,14 +777,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
 #pragma unroll
               for (int i = 0; i < 32; ++i) pm |= __uint_as_float(u[i]) >= tthr ? (1u << i) : 0u;
               if (!valid) pm = 0u;
-              while (pm) {
-                const int kk = c0 + __ffs(pm) - 1;
-                pm &= pm - 1u;
-                if (cnt < kCSG) {
-                  ck[cnt * kBM + r] = (uint16_t)(j * kBN + kk);
-                  ++cnt;
-                } else {
-                  dropped = INFINITY;  // list full: the row goes to the CUDA-core path
+              if constexpr (MODE == MODE_EM) {
+                if (!isfinite(rn)) pm = 0u;  // handed over (non-finite input)
+                // append; when a list is full the warp refines its lists,
+                // folds them into the running log-sum-exp and writes their
+                // records (a flush), then goes on appending
+                for (;;) {
+                  while (pm && cnt < kCSG) {
+                    const int kk = c0 + __ffs(pm) - 1;
+                    pm &= pm - 1u;
+                    ck[cnt * kBM + r] = (uint16_t)(j * kBN + kk);
+                    ++cnt;
+                  }
+                  if (!__any_sync(0xffffffffu, pm != 0u)) break;
+                  refine_lists<D, XT>(a.X, tile, q, lane, cnt, cub, ck, g_mu, g_prec, g_c, iso);
+                  fold_lse(cub, r, cnt, &mx, &ssum);
+                  emit_records(lane, r, cnt, cub, ck, cur, a.recs + (size_t)tile * a.rec_cap,
+                               a.rec_cap, false);
+                  nrec += cnt;
+                  flushed = flushed || cnt > 0;
+                  cnt = 0;
+                  __syncwarp();
+                }
+              } else {
+                while (pm) {
+                  const int kk = c0 + __ffs(pm) - 1;
+                  pm &= pm - 1u;
+                  if (cnt < kCSG) {
+                    ck[cnt * kBM + r] = (uint16_t)(j * kBN + kk);
+                    ++cnt;
+                  } else {
+                    dropped = INFINITY;  // list full: the row goes to the CUDA-core path
+                  }
                 }
               }
             }
@@ -704,48 +822,58 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       }
       __syncwarp();
       if (!ok) break;
+      if constexpr (MODE == MODE_EM) {
+        // the rows' record counts (flushed + remaining; bit 15: a list was
+        // flushed) -> the tile's record total, the same on every run
+        uint16_t* xg = xcg + (g * 2 + (s & 1)) * kBM;
+        xg[r] = (uint16_t)((nrec + cnt) | (flushed ? 0x8000 : 0));
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[EXG + g]);
+        if (!warp_wait(&bar[EXG + g], s & 1)) { fail(); break; }
+        // the cursor of the group's tile s + 2 was last used by tile s - 1,
+        // which every warp of the group has finished
+        if (q == 0 && lane == 0) cursors[g * 3 + (s + 2) % 3] = 0u;
+        int rem = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) rem += xg[lane * 4 + t] & 0x7fff;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) rem += __shfl_xor_sync(0xffffffffu, rem, o);
+        const uint32_t total = (uint32_t)rem;
+        const bool overflow = total > (uint32_t)a.rec_cap;
+        const bool exact = valid && isfinite(rn) && (cnt > 0 || flushed);
+        // a point with a single candidate has gamma = 1 (every other
+        // component lies more than 40 nats below it); unless LSE_n is wanted
+        // (or the tile's records do not fit) its exact log joint is not
+        // needed here: the statistics give its log-likelihood term
+        const bool single = exact && !flushed && cnt == 1 && !a.want_lse && !overflow;
+        refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu,
+                            g_prec, g_c, iso);
+        if (exact && !single) fold_lse(cub, r, cnt, &mx, &ssum);
+        emit_records(lane, r, exact ? cnt : 0, cub, ck, cur, a.recs + (size_t)tile * a.rec_cap,
+                     a.rec_cap, single);
+        if (exact && !single) {
+          const float lse = mx + logf(ssum);
+          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+          a.lse[n] = lse;
+          ll_acc += (double)lse;
+        } else if (valid && !exact) {
+          // non-finite input (the only way a row keeps no candidate): the
+          // step reports it, and its log-likelihood is not finite
+          raise_status(a.st, GMM_ERR_NONFINITE);
+          a.lse[n] = __int_as_float(0x7fc00000);
+          ll_acc += (double)__int_as_float(0x7fc00000);
+        }
+        if (q == 0 && lane == 0) a.tile_cnt[tile] = total;
+      } else {
       const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
       // a point with a single candidate has gamma = 1 (every other component
       // lies more than 40 nats below it); unless LSE_n is wanted its exact
       // log joint is not needed here (the statistics give its
       // log-likelihood term)
       const bool single = exact && cnt == 1 && a.lse == nullptr;
-      // exact log joints of the other points' candidates (same arithmetic as
-      // the CUDA-core kernels): the warp's (row, candidate) pairs are
-      // numbered by an exclusive scan of the counts and taken eight at a time
-      {
-        const int mycnt = (exact && !single) ? cnt : 0;
-        int incl = mycnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const int excl = incl - mycnt;
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        // eight pairs per round, one per group of four lanes
-        const int grp = lane >> 2, gq = lane & 3;
-        for (int p0 = 0; p0 < total; p0 += 8) {
-          const int pidx = p0 + grp;
-          const bool live = pidx < total;
-          // owner lane of pair pidx: the last lane whose excl <= pidx
-          int owner = 0;
-#pragma unroll
-          for (int st = 16; st > 0; st >>= 1) {
-            const int cand = owner + st;
-            const int ev = __shfl_sync(0xffffffffu, excl, cand & 31);
-            if (cand < 32 && ev <= pidx) owner = cand;
-          }
-          const int e = pidx - __shfl_sync(0xffffffffu, excl, owner);
-          const int rr = q * 32 + owner;
-          const int k = live ? (int)ck[e * kBM + rr] : 0;
-          // (idle groups evaluate row 0 of the tile, which always exists)
-          const float d2 = group_d2<D, XT>(a.X, tile * kBM + (live ? rr : 0), g_mu + (size_t)k * D,
-                                           iso ? g_prec + k : g_prec + (size_t)k * D, iso, gq);
-          if (live && gq == 0) cub[e * kBM + rr] = __ldg(g_c + k) - 0.5f * d2;
-        }
-        __syncwarp();
-      }
+      // exact log joints of the other points' candidates
+      refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu, g_prec,
+                          g_c, iso);
       float lse = 0.f;
       if (exact && !single) {
         float mx = -INFINITY, sum = 0.f;
@@ -753,61 +881,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
         for (int e = 0; e < cnt; ++e) sum += expf(cub[e * kBM + r] - mx);
         lse = mx + logf(sum);
       }
-      if constexpr (MODE == MODE_EM) {
-        // responsibility records of this tile, in row order: an exclusive
-        // prefix sum of the rows' counts over the 128 rows (published by the
-        // group's four warps).  Rows past the capacity go to the row list.
-        const int my = exact ? cnt : 0;
-        uint16_t* xg = xcg + (g * 2 + (s & 1)) * kBM;
-        xg[r] = (uint16_t)my;
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar[EXG + g]);
-        if (!warp_wait(&bar[EXG + g], s & 1)) { fail(); break; }
-        // every warp reads all 128 rows' counts (lane: rows 4 lane .. 4 lane + 3)
-        int rc[4], tsum = 0;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          rc[t] = xg[lane * 4 + t];
-          tsum += rc[t];
-        }
-        int incl = tsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const int all = __shfl_sync(0xffffffffu, incl, 31);
-        // exclusive offset of row r = prefix of its group of four + earlier rows in it
-        const int grp4 = r >> 2;
-        int off = __shfl_sync(0xffffffffu, incl - tsum, grp4);
-        const int r0c = __shfl_sync(0xffffffffu, rc[0], grp4);
-        const int r1c = __shfl_sync(0xffffffffu, rc[1], grp4);
-        const int r2c = __shfl_sync(0xffffffffu, rc[2], grp4);
-        const int within = r & 3;
-        off += (within > 0 ? r0c : 0) + (within > 1 ? r1c : 0) + (within > 2 ? r2c : 0);
-        const bool fits = exact && off + my <= a.rec_cap;
-        if (exact && off <= a.rec_cap && off + my > a.rec_cap) a.tile_cnt[tile] = (uint32_t)off;
-        if (r == kBM - 1 && all <= a.rec_cap) a.tile_cnt[tile] = (uint32_t)all;
-        if (fits) {
-          uint2* out = a.recs + (size_t)tile * a.rec_cap + off;
-          if (single) {
-            // flagged record: gamma 1, log-likelihood term from the statistics
-            out[0] = make_uint2(kRecSingle | ((uint32_t)ck[r] << 7) | (uint32_t)r,
-                                __float_as_uint(1.f));
-          } else {
-            if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
-            if (a.lse) a.lse[n] = lse;
-            ll_acc += (double)lse;
-            for (int e = 0; e < cnt; ++e) {
-              const uint32_t k = ck[e * kBM + r];
-              const float gm = expf(cub[e * kBM + r] - lse);
-              out[e] = make_uint2((k << 7) | (uint32_t)r, __float_as_uint(gm));
-            }
-          }
-        }
-        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !fits);
-        if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
-      } else {
         if (single) {
           a.ids[n * a.m] = ck[r];
           a.gamma[n * a.m] = 1.f;
@@ -848,8 +921,179 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       const double sacc = warp_sum(ll_acc);
       if (lane == 0) ll_red[warp] = sacc;
     }
+    } else if constexpr (MODE == MODE_EM) {
+    // --------------------------- epilogue (streamed parameters, EM mode)
+    // warp w reads lane quarter q = w % 4 and column half h = w / 4 of every
+    // chunk.  Each chunk is contracted once and swept once: per block of 32
+    // columns the largest lower bound joins a running best (ref, this half's),
+    // then every column whose upper bound reaches ref - 40 is a candidate.
+    // ref only grows, so the candidates are a superset of the window against
+    // the final best lower bound; a candidate far below the best carries a
+    // negligible responsibility, and its record is harmless.
+    const int q = warp & 3, h = warp >> 2;
+    const int r = q * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float* __restrict__ cub = sCUB + h * kCS * kBM;     // this half's candidate list
+    uint16_t* __restrict__ ck = sCK + h * kCS * kBM;
+    uint32_t* xtot = reinterpret_cast<uint32_t*>(xref);  // [2][128] records per row and half
+    double ll_acc = 0.0;
+    for (int it = 0; it < my_tiles; ++it) {
+      if (warp_aborted(abort_flag)) break;
+      const int64_t tile = blockIdx.x + (int64_t)it * gridDim.x;
+      const int64_t n = tile * kBM + r;
+      const bool valid = n < a.N;
+      if (!warp_wait(&bar[R_FULL + (it & 1)], (it >> 1) & 1)) { fail(); break; }
+      const float rn = sRN[(it & 1) * kBM + r];
+      const float rnk = kKappa * rn;
+      // the slot holds only the row norms: hand it back at once
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[R_FREE + (it & 1)]);
+      const bool rowok = valid && isfinite(rn);
+      float ref = -INFINITY;
+      float mx = -INFINITY, ssum = 0.f;
+      int cnt = 0, nrec = 0;
+      bool flushed = false, ok = true;
+      uint32_t* cur = cursors + it % 3;
+      uint2* rout = a.recs + (size_t)tile * a.rec_cap;
+      for (int j = 0; j < nch && ok; ++j) {
+        const int64_t gq = (int64_t)it * nch + j;
+        const int buf = (int)(gq & 1);             // TMEM buffer and trailer slot
+        const uint32_t use = (uint32_t)(gq >> 1);
+        if (!warp_wait(&bar[T_FULL + buf], use & 1) || !warp_wait(&bar[TR_FULL + buf], use & 1)) {
+          fail(); ok = false; break;
+        }
+        tc::tc_fence_after();
+        const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4) + h * kHalf;
+        const float* __restrict__ tcn = tsc + kBN;
+        const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
+        const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
+        const float Sj = tsc[0];  // the chunk's common scale (every slot holds it)
+        const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
+        uint32_t pms[kHalf / 32];
+#pragma unroll
+        for (int b = 0; b < kHalf / 32; ++b) {
+          const int c0 = b * 32;
+          uint32_t u[32];
+          tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+          tc::tmem_wait32(u);
+          // lower bounds lo = s v + (bias - delta) - rnk |b| of the block
+          float best0 = -INFINITY, best1 = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float nb[4], bb[4];
+            ld_trail4(tcn + c0 + i, nb);
+            ld_trail4(tbl + c0 + i, bb);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float lo = fmaf(__uint_as_float(u[i + t]), Sj, fmaf(-rnk, nb[t], bb[t]));
+              if (t & 1) best1 = fmaxf(best1, lo);
+              else best0 = fmaxf(best0, lo);
+            }
+          }
+          ref = fmaxf(ref, fmaxf(best0, best1));
+          // every column whose upper bound hi = s v + (bias + delta) + rnk |b|
+          // reaches the window (never for an excluded component: its bound is -inf)
+          const float thr = fmaxf(ref - kT, -FLT_MAX);
+          uint32_t pm = 0u;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float nb[4], bb[4];
+            ld_trail4(tcn + c0 + i, nb);
+            ld_trail4(tbh + c0 + i, bb);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float hi = fmaf(__uint_as_float(u[i + t]), Sj, fmaf(rnk, nb[t], bb[t]));
+              pm |= hi >= thr ? (1u << (i + t)) : 0u;
+            }
+          }
+          pms[b] = rowok ? pm : 0u;
+        }
+        // the accumulators and the trailer slot are read: hand them back
+        // before the (possibly long) appends and flushes
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
+#pragma unroll
+        for (int b = 0; b < kHalf / 32; ++b) {
+          uint32_t pm = pms[b];
+          const int kb = j * kBN + h * kHalf + b * 32;
+          for (;;) {
+            while (pm && cnt < kCS) {
+              const int kk = __ffs(pm) - 1;
+              pm &= pm - 1u;
+              ck[cnt * kBM + r] = (uint16_t)(kb + kk);
+              ++cnt;
+            }
+            if (!__any_sync(0xffffffffu, pm != 0u)) break;
+            // a list is full: refine the warp's lists, fold, write records
+            refine_lists<D, XT>(a.X, tile, q, lane, cnt, cub, ck, g_mu, g_prec, g_c, iso);
+            fold_lse(cub, r, cnt, &mx, &ssum);
+            emit_records(lane, r, cnt, cub, ck, cur, rout, a.rec_cap, false);
+            nrec += cnt;
+            flushed = flushed || cnt > 0;
+            cnt = 0;
+            __syncwarp();
+          }
+        }
+      }
+      if (!ok) break;
+      // exchange A: records per row and half (bit 31: a list was flushed)
+      xtot[h * kBM + r] = (uint32_t)(nrec + cnt) | (flushed ? 0x80000000u : 0u);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
+      if (!warp_wait(&bar[EX_A], it & 1)) { fail(); break; }
+      // the cursor of tile it + 2 was last used by tile it - 1, which every
+      // warp has finished
+      if (warp == 0 && lane == 0) cursors[(it + 2) % 3] = 0u;
+      uint32_t rem = 0;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) rem += xtot[lane * 8 + t] & 0x7fffffffu;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) rem += __shfl_xor_sync(0xffffffffu, rem, o);
+      const uint32_t total = rem;
+      const bool overflow = total > (uint32_t)a.rec_cap;
+      const uint32_t t0 = xtot[r], t1 = xtot[kBM + r];
+      const bool anyflush = ((t0 | t1) >> 31) != 0u;
+      const uint32_t both = (t0 & 0x7fffffffu) + (t1 & 0x7fffffffu);
+      const bool exact = rowok && both > 0;
+      const bool single = exact && !anyflush && both == 1 && !a.want_lse && !overflow;
+      refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu, g_prec,
+                          g_c, iso);
+      if (exact && !single) fold_lse(cub, r, cnt, &mx, &ssum);
+      emit_records(lane, r, exact ? cnt : 0, cub, ck, cur, rout, a.rec_cap, single);
+      // exchange B: both halves' partial log-sum-exp
+      xmx[h * kBM + r] = mx;
+      xsum[h * kBM + r] = ssum;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[EX_B]);
+      if (!warp_wait(&bar[EX_B], it & 1)) { fail(); break; }
+      if (h == 0) {
+        if (exact && !single) {
+          const float m0 = xmx[r], m1 = xmx[kBM + r];
+          const float M = fmaxf(m0, m1);
+          float sum = 0.f;
+          if (m0 > -INFINITY) sum += xsum[r] * expf(m0 - M);
+          if (m1 > -INFINITY) sum += xsum[kBM + r] * expf(m1 - M);
+          const float lse = M + logf(sum);
+          if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
+          a.lse[n] = lse;
+          ll_acc += (double)lse;
+        } else if (valid && !exact) {
+          // non-finite input (the only way a row keeps no candidate)
+          raise_status(a.st, GMM_ERR_NONFINITE);
+          a.lse[n] = __int_as_float(0x7fc00000);
+          ll_acc += (double)__int_as_float(0x7fc00000);
+        }
+        if (q == 0 && lane == 0) a.tile_cnt[tile] = total;
+      }
+      __syncwarp();
+    }
+    {
+      const double sacc = warp_sum(ll_acc);
+      if (lane == 0) ll_red[warp] = sacc;
+    }
     } else {
-    // ------------------------------------ epilogue (streamed parameters)
+    // ------------------------- epilogue (streamed parameters, assignment)
     const int q = warp & 3, h = warp >> 2;
     const int r = q * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -1256,18 +1500,20 @@ int tc_screen_grid(int64_t N) {
 }
 
 // mode 0: EM (lse, ll_part); mode 1: assign (top-m).
+// EM mode: lse (every point's LSE_n, written for all points but those with a
+// single candidate unless want_lse) and the records are required.
 cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
-                      const void* prepared, int mode, float* lse, double* ll_part, int m,
-                      int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
+                      const void* prepared, int mode, float* lse, int want_lse, double* ll_part,
+                      int m, int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
                       uint32_t* tile_cnt, int rec_cap, DeviceStatus* st, cudaStream_t s) {
   ScreenArgs a;
   a.X = X; a.N = N; a.K = K; a.m = m; a.prepared = prepared;
   a.L = PreparedLayout::make(D, K, cov);
-  a.lse = lse; a.ll_part = ll_part; a.ids = ids; a.gamma = gamma;
+  a.lse = lse; a.want_lse = want_lse; a.ll_part = ll_part; a.ids = ids; a.gamma = gamma;
   a.fb_mask = fb_mask; a.st = st;
   a.recs = recs; a.tile_cnt = tile_cnt; a.rec_cap = rec_cap;
   if (!a.L.tc_chunks || N < 1) return cudaErrorInvalidValue;
-  if (mode == MODE_EM && (!recs || !tile_cnt || rec_cap < kBM)) return cudaErrorInvalidValue;
+  if (mode == MODE_EM && (!recs || !tile_cnt || !lse || rec_cap < kBM)) return cudaErrorInvalidValue;
   const int grid = tc_screen_grid(N);
 #define GMM_SCREEN(DD, XX)                                                              \
   return mode == MODE_EM ? run_screen<DD, XX, MODE_EM>(a, grid, s)                      \
