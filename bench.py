@@ -4,8 +4,13 @@
 One step = one EM iteration over the whole workload (prepare, E-step with
 log-sum-exp, statistics, reduction, M-step), inputs resident in HBM.
 Prints ONE JSON line (rank 0).  Workloads are the synthetic ones of
-datagen.WORKLOADS; the default is the 10M-point, D=128, K=256 fp16 diagonal
-EM workload.
+datagen.WORKLOADS; the default is the largest one that fits one GPU: 2e8
+points, D=128, K=1024, bf16 X (51 GB), diagonal EM, 5 iterations.
+
+The timed steps are the workload's own EM schedule from theta_0 (its
+iteration count unless --steps says otherwise), after --warmup untimed
+iterations from theta_0; the value is the mean over the timed iterations,
+and the line also gives each iteration's time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-cpu-baseline] [--no-e2e]
@@ -36,7 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused EM step N*K pairs/s (1 x GB300)"
 METRIC_ASSIGN = "top-m soft assignment N*K pairs/s (1 x GB300)"
 UNIT = "pairs/s"
-DEFAULT_WORKLOAD = "embed_diag"
+DEFAULT_WORKLOAD = "large_diag"
 COV_NAMES = {0: "full", 1: "diag", 2: "iso"}
 XNAMES = {0: "f32", 1: "f16", 2: "bf16"}
 
@@ -59,13 +64,18 @@ def measured_peaks():
 
 # ---------------------------------------------------------------- work model
 
-SLAB_ROWS = 1 << 21  # rows per screening launch of the tensor-core path
+def slab_rows(wl):
+    """Rows per screening launch of the tensor-core path (the library's rule:
+    its record buffer stays at 1 GiB)."""
+    if wl.m:
+        return 1 << 19 if wl.K > 128 else 1 << 20
+    return 1 << 19 if wl.K > 128 else 1 << 20
 
 
 def tc_path(wl):
     """The tensor-core E-step runs for diagonal / isotropic covariance with
-    D = 64 or 128 and K <= 16384 (the library's own rule)."""
-    return wl.cov_type != 0 and wl.D in (64, 128) and wl.K <= 16384
+    D = 64 or 128 (the library's own rule)."""
+    return wl.cov_type != 0 and wl.D in (64, 128)
 
 
 def work_model(wl):
@@ -74,7 +84,8 @@ def work_model(wl):
     [x, x^2] . [mu/var, -1/(2 var)], 2 * 2D flops per pair, plus 4D for the
     statistics; full: D(D+1) for the triangular solve and D(D+1) + 2D for the
     statistics.  The screening kernel is counted at one contraction of its
-    rows (it runs two: bounds, then candidates); its bytes are its rows of X."""
+    rows (the EM mode runs exactly one; the assignment mode's streamed
+    parameters two: bounds, then candidates); its bytes are its rows of X."""
     N, D, K = wl.N, wl.D, wl.K
     esz = 4 if wl.dtype == 0 else 2
     pairs = N * K
@@ -85,7 +96,7 @@ def work_model(wl):
         e_flops, s_flops = 4 * D, 4 * D
         pbytes = 4 * K * (1 + 2 * D)
     x_bytes = N * D * esz
-    slabs = -(-N // SLAB_ROWS)
+    slabs = -(-N // slab_rows(wl))
     rows_per_launch = N / slabs
     return dict(
         pairs=pairs,
@@ -368,6 +379,8 @@ def run_ours(args, wl):
     st = GMMState(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, device=dev)
     for k, v in opts.items():
         setattr(st.opts, k, v)
+    steps = args.steps
+    # warm-up: W untimed iterations from theta_0
     st.set_params(*theta0)
     for _ in range(args.warmup):
         st.step(X)
@@ -376,27 +389,30 @@ def run_ours(args, wl):
     if status != 0:
         log("device status after warm-up:", G.status_string(status))
 
-    # timed region: device-resident X, CUDA events on the launching stream
+    # timed region: the workload's EM schedule from theta_0 on device-resident
+    # X, CUDA events on the launching stream (one per iteration)
+    st.set_params(*theta0)
     G.gmm_profile_reset()
     G.gmm_profile_enable(True)
     clocks = ClockSampler(dev.index)
     clocks.start()
     stream = torch.cuda.current_stream()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ev0.record(stream)
-    for _ in range(args.steps):
+    evs[0].record(stream)
+    for i in range(steps):
         st.step(X)
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     G.gmm_profile_enable(False)
     prof = G.gmm_profile_read()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
+    per_iter = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]) / steps, dev)
     status = st.device_status()
     ll = float(st.loglik.item())
     value = job_rate(world, wm["pairs"], ms / 1e3)
@@ -432,31 +448,34 @@ def run_ours(args, wl):
                       wm["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
 
     # end to end through the host-buffer entry point: X streamed from pinned
-    # host memory every step, log-likelihood read back every step
+    # host memory every iteration, the log-likelihood read back every
+    # iteration; the same schedule (W untimed iterations from theta_0, then
+    # the timed ones from theta_0)
     e2e = None
     if not args.no_e2e:
         chunk = max(1, min(wl.N, (256 << 20) // (wl.D * esz)))
         st2 = GMMState(wl.N, wl.D, wl.K, wl.cov_type, wl.dtype, device=dev, chunk_rows=chunk)
         for k, v in opts.items():
             setattr(st2.opts, k, v)
-        st2.set_params(*theta0)
         host = torch.empty(wl.N * wl.D * esz, dtype=torch.uint8, pin_memory=True)
         host.copy_(X)
         ll_host = torch.zeros(1, dtype=torch.float64, pin_memory=True)
         del X
+        del st
         torch.cuda.empty_cache()
-        # the same EM iterations as the device-timed loop: W untimed steps
-        # from theta_0, then the K timed ones
-        for _ in range(max(1, args.warmup)):
+        st2.set_params(*theta0)
+        for _ in range(args.warmup):
             st2.step_host(host, loglik_host=ll_host)
+        st2.set_params(*theta0)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(args.steps):
+        for _ in range(steps):
             st2.step_host(host, loglik_host=ll_host)
-        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, dev)
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / steps, dev)
         e2e = dict(value=job_rate(world, wm["pairs"], e2e_s), unit=UNIT,
                    h2d_bytes_per_step=wm["x_bytes"], d2h_bytes_per_step=8,
                    ms_per_step=e2e_s * 1e3, chunk_rows=chunk)
+        del host
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -474,6 +493,10 @@ def run_ours(args, wl):
             # screening contraction runs on fp16 tensor cores (fp32 accumulate)
             config=config_dict(wl, extra=dict(
                 iters_per_s=1e3 / ms, parallelism="replicas" if world > 1 else "single",
+                schedule="iterations 0..%d from theta_0 (after %d untimed ones from theta_0)"
+                         % (steps - 1, args.warmup),
+                ms_per_iteration=[round(t, 4) for t in per_iter],
+                steady_ms_per_step=per_iter[-1],
                 e_step="tensor-core screen (fp16) + exact fp32 refine" if tc_path(wl)
                 else "CUDA-core fp32",
                 loglik=ll, device_status=G.status_string(status),
@@ -617,7 +640,9 @@ def run_assign(args, wl):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed iterations (default: the workload's own EM schedule; 5 for "
+                         "assignment workloads)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -630,6 +655,8 @@ def main(argv=None):
     wl = datagen.WORKLOADS[args.workload]
     if args.n:
         wl = wl.with_n(args.n)
+    if args.steps is None:
+        args.steps = wl.iters if not wl.m else 5
     if args.impl == "reference":
         return run_reference(args, wl)
     if wl.m:

@@ -35,12 +35,12 @@ cudaError_t simt_stats_rows(const void* X, int xdtype, int64_t N, int D, int K, 
                             const void* prepared, const float* lse, int parts, double* part,
                             int accumulate, const uint32_t* rows, const uint32_t* row_count,
                             cudaStream_t s);
-int chunk_stats_blocks(int D, int K);
-int chunk_stats_parts(int D, int K);
-cudaError_t chunk_stats(const void* X, int xdtype, int64_t N, int D, int K, int cov,
-                        const void* prepared, const float* lse, const uint2* recs,
-                        const uint32_t* tile_cnt, int rec_cap, double* part, int accumulate,
-                        double* ll_part, cudaStream_t s);
+size_t sparse_stats_ws_bytes(int64_t rows, int D, int K, int rec_cap);
+bool sparse_stats_supported(int K);
+cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
+                         int cov, const float* lse, const uint32_t* tile_cnt, const uint2* recs,
+                         int rec_cap, void* sws, double* part, int accumulate, double* ll,
+                         DeviceStatus* st, cudaStream_t s);
 int simt_stat_chunk(int D, int cov);
 cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
                          const float* centre, const int32_t* prep_flags, float var_floor,
@@ -53,8 +53,9 @@ namespace {
 constexpr int kTargetCtas = 608;   // 4 x 152 SMs: statistics blocks per launch
 constexpr int kListGrid = 304;     // blocks of the CUDA-core pass over handed-over rows
 constexpr int kMaxScreenGrid = 1024;  // upper bound of tc_screen_grid (SM count)
-// Tensor-core path: records {key, exact log joint} per 128-point tile (a
-// tile past it is taken densely by the statistics) and rows per slab (one
+// Tensor-core path: records {key, exact log joint} per 128-point tile, in
+// eight regions (one per epilogue warp and column half; a warp whose records
+// do not fit hands its rows to the CUDA-core path), and rows per slab (one
 // screening launch; its records are consumed before the next slab), so the
 // record buffer stays at 1 GiB: 128 records a point on average for K <= 128,
 // 256 beyond (the early EM iterations keep about a hundred candidates a
@@ -79,18 +80,17 @@ int stat_parts(int64_t N, int D, int K, int cov) {
 
 struct WsLayout {
   size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_fb,
-      off_fbm, off_fbseg, off_rec, off_tcnt, off_stage, bytes;
+      off_fbm, off_fbseg, off_rec, off_tcnt, off_sws, off_stage, bytes;
   int parts;          // statistics partials of the CUDA-core path
-  int sp_parts;       // tensor-core path: the partitions of the statistics blocks
-  int cs_blocks;      // statistics blocks per slab (log-likelihood partials)
+  int sp_parts;       // tensor-core path: the records' partial (1) ...
+  int lp_parts;       // ... followed by those of the row-list pass
   int64_t lse_rows;
 };
 
 // The tensor-core E-step of an EM iteration (screening + statistics from
 // its records).
 bool use_tc(int D, int K, int cov, const gmm_opts& o) {
-  (void)K;
-  return tc_eligible(D, cov) && !(o.flags & GMM_OPT_CUDA_CORES);
+  return tc_eligible(D, cov) && sparse_stats_supported(K) && !(o.flags & GMM_OPT_CUDA_CORES);
 }
 
 // rows: rows processed per launch (N, or the chunk size of the host path);
@@ -103,21 +103,22 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.lse_rows = rows;
   W.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)rows);
   const bool tc = tc_eligible(D, cov);
-  W.cs_blocks = tc ? chunk_stats_blocks(D, K) * chunk_stats_parts(D, K) : 0;
   {
     // dense LSE blocks, or the tensor-core CTAs followed by the list blocks
-    // and the statistics blocks
     const size_t dense = (size_t)((rows + kLseRows - 1) / kLseRows);
-    const size_t tcl = (size_t)(kMaxScreenGrid + kListGrid) + (size_t)W.cs_blocks;
+    const size_t tcl = (size_t)(kMaxScreenGrid + kListGrid);
     W.off_llpart = o; o = align_up(o + sizeof(double) * (dense > tcl ? dense : tcl));
   }
   W.off_ll = o;     o = align_up(o + sizeof(double));
   W.parts = stat_parts(rows, D, K, cov);
-  W.sp_parts = 0;
+  W.sp_parts = W.lp_parts = 0;
   int slots = W.parts;
   if (tc) {
-    W.sp_parts = chunk_stats_parts(D, K);
-    if (W.sp_parts > slots) slots = W.sp_parts;
+    W.sp_parts = 1;
+    const int kc = simt_stat_chunk(D, cov);
+    const int chunks = (K + kc - 1) / kc;
+    W.lp_parts = (kListGrid + chunks - 1) / chunks;
+    if (W.sp_parts + W.lp_parts > slots) slots = W.sp_parts + W.lp_parts;
   }
   W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)slots * K * stat_width(D, cov));
   W.off_flags = o;  o = align_up(o + sizeof(int32_t) * K);
@@ -128,7 +129,9 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_fbm = o;    o = align_up(o + sizeof(uint32_t) * 4 * slab_tiles);
   W.off_fbseg = o;  o = align_up(o + sizeof(uint32_t) * (tc ? fb_compact_segments(slab) : 0));
   W.off_rec = o;    o = align_up(o + sizeof(uint2) * slab_tiles * (size_t)rec_cap_for(K));
-  W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * slab_tiles);
+  W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * 8 * slab_tiles);
+  W.off_sws = o;
+  o = align_up(o + (tc ? sparse_stats_ws_bytes(slab, D, K, rec_cap_for(K)) : 0));
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
@@ -195,12 +198,16 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
   double* llp = at<double>(ws, W.off_llpart);
   if (tc) {
     // Slabs of rows.  Per slab: screen on the tensor cores (exact LSE_n of
-    // every point and records of its candidates), statistics from the
-    // records, the log-likelihood.
+    // the points and records of their candidates), the CUDA-core pass over
+    // the rows handed over (a warp's records past its region, non-finite
+    // input), the log-likelihood, statistics from the records and the
+    // CUDA-core statistics of the handed-over rows.
+    uint32_t* fb = at<uint32_t>(ws, W.off_fb);
     uint32_t* fbm = at<uint32_t>(ws, W.off_fbm);
     uint2* recs = at<uint2>(ws, W.off_rec);
     uint32_t* tcnt = at<uint32_t>(ws, W.off_tcnt);
     double* part = at<double>(ws, W.off_part);
+    double* lpart = part + (size_t)W.sp_parts * K * stat_width(D, cov);
     const int64_t slab_rows = slab_rows_for(K);
     const int rec_cap = rec_cap_for(K);
     for (int64_t r0 = 0; r0 < rows; r0 += slab_rows) {
@@ -215,13 +222,26 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
                           nullptr, nullptr, fbm, recs, tcnt, rec_cap, st, s));
       }
       {
-        GMM_PROF("chunk_stats_kernel");
-        GMM_TRY(chunk_stats(Xs, xdtype, sn, D, K, cov, prep, ls, recs, tcnt, rec_cap, part, acc,
-                            llp + g1, s));
+        GMM_PROFN("fb_compact_kernel", 2);
+        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
+      }
+      {
+        GMM_PROF("lse_rows_kernel");
+        GMM_TRY(simt_lse_rows(Xs, xdtype, sn, D, K, cov, prep, ls, llp + g1, 0, nullptr,
+                              nullptr, st, fb, &st->fb_count, kListGrid, s));
       }
       {
         GMM_PROF("ll_finalize_kernel");
-        GMM_TRY(launch_ll_finalize(llp, g1 + W.cs_blocks, at<double>(ws, W.off_ll), acc, s));
+        GMM_TRY(launch_ll_finalize(llp, g1 + kListGrid, at<double>(ws, W.off_ll), acc, s));
+      }
+      {
+        GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, ls, tcnt, recs, rec_cap,
+                             at<char>(ws, W.off_sws), part, acc, at<double>(ws, W.off_ll), st, s));
+      }
+      {
+        GMM_PROF("stats_rows_kernel");
+        GMM_TRY(simt_stats_rows(Xs, xdtype, sn, D, K, cov, prep, ls, W.lp_parts, lpart, acc, fb,
+                                &st->fb_count, s));
       }
     }
     return GMM_OK;
@@ -244,7 +264,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
 }
 
 // Partials the M-step merges for the path taken.
-int mstep_parts(const WsLayout& W, bool tc) { return tc ? W.sp_parts : W.parts; }
+int mstep_parts(const WsLayout& W, bool tc) { return tc ? W.sp_parts + W.lp_parts : W.parts; }
 
 // Library-owned copy stream and events of the host path (one set per device).
 struct HostPathRes {

@@ -357,13 +357,15 @@ __device__ __forceinline__ void fold_lse(const float* cub, int r, int cnt, float
   *sum = s;
 }
 
-// Writes this row's cnt records {(k << 7) | row, l} to the tile's buffer at
-// positions taken from the tile's shared-memory cursor (one atomic per warp;
-// the order inside the buffer does not matter).  Positions past rec_cap are
-// not written; the tile's count then tells the statistics to take it densely.
+// Writes this row's cnt records {(k << 7) | row, l} (single: the flagged
+// record of a point's only candidate, no value) to the warp's region of the
+// tile's record buffer, after the records the warp wrote before (wpos, the
+// same in every lane): the order is a function of the data alone.  Records
+// past region_cap are not written; the warp's rows then take the CUDA-core
+// path.
 __device__ __forceinline__ void emit_records(int lane, int r, int cnt, const float* cub,
-                                             const uint16_t* ck, uint32_t* cursor, uint2* out,
-                                             int rec_cap, bool single) {
+                                             const uint16_t* ck, uint32_t* wpos, uint2* region,
+                                             int region_cap, bool single) {
   int incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -371,16 +373,14 @@ __device__ __forceinline__ void emit_records(int lane, int r, int cnt, const flo
     if (lane >= o) incl += v;
   }
   const int total = __shfl_sync(0xffffffffu, incl, 31);
-  uint32_t base = 0;
-  if (lane == 0 && total > 0) base = atomicAdd(cursor, (uint32_t)total);
-  base = __shfl_sync(0xffffffffu, base, 0);
-  const uint32_t p0 = base + (uint32_t)(incl - cnt);
+  const uint32_t p0 = *wpos + (uint32_t)(incl - cnt);
   for (int e = 0; e < cnt; ++e) {
-    if (p0 + e < (uint32_t)rec_cap) {
+    if (p0 + e < (uint32_t)region_cap) {
       const uint32_t key = (single ? kRecSingle : 0u) | ((uint32_t)ck[e * kBM + r] << 7) | (uint32_t)r;
-      out[p0 + e] = make_uint2(key, single ? 0u : __float_as_uint(cub[e * kBM + r]));
+      region[p0 + e] = make_uint2(key, single ? 0u : __float_as_uint(cub[e * kBM + r]));
     }
   }
+  *wpos += (uint32_t)total;
 }
 
 template <int D, int XT, int MODE, bool GRP>
@@ -403,9 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   uint64_t* bar = (uint64_t*)(sm + S::OFF_BAR);
   uint32_t* tmem_slot = (uint32_t*)(sm + S::OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + S::OFF_MISC + 4);
-  // EM: record cursors, one per tile in flight, used round robin over three
-  // (grouped: three per group)
-  uint32_t* cursors = (uint32_t*)(sm + S::OFF_MISC + 16);
   __shared__ double ll_red[kEpiWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -418,9 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
   // group's tiles keeps buffer 2g + j, contracted once and swept by both
   // passes; streamed, each pass contracts again and the contractions
   // alternate over two buffers
-  // streamed parameters, EM: one contraction per chunk, swept once against a
-  // running window; assignment: contracted twice (bounds, then candidates)
-  const int ncontr = (GRP || MODE == MODE_EM) ? nch : 2 * nch;  // contractions per tile
+  // streamed parameters: each tile contracted twice (bounds, then candidates)
+  const int ncontr = GRP ? nch : 2 * nch;  // contractions per tile
   auto tbuf = [&](int it, int gi, int* buf, uint32_t* use) {
     if constexpr (GRP) {
       *buf = 2 * (it & 1) + gi % nch;   // one contraction per chunk, swept twice
@@ -461,7 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       tc::mbar_init(&bar[EX_C], kEpiWarps);
     }
     *abort_flag = 0;
-    for (int i = 0; i < 6; ++i) cursors[i] = 0u;
     tc::mbar_fence_init();
   }
   tc::tc_fence_before();
@@ -699,11 +694,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       bool ok = true;
       float thr = -INFINITY;  // the point's window, fixed after pass 0
       // EM: running log-sum-exp of the candidates refined so far, records
-      // written by flushes of a full list, and the tile's record cursor
+      // written by flushes of a full list, and this warp's region of the
+      // tile's records (regions 2q and 2q + 1 of the eight)
       float mx = -INFINITY, ssum = 0.f;
       int nrec = 0;
       bool flushed = false;
-      uint32_t* cur = cursors + g * 3 + s % 3;
+      uint32_t wpos = 0;
+      const int rcap = a.rec_cap / 4;
+      uint2* region = a.recs + (size_t)tile * a.rec_cap + (size_t)q * rcap;
       // pass 0: lower bounds only; pass 1 (a second sweep of the same
       // accumulators): candidates against the point's final window
       for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -792,8 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
                   if (!__any_sync(0xffffffffu, pm != 0u)) break;
                   refine_lists<D, XT>(a.X, tile, q, lane, cnt, cub, ck, g_mu, g_prec, g_c, iso);
                   fold_lse(cub, r, cnt, &mx, &ssum);
-                  emit_records(lane, r, cnt, cub, ck, cur, a.recs + (size_t)tile * a.rec_cap,
-                               a.rec_cap, false);
+                  emit_records(lane, r, cnt, cub, ck, &wpos, region, rcap, false);
                   nrec += cnt;
                   flushed = flushed || cnt > 0;
                   cnt = 0;
@@ -823,47 +820,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       __syncwarp();
       if (!ok) break;
       if constexpr (MODE == MODE_EM) {
-        // the rows' record counts (flushed + remaining; bit 15: a list was
-        // flushed) -> the tile's record total, the same on every run
-        uint16_t* xg = xcg + (g * 2 + (s & 1)) * kBM;
-        xg[r] = (uint16_t)((nrec + cnt) | (flushed ? 0x8000 : 0));
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar[EXG + g]);
-        if (!warp_wait(&bar[EXG + g], s & 1)) { fail(); break; }
-        // the cursor of the group's tile s + 2 was last used by tile s - 1,
-        // which every warp of the group has finished
-        if (q == 0 && lane == 0) cursors[g * 3 + (s + 2) % 3] = 0u;
-        int rem = 0;
+        // this warp's record count (flushed + remaining): past its region's
+        // capacity the warp's rows take the CUDA-core path
+        int mine = nrec + cnt;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) rem += xg[lane * 4 + t] & 0x7fff;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) rem += __shfl_xor_sync(0xffffffffu, rem, o);
-        const uint32_t total = (uint32_t)rem;
-        const bool overflow = total > (uint32_t)a.rec_cap;
-        const bool exact = valid && isfinite(rn) && (cnt > 0 || flushed);
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        const bool overflow = mine > rcap;
+        const bool exact = valid && isfinite(rn) && (cnt > 0 || flushed) && !overflow;
         // a point with a single candidate has gamma = 1 (every other
         // component lies more than 40 nats below it); unless LSE_n is wanted
-        // (or the tile's records do not fit) its exact log joint is not
-        // needed here: the statistics give its log-likelihood term
-        const bool single = exact && !flushed && cnt == 1 && !a.want_lse && !overflow;
+        // its exact log joint is not needed here: the statistics give its
+        // log-likelihood term
+        const bool single = exact && !flushed && cnt == 1 && !a.want_lse;
         refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu,
                             g_prec, g_c, iso);
         if (exact && !single) fold_lse(cub, r, cnt, &mx, &ssum);
-        emit_records(lane, r, exact ? cnt : 0, cub, ck, cur, a.recs + (size_t)tile * a.rec_cap,
-                     a.rec_cap, single);
+        emit_records(lane, r, exact ? cnt : 0, cub, ck, &wpos, region, rcap, single);
         if (exact && !single) {
           const float lse = mx + logf(ssum);
           if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
           a.lse[n] = lse;
           ll_acc += (double)lse;
-        } else if (valid && !exact) {
-          // non-finite input (the only way a row keeps no candidate): the
-          // step reports it, and its log-likelihood is not finite
-          raise_status(a.st, GMM_ERR_NONFINITE);
-          a.lse[n] = __int_as_float(0x7fc00000);
-          ll_acc += (double)__int_as_float(0x7fc00000);
         }
-        if (q == 0 && lane == 0) a.tile_cnt[tile] = total;
+        // rows of an overflowing warp, and rows without a candidate
+        // (non-finite input), go to the CUDA-core path
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
+        if (lane == 0) {
+          a.fb_mask[tile * 4 + q] = fbm;
+          a.tile_cnt[tile * 8 + 2 * q] = overflow ? 0u : (uint32_t)mine;
+          a.tile_cnt[tile * 8 + 2 * q + 1] = 0u;
+        }
       } else {
       const bool exact = valid && isfinite(rn) && !(dropped >= thr) && cnt > 0;
       // a point with a single candidate has gamma = 1 (every other component
@@ -924,18 +910,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     } else if constexpr (MODE == MODE_EM) {
     // --------------------------- epilogue (streamed parameters, EM mode)
     // warp w reads lane quarter q = w % 4 and column half h = w / 4 of every
-    // chunk.  Each chunk is contracted once and swept once: per block of 32
-    // columns the largest lower bound joins a running best (ref, this half's),
-    // then every column whose upper bound reaches ref - 40 is a candidate.
-    // ref only grows, so the candidates are a superset of the window against
-    // the final best lower bound; a candidate far below the best carries a
-    // negligible responsibility, and its record is harmless.
+    // chunk.  Each tile is contracted twice: pass 0 finds the best lower bound
+    // (both halves combined at barrier A), pass 1 collects every column whose
+    // upper bound reaches it minus 40 nats; a full list is refined, folded into
+    // the row's running log-sum-exp and written out (a flush), and collection
+    // goes on.  Barrier B: both halves' record counts (singles, overflow);
+    // barrier C: both halves' partial log-sum-exp.
     const int q = warp & 3, h = warp >> 2;
     const int r = q * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     float* __restrict__ cub = sCUB + h * kCS * kBM;     // this half's candidate list
     uint16_t* __restrict__ ck = sCK + h * kCS * kBM;
-    uint32_t* xtot = reinterpret_cast<uint32_t*>(xref);  // [2][128] records per row and half
+    uint32_t* xtot = reinterpret_cast<uint32_t*>(xlbm);  // [2][128] records per row and half
+    const int rcap = a.rec_cap / 8;                       // this warp's region of the tile's records
     double ll_acc = 0.0;
     for (int it = 0; it < my_tiles; ++it) {
       if (warp_aborted(abort_flag)) break;
@@ -949,124 +936,137 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[R_FREE + (it & 1)]);
       const bool rowok = valid && isfinite(rn);
-      float ref = -INFINITY;
+      float ref = -INFINITY, thr = -INFINITY;
       float mx = -INFINITY, ssum = 0.f;
       int cnt = 0, nrec = 0;
       bool flushed = false, ok = true;
-      uint32_t* cur = cursors + it % 3;
-      uint2* rout = a.recs + (size_t)tile * a.rec_cap;
-      for (int j = 0; j < nch && ok; ++j) {
-        const int64_t gq = (int64_t)it * nch + j;
-        const int buf = (int)(gq & 1);             // TMEM buffer and trailer slot
-        const uint32_t use = (uint32_t)(gq >> 1);
-        if (!warp_wait(&bar[T_FULL + buf], use & 1) || !warp_wait(&bar[TR_FULL + buf], use & 1)) {
-          fail(); ok = false; break;
+      uint32_t wpos = 0;
+      uint2* region = a.recs + (size_t)tile * a.rec_cap + (size_t)(2 * q + h) * rcap;
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        if (pass == 1) {
+          xref[h * kBM + r] = ref;
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
+          if (!warp_wait(&bar[EX_A], it & 1)) { fail(); ok = false; break; }
+          // the window (never reached by an excluded component: its bound is -inf)
+          thr = fmaxf(fmaxf(xref[r], xref[kBM + r]) - kT, -FLT_MAX);
         }
-        tc::tc_fence_after();
-        const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4) + h * kHalf;
-        const float* __restrict__ tcn = tsc + kBN;
-        const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
-        const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
-        const float Sj = tsc[0];  // the chunk's common scale (every slot holds it)
-        const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
-        uint32_t pms[kHalf / 32];
-#pragma unroll
-        for (int b = 0; b < kHalf / 32; ++b) {
-          const int c0 = b * 32;
-          uint32_t u[32];
-          tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
-          tc::tmem_wait32(u);
-          // lower bounds lo = s v + (bias - delta) - rnk |b| of the block
-          float best0 = -INFINITY, best1 = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float nb[4], bb[4];
-            ld_trail4(tcn + c0 + i, nb);
-            ld_trail4(tbl + c0 + i, bb);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float lo = fmaf(__uint_as_float(u[i + t]), Sj, fmaf(-rnk, nb[t], bb[t]));
-              if (t & 1) best1 = fmaxf(best1, lo);
-              else best0 = fmaxf(best0, lo);
-            }
+        for (int j = 0; j < nch; ++j) {
+          const int64_t gq = ((int64_t)it * 2 + pass) * nch + j;
+          const int buf = (int)(gq & 1);             // TMEM buffer and trailer slot
+          const uint32_t use = (uint32_t)(gq >> 1);
+          if (!warp_wait(&bar[T_FULL + buf], use & 1) || !warp_wait(&bar[TR_FULL + buf], use & 1)) {
+            fail(); ok = false; break;
           }
-          ref = fmaxf(ref, fmaxf(best0, best1));
-          // every column whose upper bound hi = s v + (bias + delta) + rnk |b|
-          // reaches the window (never for an excluded component: its bound is -inf)
-          const float thr = fmaxf(ref - kT, -FLT_MAX);
-          uint32_t pm = 0u;
+          tc::tc_fence_after();
+          const float* __restrict__ tsc = sT + buf * (S::T_BYTES / 4) + h * kHalf;
+          const float* __restrict__ tcn = tsc + kBN;
+          const float* __restrict__ tbl = tsc + 2 * kBN;   // bias - delta
+          const float* __restrict__ tbh = tsc + 3 * kBN;   // bias + delta
+          const float Sj = tsc[0];  // the chunk's common scale (every slot holds it)
+          const uint32_t tcol = tmem_base + lane_base + (uint32_t)(buf * kBN + h * kHalf);
+          uint32_t pms[kHalf / 32];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float nb[4], bb[4];
-            ld_trail4(tcn + c0 + i, nb);
-            ld_trail4(tbh + c0 + i, bb);
+          for (int b = 0; b < kHalf / 32; ++b) {
+            const int c0 = b * 32;
+            uint32_t u[32];
+            tc::tmem_ld32_issue(tcol + (uint32_t)c0, u);
+            tc::tmem_wait32(u);
+            uint32_t pm = 0u;
+            if (pass == 0) {
+              // lower bounds lo = s v + (bias - delta) - rnk |b|
+              float best0 = -INFINITY, best1 = -INFINITY;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float hi = fmaf(__uint_as_float(u[i + t]), Sj, fmaf(rnk, nb[t], bb[t]));
-              pm |= hi >= thr ? (1u << (i + t)) : 0u;
+              for (int i = 0; i < 32; i += 4) {
+                float nb[4], bb[4];
+                ld_trail4(tcn + c0 + i, nb);
+                ld_trail4(tbl + c0 + i, bb);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const float lo = fmaf(__uint_as_float(u[i + t]), Sj, fmaf(-rnk, nb[t], bb[t]));
+                  if (t & 1) best1 = fmaxf(best1, lo);
+                  else best0 = fmaxf(best0, lo);
+                }
+              }
+              ref = fmaxf(ref, fmaxf(best0, best1));
+            } else {
+              // every column whose upper bound hi = s v + (bias + delta) + rnk |b|
+              // reaches the window
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                float nb[4], bb[4];
+                ld_trail4(tcn + c0 + i, nb);
+                ld_trail4(tbh + c0 + i, bb);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const float hi = fmaf(__uint_as_float(u[i + t]), Sj, fmaf(rnk, nb[t], bb[t]));
+                  pm |= hi >= thr ? (1u << (i + t)) : 0u;
+                }
+              }
             }
+            pms[b] = rowok ? pm : 0u;
           }
-          pms[b] = rowok ? pm : 0u;
-        }
-        // the accumulators and the trailer slot are read: hand them back
-        // before the (possibly long) appends and flushes
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
+          // the accumulators and the trailer slot are read: hand them back
+          // before the (possibly long) appends and flushes
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
+          if (pass == 1) {
 #pragma unroll
-        for (int b = 0; b < kHalf / 32; ++b) {
-          uint32_t pm = pms[b];
-          const int kb = j * kBN + h * kHalf + b * 32;
-          for (;;) {
-            while (pm && cnt < kCS) {
-              const int kk = __ffs(pm) - 1;
-              pm &= pm - 1u;
-              ck[cnt * kBM + r] = (uint16_t)(kb + kk);
-              ++cnt;
+            for (int b = 0; b < kHalf / 32; ++b) {
+              uint32_t pm = pms[b];
+              const int kb = j * kBN + h * kHalf + b * 32;
+              for (;;) {
+                while (pm && cnt < kCS) {
+                  const int kk = __ffs(pm) - 1;
+                  pm &= pm - 1u;
+                  ck[cnt * kBM + r] = (uint16_t)(kb + kk);
+                  ++cnt;
+                }
+                if (!__any_sync(0xffffffffu, pm != 0u)) break;
+                // a list is full: refine the warp's lists, fold, write records
+                refine_lists<D, XT>(a.X, tile, q, lane, cnt, cub, ck, g_mu, g_prec, g_c, iso);
+                fold_lse(cub, r, cnt, &mx, &ssum);
+                emit_records(lane, r, cnt, cub, ck, &wpos, region, rcap, false);
+                nrec += cnt;
+                flushed = flushed || cnt > 0;
+                cnt = 0;
+                __syncwarp();
+              }
             }
-            if (!__any_sync(0xffffffffu, pm != 0u)) break;
-            // a list is full: refine the warp's lists, fold, write records
-            refine_lists<D, XT>(a.X, tile, q, lane, cnt, cub, ck, g_mu, g_prec, g_c, iso);
-            fold_lse(cub, r, cnt, &mx, &ssum);
-            emit_records(lane, r, cnt, cub, ck, cur, rout, a.rec_cap, false);
-            nrec += cnt;
-            flushed = flushed || cnt > 0;
-            cnt = 0;
-            __syncwarp();
           }
         }
       }
       if (!ok) break;
-      // exchange A: records per row and half (bit 31: a list was flushed)
+      // barrier B: records per row and half (bit 31: a list was flushed)
       xtot[h * kBM + r] = (uint32_t)(nrec + cnt) | (flushed ? 0x80000000u : 0u);
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar[EX_A]);
-      if (!warp_wait(&bar[EX_A], it & 1)) { fail(); break; }
-      // the cursor of tile it + 2 was last used by tile it - 1, which every
-      // warp has finished
-      if (warp == 0 && lane == 0) cursors[(it + 2) % 3] = 0u;
-      uint32_t rem = 0;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) rem += xtot[lane * 8 + t] & 0x7fffffffu;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) rem += __shfl_xor_sync(0xffffffffu, rem, o);
-      const uint32_t total = rem;
-      const bool overflow = total > (uint32_t)a.rec_cap;
-      const uint32_t t0 = xtot[r], t1 = xtot[kBM + r];
-      const bool anyflush = ((t0 | t1) >> 31) != 0u;
-      const uint32_t both = (t0 & 0x7fffffffu) + (t1 & 0x7fffffffu);
-      const bool exact = rowok && both > 0;
-      const bool single = exact && !anyflush && both == 1 && !a.want_lse && !overflow;
-      refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu, g_prec,
-                          g_c, iso);
-      if (exact && !single) fold_lse(cub, r, cnt, &mx, &ssum);
-      emit_records(lane, r, exact ? cnt : 0, cub, ck, cur, rout, a.rec_cap, single);
-      // exchange B: both halves' partial log-sum-exp
-      xmx[h * kBM + r] = mx;
-      xsum[h * kBM + r] = ssum;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[EX_B]);
       if (!warp_wait(&bar[EX_B], it & 1)) { fail(); break; }
+      const uint32_t t0 = xtot[r], t1 = xtot[kBM + r];
+      // this quarter's two regions: past either one's capacity, the
+      // quarter's rows take the CUDA-core path
+      uint32_t w0 = t0 & 0x7fffffffu, w1 = t1 & 0x7fffffffu;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        w0 += __shfl_xor_sync(0xffffffffu, w0, o);
+        w1 += __shfl_xor_sync(0xffffffffu, w1, o);
+      }
+      const bool overflow = w0 > (uint32_t)rcap || w1 > (uint32_t)rcap;
+      const bool anyflush = ((t0 | t1) >> 31) != 0u;
+      const uint32_t both = (t0 & 0x7fffffffu) + (t1 & 0x7fffffffu);
+      const bool exact = rowok && both > 0 && !overflow;
+      const bool single = exact && !anyflush && both == 1 && !a.want_lse;
+      refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu, g_prec,
+                          g_c, iso);
+      if (exact && !single) fold_lse(cub, r, cnt, &mx, &ssum);
+      emit_records(lane, r, exact ? cnt : 0, cub, ck, &wpos, region, rcap, single);
+      // barrier C: both halves' partial log-sum-exp
+      xmx[h * kBM + r] = mx;
+      xsum[h * kBM + r] = ssum;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[EX_C]);
+      if (!warp_wait(&bar[EX_C], it & 1)) { fail(); break; }
       if (h == 0) {
         if (exact && !single) {
           const float m0 = xmx[r], m1 = xmx[kBM + r];
@@ -1078,14 +1078,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           if (!isfinite(lse)) raise_status(a.st, GMM_ERR_NONFINITE);
           a.lse[n] = lse;
           ll_acc += (double)lse;
-        } else if (valid && !exact) {
-          // non-finite input (the only way a row keeps no candidate)
-          raise_status(a.st, GMM_ERR_NONFINITE);
-          a.lse[n] = __int_as_float(0x7fc00000);
-          ll_acc += (double)__int_as_float(0x7fc00000);
         }
-        if (q == 0 && lane == 0) a.tile_cnt[tile] = total;
+        // rows of an overflowing quarter, and rows without a candidate
+        // (non-finite input), go to the CUDA-core path
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
+        if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
       }
+      if (lane == 0) a.tile_cnt[tile * 8 + 2 * q + h] = overflow ? 0u : (h == 0 ? w0 : w1);
       __syncwarp();
     }
     {

@@ -413,12 +413,12 @@ def test_full_lists_flush_and_match_oracle():
         assert not fails, "\n".join(fails[:10])
 
 
-def test_tile_records_overflow_taken_densely():
+def test_region_overflow_takes_the_cuda_core_path():
     """K = 300 components with nearly the same mean and variance: every
-    point keeps all 300 as candidates, more records than a tile's buffer
-    holds (256 a point on average), so the statistics evaluate those tiles
-    densely.  Steps from these parameters and from the oracle's next iterate
-    match the oracle."""
+    point keeps all 300 as candidates, more records than a warp's region of
+    the tile buffer holds (128 a point on average per column half), so those
+    rows take the CUDA-core path.  Steps from these parameters and from the
+    oracle's next iterate match the oracle."""
     rng = np.random.default_rng(41)
     N, D, K = 4000, 128, 300
     X = (rng.standard_normal((N, D)) * 0.5).astype(np.float16)
@@ -433,8 +433,11 @@ def test_tile_records_overflow_taken_densely():
     for step in range(2):
         ref = oracle_step(bits, datagen.F16, theta, wl.cov_type, opts=opts, want_lse=True)
         for want_lse in (False, True):
-            got = gpu_step(make_state(wl), Xd, theta, want_lse=want_lse, opts=opts)
+            st = make_state(wl)
+            got = gpu_step(st, Xd, theta, want_lse=want_lse, opts=opts)
             assert got["status"] == 0, got["status"]
+            if step == 0:
+                assert int(st.ws[8:12].cpu().numpy().view(np.uint32)[0]) > 0
             fails = parity.compare_step(got, ref, "dense step %d lse=%d" % (step, want_lse), 0.5)
             assert not fails, "\n".join(fails[:10])
             if want_lse:
