@@ -56,12 +56,19 @@ constexpr int kMaxScreenGrid = 1024;  // upper bound of tc_screen_grid (SM count
 // Tensor-core path: records {key, exact log joint} per 128-point tile, in
 // eight regions (one per epilogue warp and column half; a warp whose records
 // do not fit hands its rows to the CUDA-core path), and rows per slab (one
-// screening launch; its records are consumed before the next slab), so the
-// record buffer stays at 1 GiB: 128 records a point on average for K <= 128,
-// 256 beyond (the early EM iterations keep about a hundred candidates a
-// point on the 128-dimensional workloads).
-int rec_cap_for(int K) { return K <= 128 ? 16384 : 32768; }
-int64_t slab_rows_for(int K) { return K <= 128 ? (int64_t)1 << 20 : (int64_t)1 << 19; }
+// screening launch; its records are consumed before the next slab).  A tile
+// holds min(K/2, 256) records a point on average (at least 32): the early EM
+// iterations keep tens to about a hundred candidates a point on the
+// 128-dimensional workloads, and the buffer with its sorted copy stays below
+// an N x K fp32 matrix (and at 4 GiB for the largest K).
+int rec_cap_for(int K) {
+  const int per_row = K / 2 < 32 ? 32 : (K / 2 > 256 ? 256 : K / 2 / 8 * 8);
+  return 128 * per_row;
+}
+int64_t slab_rows_for(int K) {
+  (void)K;
+  return (int64_t)1 << 20;
+}
 
 bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
 size_t esize(int xdtype) { return xdtype == GMM_F32 ? 4 : 2; }
@@ -104,9 +111,11 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_lse = o;    o = align_up(o + sizeof(float) * (size_t)rows);
   const bool tc = tc_eligible(D, cov);
   {
-    // dense LSE blocks, or the tensor-core CTAs followed by the list blocks
+    // dense LSE blocks, or per slab the tensor-core CTAs and the components
+    // (single-candidate points), then the list blocks
     const size_t dense = (size_t)((rows + kLseRows - 1) / kLseRows);
-    const size_t tcl = (size_t)(kMaxScreenGrid + kListGrid);
+    const size_t nslabs = (size_t)((rows + slab_rows_for(K) - 1) / slab_rows_for(K));
+    const size_t tcl = tc ? nslabs * (size_t)(kMaxScreenGrid + K) + kListGrid : 0;
     W.off_llpart = o; o = align_up(o + sizeof(double) * (dense > tcl ? dense : tcl));
   }
   W.off_ll = o;     o = align_up(o + sizeof(double));
@@ -124,10 +133,11 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_flags = o;  o = align_up(o + sizeof(int32_t) * K);
   const int64_t slab_max = slab_rows_for(K);
   const int64_t slab = rows < slab_max ? rows : slab_max;
-  W.off_fb = o;     o = align_up(o + sizeof(uint32_t) * (size_t)(tc ? slab : rows));
+  // hand-over bitmap and row list: for all rows of the call (handled once, after the slabs)
+  W.off_fb = o;     o = align_up(o + sizeof(uint32_t) * (size_t)rows);
   const size_t slab_tiles = tc ? (size_t)((slab + 127) / 128) : 0;
-  W.off_fbm = o;    o = align_up(o + sizeof(uint32_t) * 4 * slab_tiles);
-  W.off_fbseg = o;  o = align_up(o + sizeof(uint32_t) * (tc ? fb_compact_segments(slab) : 0));
+  W.off_fbm = o;    o = align_up(o + sizeof(uint32_t) * 4 * (size_t)((rows + 127) / 128));
+  W.off_fbseg = o;  o = align_up(o + sizeof(uint32_t) * (tc ? fb_compact_segments(rows) : 0));
   W.off_rec = o;    o = align_up(o + sizeof(uint2) * slab_tiles * (size_t)rec_cap_for(K));
   W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * 8 * slab_tiles);
   W.off_sws = o;
@@ -198,10 +208,11 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
   double* llp = at<double>(ws, W.off_llpart);
   if (tc) {
     // Slabs of rows.  Per slab: screen on the tensor cores (exact LSE_n of
-    // the points and records of their candidates), the CUDA-core pass over
-    // the rows handed over (a warp's records past its region, non-finite
-    // input), the log-likelihood, statistics from the records and the
-    // CUDA-core statistics of the handed-over rows.
+    // the points and records of their candidates) and statistics from the
+    // records.  Then, once for all rows: the CUDA-core passes over the rows
+    // handed over (a warp's records past its region, non-finite input) and
+    // the log-likelihood from every partial (zeroed first, so unused slots
+    // count nothing).
     uint32_t* fb = at<uint32_t>(ws, W.off_fb);
     uint32_t* fbm = at<uint32_t>(ws, W.off_fbm);
     uint2* recs = at<uint2>(ws, W.off_rec);
@@ -210,39 +221,43 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
     double* lpart = part + (size_t)W.sp_parts * K * stat_width(D, cov);
     const int64_t slab_rows = slab_rows_for(K);
     const int rec_cap = rec_cap_for(K);
-    for (int64_t r0 = 0; r0 < rows; r0 += slab_rows) {
+    const int64_t nslabs = (rows + slab_rows - 1) / slab_rows;
+    const size_t lls = (size_t)kMaxScreenGrid + (size_t)K;  // log-likelihood partials per slab
+    const size_t nll = (size_t)nslabs * lls + kListGrid;
+    GMM_TRY(cudaMemsetAsync(llp, 0, sizeof(double) * nll, s));
+    for (int64_t si = 0; si < nslabs; ++si) {
+      const int64_t r0 = si * slab_rows;
       const int64_t sn = (rows - r0) < slab_rows ? (rows - r0) : slab_rows;
       const void* Xs = (const char*)X + (size_t)r0 * D * esize(xdtype);
       float* ls = lse + r0;
       const int acc = accumulate || r0 > 0;
-      const int g1 = tc_screen_grid(sn);
+      double* llp_s = llp + (size_t)si * lls;
       {
         GMM_PROF("tc_screen_kernel");
-        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, ls, want_lse ? 1 : 0, llp, 0,
-                          nullptr, nullptr, fbm, recs, tcnt, rec_cap, st, s));
+        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, ls, want_lse ? 1 : 0, llp_s, 0,
+                          nullptr, nullptr, fbm + (size_t)(r0 / 128) * 4, recs, tcnt, rec_cap, st,
+                          s));
       }
-      {
-        GMM_PROFN("fb_compact_kernel", 2);
-        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
-      }
-      {
-        GMM_PROF("lse_rows_kernel");
-        GMM_TRY(simt_lse_rows(Xs, xdtype, sn, D, K, cov, prep, ls, llp + g1, 0, nullptr,
-                              nullptr, st, fb, &st->fb_count, kListGrid, s));
-      }
-      {
-        GMM_PROF("ll_finalize_kernel");
-        GMM_TRY(launch_ll_finalize(llp, g1 + kListGrid, at<double>(ws, W.off_ll), acc, s));
-      }
-      {
-        GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, ls, tcnt, recs, rec_cap,
-                             at<char>(ws, W.off_sws), part, acc, at<double>(ws, W.off_ll), st, s));
-      }
-      {
-        GMM_PROF("stats_rows_kernel");
-        GMM_TRY(simt_stats_rows(Xs, xdtype, sn, D, K, cov, prep, ls, W.lp_parts, lpart, acc, fb,
-                                &st->fb_count, s));
-      }
+      GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, ls, tcnt, recs, rec_cap,
+                           at<char>(ws, W.off_sws), part, acc, llp_s + kMaxScreenGrid, st, s));
+    }
+    {
+      GMM_PROFN("fb_compact_kernel", 2);
+      GMM_TRY(fb_compact(fbm, rows, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
+    }
+    {
+      GMM_PROF("lse_rows_kernel");
+      GMM_TRY(simt_lse_rows(X, xdtype, rows, D, K, cov, prep, lse, llp + (size_t)nslabs * lls, 0,
+                            nullptr, nullptr, st, fb, &st->fb_count, kListGrid, s));
+    }
+    {
+      GMM_PROF("stats_rows_kernel");
+      GMM_TRY(simt_stats_rows(X, xdtype, rows, D, K, cov, prep, lse, W.lp_parts, lpart,
+                              accumulate, fb, &st->fb_count, s));
+    }
+    {
+      GMM_PROF("ll_finalize_kernel");
+      GMM_TRY(launch_ll_finalize(llp, (int64_t)nll, at<double>(ws, W.off_ll), accumulate, s));
     }
     return GMM_OK;
   }

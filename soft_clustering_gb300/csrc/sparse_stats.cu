@@ -52,7 +52,7 @@ constexpr int kMaxSparseK = 16384;
 
 struct SparseLayout {
   int64_t ntiles, nb, max_recs, max_chunks;
-  size_t off_counts, off_ktot, off_cstart, off_kstart, off_sorted, off_cpart, off_llk, bytes;
+  size_t off_counts, off_ktot, off_cstart, off_kstart, off_sorted, off_cpart, bytes;
   static SparseLayout make(int64_t rows, int D, int K, int rec_cap) {
     SparseLayout S;
     S.ntiles = (rows + kTile - 1) / kTile;
@@ -66,7 +66,6 @@ struct SparseLayout {
     S.off_kstart = o; o = align_up(o + sizeof(uint32_t) * (size_t)(K + 1));
     S.off_sorted = o; o = align_up(o + sizeof(uint2) * (size_t)S.max_recs);
     S.off_cpart = o;  o = align_up(o + sizeof(float) * (size_t)S.max_chunks * (2 + 3 * D));
-    S.off_llk = o;    o = align_up(o + sizeof(double) * (size_t)K);
     S.bytes = o;
     return S;
   }
@@ -514,13 +513,14 @@ bool sparse_stats_supported(int K) { return K <= kMaxSparseK; }
 
 // Diagonal / isotropic statistics (the partial layout is the same for both;
 // the isotropic M-step averages the diagonal) into ONE partial slot, part;
-// adds the log-likelihood of the single-candidate points to *ll.
+// llk[k] (K doubles) receives the log-likelihood of component k's
+// single-candidate points.
 // prepared: the block written for this call's parameters (its mean array is
 // the centre c).  accumulate: continue the partial of an earlier call.
 // sws: sparse_stats_ws_bytes(N, D, K, rec_cap) bytes, 256-byte aligned.
 cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
                          int cov, const float* lse, const uint32_t* tile_cnt, const uint2* recs,
-                         int rec_cap, void* sws, double* part, int accumulate, double* ll,
+                         int rec_cap, void* sws, double* part, int accumulate, double* llk,
                          DeviceStatus* st, cudaStream_t s) {
   if (K > kMaxSparseK || (D != 64 && D != 128)) return cudaErrorInvalidValue;
   const SparseLayout S = SparseLayout::make(N, D, K, rec_cap);
@@ -603,7 +603,6 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
 
   const float* bias_c = at<float>(prepared, L.off_c);
   const float* prec = at<float>(prepared, L.off_prec);
-  double* llk = at<double>(sws, S.off_llk);
   const bool iso = cov == GMM_COV_ISO;
   {
     ProfScope prof_merge("rec_merge_kernel", s);
@@ -615,9 +614,7 @@ cudaError_t sparse_stats(const void* X, int xdtype, int64_t N, int D, int K, con
                                             accumulate);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // the single-candidate points' log-likelihood joins the total
-  ProfScope prof_ll("ll_finalize_kernel", s);
-  return launch_ll_finalize(llk, K, ll, 1, s);
+  return cudaSuccess;
 }
 
 }  // namespace gmm

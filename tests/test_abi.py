@@ -100,6 +100,6 @@ def test_host_streaming_workspace_is_bounded_by_the_chunk(lib):
         small = G.gmm_workspace_bytes_host(chunk, D, K, cov, G.GMM_BF16, chunk)
         huge = G.gmm_workspace_bytes_host(10 ** 10, D, K, cov, G.GMM_BF16, chunk)  # 2.5 TB of X at D=128
         assert 0 < small == huge, (small, huge)
-        assert huge < 10 ** 10 * D * 2 / 1000
+        assert huge < 8 << 30  # a few GiB for 2.5 TB of X
         assert G.gmm_workspace_bytes_host(10 ** 10, D, K, cov, G.GMM_BF16, 2 * chunk) > huge
 
