@@ -430,10 +430,12 @@ def test_region_overflow_takes_the_cuda_core_path():
     oracle's next iterate match the oracle."""
     rng = np.random.default_rng(41)
     N, D, K = 4000, 128, 300
-    X = (rng.standard_normal((N, D)) * 0.5).astype(np.float16)
+    # data and means away from the origin, so that every mean entry is of
+    # the order of the mean array's scale (the tolerance's reference)
+    X = (1.0 + rng.standard_normal((N, D)) * 0.5).astype(np.float16)
     bits = X.view(np.uint16)
     pi = np.full(K, 1.0 / K, dtype=np.float32)
-    mu = (rng.standard_normal((K, D)) * 0.01).astype(np.float32)
+    mu = (1.0 + rng.standard_normal((K, D)) * 0.01).astype(np.float32)
     var = np.full((K, D), 0.25, dtype=np.float32) * rng.uniform(0.99, 1.01, (K, 1)).astype(np.float32)
     opts = dict(var_floor=1e-6, min_s0=0.5)
     wl = datagen.Workload("dense", 0, N, D, K, datagen.F16, datagen.COV_DIAG, 1, 0, {})
