@@ -87,9 +87,10 @@ typedef struct {
   int flags;
 } gmm_opts;
 
-/* Defaults: ridge_rel 0, var_floor 0, min_s0 0.5, flags 0.  (A component
- * holding less than half of one point's worth of responsibility has no mean
- * the data determine: it is a weighted average of a few far tail points.) */
+/* Defaults: ridge_rel 0, var_floor 0, min_s0 0.5, flags 0.  (Below s0 = 1/2
+ * every point's responsibility for the component is below 1/2 - each point
+ * belongs more to the rest of the mixture - so the updated mean would be an
+ * average of other components' tail points.) */
 gmm_opts gmm_default_opts(void);
 
 /* Human-readable name of a status code (static string). */
