@@ -65,11 +65,8 @@ def measured_peaks():
 # ---------------------------------------------------------------- work model
 
 def slab_rows(wl):
-    """Rows per screening launch of the tensor-core path (the library's rule:
-    its record buffer stays at 1 GiB)."""
-    if wl.m:
-        return 1 << 19 if wl.K > 128 else 1 << 20
-    return 1 << 19 if wl.K > 128 else 1 << 20
+    """Rows per screening launch of the tensor-core path (the library's rule)."""
+    return 1 << 20
 
 
 def tc_path(wl):
