@@ -1,0 +1,428 @@
+// dense_rows.cu - exact log-sum-exp and sufficient statistics of the points
+// whose candidate lists overflowed in the screening kernel.
+//
+// In the first EM iterations from theta_0 a point keeps tens to hundreds of
+// components within 40 nats of its best log joint (every one of them is
+// evaluated exactly: "low-precision GMM operator" notes, sec. 3.2 / 4.2,
+// fp32 log-densities and log-sum-exp; Flash-GMM summary, Method: statistics
+// of all components of a tile).  Evaluated one pair at a time inside the
+// screening kernel, each pair would fetch its component's mean and inverse
+// variances (1 KB at D = 128) from L2.  Here the screening kernel leaves such
+// points with their candidate masks (one bit per component, the exact 40-nat
+// window of the rigorous screen), and three kernels take them with the
+// parameters staged in shared memory:
+//   dense_lse     block (mask chunk of 128 components, partition): a warp
+//                 per point, its four groups of eight lanes taking the
+//                 chunk's candidates in turn, each evaluated in the centred
+//                 fp32 form sum_d w_d (x_d - mu_d)^2 (lane: D/8 dimensions,
+//                 then a butterfly sum over the group), the groups' running
+//                 max and sum combined into the point's over the chunk
+//   dense_combine LSE_n from the chunks' (max, sum), the log-likelihood
+//   dense_stats   block (group of 8192/D components, partition): a thread
+//                 per (component, 32 dimensions) keeps the component's sums
+//                 s0, sum g (x - mu) and sum g (x - mu)^2 in registers over
+//                 the block's points, g = exp(l - LSE_n) recomputed for every
+//                 candidate; at the end they join the block's fp64 partial
+//                 slot with the pairwise update of Chan, Golub and LeVeque.
+// Every sum has a fixed order, so the results are the same on every run.
+#include <math.h>
+
+#include "gmm_internal.cuh"
+
+namespace gmm {
+namespace {
+
+constexpr int kChunk = kTcChunk;  // components per mask chunk
+constexpr int kThreads = 256;
+constexpr int kCombineGrid = 256;  // blocks of the combine kernel (log-likelihood partials)
+constexpr int kRowsPerTile = 64;   // points per tile of the statistics kernel
+
+template <int XT>
+__device__ __forceinline__ void load_x_vec(const void* X, size_t e0, int n, float* v) {
+  if constexpr (XT == GMM_F32) {
+    const float* p = static_cast<const float*>(X) + e0;
+    if (n == 4) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+      const float2 q = __ldg(reinterpret_cast<const float2*>(p));
+      v[0] = q.x; v[1] = q.y;
+    }
+  } else {
+    const uint16_t* p = static_cast<const uint16_t*>(X) + e0;
+    uint32_t u[2];
+    if (n == 4) {
+      const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+      u[0] = q.x; u[1] = q.y;
+    } else {
+      u[0] = __ldg(reinterpret_cast<const unsigned int*>(p));
+    }
+    for (int i = 0; i < n / 2; ++i) {
+      float2 f;
+      if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+      v[2 * i] = f.x; v[2 * i + 1] = f.y;
+    }
+  }
+}
+
+struct DenseArgs {
+  const void* X;            // the slab's rows
+  const uint32_t* rows;     // points left to these kernels (slab rows, ascending)
+  const uint32_t* count;    // how many (on the device)
+  int D, K, nch;
+  const float* mu;          // prepared means [K][D]
+  const float* prec;        // prepared inverse variances [K][D] (iso: [K])
+  const float* bias;        // prepared log pi - log|S|/2 - (D/2) log 2 pi [K]
+  bool iso;
+  const uint32_t* cmask;    // [slab rows][nch][4] candidate masks
+  float2* part;             // [points][nch] (max, sum) per chunk
+  float* lse;               // the slab's LSE_n
+  double* ll_part;          // [kCombineGrid]
+  double* stat;             // [P][K][1 + 2D] fp64 partials
+  int accumulate;
+  DeviceStatus* st;
+};
+
+template <int D, int XT>
+__global__ void __launch_bounds__(kThreads) dense_lse_kernel(const DenseArgs a) {
+  constexpr int CPL = D / 32;  // 4-dimension pieces per lane: lane g of a group of eight
+                               // holds dimensions 4 (g + 8 i) .. + 3, i < CPL
+  constexpr int RS = D + 4;    // padded table row (floats)
+  extern __shared__ __align__(16) float smf[];
+  float* s_mu = smf;                 // [128][RS]
+  float* s_w = s_mu + kChunk * RS;   // [128][RS]
+  float* s_c = s_w + kChunk * RS;    // [128]
+  const uint32_t n = *a.count;
+  if (n == 0) return;
+  const int j = blockIdx.x, P = gridDim.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane >> 3, gl = lane & 7;
+  for (int i = tid; i < kChunk * D; i += kThreads) {
+    const int kr = i / D, d = i % D, k = j * kChunk + kr;
+    float m = 0.f, w = 0.f;
+    if (k < a.K) {
+      m = __ldg(a.mu + (size_t)k * D + d);
+      w = a.iso ? __ldg(a.prec + k) : __ldg(a.prec + (size_t)k * D + d);
+    }
+    s_mu[kr * RS + d] = m;
+    s_w[kr * RS + d] = w;
+  }
+  for (int i = tid; i < kChunk; i += kThreads) {
+    const int k = j * kChunk + i;
+    s_c[i] = k < a.K ? __ldg(a.bias + k) : -INFINITY;
+  }
+  __syncthreads();
+  // a warp per point; its four groups of eight lanes take the point's
+  // candidates in turn (candidate t of the chunk to group t % 4)
+  for (uint32_t i = blockIdx.y * (kThreads / 32) + warp; i < n; i += P * (kThreads / 32)) {
+    const uint32_t row = a.rows[i];
+    float x[CPL][4];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) load_x_vec<XT>(a.X, (size_t)row * D + 4 * (gl + 8 * c), 4, x[c]);
+    const uint4 mw = __ldg(reinterpret_cast<const uint4*>(a.cmask + ((size_t)row * a.nch + j) * 4));
+    uint32_t bits[4] = {mw.x, mw.y, mw.z, mw.w};
+    int wi = 0;
+    // the next candidate column (in column order), -1 when none is left
+    auto next_col = [&]() -> int {
+      while (wi < 4 && bits[wi] == 0u) ++wi;
+      if (wi == 4) return -1;
+      const int c = wi * 32 + __ffs(bits[wi]) - 1;
+      bits[wi] &= bits[wi] - 1u;
+      return c;
+    };
+    float mx = -INFINITY, sum = 0.f;
+    for (;;) {
+      const int c0 = next_col(), c1 = next_col(), c2 = next_col(), c3 = next_col();
+      if (c0 < 0) break;
+      const int col = grp == 0 ? c0 : (grp == 1 ? c1 : (grp == 2 ? c2 : c3));
+      float acc = 0.f;
+      if (col >= 0) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const float4 m4 = *reinterpret_cast<const float4*>(s_mu + col * RS + 4 * (gl + 8 * c));
+          const float4 w4 = *reinterpret_cast<const float4*>(s_w + col * RS + 4 * (gl + 8 * c));
+          const float u0 = x[c][0] - m4.x, u1 = x[c][1] - m4.y;
+          const float u2 = x[c][2] - m4.z, u3 = x[c][3] - m4.w;
+          acc = fmaf(u0 * u0, w4.x, acc);
+          acc = fmaf(u1 * u1, w4.y, acc);
+          acc = fmaf(u2 * u2, w4.z, acc);
+          acc = fmaf(u3 * u3, w4.w, acc);
+        }
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (col >= 0) {
+        const float l = s_c[col] - 0.5f * acc;
+        // the group's running log-sum-exp
+        if (l > mx) {
+          sum = sum * expf(mx - l) + 1.f;
+          mx = l;
+        } else {
+          sum += expf(l - mx);
+        }
+      }
+    }
+    // the four groups' partial sums, combined in group order
+    float gm[4], gs[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      gm[q] = __shfl_sync(0xffffffffu, mx, q * 8);
+      gs[q] = __shfl_sync(0xffffffffu, sum, q * 8);
+    }
+    if (lane == 0) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (gs[q] > 0.f) M = fmaxf(M, gm[q]);
+      float S = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (gs[q] > 0.f) S += gs[q] * expf(gm[q] - M);
+      a.part[(size_t)i * a.nch + j] = make_float2(M, S);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) dense_combine_kernel(const DenseArgs a) {
+  __shared__ double red[kThreads / 32];
+  const uint32_t n = *a.count;
+  double acc = 0.0;
+  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < n; i += gridDim.x * kThreads) {
+    const float2* p = a.part + (size_t)i * a.nch;
+    float M = -INFINITY;
+    for (int j = 0; j < a.nch; ++j)
+      if (p[j].y > 0.f) M = fmaxf(M, p[j].x);
+    float S = 0.f;
+    for (int j = 0; j < a.nch; ++j)
+      if (p[j].y > 0.f) S += p[j].y * expf(p[j].x - M);
+    const float l = M + logf(S);
+    if (!isfinite(l)) raise_status(a.st, GMM_ERR_NONFINITE);
+    a.lse[a.rows[i]] = l;
+    acc += (double)l;
+  }
+  acc = warp_sum(acc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+    a.ll_part[blockIdx.x] = s;
+  }
+}
+
+// 32 dimensions per thread, D/32 threads per component, 256 threads: a block
+// takes 8192/D components.
+template <int D>
+struct DsShape {
+  static constexpr int TPC = D / 32;
+  static constexpr int CPB = kThreads / TPC;
+  static constexpr int WPR = CPB / 32;  // mask words of a block's components per point
+};
+
+template <int D, int XT>
+__global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArgs a) {
+  using SH = DsShape<D>;
+  constexpr int TPC = SH::TPC, CPB = SH::CPB, WPR = SH::WPR, F = 1 + 2 * D;
+  constexpr int ESZ = XT == GMM_F32 ? 4 : 2;
+  constexpr int ROWB = D * ESZ;
+  constexpr int C16 = ROWB / 16;
+  constexpr int TC16 = 32 * ESZ / 16;  // 16-byte chunks of a thread's dimensions
+  constexpr int VPC = 16 / ESZ;        // values per chunk
+  __shared__ __align__(16) unsigned char xs[kRowsPerTile * ROWB];
+  __shared__ float lse_t[kRowsPerTile];
+  __shared__ uint32_t cm[CPB][kRowsPerTile / 32];
+  const uint32_t n = *a.count;
+  if (n == 0 && a.accumulate) return;  // nothing to add to the partials
+  const int tid = threadIdx.x;
+  const int kl = tid / TPC, h = tid % TPC;
+  const int g = blockIdx.x, p = blockIdx.y, P = gridDim.y;
+  const int k = g * CPB + kl;
+  const bool kin = k < a.K;
+  const int d0 = h * 32;
+  const unsigned grp_mask = ((1u << TPC) - 1u) << ((tid & 31) & ~(TPC - 1));
+  const float ck = kin ? __ldg(a.bias + k) : -INFINITY;
+  float mu[32], w[32], s1[32], s2[32], s0 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    mu[i] = kin ? __ldg(a.mu + (size_t)k * D + d0 + i) : 0.f;
+    w[i] = kin ? (a.iso ? __ldg(a.prec + k) : __ldg(a.prec + (size_t)k * D + d0 + i)) : 0.f;
+    s1[i] = s2[i] = 0.f;
+  }
+  // the block's components are mask words [wk0, wk0 + WPR) of mask chunk j
+  const int j = (g * CPB) / kChunk, wk0 = ((g * CPB) % kChunk) / 32;
+  const uint32_t ntiles = (n + kRowsPerTile - 1) / kRowsPerTile;
+  for (uint32_t t = p; t < ntiles; t += P) {
+    __syncthreads();
+    const uint32_t i0 = t * kRowsPerTile;
+    const int rows = (int)min((uint32_t)kRowsPerTile, n - i0);
+    for (int i = tid; i < CPB * (kRowsPerTile / 32); i += kThreads) (&cm[0][0])[i] = 0u;
+    for (int i = tid; i < rows * C16; i += kThreads) {
+      const int r = i / C16, q = i % C16;
+      const uint32_t row = a.rows[i0 + r];
+      *reinterpret_cast<uint4*>(xs + r * ROWB + ((q ^ (r & 7)) << 4)) =
+          __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.X) +
+                                               (size_t)row * ROWB) + q);
+    }
+    for (int i = tid; i < kRowsPerTile; i += kThreads)
+      lse_t[i] = i < rows ? a.lse[a.rows[i0 + i]] : 0.f;
+    __syncthreads();
+    // candidate masks, point-major -> component-major
+    for (int i = tid; i < rows * WPR; i += kThreads) {
+      const int r = i / WPR, wq = i % WPR;
+      uint32_t bits = __ldg(a.cmask + ((size_t)a.rows[i0 + r] * a.nch + j) * 4 + wk0 + wq);
+      while (bits) {
+        const int c = wq * 32 + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        atomicOr(&cm[c][r >> 5], 1u << (r & 31));
+      }
+    }
+    __syncthreads();
+    if (!kin || ck == -INFINITY) continue;
+#pragma unroll 1
+    for (int rw = 0; rw < kRowsPerTile / 32; ++rw) {
+      uint32_t m = cm[kl][rw];
+      while (m) {
+        const int r = rw * 32 + __ffs(m) - 1;
+        m &= m - 1u;
+        float xv[32];
+#pragma unroll
+        for (int c16 = 0; c16 < TC16; ++c16) {
+          const uint4 u = *reinterpret_cast<const uint4*>(
+              xs + r * ROWB + (((d0 * ESZ / 16 + c16) ^ (r & 7)) << 4));
+          if constexpr (XT == GMM_F32) {
+            xv[c16 * 4 + 0] = __uint_as_float(u.x); xv[c16 * 4 + 1] = __uint_as_float(u.y);
+            xv[c16 * 4 + 2] = __uint_as_float(u.z); xv[c16 * 4 + 3] = __uint_as_float(u.w);
+          } else {
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float2 f;
+              if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
+              else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
+              xv[c16 * VPC + 2 * q] = f.x; xv[c16 * VPC + 2 * q + 1] = f.y;
+            }
+          }
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float u = xv[i] - mu[i];
+          acc[i & 3] = fmaf(u * u, w[i], acc[i & 3]);
+        }
+        float d2 = (acc[0] + acc[2]) + (acc[1] + acc[3]);
+#pragma unroll
+        for (int o = 1; o < TPC; o <<= 1) d2 += __shfl_xor_sync(grp_mask, d2, o);
+        const float gm = expf(ck - 0.5f * d2 - lse_t[r]);
+        s0 += gm;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float y = xv[i] - mu[i];
+          const float gy = gm * y;
+          s1[i] += gy;
+          s2[i] = fmaf(gy, y, s2[i]);
+        }
+      }
+    }
+  }
+  // this block's sums join slot p's fp64 partial [S0 | S1 about mu | M2 about the mean]
+  if (kin) {
+    double* o = a.stat + ((size_t)p * a.K + k) * F;
+    const double b0 = (double)s0;
+    const double S0o = a.accumulate ? o[0] : 0.0;
+    const double S0 = S0o + b0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int d = d0 + i;
+      const double b1 = (double)s1[i];
+      const double m2b = b0 > 0.0 ? (double)s2[i] - b1 * b1 / b0 : 0.0;
+      double S1 = b1, M2 = m2b;
+      if (a.accumulate) {
+        const double o1 = o[1 + d], om = o[1 + D + d];
+        S1 = o1 + b1;
+        M2 = om + m2b;
+        if (S0o > 0.0 && b0 > 0.0) {
+          const double dm = b1 / b0 - o1 / S0o;
+          M2 += dm * dm * (S0o * b0 / S0);
+        }
+      }
+      o[1 + d] = S1;
+      o[1 + D + d] = M2;
+    }
+    __syncwarp(grp_mask);  // every thread of the component has read o[0] before it changes
+    if (h == 0) o[0] = S0;
+  }
+}
+
+template <int D, int XT>
+cudaError_t run_dense(const DenseArgs& a, int pa, int pb, cudaStream_t s) {
+  const size_t smem_a = sizeof(float) * ((size_t)2 * kChunk * (D + 4) + kChunk);
+  cudaError_t e = cudaFuncSetAttribute(dense_lse_kernel<D, XT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a);
+  if (e != cudaSuccess) return e;
+  {
+    ProfScope prof("dense_lse_kernel", s);
+    dense_lse_kernel<D, XT><<<dim3(a.nch, pa), kThreads, smem_a, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    ProfScope prof("dense_combine_kernel", s);
+    dense_combine_kernel<<<kCombineGrid, kThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    ProfScope prof("dense_stats_kernel", s);
+    const int ng = (a.K + DsShape<D>::CPB - 1) / DsShape<D>::CPB;
+    dense_stats_kernel<D, XT><<<dim3(ng, pb), kThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int dense_ll_parts() { return kCombineGrid; }
+
+// Partitions of the dense statistics blocks (fixed by D and K: the order of
+// the sums never depends on the device or on N).
+int dense_stat_parts(int D, int K) {
+  const int cpb = kThreads / (D / 32);
+  const int ng = (K + cpb - 1) / cpb;
+  const int p = (152 + ng - 1) / ng;
+  return p < 1 ? 1 : p;
+}
+
+// The points rows[0 .. *count) of a slab (X: the slab's rows): LSE_n into
+// lse, the log-likelihood into ll_part[0 .. dense_ll_parts()), statistics into
+// partial slots [0, dense_stat_parts(D, K)) of stat.  part: scratch of
+// (slab rows) x nch float2.
+cudaError_t dense_rows(const void* X, int xdtype, int D, int K, int cov, const void* prepared,
+                       const uint32_t* rows, const uint32_t* count, const uint32_t* cmask,
+                       float2* part, float* lse, double* ll_part, double* stat, int accumulate,
+                       DeviceStatus* st, cudaStream_t s) {
+  const PreparedLayout L = PreparedLayout::make(D, K, cov);
+  DenseArgs a;
+  a.X = X; a.rows = rows; a.count = count; a.D = D; a.K = K;
+  a.nch = (K + kChunk - 1) / kChunk;
+  a.mu = at<float>(prepared, L.off_mu);
+  a.prec = at<float>(prepared, L.off_prec);
+  a.bias = at<float>(prepared, L.off_c);
+  a.iso = cov == GMM_COV_ISO;
+  a.cmask = cmask; a.part = part; a.lse = lse; a.ll_part = ll_part; a.stat = stat;
+  a.accumulate = accumulate; a.st = st;
+  const int pa = (152 * 2 + a.nch - 1) / a.nch;
+  const int pb = dense_stat_parts(D, K);
+  if (D == 128) {
+    if (xdtype == GMM_F16) return run_dense<128, GMM_F16>(a, pa, pb, s);
+    if (xdtype == GMM_BF16) return run_dense<128, GMM_BF16>(a, pa, pb, s);
+    return run_dense<128, GMM_F32>(a, pa, pb, s);
+  }
+  if (D == 64) {
+    if (xdtype == GMM_F16) return run_dense<64, GMM_F16>(a, pa, pb, s);
+    if (xdtype == GMM_BF16) return run_dense<64, GMM_BF16>(a, pa, pb, s);
+    return run_dense<64, GMM_F32>(a, pa, pb, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gmm

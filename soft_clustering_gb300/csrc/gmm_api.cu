@@ -22,8 +22,15 @@ cudaError_t simt_lse_rows(const void* X, int xdtype, int64_t N, int D, int K, in
                           const uint32_t* row_count, int grid, cudaStream_t s);
 cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                       const void* prepared, int mode, float* lse, int want_lse, double* ll_part,
-                      int m, int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
-                      uint32_t* tile_cnt, int rec_cap, DeviceStatus* st, cudaStream_t s);
+                      int m, int32_t* ids, float* gamma, uint32_t* fb_mask, uint32_t* cmask,
+                      uint32_t* dmask, uint2* recs, uint32_t* tile_cnt, int rec_cap,
+                      DeviceStatus* st, cudaStream_t s);
+int dense_ll_parts();
+int dense_stat_parts(int D, int K);
+cudaError_t dense_rows(const void* X, int xdtype, int D, int K, int cov, const void* prepared,
+                       const uint32_t* rows, const uint32_t* count, const uint32_t* cmask,
+                       float2* part, float* lse, double* ll_part, double* stat, int accumulate,
+                       DeviceStatus* st, cudaStream_t s);
 int tc_screen_grid(int64_t N);
 cudaError_t fb_compact(const uint32_t* fb_mask, int64_t N, uint32_t* rows, uint32_t* count,
                        uint32_t* segcnt, cudaStream_t s);
@@ -87,10 +94,12 @@ int stat_parts(int64_t N, int D, int K, int cov) {
 
 struct WsLayout {
   size_t off_status, off_prep, off_lse, off_llpart, off_ll, off_part, off_flags, off_fb,
-      off_fbm, off_fbseg, off_rec, off_tcnt, off_sws, off_stage, bytes;
+      off_fbm, off_fbseg, off_rec, off_tcnt, off_sws, off_cmask, off_dmask, off_drows, off_dpart,
+      off_stage, bytes;
   int parts;          // statistics partials of the CUDA-core path
   int sp_parts;       // tensor-core path: the records' partial (1) ...
-  int lp_parts;       // ... followed by those of the row-list pass
+  int lp_parts;       // ... followed by those of the row-list pass ...
+  int dp_parts;       // ... and those of the dense-row kernels (streamed parameters)
   int64_t lse_rows;
 };
 
@@ -115,19 +124,22 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
     // (single-candidate points), then the list blocks
     const size_t dense = (size_t)((rows + kLseRows - 1) / kLseRows);
     const size_t nslabs = (size_t)((rows + slab_rows_for(K) - 1) / slab_rows_for(K));
-    const size_t tcl = tc ? nslabs * (size_t)(kMaxScreenGrid + K) + kListGrid : 0;
+    const size_t tcl =
+        tc ? nslabs * (size_t)(kMaxScreenGrid + K + dense_ll_parts()) + kListGrid : 0;
     W.off_llpart = o; o = align_up(o + sizeof(double) * (dense > tcl ? dense : tcl));
   }
   W.off_ll = o;     o = align_up(o + sizeof(double));
   W.parts = stat_parts(rows, D, K, cov);
-  W.sp_parts = W.lp_parts = 0;
+  W.sp_parts = W.lp_parts = W.dp_parts = 0;
   int slots = W.parts;
+  const bool streamed = tc && !tc_fold((K + kTcChunk - 1) / kTcChunk);
   if (tc) {
     W.sp_parts = 1;
     const int kc = simt_stat_chunk(D, cov);
     const int chunks = (K + kc - 1) / kc;
     W.lp_parts = (kListGrid + chunks - 1) / chunks;
-    if (W.sp_parts + W.lp_parts > slots) slots = W.sp_parts + W.lp_parts;
+    W.dp_parts = streamed ? dense_stat_parts(D, K) : 0;
+    if (W.sp_parts + W.lp_parts + W.dp_parts > slots) slots = W.sp_parts + W.lp_parts + W.dp_parts;
   }
   W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)slots * K * stat_width(D, cov));
   W.off_flags = o;  o = align_up(o + sizeof(int32_t) * K);
@@ -142,6 +154,13 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * 8 * slab_tiles);
   W.off_sws = o;
   o = align_up(o + (tc ? sparse_stats_ws_bytes(slab, D, K, rec_cap_for(K)) : 0));
+  // streamed parameters: every row's candidate masks, the rows left to the
+  // dense-row kernels (bitmap, list) and their per-chunk log-sum-exp
+  const size_t nch = (size_t)((K + kTcChunk - 1) / kTcChunk);
+  W.off_cmask = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * 4 * nch * (size_t)slab : 0));
+  W.off_dmask = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * 4 * slab_tiles : 0));
+  W.off_drows = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * (size_t)slab : 0));
+  W.off_dpart = o;  o = align_up(o + (streamed ? sizeof(float2) * nch * (size_t)slab : 0));
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
@@ -222,8 +241,12 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
     const int64_t slab_rows = slab_rows_for(K);
     const int rec_cap = rec_cap_for(K);
     const int64_t nslabs = (rows + slab_rows - 1) / slab_rows;
-    const size_t lls = (size_t)kMaxScreenGrid + (size_t)K;  // log-likelihood partials per slab
+    // log-likelihood partials per slab: screening blocks, components
+    // (single-candidate points), dense-row blocks
+    const size_t lls = (size_t)kMaxScreenGrid + (size_t)K + (size_t)dense_ll_parts();
     const size_t nll = (size_t)nslabs * lls + kListGrid;
+    const bool streamed = W.dp_parts > 0;
+    double* dpart = lpart + (size_t)W.lp_parts * K * stat_width(D, cov);
     GMM_TRY(cudaMemsetAsync(llp, 0, sizeof(double) * nll, s));
     for (int64_t si = 0; si < nslabs; ++si) {
       const int64_t r0 = si * slab_rows;
@@ -232,14 +255,26 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
       float* ls = lse + r0;
       const int acc = accumulate || r0 > 0;
       double* llp_s = llp + (size_t)si * lls;
+      uint32_t* dmask = streamed ? at<uint32_t>(ws, W.off_dmask) : nullptr;
+      uint32_t* cmask = streamed ? at<uint32_t>(ws, W.off_cmask) : nullptr;
       {
         GMM_PROF("tc_screen_kernel");
         GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, ls, want_lse ? 1 : 0, llp_s, 0,
-                          nullptr, nullptr, fbm + (size_t)(r0 / 128) * 4, recs, tcnt, rec_cap, st,
-                          s));
+                          nullptr, nullptr, fbm + (size_t)(r0 / 128) * 4, cmask, dmask, recs,
+                          tcnt, rec_cap, st, s));
       }
       GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, ls, tcnt, recs, rec_cap,
                            at<char>(ws, W.off_sws), part, acc, llp_s + kMaxScreenGrid, st, s));
+      if (streamed) {
+        uint32_t* drows = at<uint32_t>(ws, W.off_drows);
+        {
+          GMM_PROFN("fb_compact_kernel", 2);
+          GMM_TRY(fb_compact(dmask, sn, drows, &st->dense_count, at<uint32_t>(ws, W.off_fbseg), s));
+        }
+        GMM_TRY(dense_rows(Xs, xdtype, D, K, cov, prep, drows, &st->dense_count, cmask,
+                           at<float2>(ws, W.off_dpart), ls, llp_s + kMaxScreenGrid + K, dpart, acc,
+                           st, s));
+      }
     }
     {
       GMM_PROFN("fb_compact_kernel", 2);
@@ -279,7 +314,9 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
 }
 
 // Partials the M-step merges for the path taken.
-int mstep_parts(const WsLayout& W, bool tc) { return tc ? W.sp_parts + W.lp_parts : W.parts; }
+int mstep_parts(const WsLayout& W, bool tc) {
+  return tc ? W.sp_parts + W.lp_parts + W.dp_parts : W.parts;
+}
 
 // Library-owned copy stream and events of the host path (one set per device).
 struct HostPathRes {
@@ -522,7 +559,7 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
       {
         GMM_PROF("tc_screen_kernel");
         GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prepared, 1, ls, 0, nullptr, m, is, gs, fbm,
-                          nullptr, nullptr, 0, st, s));
+                          nullptr, nullptr, nullptr, nullptr, 0, st, s));
       }
       {
         GMM_PROFN("fb_compact_kernel", 2);

@@ -40,7 +40,8 @@ struct DeviceStatus {
   int32_t code;        // gmm_status of the first device-side failure (0 = none)
   int32_t detail;      // OR of (1 << gmm_status) for every failure seen
   uint32_t fb_count;   // rows the tensor-core kernel handed to the CUDA-core path
-  int32_t pad[61];
+  uint32_t dense_count;  // rows whose candidates went to the dense-row kernels (last slab)
+  int32_t pad[60];
 };
 
 __device__ inline void raise_status(DeviceStatus* st, int code) {

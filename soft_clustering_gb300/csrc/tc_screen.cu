@@ -83,6 +83,9 @@ struct ScreenArgs {
   float* gamma;          // [N*m] (assign)
   uint32_t* fb_mask;     // assign: [tiles * 4] bit r % 32 of word n / 32: row n
                          // handed to the CUDA-core path
+  uint32_t* cmask;       // EM, streamed parameters: [rows][chunks][4] candidate masks
+                         // (word 2h + b: columns 64h + 32b .. + 31 of the chunk)
+  uint32_t* dmask;       // EM, streamed parameters: [tiles * 4] rows left to the dense-row kernels
   uint2* recs;           // EM: [tiles][rec_cap] records {key, exact log joint}
   uint32_t* tile_cnt;    // EM: [tiles] records of the tile (> rec_cap: they did not fit)
   int rec_cap;
@@ -912,10 +915,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
     // warp w reads lane quarter q = w % 4 and column half h = w / 4 of every
     // chunk.  Each tile is contracted twice: pass 0 finds the best lower bound
     // (both halves combined at barrier A), pass 1 collects every column whose
-    // upper bound reaches it minus 40 nats; a full list is refined, folded into
-    // the row's running log-sum-exp and written out (a flush), and collection
-    // goes on.  Barrier B: both halves' record counts (singles, overflow);
-    // barrier C: both halves' partial log-sum-exp.
+    // upper bound reaches it minus 40 nats, and writes every row's candidate
+    // masks.  A row with more candidates than a half's list holds is left to
+    // the dense-row kernels, which evaluate its candidates from the masks with
+    // the parameters staged in shared memory.  Barrier B: both halves' counts
+    // (singles, overflow, left rows); barrier C: both halves' partial
+    // log-sum-exp.
     const int q = warp & 3, h = warp >> 2;
     const int r = q * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -938,10 +943,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       const bool rowok = valid && isfinite(rn);
       float ref = -INFINITY, thr = -INFINITY;
       float mx = -INFINITY, ssum = 0.f;
-      int cnt = 0, nrec = 0;
-      bool flushed = false, ok = true;
+      int cnt = 0;
+      bool deferred = false, ok = true;
       uint32_t wpos = 0;
       uint2* region = a.recs + (size_t)tile * a.rec_cap + (size_t)(2 * q + h) * rcap;
+      uint32_t* rmask = a.cmask + (size_t)(tile * kBM + r) * nch * 4 + 2 * h;
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) {
           xref[h * kBM + r] = ref;
@@ -1012,51 +1018,48 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&bar[T_EMPTY + buf]);
           if (pass == 1) {
+            // the row's masks (read back only for rows left to the dense-row kernels)
+            if (valid) *reinterpret_cast<uint2*>(rmask + j * 4) = make_uint2(pms[0], pms[1]);
 #pragma unroll
             for (int b = 0; b < kHalf / 32; ++b) {
-              uint32_t pm = pms[b];
+              uint32_t pm = deferred ? 0u : pms[b];
               const int kb = j * kBN + h * kHalf + b * 32;
-              for (;;) {
-                while (pm && cnt < kCS) {
-                  const int kk = __ffs(pm) - 1;
-                  pm &= pm - 1u;
+              while (pm) {
+                const int kk = __ffs(pm) - 1;
+                pm &= pm - 1u;
+                if (cnt < kCS) {
                   ck[cnt * kBM + r] = (uint16_t)(kb + kk);
                   ++cnt;
+                } else {
+                  deferred = true;  // the list is full: the row goes to the dense-row kernels
+                  pm = 0u;
                 }
-                if (!__any_sync(0xffffffffu, pm != 0u)) break;
-                // a list is full: refine the warp's lists, fold, write records
-                refine_lists<D, XT>(a.X, tile, q, lane, cnt, cub, ck, g_mu, g_prec, g_c, iso);
-                fold_lse(cub, r, cnt, &mx, &ssum);
-                emit_records(lane, r, cnt, cub, ck, &wpos, region, rcap, false);
-                nrec += cnt;
-                flushed = flushed || cnt > 0;
-                cnt = 0;
-                __syncwarp();
               }
             }
           }
         }
       }
       if (!ok) break;
-      // barrier B: records per row and half (bit 31: a list was flushed)
-      xtot[h * kBM + r] = (uint32_t)(nrec + cnt) | (flushed ? 0x80000000u : 0u);
+      // barrier B: candidates per row and half (bit 31: the half's list was
+      // full, the row is left to the dense-row kernels)
+      xtot[h * kBM + r] = (uint32_t)cnt | (deferred ? 0x80000000u : 0u);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[EX_B]);
       if (!warp_wait(&bar[EX_B], it & 1)) { fail(); break; }
       const uint32_t t0 = xtot[r], t1 = xtot[kBM + r];
+      const bool left = ((t0 | t1) >> 31) != 0u;
       // this quarter's two regions: past either one's capacity, the
       // quarter's rows take the CUDA-core path
-      uint32_t w0 = t0 & 0x7fffffffu, w1 = t1 & 0x7fffffffu;
+      uint32_t w0 = left ? 0u : (t0 & 0x7fffffffu), w1 = left ? 0u : (t1 & 0x7fffffffu);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         w0 += __shfl_xor_sync(0xffffffffu, w0, o);
         w1 += __shfl_xor_sync(0xffffffffu, w1, o);
       }
       const bool overflow = w0 > (uint32_t)rcap || w1 > (uint32_t)rcap;
-      const bool anyflush = ((t0 | t1) >> 31) != 0u;
       const uint32_t both = (t0 & 0x7fffffffu) + (t1 & 0x7fffffffu);
-      const bool exact = rowok && both > 0 && !overflow;
-      const bool single = exact && !anyflush && both == 1 && !a.want_lse;
+      const bool exact = rowok && !left && both > 0 && !overflow;
+      const bool single = exact && both == 1 && !a.want_lse;
       refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu, g_prec,
                           g_c, iso);
       if (exact && !single) fold_lse(cub, r, cnt, &mx, &ssum);
@@ -1080,9 +1083,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           ll_acc += (double)lse;
         }
         // rows of an overflowing quarter, and rows without a candidate
-        // (non-finite input), go to the CUDA-core path
-        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
-        if (lane == 0) a.fb_mask[tile * 4 + q] = fbm;
+        // (non-finite input), go to the CUDA-core path; rows with a full list
+        // to the dense-row kernels
+        const bool dense = rowok && left && !overflow;
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact && !dense);
+        const unsigned dbm = __ballot_sync(0xffffffffu, dense);
+        if (lane == 0) {
+          a.fb_mask[tile * 4 + q] = fbm;
+          a.dmask[tile * 4 + q] = dbm;
+        }
       }
       if (lane == 0) a.tile_cnt[tile * 8 + 2 * q + h] = overflow ? 0u : (h == 0 ? w0 : w1);
       __syncwarp();
@@ -1498,14 +1507,17 @@ int tc_screen_grid(int64_t N) {
   return (int)(tiles < sms ? tiles : sms);
 }
 
-// mode 0: EM (lse, ll_part); mode 1: assign (top-m).
+// mode 0: EM (lse, ll_part, records; streamed parameters also the candidate
+// masks and the rows left to the dense-row kernels); mode 1: assign (top-m).
 // EM mode: lse (every point's LSE_n, written for all points but those with a
 // single candidate unless want_lse) and the records are required.
 cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int cov,
                       const void* prepared, int mode, float* lse, int want_lse, double* ll_part,
-                      int m, int32_t* ids, float* gamma, uint32_t* fb_mask, uint2* recs,
-                      uint32_t* tile_cnt, int rec_cap, DeviceStatus* st, cudaStream_t s) {
+                      int m, int32_t* ids, float* gamma, uint32_t* fb_mask, uint32_t* cmask,
+                      uint32_t* dmask, uint2* recs, uint32_t* tile_cnt, int rec_cap,
+                      DeviceStatus* st, cudaStream_t s) {
   ScreenArgs a;
+  a.cmask = cmask; a.dmask = dmask;
   a.X = X; a.N = N; a.K = K; a.m = m; a.prepared = prepared;
   a.L = PreparedLayout::make(D, K, cov);
   a.lse = lse; a.want_lse = want_lse; a.ll_part = ll_part; a.ids = ids; a.gamma = gamma;
@@ -1513,6 +1525,7 @@ cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int co
   a.recs = recs; a.tile_cnt = tile_cnt; a.rec_cap = rec_cap;
   if (!a.L.tc_chunks || N < 1) return cudaErrorInvalidValue;
   if (mode == MODE_EM && (!recs || !tile_cnt || !lse || rec_cap < kBM)) return cudaErrorInvalidValue;
+  if (mode == MODE_EM && !tc_fold(a.L.tc_chunks) && (!cmask || !dmask)) return cudaErrorInvalidValue;
   const int grid = tc_screen_grid(N);
 #define GMM_SCREEN(DD, XX)                                                              \
   return mode == MODE_EM ? run_screen<DD, XX, MODE_EM>(a, grid, s)                      \

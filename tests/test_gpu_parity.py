@@ -422,12 +422,12 @@ def test_full_lists_flush_and_match_oracle():
         assert not fails, "\n".join(fails[:10])
 
 
-def test_region_overflow_takes_the_cuda_core_path():
+def test_many_candidates_take_the_dense_row_kernels():
     """K = 300 components with nearly the same mean and variance: every
-    point keeps all 300 as candidates, more records than a warp's region of
-    the tile buffer holds (128 a point on average per column half), so those
-    rows take the CUDA-core path.  Steps from these parameters and from the
-    oracle's next iterate match the oracle."""
+    point keeps all 300 as candidates, more than the screening kernel's
+    lists hold, so the points go with their candidate masks to the dense-row
+    kernels (parameters staged in shared memory).  Steps from these
+    parameters and from the oracle's next iterate match the oracle."""
     rng = np.random.default_rng(41)
     N, D, K = 4000, 128, 300
     # data and means away from the origin, so that every mean entry is of
@@ -448,7 +448,8 @@ def test_region_overflow_takes_the_cuda_core_path():
             got = gpu_step(st, Xd, theta, want_lse=want_lse, opts=opts)
             assert got["status"] == 0, got["status"]
             if step == 0:
-                assert int(st.ws[8:12].cpu().numpy().view(np.uint32)[0]) > 0
+                # status word: code, detail, rows to the CUDA-core path, rows to the dense kernels
+                assert int(st.ws[12:16].cpu().numpy().view(np.uint32)[0]) > N // 2
             fails = parity.compare_step(got, ref, "dense step %d lse=%d" % (step, want_lse), 0.5)
             assert not fails, "\n".join(fails[:10])
             if want_lse:
