@@ -19,7 +19,7 @@
 //                 max and sum combined into the point's over the chunk
 //   dense_combine LSE_n from the chunks' (max, sum), the log-likelihood
 //   dense_stats   block (group of 8192/D components, partition): a thread
-//                 per (component, 32 dimensions) keeps the component's sums
+//                 per (component, 16 dimensions) keeps the component's sums
 //                 s0, sum g (x - mu) and sum g (x - mu)^2 in registers over
 //                 the block's points, g = exp(l - LSE_n) recomputed for every
 //                 candidate; at the end they join the block's fp64 partial
@@ -76,7 +76,7 @@ struct DenseArgs {
   const float* bias;        // prepared log pi - log|S|/2 - (D/2) log 2 pi [K]
   bool iso;
   const uint32_t* cmask;    // [slab rows][nch][4] candidate masks
-  float2* part;             // [points][nch] (max, sum) per chunk
+  float2* part;             // [points][2 nch] (max, sum) per half chunk
   float* lse;               // the slab's LSE_n
   double* ll_part;          // [kCombineGrid]
   double* stat;             // [P][K][1 + 2D] fp64 partials
@@ -84,22 +84,28 @@ struct DenseArgs {
   DeviceStatus* st;
 };
 
+// Components per block of the log-sum-exp kernel: half a mask chunk, so that
+// three blocks fit an SM.
+constexpr int kLseComps = kChunk / 2;
+
 template <int D, int XT>
-__global__ void __launch_bounds__(kThreads) dense_lse_kernel(const DenseArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs a) {
   constexpr int CPL = D / 32;  // 4-dimension pieces per lane: lane g of a group of eight
                                // holds dimensions 4 (g + 8 i) .. + 3, i < CPL
   constexpr int RS = D + 4;    // padded table row (floats)
   extern __shared__ __align__(16) float smf[];
-  float* s_mu = smf;                 // [128][RS]
-  float* s_w = s_mu + kChunk * RS;   // [128][RS]
-  float* s_c = s_w + kChunk * RS;    // [128]
+  float* s_mu = smf;                    // [64][RS]
+  float* s_w = s_mu + kLseComps * RS;   // [64][RS]
+  float* s_c = s_w + kLseComps * RS;    // [64]
   const uint32_t n = *a.count;
   if (n == 0) return;
-  const int j = blockIdx.x, P = gridDim.y;
+  // block x: half hf of mask chunk j (mask words 2 hf, 2 hf + 1)
+  const int j = blockIdx.x >> 1, hf = blockIdx.x & 1, P = gridDim.y;
+  const int kc0 = j * kChunk + hf * kLseComps;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane >> 3, gl = lane & 7;
-  for (int i = tid; i < kChunk * D; i += kThreads) {
-    const int kr = i / D, d = i % D, k = j * kChunk + kr;
+  for (int i = tid; i < kLseComps * D; i += kThreads) {
+    const int kr = i / D, d = i % D, k = kc0 + kr;
     float m = 0.f, w = 0.f;
     if (k < a.K) {
       m = __ldg(a.mu + (size_t)k * D + d);
@@ -108,25 +114,39 @@ __global__ void __launch_bounds__(kThreads) dense_lse_kernel(const DenseArgs a) 
     s_mu[kr * RS + d] = m;
     s_w[kr * RS + d] = w;
   }
-  for (int i = tid; i < kChunk; i += kThreads) {
-    const int k = j * kChunk + i;
+  for (int i = tid; i < kLseComps; i += kThreads) {
+    const int k = kc0 + i;
     s_c[i] = k < a.K ? __ldg(a.bias + k) : -INFINITY;
   }
   __syncthreads();
   // a warp per point; its four groups of eight lanes take the point's
-  // candidates in turn (candidate t of the chunk to group t % 4)
-  for (uint32_t i = blockIdx.y * (kThreads / 32) + warp; i < n; i += P * (kThreads / 32)) {
-    const uint32_t row = a.rows[i];
+  // candidates in turn (candidate t of the half chunk to group t % 4).  The
+  // next point's row, masks and coordinates are requested before this one is
+  // evaluated.
+  const uint32_t stride = (uint32_t)P * (kThreads / 32);
+  uint32_t i = blockIdx.y * (kThreads / 32) + warp;
+  float xn[CPL][4];
+  uint2 mn = make_uint2(0u, 0u);
+  auto fetch = [&](uint32_t ii) {
+    const uint32_t row = a.rows[ii];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) load_x_vec<XT>(a.X, (size_t)row * D + 4 * (gl + 8 * c), 4, xn[c]);
+    mn = __ldg(reinterpret_cast<const uint2*>(a.cmask + ((size_t)row * a.nch + j) * 4 + 2 * hf));
+  };
+  if (i < n) fetch(i);
+  for (; i < n; i += stride) {
     float x[CPL][4];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) load_x_vec<XT>(a.X, (size_t)row * D + 4 * (gl + 8 * c), 4, x[c]);
-    const uint4 mw = __ldg(reinterpret_cast<const uint4*>(a.cmask + ((size_t)row * a.nch + j) * 4));
-    uint32_t bits[4] = {mw.x, mw.y, mw.z, mw.w};
+    for (int c = 0; c < CPL; ++c)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) x[c][t] = xn[c][t];
+    uint32_t bits[2] = {mn.x, mn.y};
+    if (i + stride < n) fetch(i + stride);
     int wi = 0;
     // the next candidate column (in column order), -1 when none is left
     auto next_col = [&]() -> int {
-      while (wi < 4 && bits[wi] == 0u) ++wi;
-      if (wi == 4) return -1;
+      while (wi < 2 && bits[wi] == 0u) ++wi;
+      if (wi == 2) return -1;
       const int c = wi * 32 + __ffs(bits[wi]) - 1;
       bits[wi] &= bits[wi] - 1u;
       return c;
@@ -179,7 +199,7 @@ __global__ void __launch_bounds__(kThreads) dense_lse_kernel(const DenseArgs a) 
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (gs[q] > 0.f) S += gs[q] * expf(gm[q] - M);
-      a.part[(size_t)i * a.nch + j] = make_float2(M, S);
+      a.part[(size_t)i * (2 * a.nch) + blockIdx.x] = make_float2(M, S);
     }
   }
 }
@@ -189,12 +209,12 @@ __global__ void __launch_bounds__(kThreads) dense_combine_kernel(const DenseArgs
   const uint32_t n = *a.count;
   double acc = 0.0;
   for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < n; i += gridDim.x * kThreads) {
-    const float2* p = a.part + (size_t)i * a.nch;
+    const float2* p = a.part + (size_t)i * (2 * a.nch);
     float M = -INFINITY;
-    for (int j = 0; j < a.nch; ++j)
+    for (int j = 0; j < 2 * a.nch; ++j)
       if (p[j].y > 0.f) M = fmaxf(M, p[j].x);
     float S = 0.f;
-    for (int j = 0; j < a.nch; ++j)
+    for (int j = 0; j < 2 * a.nch; ++j)
       if (p[j].y > 0.f) S += p[j].y * expf(p[j].x - M);
     const float l = M + logf(S);
     if (!isfinite(l)) raise_status(a.st, GMM_ERR_NONFINITE);
@@ -211,24 +231,28 @@ __global__ void __launch_bounds__(kThreads) dense_combine_kernel(const DenseArgs
   }
 }
 
-// 32 dimensions per thread, D/32 threads per component, 256 threads: a block
-// takes 8192/D components.
+// 16 dimensions per thread, D/16 threads per component, 512 threads: a block
+// takes 8192/D components (64 at D = 128, 128 at D = 64).
+constexpr int kStatThreads = 512;
 template <int D>
 struct DsShape {
-  static constexpr int TPC = D / 32;
-  static constexpr int CPB = kThreads / TPC;
+  static constexpr int DPT = 16;
+  static constexpr int TPC = D / DPT;
+  static constexpr int CPB = kStatThreads / TPC;
   static constexpr int WPR = CPB / 32;  // mask words of a block's components per point
 };
 
 template <int D, int XT>
-__global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArgs a) {
+__global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const DenseArgs a) {
   using SH = DsShape<D>;
-  constexpr int TPC = SH::TPC, CPB = SH::CPB, WPR = SH::WPR, F = 1 + 2 * D;
+  constexpr int DPT = SH::DPT, TPC = SH::TPC, CPB = SH::CPB, WPR = SH::WPR, F = 1 + 2 * D;
   constexpr int ESZ = XT == GMM_F32 ? 4 : 2;
   constexpr int ROWB = D * ESZ;
   constexpr int C16 = ROWB / 16;
-  constexpr int TC16 = 32 * ESZ / 16;  // 16-byte chunks of a thread's dimensions
-  constexpr int VPC = 16 / ESZ;        // values per chunk
+  constexpr int TC16 = DPT * ESZ / 16;           // 16-byte chunks of a thread's dimensions
+  constexpr int VPC = 16 / ESZ;                  // values per chunk
+  constexpr int XPT = kRowsPerTile * C16 / kStatThreads;  // chunks of the tile per thread
+  static_assert(XPT >= 1 && XPT * kStatThreads == kRowsPerTile * C16, "tile load split");
   __shared__ __align__(16) unsigned char xs[kRowsPerTile * ROWB];
   __shared__ float lse_t[kRowsPerTile];
   __shared__ uint32_t cm[CPB][kRowsPerTile / 32];
@@ -239,12 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArg
   const int g = blockIdx.x, p = blockIdx.y, P = gridDim.y;
   const int k = g * CPB + kl;
   const bool kin = k < a.K;
-  const int d0 = h * 32;
+  const int d0 = h * DPT;
   const unsigned grp_mask = ((1u << TPC) - 1u) << ((tid & 31) & ~(TPC - 1));
   const float ck = kin ? __ldg(a.bias + k) : -INFINITY;
-  float mu[32], w[32], s1[32], s2[32], s0 = 0.f;
+  float mu[DPT], w[DPT], s1[DPT], s2[DPT], s0 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < DPT; ++i) {
     mu[i] = kin ? __ldg(a.mu + (size_t)k * D + d0 + i) : 0.f;
     w[i] = kin ? (a.iso ? __ldg(a.prec + k) : __ldg(a.prec + (size_t)k * D + d0 + i)) : 0.f;
     s1[i] = s2[i] = 0.f;
@@ -252,31 +276,55 @@ __global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArg
   // the block's components are mask words [wk0, wk0 + WPR) of mask chunk j
   const int j = (g * CPB) / kChunk, wk0 = ((g * CPB) % kChunk) / 32;
   const uint32_t ntiles = (n + kRowsPerTile - 1) / kRowsPerTile;
-  for (uint32_t t = p; t < ntiles; t += P) {
-    __syncthreads();
+  // the next tile's data is fetched into registers while this one is used:
+  // its rows of X (XPT chunks a thread), LSE and candidate masks
+  uint4 xr[XPT];
+  float lr = 0.f;
+  uint32_t mr = 0u, rr = 0u;
+  auto fetch = [&](uint32_t t) {
     const uint32_t i0 = t * kRowsPerTile;
     const int rows = (int)min((uint32_t)kRowsPerTile, n - i0);
-    for (int i = tid; i < CPB * (kRowsPerTile / 32); i += kThreads) (&cm[0][0])[i] = 0u;
-    for (int i = tid; i < rows * C16; i += kThreads) {
-      const int r = i / C16, q = i % C16;
-      const uint32_t row = a.rows[i0 + r];
-      *reinterpret_cast<uint4*>(xs + r * ROWB + ((q ^ (r & 7)) << 4)) =
-          __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.X) +
-                                               (size_t)row * ROWB) + q);
+#pragma unroll
+    for (int c = 0; c < XPT; ++c) {
+      const int e = tid + c * kStatThreads, r = e / C16, q = e % C16;
+      xr[c] = r < rows ? __ldg(reinterpret_cast<const uint4*>(
+                             static_cast<const unsigned char*>(a.X) +
+                             (size_t)__ldg(a.rows + i0 + r) * ROWB) + q)
+                       : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int i = tid; i < kRowsPerTile; i += kThreads)
-      lse_t[i] = i < rows ? a.lse[a.rows[i0 + i]] : 0.f;
+    if (tid < kRowsPerTile) {
+      rr = tid < rows ? __ldg(a.rows + i0 + tid) : 0u;
+      lr = tid < rows ? a.lse[rr] : 0.f;
+    }
+    if (tid < kRowsPerTile * WPR) {
+      const int r = tid / WPR, wq = tid % WPR;
+      mr = r < rows ? __ldg(a.cmask + ((size_t)__ldg(a.rows + i0 + r) * a.nch + j) * 4 + wk0 + wq)
+                    : 0u;
+    }
+  };
+  if ((uint32_t)p < ntiles) fetch(p);
+  for (uint32_t t = p; t < ntiles; t += P) {
+    __syncthreads();  // the previous tile's tables are no longer read
+    for (int i = tid; i < CPB * (kRowsPerTile / 32); i += kStatThreads) (&cm[0][0])[i] = 0u;
+#pragma unroll
+    for (int c = 0; c < XPT; ++c) {
+      const int e = tid + c * kStatThreads, r = e / C16, q = e % C16;
+      *reinterpret_cast<uint4*>(xs + r * ROWB + ((q ^ (r & 7)) << 4)) = xr[c];
+    }
+    if (tid < kRowsPerTile) lse_t[tid] = lr;
+    const uint32_t mcur = mr;
     __syncthreads();
     // candidate masks, point-major -> component-major
-    for (int i = tid; i < rows * WPR; i += kThreads) {
-      const int r = i / WPR, wq = i % WPR;
-      uint32_t bits = __ldg(a.cmask + ((size_t)a.rows[i0 + r] * a.nch + j) * 4 + wk0 + wq);
+    if (tid < kRowsPerTile * WPR) {
+      const int r = tid / WPR, wq = tid % WPR;
+      uint32_t bits = mcur;
       while (bits) {
         const int c = wq * 32 + __ffs(bits) - 1;
         bits &= bits - 1u;
         atomicOr(&cm[c][r >> 5], 1u << (r & 31));
       }
     }
+    if (t + P < ntiles) fetch(t + P);
     __syncthreads();
     if (!kin || ck == -INFINITY) continue;
 #pragma unroll 1
@@ -285,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArg
       while (m) {
         const int r = rw * 32 + __ffs(m) - 1;
         m &= m - 1u;
-        float xv[32];
+        float xv[DPT];
 #pragma unroll
         for (int c16 = 0; c16 < TC16; ++c16) {
           const uint4 u = *reinterpret_cast<const uint4*>(
@@ -306,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArg
         }
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < DPT; ++i) {
           const float u = xv[i] - mu[i];
           acc[i & 3] = fmaf(u * u, w[i], acc[i & 3]);
         }
@@ -316,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArg
         const float gm = expf(ck - 0.5f * d2 - lse_t[r]);
         s0 += gm;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < DPT; ++i) {
           const float y = xv[i] - mu[i];
           const float gy = gm * y;
           s1[i] += gy;
@@ -332,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArg
     const double S0o = a.accumulate ? o[0] : 0.0;
     const double S0 = S0o + b0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < DPT; ++i) {
       const int d = d0 + i;
       const double b1 = (double)s1[i];
       const double m2b = b0 > 0.0 ? (double)s2[i] - b1 * b1 / b0 : 0.0;
@@ -356,13 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const DenseArg
 
 template <int D, int XT>
 cudaError_t run_dense(const DenseArgs& a, int pa, int pb, cudaStream_t s) {
-  const size_t smem_a = sizeof(float) * ((size_t)2 * kChunk * (D + 4) + kChunk);
+  const size_t smem_a = sizeof(float) * ((size_t)2 * kLseComps * (D + 4) + kLseComps);
   cudaError_t e = cudaFuncSetAttribute(dense_lse_kernel<D, XT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a);
   if (e != cudaSuccess) return e;
   {
     ProfScope prof("dense_lse_kernel", s);
-    dense_lse_kernel<D, XT><<<dim3(a.nch, pa), kThreads, smem_a, s>>>(a);
+    dense_lse_kernel<D, XT><<<dim3(2 * a.nch, pa), kThreads, smem_a, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
@@ -373,7 +421,7 @@ cudaError_t run_dense(const DenseArgs& a, int pa, int pb, cudaStream_t s) {
   {
     ProfScope prof("dense_stats_kernel", s);
     const int ng = (a.K + DsShape<D>::CPB - 1) / DsShape<D>::CPB;
-    dense_stats_kernel<D, XT><<<dim3(ng, pb), kThreads, 0, s>>>(a);
+    dense_stats_kernel<D, XT><<<dim3(ng, pb), kStatThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -386,7 +434,7 @@ int dense_ll_parts() { return kCombineGrid; }
 // Partitions of the dense statistics blocks (fixed by D and K: the order of
 // the sums never depends on the device or on N).
 int dense_stat_parts(int D, int K) {
-  const int cpb = kThreads / (D / 32);
+  const int cpb = kStatThreads / (D / 16);
   const int ng = (K + cpb - 1) / cpb;
   const int p = (152 + ng - 1) / ng;
   return p < 1 ? 1 : p;
@@ -395,7 +443,7 @@ int dense_stat_parts(int D, int K) {
 // The points rows[0 .. *count) of a slab (X: the slab's rows): LSE_n into
 // lse, the log-likelihood into ll_part[0 .. dense_ll_parts()), statistics into
 // partial slots [0, dense_stat_parts(D, K)) of stat.  part: scratch of
-// (slab rows) x nch float2.
+// (slab rows) x 2 nch float2.
 cudaError_t dense_rows(const void* X, int xdtype, int D, int K, int cov, const void* prepared,
                        const uint32_t* rows, const uint32_t* count, const uint32_t* cmask,
                        float2* part, float* lse, double* ll_part, double* stat, int accumulate,
@@ -410,7 +458,7 @@ cudaError_t dense_rows(const void* X, int xdtype, int D, int K, int cov, const v
   a.iso = cov == GMM_COV_ISO;
   a.cmask = cmask; a.part = part; a.lse = lse; a.ll_part = ll_part; a.stat = stat;
   a.accumulate = accumulate; a.st = st;
-  const int pa = (152 * 2 + a.nch - 1) / a.nch;
+  const int pa = (152 * 3 + 2 * a.nch - 1) / (2 * a.nch);
   const int pb = dense_stat_parts(D, K);
   if (D == 128) {
     if (xdtype == GMM_F16) return run_dense<128, GMM_F16>(a, pa, pb, s);

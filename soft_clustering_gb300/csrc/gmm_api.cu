@@ -160,7 +160,7 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_cmask = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * 4 * nch * (size_t)slab : 0));
   W.off_dmask = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * 4 * slab_tiles : 0));
   W.off_drows = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * (size_t)slab : 0));
-  W.off_dpart = o;  o = align_up(o + (streamed ? sizeof(float2) * nch * (size_t)slab : 0));
+  W.off_dpart = o;  o = align_up(o + (streamed ? sizeof(float2) * 2 * nch * (size_t)slab : 0));
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
