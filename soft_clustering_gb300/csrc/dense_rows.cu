@@ -436,7 +436,7 @@ int dense_ll_parts() { return kCombineGrid; }
 int dense_stat_parts(int D, int K) {
   const int cpb = kStatThreads / (D / 16);
   const int ng = (K + cpb - 1) / cpb;
-  const int p = (152 + ng - 1) / ng;
+  const int p = 152 / ng;  // one wave of one block per SM
   return p < 1 ? 1 : p;
 }
 
@@ -458,7 +458,8 @@ cudaError_t dense_rows(const void* X, int xdtype, int D, int K, int cov, const v
   a.iso = cov == GMM_COV_ISO;
   a.cmask = cmask; a.part = part; a.lse = lse; a.ll_part = ll_part; a.stat = stat;
   a.accumulate = accumulate; a.st = st;
-  const int pa = (152 * 3 + 2 * a.nch - 1) / (2 * a.nch);
+  int pa = 152 * 3 / (2 * a.nch);  // one wave of three blocks per SM
+  if (pa < 1) pa = 1;
   const int pb = dense_stat_parts(D, K);
   if (D == 128) {
     if (xdtype == GMM_F16) return run_dense<128, GMM_F16>(a, pa, pb, s);
