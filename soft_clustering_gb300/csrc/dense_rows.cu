@@ -11,15 +11,17 @@
 // points with their candidate masks (one bit per component, the exact 40-nat
 // window of the rigorous screen), and three kernels take them with the
 // parameters staged in shared memory:
-//   dense_lse     block (mask chunk of 128 components, partition): a warp
-//                 per point, its four groups of eight lanes taking the
-//                 chunk's candidates in turn, each evaluated in the centred
-//                 fp32 form sum_d w_d (x_d - mu_d)^2 (lane: D/8 dimensions,
-//                 then a butterfly sum over the group), the groups' running
-//                 max and sum combined into the point's over the chunk
+//   dense_lse     block (half a mask chunk: 64 components, partition): a
+//                 warp per point, its four groups of eight lanes taking the
+//                 candidates of 16 columns each, each evaluated in the
+//                 centred fp32 form sum_d w_d (x_d - mu_d)^2 (lane: D/8
+//                 dimensions, then a butterfly sum over the group), the
+//                 groups' running max and sum (base 2) combined into the
+//                 point's over the half chunk
 //   dense_combine LSE_n from the chunks' (max, sum), the log-likelihood
 //   dense_stats   block (group of 8192/D components, partition): a thread
-//                 per (component, 16 dimensions) keeps the component's sums
+//                 per (component, 16 dimensions: every eighth 16-byte chunk
+//                 of the row at D = 128) keeps the component's sums
 //                 s0, sum g (x - mu) and sum g (x - mu)^2 in registers over
 //                 the block's points, g = exp(l - LSE_n) recomputed for every
 //                 candidate; at the end they join the block's fp64 partial
@@ -66,6 +68,38 @@ __device__ __forceinline__ void load_x_vec(const void* X, size_t e0, int n, floa
   }
 }
 
+// Pairs of fp32 operations issued as one packed instruction (each half an
+// IEEE fp32 operation rounded to nearest, as the scalar forms).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 struct DenseArgs {
   const void* X;            // the slab's rows
   const uint32_t* rows;     // points left to these kernels (slab rows, ascending)
@@ -76,7 +110,7 @@ struct DenseArgs {
   const float* bias;        // prepared log pi - log|S|/2 - (D/2) log 2 pi [K]
   bool iso;
   const uint32_t* cmask;    // [slab rows][nch][4] candidate masks
-  float2* part;             // [points][2 nch] (max, sum) per half chunk
+  float2* part;             // [points][2 nch] (max, sum) per half chunk, base 2
   float* lse;               // the slab's LSE_n
   double* ll_part;          // [kCombineGrid]
   double* stat;             // [P][K][1 + 2D] fp64 partials
@@ -119,10 +153,11 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
     s_c[i] = k < a.K ? __ldg(a.bias + k) : -INFINITY;
   }
   __syncthreads();
-  // a warp per point; its four groups of eight lanes take the point's
-  // candidates in turn (candidate t of the half chunk to group t % 4).  The
-  // next point's row, masks and coordinates are requested before this one is
-  // evaluated.
+  // a warp per point; group q of eight lanes takes the point's candidates
+  // among columns 16 q .. 16 q + 15 of the half chunk, in column order.  The
+  // log-sum-exp runs in base 2 (values l log2(e)).  The next point's row,
+  // masks and coordinates are requested before this one is evaluated.
+  constexpr float kLog2e = 1.4426950408889634f;
   const uint32_t stride = (uint32_t)P * (kThreads / 32);
   uint32_t i = blockIdx.y * (kThreads / 32) + warp;
   float xn[CPL][4];
@@ -140,46 +175,40 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
     for (int c = 0; c < CPL; ++c)
 #pragma unroll
       for (int t = 0; t < 4; ++t) x[c][t] = xn[c][t];
-    uint32_t bits[2] = {mn.x, mn.y};
+    // this group's 16 columns
+    uint32_t bits = ((grp < 2 ? mn.x : mn.y) >> (16 * (grp & 1))) & 0xffffu;
     if (i + stride < n) fetch(i + stride);
-    int wi = 0;
-    // the next candidate column (in column order), -1 when none is left
-    auto next_col = [&]() -> int {
-      while (wi < 2 && bits[wi] == 0u) ++wi;
-      if (wi == 2) return -1;
-      const int c = wi * 32 + __ffs(bits[wi]) - 1;
-      bits[wi] &= bits[wi] - 1u;
-      return c;
-    };
+    int steps = __popc(bits);
+    steps = max(steps, __shfl_xor_sync(0xffffffffu, steps, 8));
+    steps = max(steps, __shfl_xor_sync(0xffffffffu, steps, 16));
     float mx = -INFINITY, sum = 0.f;
-    for (;;) {
-      const int c0 = next_col(), c1 = next_col(), c2 = next_col(), c3 = next_col();
-      if (c0 < 0) break;
-      const int col = grp == 0 ? c0 : (grp == 1 ? c1 : (grp == 2 ? c2 : c3));
+    for (int st = 0; st < steps; ++st) {
+      const int col = bits ? 16 * grp + __ffs(bits) - 1 : -1;
+      bits &= bits - 1u;
       float acc = 0.f;
       if (col >= 0) {
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           const float4 m4 = *reinterpret_cast<const float4*>(s_mu + col * RS + 4 * (gl + 8 * c));
           const float4 w4 = *reinterpret_cast<const float4*>(s_w + col * RS + 4 * (gl + 8 * c));
-          const float u0 = x[c][0] - m4.x, u1 = x[c][1] - m4.y;
-          const float u2 = x[c][2] - m4.z, u3 = x[c][3] - m4.w;
-          acc = fmaf(u0 * u0, w4.x, acc);
-          acc = fmaf(u1 * u1, w4.y, acc);
-          acc = fmaf(u2 * u2, w4.z, acc);
-          acc = fmaf(u3 * u3, w4.w, acc);
+          const float2 u01 = sub2(make_float2(x[c][0], x[c][1]), make_float2(m4.x, m4.y));
+          const float2 u23 = sub2(make_float2(x[c][2], x[c][3]), make_float2(m4.z, m4.w));
+          a01 = fma2(mul2(u01, u01), make_float2(w4.x, w4.y), a01);
+          a23 = fma2(mul2(u23, u23), make_float2(w4.z, w4.w), a23);
         }
+        acc = (a01.x + a23.x) + (a01.y + a23.y);
       }
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (col >= 0) {
-        const float l = s_c[col] - 0.5f * acc;
-        // the group's running log-sum-exp
-        if (l > mx) {
-          sum = sum * expf(mx - l) + 1.f;
-          mx = l;
+        const float l2 = (s_c[col] - 0.5f * acc) * kLog2e;
+        // the group's running log-sum-exp (base 2)
+        if (l2 > mx) {
+          sum = sum * exp2f(mx - l2) + 1.f;
+          mx = l2;
         } else {
-          sum += expf(l - mx);
+          sum += exp2f(l2 - mx);
         }
       }
     }
@@ -198,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
       float S = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (gs[q] > 0.f) S += gs[q] * expf(gm[q] - M);
+        if (gs[q] > 0.f) S += gs[q] * exp2f(gm[q] - M);
       a.part[(size_t)i * (2 * a.nch) + blockIdx.x] = make_float2(M, S);
     }
   }
@@ -215,8 +244,9 @@ __global__ void __launch_bounds__(kThreads) dense_combine_kernel(const DenseArgs
       if (p[j].y > 0.f) M = fmaxf(M, p[j].x);
     float S = 0.f;
     for (int j = 0; j < 2 * a.nch; ++j)
-      if (p[j].y > 0.f) S += p[j].y * expf(p[j].x - M);
-    const float l = M + logf(S);
+      if (p[j].y > 0.f) S += p[j].y * exp2f(p[j].x - M);
+    // the partials are in base 2 (values l log2(e))
+    const float l = (M + log2f(S)) * 0.6931471805599453f;
     if (!isfinite(l)) raise_status(a.st, GMM_ERR_NONFINITE);
     a.lse[a.rows[i]] = l;
     acc += (double)l;
@@ -263,15 +293,24 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
   const int g = blockIdx.x, p = blockIdx.y, P = gridDim.y;
   const int k = g * CPB + kl;
   const bool kin = k < a.K;
-  const int d0 = h * DPT;
+  // thread h holds the 16-byte chunks h, h + TPC, h + 2 TPC, ... of a row, so
+  // the TPC threads reading one row at a time touch TPC distinct chunks of
+  // one span of 16 TPC bytes (at D = 128 a quarter warp reads 128 bytes with
+  // no shared-memory bank conflict)
+  auto dim_of = [&](int i) { return ((i / VPC) * TPC + h) * VPC + i % VPC; };
   const unsigned grp_mask = ((1u << TPC) - 1u) << ((tid & 31) & ~(TPC - 1));
   const float ck = kin ? __ldg(a.bias + k) : -INFINITY;
-  float mu[DPT], w[DPT], s1[DPT], s2[DPT], s0 = 0.f;
+  constexpr int DP = DPT / 2;  // dimension pairs
+  float2 mu[DP], w[DP], s1[DP], s2[DP];
+  float s0 = 0.f;
 #pragma unroll
-  for (int i = 0; i < DPT; ++i) {
-    mu[i] = kin ? __ldg(a.mu + (size_t)k * D + d0 + i) : 0.f;
-    w[i] = kin ? (a.iso ? __ldg(a.prec + k) : __ldg(a.prec + (size_t)k * D + d0 + i)) : 0.f;
-    s1[i] = s2[i] = 0.f;
+  for (int i = 0; i < DP; ++i) {
+    const int d = dim_of(2 * i);  // pairs never straddle a chunk
+    mu[i] = kin ? __ldg(reinterpret_cast<const float2*>(a.mu + (size_t)k * D + d)) : make_float2(0.f, 0.f);
+    if (!kin) w[i] = make_float2(0.f, 0.f);
+    else if (a.iso) w[i] = make_float2(__ldg(a.prec + k), __ldg(a.prec + k));
+    else w[i] = __ldg(reinterpret_cast<const float2*>(a.prec + (size_t)k * D + d));
+    s1[i] = s2[i] = make_float2(0.f, 0.f);
   }
   // the block's components are mask words [wk0, wk0 + WPR) of mask chunk j
   const int j = (g * CPB) / kChunk, wk0 = ((g * CPB) % kChunk) / 32;
@@ -296,8 +335,8 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
       rr = tid < rows ? __ldg(a.rows + i0 + tid) : 0u;
       lr = tid < rows ? a.lse[rr] : 0.f;
     }
-    if (tid < kRowsPerTile * WPR) {
-      const int r = tid / WPR, wq = tid % WPR;
+    if (tid < kRowsPerTile * WPR) {  // warp w: mask word w % WPR of rows 32 (w / WPR) + lane
+      const int w = tid >> 5, r = (w / WPR) * 32 + (tid & 31), wq = w % WPR;
       mr = r < rows ? __ldg(a.cmask + ((size_t)__ldg(a.rows + i0 + r) * a.nch + j) * 4 + wk0 + wq)
                     : 0u;
     }
@@ -305,27 +344,26 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
   if ((uint32_t)p < ntiles) fetch(p);
   for (uint32_t t = p; t < ntiles; t += P) {
     __syncthreads();  // the previous tile's tables are no longer read
-    for (int i = tid; i < CPB * (kRowsPerTile / 32); i += kStatThreads) (&cm[0][0])[i] = 0u;
 #pragma unroll
     for (int c = 0; c < XPT; ++c) {
       const int e = tid + c * kStatThreads, r = e / C16, q = e % C16;
       *reinterpret_cast<uint4*>(xs + r * ROWB + ((q ^ (r & 7)) << 4)) = xr[c];
     }
     if (tid < kRowsPerTile) lse_t[tid] = lr;
-    const uint32_t mcur = mr;
-    __syncthreads();
-    // candidate masks, point-major -> component-major
+    // candidate masks, point-major -> component-major: a 32 x 32 bit
+    // transpose per warp, one ballot per component
     if (tid < kRowsPerTile * WPR) {
-      const int r = tid / WPR, wq = tid % WPR;
-      uint32_t bits = mcur;
-      while (bits) {
-        const int c = wq * 32 + __ffs(bits) - 1;
-        bits &= bits - 1u;
-        atomicOr(&cm[c][r >> 5], 1u << (r & 31));
+      const int ln = tid & 31, w = tid >> 5;
+      uint32_t mine = 0u;
+#pragma unroll 8
+      for (int b = 0; b < 32; ++b) {
+        const uint32_t v = __ballot_sync(0xffffffffu, (mr >> b) & 1u);
+        if (ln == b) mine = v;
       }
+      cm[(w % WPR) * 32 + ln][w / WPR] = mine;
     }
-    if (t + P < ntiles) fetch(t + P);
     __syncthreads();
+    if (t + P < ntiles) fetch(t + P);
     if (!kin || ck == -INFINITY) continue;
 #pragma unroll 1
     for (int rw = 0; rw < kRowsPerTile / 32; ++rw) {
@@ -333,42 +371,40 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
       while (m) {
         const int r = rw * 32 + __ffs(m) - 1;
         m &= m - 1u;
-        float xv[DPT];
+        float2 y[DP];  // x - mu
 #pragma unroll
         for (int c16 = 0; c16 < TC16; ++c16) {
           const uint4 u = *reinterpret_cast<const uint4*>(
-              xs + r * ROWB + (((d0 * ESZ / 16 + c16) ^ (r & 7)) << 4));
+              xs + r * ROWB + (((c16 * TPC + h) ^ (r & 7)) << 4));
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
           if constexpr (XT == GMM_F32) {
-            xv[c16 * 4 + 0] = __uint_as_float(u.x); xv[c16 * 4 + 1] = __uint_as_float(u.y);
-            xv[c16 * 4 + 2] = __uint_as_float(u.z); xv[c16 * 4 + 3] = __uint_as_float(u.w);
+            y[c16 * 2 + 0] = make_float2(__uint_as_float(w4[0]), __uint_as_float(w4[1]));
+            y[c16 * 2 + 1] = make_float2(__uint_as_float(w4[2]), __uint_as_float(w4[3]));
           } else {
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              float2 f;
-              if constexpr (XT == GMM_F16) f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
-              else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
-              xv[c16 * VPC + 2 * q] = f.x; xv[c16 * VPC + 2 * q + 1] = f.y;
+              if constexpr (XT == GMM_F16) y[c16 * 4 + q] = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
+              else y[c16 * 4 + q] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
             }
           }
         }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < DPT; ++i) {
-          const float u = xv[i] - mu[i];
-          acc[i & 3] = fmaf(u * u, w[i], acc[i & 3]);
+        for (int i = 0; i < DP; ++i) {
+          y[i] = sub2(y[i], mu[i]);
+          acc[i & 1] = fma2(mul2(y[i], y[i]), w[i], acc[i & 1]);
         }
-        float d2 = (acc[0] + acc[2]) + (acc[1] + acc[3]);
+        float d2 = (acc[0].x + acc[1].x) + (acc[0].y + acc[1].y);
 #pragma unroll
         for (int o = 1; o < TPC; o <<= 1) d2 += __shfl_xor_sync(grp_mask, d2, o);
-        const float gm = expf(ck - 0.5f * d2 - lse_t[r]);
+        const float gm = exp2f((ck - 0.5f * d2 - lse_t[r]) * 1.4426950408889634f);
         s0 += gm;
+        const float2 g2 = make_float2(gm, gm);
 #pragma unroll
-        for (int i = 0; i < DPT; ++i) {
-          const float y = xv[i] - mu[i];
-          const float gy = gm * y;
-          s1[i] += gy;
-          s2[i] = fmaf(gy, y, s2[i]);
+        for (int i = 0; i < DP; ++i) {
+          const float2 gy = mul2(g2, y[i]);
+          s1[i] = add2(s1[i], gy);
+          s2[i] = fma2(gy, y[i], s2[i]);
         }
       }
     }
@@ -381,9 +417,10 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
     const double S0 = S0o + b0;
 #pragma unroll
     for (int i = 0; i < DPT; ++i) {
-      const int d = d0 + i;
-      const double b1 = (double)s1[i];
-      const double m2b = b0 > 0.0 ? (double)s2[i] - b1 * b1 / b0 : 0.0;
+      const int d = dim_of(i);
+      const double b1 = (double)((i & 1) ? s1[i / 2].y : s1[i / 2].x);
+      const double q2 = (double)((i & 1) ? s2[i / 2].y : s2[i / 2].x);
+      const double m2b = b0 > 0.0 ? q2 - b1 * b1 / b0 : 0.0;
       double S1 = b1, M2 = m2b;
       if (a.accumulate) {
         const double o1 = o[1 + d], om = o[1 + D + d];
