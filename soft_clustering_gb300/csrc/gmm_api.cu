@@ -54,6 +54,11 @@ cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K,
                          float min_s0, gmm_params* p, int32_t* flags_out, cudaStream_t s);
 cudaError_t launch_ll_finalize(const double* ll_part, int64_t n, double* out, int accumulate,
                                cudaStream_t s);
+bool fc_eligible(int D, int K, int cov);
+int fc_ll_parts(int64_t N);
+cudaError_t fc_estep(const void* X, int xdtype, int64_t N, int D, int K, const void* prepared,
+                     uint32_t* mask, bool screen, float* lse, double* ll_part, double* stat,
+                     int parts, int accumulate, DeviceStatus* st, cudaStream_t s);
 
 namespace {
 
@@ -107,6 +112,12 @@ struct WsLayout {
 // its records).
 bool use_tc(int D, int K, int cov, const gmm_opts& o) {
   return tc_eligible(D, cov) && sparse_stats_supported(K) && !(o.flags & GMM_OPT_CUDA_CORES);
+}
+
+// The full-covariance path for few components (candidate masks, exact
+// log joints and statistics with every W in shared memory).
+bool use_fc(int D, int K, int cov, const gmm_opts& o) {
+  return fc_eligible(D, K, cov) && !(o.flags & GMM_OPT_CUDA_CORES);
 }
 
 // rows: rows processed per launch (N, or the chunk size of the host path);
@@ -221,10 +232,21 @@ cudaEvent_t prof_event() {
 // points with a single candidate).
 gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int K, int cov,
                       const WsLayout& W, void* ws, float* lse, bool want_lse, int accumulate,
-                      bool tc, cudaStream_t s) {
+                      bool tc, bool fc, cudaStream_t s) {
   DeviceStatus* st = at<DeviceStatus>(ws, W.off_status);
   const void* prep = at<char>(ws, W.off_prep);
   double* llp = at<double>(ws, W.off_llpart);
+  if (fc) {
+    // candidate masks (in the hand-over bitmap's space: one word a row),
+    // exact LSE_n and statistics of the candidates, the log-likelihood
+    GMM_TRY(fc_estep(X, xdtype, rows, D, K, prep, at<uint32_t>(ws, W.off_fb), true, lse, llp,
+                     at<double>(ws, W.off_part), W.parts, accumulate, st, s));
+    {
+      GMM_PROF("ll_finalize_kernel");
+      GMM_TRY(launch_ll_finalize(llp, fc_ll_parts(rows), at<double>(ws, W.off_ll), accumulate, s));
+    }
+    return GMM_OK;
+  }
   if (tc) {
     // Slabs of rows.  Per slab: screen on the tensor cores (exact LSE_n of
     // the points and records of their candidates) and statistics from the
@@ -455,7 +477,7 @@ gmm_status gmm_em_step(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
   }
   float* lse = lse_dev ? lse_dev : at<float>(ws, W.off_lse);
   gmm_status r = estep_rows(X, xdtype, N, D, K, cov, W, ws, lse, lse_dev != nullptr, 0,
-                            use_tc(D, K, cov, o), s);
+                            use_tc(D, K, cov, o), use_fc(D, K, cov, o), s);
   if (r != GMM_OK) return r;
   {
     GMM_PROF("mstep_kernel");
@@ -512,7 +534,7 @@ gmm_status gmm_em_step_host(const void* X_host, gmm_dtype xdtype, int64_t N, int
     GMM_TRY(cudaEventRecord(res->copied[b], res->copy));
     GMM_TRY(cudaStreamWaitEvent(s, res->copied[b], 0));
     gmm_status r = estep_rows(stage[b], xdtype, rn, D, K, cov, W, ws, at<float>(ws, W.off_lse),
-                              false, ci > 0, use_tc(D, K, cov, o), s);
+                              false, ci > 0, use_tc(D, K, cov, o), use_fc(D, K, cov, o), s);
     if (r != GMM_OK) return r;
     GMM_TRY(cudaEventRecord(res->consumed[b], s));
   }
