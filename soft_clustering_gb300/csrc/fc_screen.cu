@@ -25,6 +25,14 @@
 // bound less 41 nats: every component within 40 nats of the point's best.  A
 // point with a non-finite coordinate gets every component (the exact kernels
 // then report it).
+//
+// One persistent CTA of 8 warps per SM.  The B image and the per-component
+// constants (written by gmm_prepare) arrive by bulk copies once.  Per tile the
+// columns go in quarters of 256 (four components at D = 64) through two TMEM
+// buffers, so the contraction of quarter q + 1 runs while the epilogue reads
+// quarter q; warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (a point
+// each) and split every quarter's components.  The next tile's rows are
+// loaded into registers while the current tile is screened.
 #include <math.h>
 
 #include "gmm_internal.cuh"
@@ -33,38 +41,35 @@
 namespace gmm {
 namespace {
 
-constexpr int kScrThreads = 128;   // 4 warps: a point (TMEM lane) per thread
-constexpr int kScrRows = 128;      // points per tile (MMA M)
+constexpr int kScrThreads = 256;   // 8 warps: two threads per point
+constexpr int kScrRows = 128;      // points per tile (MMA M, TMEM lanes)
 constexpr int kScrGrid = 152;
-constexpr int kScrMaxK = 32;
-constexpr int kHalfCols = 512;     // TMEM columns
+constexpr int kQCols = 256;        // columns per quarter (MMA N) and per TMEM buffer
 constexpr uint32_t kScrWait = 1u << 22;
 
 struct ScrArgs {
   const __half* X;
   int64_t N;
   int K;
-  const float* W;      // [K][D][D] W = L^-1 (lower)
-  const float* mu;     // [K][D]
-  const float* bias;   // [K]
-  uint32_t* mask;      // [N]
+  const unsigned char* B;  // prepared B image [K D][128]
+  const float* T;          // prepared constants [4 kFcMaxK + K D]
+  uint32_t* mask;          // [N]
   DeviceStatus* st;
 };
 
-// Shared memory (offsets from a 1024-byte aligned base): B image (K*D rows of
-// 128 bytes, 128-byte swizzle), A tile, b_k, per-component constants.
+// Shared memory from a 1024-byte aligned base: B image, A tile, constants,
+// exchange between the two threads of a point, barriers.
 struct ScrLayout {
-  size_t b_img, a_img, bk, cst, red, bar, slot, bytes;
+  size_t b_img, a_img, cst, xch, bar, slot, bytes;
   __host__ __device__ static ScrLayout make(int D, int K) {
     ScrLayout L;
     size_t o = 0;
     L.b_img = o; o += (size_t)K * D * 128;
     o = (o + 1023) / 1024 * 1024;
     L.a_img = o; o += (size_t)kScrRows * 128;
-    L.bk = o;    o += sizeof(float) * (size_t)K * D;
-    L.cst = o;   o += sizeof(float) * 4 * kScrMaxK;
-    L.red = o;   o += sizeof(float) * 3 * (kScrThreads / 32);
-    L.bar = (o + 7) / 8 * 8; o = L.bar + 8;
+    L.cst = o;   o += sizeof(float) * (4 * kFcMaxK + (size_t)K * D);
+    L.xch = o;   o += sizeof(float) * 4 * kScrRows;
+    L.bar = (o + 7) / 8 * 8; o = L.bar + 3 * 8;
     L.slot = o;  o += 8;
     L.bytes = o + 1024;  // room to align the base
     return L;
@@ -73,8 +78,8 @@ struct ScrLayout {
 
 template <int D>
 __global__ void __launch_bounds__(kScrThreads, 1) fc_screen_kernel(const ScrArgs a) {
-  constexpr int CPH = kHalfCols / D;  // components per TMEM half
-  constexpr int KS = 4;               // K steps of 16 (K dimension padded to 64)
+  constexpr int CPQ = kQCols / D;  // components per quarter
+  constexpr int KS = 4;            // K steps of 16 (contraction dimension padded to 64)
   extern __shared__ unsigned char smraw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -82,207 +87,178 @@ __global__ void __launch_bounds__(kScrThreads, 1) fc_screen_kernel(const ScrArgs
   const ScrLayout L = ScrLayout::make(D, K);
   unsigned char* sB = sm + L.b_img;
   unsigned char* sA = sm + L.a_img;
-  float* sb = reinterpret_cast<float*>(sm + L.bk);          // b_k = W_k mu_k  [K*D]
-  float* cs = reinterpret_cast<float*>(sm + L.cst);         // s_k, c_k, ex_k, em_k
-  float* red = reinterpret_cast<float*>(sm + L.red);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);
+  float* cs = reinterpret_cast<float*>(sm + L.cst);  // s_k | bias_k | ex_k | em_k | b_k
+  float* xch = reinterpret_cast<float*>(sm + L.xch);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);  // full[2], operands
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + L.slot);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = tid & (kScrRows - 1), hh = tid >> 7;  // the point (TMEM lane) and half
 
   if (warp == 0) {
-    tc::tmem_alloc(slot, kHalfCols);
+    tc::tmem_alloc(slot, 2 * kQCols);
     tc::tmem_relinquish();
   }
+  const uint32_t b_bytes = (uint32_t)(K * D * 128);
+  const uint32_t t_bytes = (uint32_t)(sizeof(float) * (4 * kFcMaxK + K * D));
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    tc::mbar_init(&bar[2], 1);
     tc::mbar_fence_init();
   }
-  // per component: the scale, |W|_F and |mu| (block reductions), the bias
-  for (int k = 0; k < K; ++k) {
-    const float* Wk = a.W + (size_t)k * D * D;
-    float mx = 0.f, f2 = 0.f, m2 = 0.f;
-    for (int e = tid; e < D * D; e += kScrThreads) {
-      const int i = e / D, j = e % D;
-      if (j <= i) {
-        const float w = __ldg(Wk + e);
-        mx = fmaxf(mx, fabsf(w));
-        f2 = fmaf(w, w, f2);
-      }
-    }
-    for (int d = tid; d < D; d += kScrThreads) {
-      const float m = __ldg(a.mu + (size_t)k * D + d);
-      m2 = fmaf(m, m, m2);
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      f2 += __shfl_xor_sync(0xffffffffu, f2, o);
-      m2 += __shfl_xor_sync(0xffffffffu, m2, o);
-    }
-    __syncthreads();
-    if (lane == 0) { red[warp] = mx; red[4 + warp] = f2; red[8 + warp] = m2; }
-    __syncthreads();
-    if (tid == 0) {
-      float M = 0.f, F2 = 0.f, M2 = 0.f;
-      for (int w = 0; w < kScrThreads / 32; ++w) {
-        M = fmaxf(M, red[w]);
-        F2 += red[4 + w];
-        M2 += red[8 + w];
-      }
-      // s = 2^e with max |W| / s in [2^14, 2^15)
-      int e2 = 0;
-      frexpf(M > 0.f ? M : 1.f, &e2);  // M = f 2^e2, f in [0.5, 1)
-      const float s = ldexpf(1.f, e2 - 15);
-      const float F = sqrtf(F2) * (1.f + 1e-5f);
-      const float mun = sqrtf(M2) * (1.f + 1e-5f);
-      cs[k] = s;
-      cs[kScrMaxK + k] = __ldg(a.bias + k);
-      cs[2 * kScrMaxK + k] = 1.01f * ((0.00048828125f + 1.52587890625e-05f) * F +
-                                     2.98023223876953125e-08f * s * (float)D);
-      cs[3 * kScrMaxK + k] = 1.01f * 3.814697265625e-06f * F * mun;
-    }
-  }
   __syncthreads();
-  // B image: row n = k D + i holds fp16(W_k[i][j] / s_k) for j <= i, else 0;
-  // and b_k = W_k mu_k
-  for (int u = tid; u < K * D * 8; u += kScrThreads) {
-    const int n = u >> 3, c = u & 7, k = n / D, i = n % D;
-    const float inv = 1.f / cs[k];
-    const float* Wr = a.W + ((size_t)k * D + i) * D;
-    __align__(16) __half h[8];
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bar[2], b_bytes + t_bytes);
+    for (uint32_t o = 0; o < b_bytes; o += 16384)
+      tc::bulk_g2s(sB + o, a.B + o, min(16384u, b_bytes - o), &bar[2]);
+    tc::bulk_g2s(cs, a.T, t_bytes, &bar[2]);
+  }
+  const int64_t ntiles = (a.N + kScrRows - 1) / kScrRows;
+  // this thread's half of its point's row: chunks 4 hh .. 4 hh + 3
+  uint4 xr[4];
+  auto fetch = [&](int64_t t) {
+    const int64_t row = t * kScrRows + r;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int j = 8 * c + t;
-      h[t] = __float2half_rn(j < D && j <= i ? __ldg(Wr + j) * inv : 0.f);
+    for (int c = 0; c < 4; ++c) {
+      const int cc = 4 * hh + c;
+      xr[c] = (cc < D / 8 && row < a.N)
+                  ? __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)row * D) + cc)
+                  : make_uint4(0u, 0u, 0u, 0u);
     }
-    *reinterpret_cast<uint4*>(sB + n * 128 + ((c ^ (n & 7)) << 4)) = *reinterpret_cast<const uint4*>(h);
-  }
-  for (int n = tid; n < K * D; n += kScrThreads) {
-    const int k = n / D, i = n % D;
-    const float* Wr = a.W + ((size_t)k * D + i) * D;
-    const float* mk = a.mu + (size_t)k * D;
-    float s = 0.f;
-    for (int j = 0; j <= i; ++j) s = fmaf(__ldg(Wr + j), __ldg(mk + j), s);
-    sb[n] = s;
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
+  };
+  if ((int64_t)blockIdx.x < ntiles) fetch(blockIdx.x);
+  const bool loaded = __syncthreads_and(tc::mbar_wait(&bar[2], 0, kScrWait)) != 0;
+  if (!loaded && tid == 0) raise_status(a.st, GMM_ERR_TIMEOUT);
   tc::tc_fence_after();
   const uint32_t tmem = *slot;
   uint32_t valid = 0u;
   for (int k = 0; k < K; ++k)
-    if (cs[kScrMaxK + k] > -INFINITY) valid |= 1u << k;
-  const int halves = (K * D + kHalfCols - 1) / kHalfCols;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  uint32_t phase = 0;
-  bool ok = true;
-  const int64_t ntiles = (a.N + kScrRows - 1) / kScrRows;
+    if (cs[kFcMaxK + k] > -INFINITY) valid |= 1u << k;
+  const int nq = (K * D + kQCols - 1) / kQCols;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  uint32_t uses[2] = {0u, 0u};
+  bool ok = loaded;
+
+  auto issue = [&](int q) {  // thread 0: quarter q into TMEM buffer q & 1
+    tc::tc_fence_after();
+    const int n0 = q * kQCols, nn = min(kQCols, K * D - n0);
+    const uint32_t idesc = tc::idesc_f16_f32(kScrRows, nn);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint64_t da = tc::sdesc_k128(tc::smem_addr(sA + ks * 32));
+      const uint64_t db = tc::sdesc_k128(tc::smem_addr(sB + (size_t)n0 * 128 + ks * 32));
+      tc::mma_f16(tmem + (uint32_t)((q & 1) * kQCols), da, db, idesc, ks > 0 ? 1u : 0u);
+    }
+    tc::mma_commit(&bar[q & 1]);
+  };
+
   for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-    const int64_t row = t * kScrRows + tid;
-    const bool in = row < a.N;
-    // the A tile: this thread's row, 128-byte swizzled, K padded to 64
+    const int64_t row = t * kScrRows + r;
+    // the A tile (128-byte swizzled rows) and this half's |x|^2
     float nx2 = 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (c < D / 8 && in) {
-        v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)row * D) + c);
-        const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+    for (int c = 0; c < 4; ++c) {
+      const int cc = 4 * hh + c;
+      const __half2* h2 = reinterpret_cast<const __half2*>(&xr[c]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __half22float2(h2[q]);
-          nx2 = fmaf(f.x, f.x, nx2);
-          nx2 = fmaf(f.y, f.y, nx2);
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(h2[q]);
+        nx2 = fmaf(f.x, f.x, nx2);
+        nx2 = fmaf(f.y, f.y, nx2);
       }
-      *reinterpret_cast<uint4*>(sA + tid * 128 + ((c ^ (tid & 7)) << 4)) = v;
+      *reinterpret_cast<uint4*>(sA + r * 128 + ((cc ^ (r & 7)) << 4)) = xr[c];
     }
-    const float nx = sqrtf(nx2) * (1.f + 1e-5f);
+    xch[hh * kScrRows + r] = nx2;
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
-    float hi[kScrMaxK];
+    if (tid == 0) issue(0);
+    if (t + gridDim.x < ntiles) fetch(t + gridDim.x);
+    const float nxx = xch[r] + xch[kScrRows + r];
+    const float nx = sqrtf(nxx) * (1.f + 1e-5f);
+    // upper bounds of this thread's components: quarter q, k = q CPQ + 2 j + hh
+    float hi[4][CPQ / 2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int j = 0; j < CPQ / 2; ++j) hi[q][j] = -INFINITY;
     float best_lo = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kScrMaxK; ++k) hi[k] = -INFINITY;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (h >= halves) break;
-      if (tid == 0) {
-        tc::tc_fence_after();
-        const int ncols = min(kHalfCols, K * D - h * kHalfCols);
-        for (int n0 = 0; n0 < ncols; n0 += 256) {
-          const int nn = min(256, ncols - n0);
-          const uint32_t idesc = tc::idesc_f16_f32(kScrRows, nn);
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            const uint64_t da = tc::sdesc_k128(tc::smem_addr(sA + ks * 32));
-            const uint64_t db = tc::sdesc_k128(tc::smem_addr(sB + (size_t)(h * kHalfCols + n0) * 128 + ks * 32));
-            tc::mma_f16(tmem + (uint32_t)n0, da, db, idesc, ks > 0 ? 1u : 0u);
-          }
-        }
-        tc::mma_commit(bar);
+    for (int q = 0; q < 4; ++q) {
+      if (q >= nq) break;
+      if (tid == 0 && q + 1 < nq) issue(q + 1);
+      const bool got = tc::mbar_wait(&bar[q & 1], uses[q & 1] & 1u, kScrWait);
+      ++uses[q & 1];
+      ok = __syncthreads_and(got) != 0;
+      if (!ok) {
+        if (tid == 0) raise_status(a.st, GMM_ERR_TIMEOUT);
+        break;
       }
-      const bool got = tc::mbar_wait(bar, phase, kScrWait);
-      phase ^= 1u;
-      ok = __syncthreads_and(got) != 0;  // the same outcome in every thread
-      if (!ok && tid == 0) raise_status(a.st, GMM_ERR_TIMEOUT);
       tc::tc_fence_after();
-      if (ok) {
 #pragma unroll
-        for (int kk = 0; kk < CPH; ++kk) {
-          const int k = h * CPH + kk;
-          if (k >= K || k >= kScrMaxK) break;
-          const float s = cs[k], ck = cs[kScrMaxK + k];
-          float z2a = 0.f, z2b = 0.f;
+      for (int j = 0; j < CPQ / 2; ++j) {
+        const int kk = 2 * j + hh, k = q * CPQ + kk;
+        if (k >= K) break;
+        const float sk = cs[k], ck = cs[kFcMaxK + k];
+        const float* bk = cs + 4 * kFcMaxK + k * D;
+        float z2a = 0.f, z2b = 0.f;
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            float v[32];
-            tc::tmem_ld32(tmem + lane_base + (uint32_t)(kk * D + c0), v);
-            const float* bk = sb + k * D + c0;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(tmem + lane_base + (uint32_t)((q & 1) * kQCols + kk * D + c0), v);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float z0 = fmaf(s, v[i], -bk[i]);
-              const float z1 = fmaf(s, v[i + 1], -bk[i + 1]);
-              z2a = fmaf(z0, z0, z2a);
-              z2b = fmaf(z1, z1, z2b);
-            }
+          for (int i = 0; i < 32; i += 2) {
+            const float z0 = fmaf(sk, v[i], -bk[c0 + i]);
+            const float z1 = fmaf(sk, v[i + 1], -bk[c0 + i + 1]);
+            z2a = fmaf(z0, z0, z2a);
+            z2b = fmaf(z1, z1, z2b);
           }
-          const float nz = sqrtf(z2a + z2b);
-          const float E = cs[2 * kScrMaxK + k] * nx + cs[3 * kScrMaxK + k] + 3.0517578125e-05f * nz;
-          const float dl = fmaxf(0.f, nz - E), dh = nz + E;
-          const float lo = ck - 0.5f * dh * dh;
-          hi[k] = ck - 0.5f * dl * dl;
-          if (ck > -INFINITY) best_lo = fmaxf(best_lo, lo);
         }
+        const float nz = sqrtf(z2a + z2b);
+        const float E = cs[2 * kFcMaxK + k] * nx + cs[3 * kFcMaxK + k] + 3.0517578125e-05f * nz;
+        const float dl = fmaxf(0.f, nz - E), dh = nz + E;
+        hi[q][j] = ck - 0.5f * dl * dl;
+        if (ck > -INFINITY) best_lo = fmaxf(best_lo, ck - 0.5f * dh * dh);
       }
       tc::tc_fence_before();
       __syncthreads();
-      if (!ok) break;
     }
-    if (ok && in) {
-      uint32_t m = 0u;
+    if (!ok) break;
+    // the two threads of a point: the best lower bound, then the mask
+    xch[2 * kScrRows + hh * kScrRows + r] = best_lo;
+    __syncthreads();
+    const float b2 = fmaxf(xch[2 * kScrRows + r], xch[3 * kScrRows + r]);
+    uint32_t m = 0u;
 #pragma unroll
-      for (int k = 0; k < kScrMaxK; ++k)
-        if (k < K && hi[k] >= best_lo - 41.f) m |= 1u << k;
-      if (!isfinite(nx2) || !(best_lo > -INFINITY) || isnan(best_lo)) m = valid;
-      a.mask[row] = m & valid;
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int j = 0; j < CPQ / 2; ++j) {
+        const int k = q * CPQ + 2 * j + hh;
+        if (k < K && hi[q][j] >= b2 - 41.f) m |= 1u << k;
+      }
+    __syncthreads();  // both halves have read the lower bounds
+    reinterpret_cast<uint32_t*>(xch)[hh * kScrRows + r] = m;
+    __syncthreads();
+    if (hh == 0 && row < a.N) {
+      uint32_t mm = m | reinterpret_cast<const uint32_t*>(xch)[kScrRows + r];
+      if (!isfinite(nxx) || !(b2 > -INFINITY) || isnan(b2)) mm = valid;
+      a.mask[row] = mm & valid;
     }
+    __syncthreads();  // the exchange area and the A tile are free again
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, kHalfCols);
+    tc::tmem_dealloc(tmem, 2 * kQCols);
   }
 }
 
 }  // namespace
 
-// The screen covers fp16 X with D in {32, 64} and K D <= 1024.
+// The screen covers fp16 X with the shapes fc_tc_shape admits.
 bool fc_screen_eligible(int D, int K, int xdtype) {
-  return xdtype == GMM_F16 && (D == 32 || D == 64) && K >= 1 && K <= kScrMaxK &&
-         K * D <= 2 * kHalfCols;
+  return xdtype == GMM_F16 && fc_tc_shape(D, K, GMM_COV_FULL);
 }
 
 cudaError_t fc_screen(const void* X, int64_t N, int D, int K, const void* prepared,
@@ -291,9 +267,8 @@ cudaError_t fc_screen(const void* X, int64_t N, int D, int K, const void* prepar
   ScrArgs a;
   a.X = static_cast<const __half*>(X);
   a.N = N; a.K = K;
-  a.W = at<float>(prepared, PL.off_prec);
-  a.mu = at<float>(prepared, PL.off_mu);
-  a.bias = at<float>(prepared, PL.off_c);
+  a.B = at<unsigned char>(prepared, PL.off_fcB);
+  a.T = at<float>(prepared, PL.off_fcT);
   a.mask = mask; a.st = st;
   // at least 116 KB of shared memory, so a single block holds an SM's TMEM
   size_t smem = ScrLayout::make(D, K).bytes;

@@ -21,7 +21,7 @@
 //             the log-likelihood.
 //   fc_stats  a block per (component, partition of the points): the
 //             partition's candidates of the component, their log joints
-//             recomputed with four threads a point (bit-identical to fc_lse),
+//             recomputed a thread per point (bit-identical to fc_lse),
 //             g = exp(l - LSE_n) and y = x - mu gathered into chunks of up to
 //             256 points; per chunk s0, the chunk mean and the second moment
 //             about it in fp32 (4 x 4 register tiles of the lower triangle),
@@ -39,12 +39,11 @@ namespace gmm {
 namespace {
 
 constexpr int kFcT = 128;          // points per fc_lse tile
-constexpr int kFcThreads = 512;    // fc_lse block
+constexpr int kFcThreads = 256;    // fc_lse block (two pairs a thread)
 constexpr int kFcGrid = 152;       // fc_lse blocks (fixed: the log-likelihood partial count)
 constexpr int kFsThreads = 256;    // fc_stats block
-constexpr int kFsTile = 256;       // partition points per mask tile (one per thread)
+constexpr int kFsTile = 1024;      // partition points per mask tile (four per thread)
 constexpr int kFsChunk = 256;      // candidate points per fp32 chunk
-constexpr int kFcMaxK = 32;        // one mask word per point
 
 // Floats of one component's padded W.  The rows 4m .. 4m + 3 hold 4(m + 1)
 // floats each (zero beyond the diagonal), stored interleaved by 16-byte
@@ -116,35 +115,92 @@ __device__ __forceinline__ float fc_part(const float* __restrict__ Wk, const flo
   return __fadd_rn(s, c);
 }
 
-// Stages component k's W rows (padded, zero beyond the diagonal) at dst.
+// fc_part for two points under the same component: every W load serves
+// both, the arithmetic of each is that of fc_part.
 template <int D>
-__device__ __forceinline__ void stage_w(float* dst, const float* __restrict__ Wk, int i) {
-  const int m = i >> 2, q = i & 3;
-  float* row = dst + 8 * m * (m + 1) + 4 * q;
-  for (int j = 0; j < 4 * (m + 1); ++j)
-    row[16 * (j >> 2) + (j & 3)] = j <= i ? __ldg(Wk + (size_t)i * D + j) : 0.f;
+__device__ __forceinline__ void fc_part2(const float* __restrict__ Wk, const float2 (&ya)[D / 2],
+                                         const float2 (&yb)[D / 2], int q, float& pa, float& pb) {
+  constexpr int M = D / 4;
+  float sa = 0.f, ca = 0.f, sb = 0.f, cb = 0.f;
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const float* w = Wk + 8 * m * (m + 1) + 4 * q;
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+#pragma unroll
+    for (int bk = 0; bk <= m; ++bk) {
+      const float4 wv = *reinterpret_cast<const float4*>(w + 16 * bk);
+      a0 = fma2(make_float2(wv.x, wv.y), ya[2 * bk], a0);
+      a1 = fma2(make_float2(wv.z, wv.w), ya[2 * bk + 1], a1);
+      b0 = fma2(make_float2(wv.x, wv.y), yb[2 * bk], b0);
+      b1 = fma2(make_float2(wv.z, wv.w), yb[2 * bk + 1], b1);
+    }
+    const float za = __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y));
+    const float zb = __fadd_rn(__fadd_rn(b0.x, b0.y), __fadd_rn(b1.x, b1.y));
+    const float qa = __fmul_rn(za, za), qb = __fmul_rn(zb, zb);
+    const float ta = __fadd_rn(sa, qa), tb = __fadd_rn(sb, qb);
+    ca = __fadd_rn(ca, sa >= qa ? __fadd_rn(__fsub_rn(sa, ta), qa) : __fadd_rn(__fsub_rn(qa, ta), sa));
+    cb = __fadd_rn(cb, sb >= qb ? __fadd_rn(__fsub_rn(sb, tb), qb) : __fadd_rn(__fsub_rn(qb, tb), sb));
+    sa = ta;
+    sb = tb;
+  }
+  pa = __fadd_rn(sa, ca);
+  pb = __fadd_rn(sb, cb);
+}
+
+// Raw 16-byte chunk of stored coordinates -> four or eight floats.
+template <int XT>
+__device__ __forceinline__ void raw_to_float2(const uint4& u, float2* f) {
+  if constexpr (XT == GMM_F32) {
+    f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+    f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+  } else {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if constexpr (XT == GMM_F16) f[q] = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+      else f[q] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+    }
+  }
+}
+
+// Stages the W of components [0, nk) (padded rows, zero beyond the diagonal)
+// at dst with component stride `stride`, one element a thread per step.
+template <int D>
+__device__ __forceinline__ void stage_w(float* dst, int stride, const float* __restrict__ W, int nk,
+                                        int tid, int nthreads) {
+#pragma unroll 8
+  for (int e = tid; e < nk * D * D; e += nthreads) {
+    const int k = e / (D * D), i = (e / D) % D, j = e % D;
+    const int m = i >> 2, q = i & 3;
+    if (j < 4 * (m + 1))
+      dst[k * stride + 8 * m * (m + 1) + 4 * q + 16 * (j >> 2) + (j & 3)] = j <= i ? __ldg(W + e) : 0.f;
+  }
 }
 
 template <int D, int XT>
 __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
-  constexpr int WS = fc_wstride(D), XS = D + 4, NW = kFcT / 32;
+  constexpr int WS = fc_wstride(D), NW = kFcT / 32;
+  constexpr int ESZ = XT == GMM_F32 ? 4 : 2;
+  constexpr int RB = D * ESZ;                 // bytes of a stored row
+  constexpr int C16 = RB / 16;                // its 16-byte chunks
+  constexpr int VPC = 16 / ESZ;               // coordinates per chunk
+  constexpr int XPT = kFcT * C16 / kFcThreads;  // chunks of the tile a thread loads
+  static_assert(XPT >= 1 && XPT * kFcThreads == kFcT * C16, "tile load split");
   extern __shared__ __align__(16) float sm[];
   const int K = a.K;
   float* sW = sm;                                    // K * WS
   float* sMu = sW + K * WS;                          // K * D
   float* sC = sMu + K * D;                           // kFcMaxK
-  float* xs = sC + kFcMaxK;                          // kFcT * XS
-  float* lval = xs + kFcT * XS;                      // kFcT * K
+  unsigned char* xs = reinterpret_cast<unsigned char*>(sC + kFcMaxK);  // kFcT rows as stored
+  float* lval = reinterpret_cast<float*>(xs + kFcT * RB);             // kFcT * K
   uint32_t* cm = reinterpret_cast<uint32_t*>(lval + kFcT * K);  // K * NW
   uint32_t* msk = cm + K * NW;                       // kFcT
-  int* offs = reinterpret_cast<int*>(msk + kFcT);    // kFcMaxK + 4
-  uint8_t* prow = reinterpret_cast<uint8_t*>(offs + kFcMaxK + 4);  // kFcT * K
+  int* offs = reinterpret_cast<int*>(msk + kFcT);    // kFcMaxK + 1: pairs
+  int* toff = offs + kFcMaxK + 1;                    // kFcMaxK + 1: tasks (two pairs each)
+  uint8_t* prow = reinterpret_cast<uint8_t*>(toff + kFcMaxK + 3);  // kFcT * K
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < K * D; e += kFcThreads) {
-    const int k = e / D, i = e % D;
-    stage_w<D>(sW + k * WS, a.W + (size_t)k * D * D, i);
-    sMu[e] = __ldg(a.mu + e);
-  }
+  stage_w<D>(sW, WS, a.W, K, tid, kFcThreads);
+  for (int e = tid; e < K * D; e += kFcThreads) sMu[e] = __ldg(a.mu + e);
   for (int k = tid; k < kFcMaxK; k += kFcThreads) sC[k] = k < K ? __ldg(a.bias + k) : -INFINITY;
   __syncthreads();
   uint32_t valid = 0u;
@@ -152,39 +208,56 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
     if (sC[k] > -INFINITY) valid |= 1u << k;
   const int64_t ntiles = (a.N + kFcT - 1) / kFcT;
   double ll = 0.0;
+  // the next tile's masks and rows (as stored) are requested while this one is used
+  uint32_t mnext = 0u;
+  uint4 xnext[XPT];
+  auto fetch = [&](int64_t t) {
+    const int64_t r0 = t * kFcT;
+    const int rows = (int)min((int64_t)kFcT, a.N - r0);
+    if (tid < kFcT) mnext = tid < rows ? __ldg(a.mask + r0 + tid) : 0u;
+#pragma unroll
+    for (int c = 0; c < XPT; ++c) {
+      const int e = tid + c * kFcThreads, r = e / C16, q = e % C16;
+      xnext[c] = r < rows ? __ldg(reinterpret_cast<const uint4*>(
+                                static_cast<const unsigned char*>(a.X) + (size_t)(r0 + r) * RB) + q)
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if ((int64_t)blockIdx.x < ntiles) fetch(blockIdx.x);
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int64_t r0 = t * kFcT;
     const int rows = (int)min((int64_t)kFcT, a.N - r0);
     __syncthreads();  // the previous tile's tables are no longer read
     // masks (component-major bit columns by ballot) and the rows of X
     if (tid < kFcT) {
-      const uint32_t m = tid < rows ? __ldg(a.mask + r0 + tid) & valid : 0u;
+      const uint32_t m = mnext & valid;
       msk[tid] = m;
       for (int k = 0; k < K; ++k) {
         const uint32_t b = __ballot_sync(0xffffffffu, (m >> k) & 1u);
         if (lane == 0) cm[k * NW + warp] = b;
       }
     }
-    for (int e = tid; e < kFcT * (D / 4); e += kFcThreads) {
-      const int r = e / (D / 4), c4 = e % (D / 4);
-      const float4 v = r < rows ? load4<XT>(a.X, (size_t)(r0 + r) * D + 4 * c4)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-      *reinterpret_cast<float4*>(xs + r * XS + 4 * c4) = v;
+#pragma unroll
+    for (int c = 0; c < XPT; ++c) {
+      const int e = tid + c * kFcThreads;
+      reinterpret_cast<uint4*>(xs)[e] = xnext[c];
     }
+    if (t + gridDim.x < ntiles) fetch(t + gridDim.x);
     __syncthreads();
-    // pair offsets per component
+    // pair and task offsets per component (a task: two pairs of a component)
     if (warp == 0) {
       int cnt = 0;
       if (lane < K)
         for (int w = 0; w < NW; ++w) cnt += __popc(cm[lane * NW + w]);
-      int inc = cnt;
+      int inc = cnt, tin = (cnt + 1) >> 1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += u;
+        const int v = __shfl_up_sync(0xffffffffu, tin, o);
+        if (lane >= o) { inc += u; tin += v; }
       }
-      if (lane < K) offs[lane + 1] = inc;
-      if (lane == 0) offs[0] = 0;
+      if (lane < K) { offs[lane + 1] = inc; toff[lane + 1] = tin; }
+      if (lane == 0) { offs[0] = 0; toff[0] = 0; }
     }
     __syncthreads();
     // the pair list: component-major, rows ascending
@@ -198,23 +271,34 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
       }
     }
     __syncthreads();
-    const int np = offs[K];
+    const int nt = toff[K];
     int kk = 0;
-    for (int p = tid; p < np; p += kFcThreads) {
-      while (offs[kk + 1] <= p) ++kk;
-      const int r = prow[p];
-      float2 y2[D / 2];
+    for (int tk = tid; tk < nt; tk += kFcThreads) {
+      while (toff[kk + 1] <= tk) ++kk;
+      const int p = offs[kk] + 2 * (tk - toff[kk]);
+      const bool two = p + 1 < offs[kk + 1];
+      const int ra = prow[p], rb = prow[two ? p + 1 : p];
+      float2 ya[D / 2], yb[D / 2];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 4; ++c4) {
-        const float4 xv = *reinterpret_cast<const float4*>(xs + r * XS + 4 * c4);
-        const float4 mv = *reinterpret_cast<const float4*>(sMu + kk * D + 4 * c4);
-        y2[2 * c4] = sub2(make_float2(xv.x, xv.y), make_float2(mv.x, mv.y));
-        y2[2 * c4 + 1] = sub2(make_float2(xv.z, xv.w), make_float2(mv.z, mv.w));
+      for (int c = 0; c < C16; ++c) {
+        float2 fa[VPC / 2], fb[VPC / 2];
+        raw_to_float2<XT>(*reinterpret_cast<const uint4*>(xs + ra * RB + 16 * c), fa);
+        raw_to_float2<XT>(*reinterpret_cast<const uint4*>(xs + rb * RB + 16 * c), fb);
+#pragma unroll
+        for (int v = 0; v < VPC / 2; ++v) {
+          const float2 mv = *reinterpret_cast<const float2*>(sMu + kk * D + c * VPC + 2 * v);
+          ya[c * (VPC / 2) + v] = sub2(fa[v], mv);
+          yb[c * (VPC / 2) + v] = sub2(fb[v], mv);
+        }
       }
       const float* Wk = sW + kk * WS;
-      const float d2 = __fadd_rn(__fadd_rn(fc_part<D>(Wk, y2, 0), fc_part<D>(Wk, y2, 1)),
-                                 __fadd_rn(fc_part<D>(Wk, y2, 2), fc_part<D>(Wk, y2, 3)));
-      lval[p] = __fsub_rn(sC[kk], __fmul_rn(0.5f, d2));
+      float pa[4], pb[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) fc_part2<D>(Wk, ya, yb, q, pa[q], pb[q]);
+      const float da = __fadd_rn(__fadd_rn(pa[0], pa[1]), __fadd_rn(pa[2], pa[3]));
+      const float db = __fadd_rn(__fadd_rn(pb[0], pb[1]), __fadd_rn(pb[2], pb[3]));
+      lval[p] = __fsub_rn(sC[kk], __fmul_rn(0.5f, da));
+      if (two) lval[p + 1] = __fsub_rn(sC[kk], __fmul_rn(0.5f, db));
     }
     __syncthreads();
     // LSE_n over the point's candidates in component order
@@ -276,6 +360,7 @@ struct FsLayout {
   static constexpr size_t CAND = M2R + sizeof(double) * S::NB * 16;
   static constexpr size_t WCNT = CAND + sizeof(uint32_t) * kFsTile;
   static constexpr size_t BYTES = WCNT + sizeof(int) * (kFsThreads / 32);
+  static_assert(kFsTile == 4 * kFsThreads, "four mask words a thread");
 };
 
 template <int D, int XT>
@@ -308,8 +393,8 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
       for (int f = tid; f < F; f += kFsThreads) out[f] = 0.0;
     return;
   }
+  stage_w<D>(sW, 0, a.W + (size_t)k * D * D, 1, tid, kFsThreads);
   for (int i = tid; i < D; i += kFsThreads) {
-    stage_w<D>(sW, a.W + (size_t)k * D * D, i);
     sMu[i] = __ldg(a.mu + (size_t)k * D + i);
     s1r[i] = 0.0;
     mr[i] = 0.0;
@@ -390,60 +475,75 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
     __syncthreads();
   };
 
+  // Mask tiles of kFsTile points, four consecutive points a thread (the next
+  // tile's masks are requested before this one is used); candidates of k in
+  // point order; then a thread per candidate, in groups that fill the chunk.
   int fill = 0;
+  uint4 mnext = make_uint4(0u, 0u, 0u, 0u);
+  auto fetch = [&](int64_t t0) {
+    const int64_t rr = t0 + 4 * tid;
+    if (rr + 3 < r1) {
+      mnext = __ldg(reinterpret_cast<const uint4*>(a.mask + rr));
+    } else {
+      mnext.x = rr < r1 ? __ldg(a.mask + rr) : 0u;
+      mnext.y = rr + 1 < r1 ? __ldg(a.mask + rr + 1) : 0u;
+      mnext.z = rr + 2 < r1 ? __ldg(a.mask + rr + 2) : 0u;
+      mnext.w = rr + 3 < r1 ? __ldg(a.mask + rr + 3) : 0u;
+    }
+  };
+  if (r0 < r1) fetch(r0);
   for (int64_t t0 = r0; t0 < r1; t0 += kFsTile) {
-    const int rows = (int)min((int64_t)kFsTile, r1 - t0);
-    // the tile's candidates of component k, rows ascending
-    const bool bit = tid < rows && ((__ldg(a.mask + t0 + tid) >> k) & 1u);
-    const uint32_t bal = __ballot_sync(0xffffffffu, bit);
-    if (lane == 0) wcnt[warp] = __popc(bal);
+    const uint32_t bits = ((mnext.x >> k) & 1u) | (((mnext.y >> k) & 1u) << 1) |
+                          (((mnext.z >> k) & 1u) << 2) | (((mnext.w >> k) & 1u) << 3);
+    if (t0 + kFsTile < r1) fetch(t0 + kFsTile);
+    // block-wide exclusive count of the candidates before this thread's points
+    const int cnt = __popc(bits);
+    int inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    if (lane == 31) wcnt[warp] = inc;
     __syncthreads();
-    int base = 0, ncand = 0;
+    int base = inc - cnt, ncand = 0;
     for (int w = 0; w < kFsThreads / 32; ++w) {
       if (w < warp) base += wcnt[w];
       ncand += wcnt[w];
     }
-    if (bit) cand[base + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)(t0 + tid);
+    for (uint32_t b = bits; b; b &= b - 1u) cand[base++] = (uint32_t)(t0 + 4 * tid + __ffs(b) - 1);
     __syncthreads();
-    // groups of 64 candidates, four threads each (thread q: rows i = q mod 4)
-    for (int g0 = 0; g0 < ncand; g0 += kFsThreads / 4) {
-      const int ng = min(kFsThreads / 4, ncand - g0);
-      if (fill + ng > kFsChunk) {
-        process_chunk(fill);
-        fill = 0;
-      }
-      const int pi = tid >> 2, q = tid & 3;
-      const uint32_t row = cand[g0 + min(pi, ng - 1)];
-      float2 y2[D / 2];
+    for (int g0 = 0; g0 < ncand;) {
+      const int ng = min(min(kFsThreads, ncand - g0), kFsChunk - fill);
+      if (tid < ng) {
+        const uint32_t row = cand[g0 + tid];
+        const float lr = __ldg(a.lse + row);
+        float2 y2[D / 2];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 4; ++c4) {
-        const float4 xv = load4<XT>(a.X, (size_t)row * D + 4 * c4);
-        const float4 mv = *reinterpret_cast<const float4*>(sMu + 4 * c4);
-        y2[2 * c4] = sub2(make_float2(xv.x, xv.y), make_float2(mv.x, mv.y));
-        y2[2 * c4 + 1] = sub2(make_float2(xv.z, xv.w), make_float2(mv.z, mv.w));
-      }
-      const float part = fc_part<D>(sW, y2, q);
-      // ((p0 + p1) + (p2 + p3)), as fc_lse
-      const float u = __fadd_rn(part, __shfl_down_sync(0xffffffffu, part, 1));
-      const float d2 = __fadd_rn(u, __shfl_down_sync(0xffffffffu, u, 2));
-      const float l = __fsub_rn(ck, __fmul_rn(0.5f, d2));
-      const float g = __shfl_sync(0xffffffffu, expf(l - __ldg(a.lse + row)), lane & ~3);
-      if (pi < ng) {
-        // thread q stores the 16-byte chunks q, q + 4, ... of y (the four
-        // threads of a point write adjacent chunks: no bank conflict)
-        float* yr = ys + (fill + pi) * YS;
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          float2 v0 = y2[0], v1 = y2[1];
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
-            if (qq == q) { v0 = y2[2 * (4 * c + qq)]; v1 = y2[2 * (4 * c + qq) + 1]; }
-          *reinterpret_cast<float4*>(yr + 4 * (4 * c + q)) = make_float4(v0.x, v0.y, v1.x, v1.y);
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+          const float4 xv = load4<XT>(a.X, (size_t)row * D + 4 * c4);
+          const float4 mv = *reinterpret_cast<const float4*>(sMu + 4 * c4);
+          y2[2 * c4] = sub2(make_float2(xv.x, xv.y), make_float2(mv.x, mv.y));
+          y2[2 * c4 + 1] = sub2(make_float2(xv.z, xv.w), make_float2(mv.z, mv.w));
         }
-        if (q == 0) gch[fill + pi] = g;
+        // ((p0 + p1) + (p2 + p3)), as fc_lse
+        const float d2 = __fadd_rn(__fadd_rn(fc_part<D>(sW, y2, 0), fc_part<D>(sW, y2, 1)),
+                                   __fadd_rn(fc_part<D>(sW, y2, 2), fc_part<D>(sW, y2, 3)));
+        const float l = __fsub_rn(ck, __fmul_rn(0.5f, d2));
+        float* yr = ys + (fill + tid) * YS;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4)
+          *reinterpret_cast<float4*>(yr + 4 * c4) =
+              make_float4(y2[2 * c4].x, y2[2 * c4].y, y2[2 * c4 + 1].x, y2[2 * c4 + 1].y);
+        gch[fill + tid] = expf(l - lr);
       }
       __syncthreads();
       fill += ng;
+      g0 += ng;
+      if (fill == kFsChunk) {
+        process_chunk(fill);
+        fill = 0;
+      }
     }
   }
   if (fill > 0) process_chunk(fill);
@@ -484,16 +584,17 @@ __global__ void fc_mask_all_kernel(uint32_t* mask, int64_t N, int K, const float
     mask[i] = valid;
 }
 
-size_t fc_lse_smem(int D, int K) {
-  return sizeof(float) * ((size_t)K * fc_wstride(D) + (size_t)K * D + kFcMaxK +
-                          (size_t)kFcT * (D + 4) + (size_t)kFcT * K) +
-         sizeof(uint32_t) * ((size_t)K * (kFcT / 32) + kFcT) + sizeof(int) * (kFcMaxK + 4) +
+size_t fc_lse_smem(int D, int K, int xdtype) {
+  const size_t rb = (size_t)D * (xdtype == GMM_F32 ? 4 : 2);
+  return sizeof(float) * ((size_t)K * fc_wstride(D) + (size_t)K * D + kFcMaxK) + kFcT * rb +
+         sizeof(float) * (size_t)kFcT * K +
+         sizeof(uint32_t) * ((size_t)K * (kFcT / 32) + kFcT) + sizeof(int) * (2 * kFcMaxK + 5) +
          (size_t)kFcT * K;
 }
 
 template <int D, int XT>
 cudaError_t run_fc(const FcArgs& a, int parts, cudaStream_t s) {
-  const size_t sl = fc_lse_smem(D, a.K);
+  const size_t sl = fc_lse_smem(D, a.K, XT);
   cudaError_t e = cudaFuncSetAttribute(fc_lse_kernel<D, XT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl);
   if (e != cudaSuccess) return e;
@@ -527,7 +628,7 @@ cudaError_t fc_screen(const void* X, int64_t N, int D, int K, const void* prepar
 // shared memory of one fc_lse block.
 bool fc_eligible(int D, int K, int cov) {
   if (cov != GMM_COV_FULL || !(D == 16 || D == 32 || D == 64) || K < 1 || K > kFcMaxK) return false;
-  return fc_lse_smem(D, K) <= (size_t)200 * 1024;
+  return fc_lse_smem(D, K, GMM_F32) <= (size_t)200 * 1024;
 }
 
 // Log-likelihood partials fc_estep writes (fc_lse blocks).

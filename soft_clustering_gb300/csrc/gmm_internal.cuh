@@ -96,6 +96,17 @@ __host__ __device__ inline bool tc_fold(int chunks) { return chunks <= kTcFoldCh
 constexpr uint32_t kRecSingle = 1u << 31;
 constexpr uint32_t kRecKMask = 0xffffffu;  // component = (key >> 7) & kRecKMask
 
+// Full covariance with few components: the tensor-core screen of
+// z = W_k (x - mu_k) (fc_screen.cu) takes D = 32 or 64 and K D <= 1024.  Its
+// operands, written by gmm_prepare: the B image [K D rows][128 bytes] of
+// fp16(W_k / s_k) as 128-byte swizzled K-major rows (the contraction
+// dimension padded with zeros to 64), and fp32 [s_k (32) | bias_k (32) |
+// ex_k (32) | em_k (32) | b_k = W_k mu_k (K D)].
+constexpr int kFcMaxK = 32;
+__host__ __device__ inline bool fc_tc_shape(int D, int K, int cov) {
+  return cov == GMM_COV_FULL && (D == 32 || D == 64) && K >= 1 && K <= kFcMaxK && K * D <= 1024;
+}
+
 // Prepared-parameter block written by gmm_prepare.
 struct PreparedLayout {
   int D, K, cov;
@@ -113,6 +124,8 @@ struct PreparedLayout {
                      // bias - delta [128], bias + delta [128] (the scale is the chunk's, common to its
                      // components); folded: see tc_fold
   size_t tc_bytes;
+  size_t off_fcB;    // full covariance (fc_tc_shape): the screen's B image
+  size_t off_fcT;    // ... and its fp32 constants
   size_t bytes;
 
   __host__ __device__ static PreparedLayout make(int D, int K, int cov) {
@@ -136,6 +149,14 @@ struct PreparedLayout {
       L.off_tcT = o;
       o = align_up(o + sizeof(float) * kTcTrail * L.tc_chunks);
       L.tc_bytes = o - L.off_tcB;
+    }
+    L.off_fcB = L.off_fcT = o;
+    if (fc_tc_shape(D, K, cov)) {
+      o = align_up(o, 1024);
+      L.off_fcB = o;
+      o = align_up(o + (size_t)K * D * 128);
+      L.off_fcT = o;
+      o = align_up(o + sizeof(float) * (4 * kFcMaxK + (size_t)K * D));
     }
     L.bytes = align_up(o);
     return L;

@@ -24,14 +24,19 @@ namespace {
 // m_p = S1_p / S0_p and m = S1 / S0 (the pairwise update of Chan, Golub and
 // LeVeque, applied to all partitions at once).  centre: the mean the
 // statistics were taken about (fp32 [K*D]).  Updates params in place.
-// dynamic smem: F doubles.
+// Grid (K, Y): block (k, y) takes the second-moment entries [y B, (y + 1) B)
+// of component k (B = blockDim.x, one entry a thread; Y = 1 for diagonal and
+// isotropic covariance), every block of k the same sums S0, S1.  Block y = 0
+// writes pi and mu; flags_out (zeroed by the launcher) collects every
+// block's flags by OR.  dynamic smem: (1 + D) + parts doubles.
 __global__ void mstep_kernel(const double* __restrict__ part, int parts, int64_t N, int D, int K,
                              int cov, const float* __restrict__ centre,
                              const int32_t* __restrict__ prep_flags, float var_floor,
                              float min_s0, float* pi, float* mu, float* covp,
                              int32_t* flags_out) {
   extern __shared__ double s[];
-  const int k = blockIdx.x;
+  double* inv0 = s + 1 + D;  // 1 / S0_p (0 where S0_p = 0)
+  const int k = blockIdx.x, y = blockIdx.y;
   const int F = stat_width(D, cov);
   auto P_ = [&](int p, int f) { return part[((size_t)p * K + k) * F + f]; };
   for (int f = threadIdx.x; f <= D; f += blockDim.x) {
@@ -39,73 +44,71 @@ __global__ void mstep_kernel(const double* __restrict__ part, int parts, int64_t
     for (int p = 0; p < parts; ++p) acc += P_(p, f);
     s[f] = acc;
   }
+  for (int p = threadIdx.x; p < parts; p += blockDim.x) {
+    const double c0 = P_(p, 0);
+    inv0[p] = c0 > 0.0 ? 1.0 / c0 : 0.0;
+  }
   __syncthreads();
   const double s0 = s[0];
   const bool empty = !(s0 >= (double)min_s0) || !(s0 > 0.0);
   const int nm2 = cov == GMM_COV_FULL ? D * (D + 1) / 2 : D;
-  for (int e = threadIdx.x; e < nm2; e += blockDim.x) {
-    int a, b;
-    if (cov == GMM_COV_FULL) {
-      a = (int)((sqrt(8.0 * e + 1.0) - 1.0) * 0.5);
-      while ((a + 1) * (a + 2) / 2 <= e) ++a;
-      while (a * (a + 1) / 2 > e) --a;
-      b = e - a * (a + 1) / 2;
-    } else {
-      a = b = e;
-    }
-    double acc = 0.0;
-    if (s0 > 0.0) {
-      const double ma = s[1 + a] / s0, mb = s[1 + b] / s0;
-      for (int p = 0; p < parts; ++p) {
-        const double c0 = P_(p, 0);
-        acc += P_(p, 1 + D + e);
-        if (c0 > 0.0) acc += c0 * (P_(p, 1 + a) / c0 - ma) * (P_(p, 1 + b) / c0 - mb);
-      }
-    }
-    s[1 + D + e] = acc;
-  }
-  __syncthreads();
   __shared__ int s_floor;
   if (threadIdx.x == 0) s_floor = 0;
+  // this thread's entry (full: e enumerates the lower triangle row by row)
+  const int e = y * blockDim.x + threadIdx.x;
+  int a = e, b = e;
+  if (cov == GMM_COV_FULL && e < nm2) {
+    a = (int)((sqrt(8.0 * e + 1.0) - 1.0) * 0.5);
+    while ((a + 1) * (a + 2) / 2 <= e) ++a;
+    while (a * (a + 1) / 2 > e) --a;
+    b = e - a * (a + 1) / 2;
+  }
+  double m2 = 0.0;
+  if (e < nm2 && s0 > 0.0) {
+    const double ma = s[1 + a] / s0, mb = s[1 + b] / s0;
+    for (int p = 0; p < parts; ++p) {
+      const double c0 = P_(p, 0);
+      m2 += P_(p, 1 + D + e);
+      if (c0 > 0.0) m2 += c0 * (P_(p, 1 + a) * inv0[p] - ma) * (P_(p, 1 + b) * inv0[p] - mb);
+    }
+  }
   __syncthreads();
   int floored = 0;
-  if (!empty) {
-    const double inv = 1.0 / s0;
-    const float* c = centre + (size_t)k * D;
-    if (cov == GMM_COV_FULL) {
-      float* S = covp + (size_t)k * D * D;
-      for (int e = threadIdx.x; e < D * (D + 1) / 2; e += blockDim.x) {
-        int a = (int)((sqrt(8.0 * e + 1.0) - 1.0) * 0.5);
-        while ((a + 1) * (a + 2) / 2 <= e) ++a;
-        while (a * (a + 1) / 2 > e) --a;
-        const int b = e - a * (a + 1) / 2;
-        double v = s[1 + D + e] * inv;
-        if (a == b && v < (double)var_floor) { v = var_floor; floored = 1; }
-        S[(size_t)a * D + b] = (float)v;
-        S[(size_t)b * D + a] = (float)v;
-      }
-    } else if (cov == GMM_COV_DIAG) {
-      for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        double v = s[1 + D + d] * inv;
-        if (v < (double)var_floor) { v = var_floor; floored = 1; }
-        covp[(size_t)k * D + d] = (float)v;
-      }
-    } else if (threadIdx.x == 0) {
+  if (cov == GMM_COV_ISO) {
+    // one block (D <= blockDim): the mean of the diagonal
+    if (e < nm2) inv0[e] = m2;  // the partition reciprocals are no longer read
+    __syncthreads();
+    if (!empty && threadIdx.x == 0) {
       double acc = 0.0;
-      for (int d = 0; d < D; ++d) acc += s[1 + D + d];
-      double v = acc * inv / D;
+      for (int d = 0; d < D; ++d) acc += inv0[d];
+      double v = acc / s0 / D;
       if (v < (double)var_floor) { v = var_floor; floored = 1; }
       covp[k] = (float)v;
     }
+  } else if (!empty && e < nm2) {
+    double v = m2 / s0;
+    if (a == b && v < (double)var_floor) { v = var_floor; floored = 1; }
+    if (cov == GMM_COV_FULL) {
+      float* S = covp + (size_t)k * D * D;
+      S[(size_t)a * D + b] = (float)v;
+      S[(size_t)b * D + a] = (float)v;
+    } else {
+      covp[(size_t)k * D + e] = (float)v;
+    }
+  }
+  if (y == 0 && !empty) {
+    const double inv = 1.0 / s0;
+    const float* c = centre + (size_t)k * D;
     for (int d = threadIdx.x; d < D; d += blockDim.x)
       mu[(size_t)k * D + d] = (float)((double)c[d] + s[1 + d] * inv);
   }
   if (floored) atomicOr(&s_floor, 1);
   __syncthreads();
   if (threadIdx.x == 0) {
-    pi[k] = (float)(s0 / (double)N);
+    if (y == 0) pi[k] = (float)(s0 / (double)N);
     if (flags_out)
-      flags_out[k] = prep_flags[k] | (s_floor ? GMM_FLAG_FLOOR : 0) | (empty ? GMM_FLAG_EMPTY : 0);
+      atomicOr(flags_out + k,
+               prep_flags[k] | (s_floor ? GMM_FLAG_FLOOR : 0) | (empty ? GMM_FLAG_EMPTY : 0));
   }
 }
 
@@ -133,12 +136,18 @@ __global__ void ll_finalize_kernel(const double* __restrict__ ll_part, int64_t n
 cudaError_t launch_mstep(const double* part, int parts, int64_t N, int D, int K, int cov,
                          const float* centre, const int32_t* prep_flags, float var_floor,
                          float min_s0, gmm_params* p, int32_t* flags_out, cudaStream_t s) {
-  size_t smem = sizeof(double) * stat_width(D, cov);
+  constexpr int kThreads = 256;
+  const int nm2 = cov == GMM_COV_FULL ? D * (D + 1) / 2 : D;
+  const int ny = cov == GMM_COV_FULL ? (nm2 + kThreads - 1) / kThreads : 1;
+  const size_t smem = sizeof(double) * ((size_t)1 + D + (parts > D ? parts : D));
   cudaError_t e = cudaFuncSetAttribute(mstep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  mstep_kernel<<<K, 256, smem, s>>>(part, parts, N, D, K, cov, centre, prep_flags, var_floor,
-                                    min_s0, p->pi, p->mu, p->cov, flags_out);
+  if (flags_out && (e = cudaMemsetAsync(flags_out, 0, sizeof(int32_t) * K, s)) != cudaSuccess)
+    return e;
+  mstep_kernel<<<dim3(K, ny), kThreads, smem, s>>>(part, parts, N, D, K, cov, centre, prep_flags,
+                                                   var_floor, min_s0, p->pi, p->mu, p->cov,
+                                                   flags_out);
   return cudaGetLastError();
 }
 

@@ -112,13 +112,13 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
       }
       __syncthreads();
       if (s_fail) break;
-      const double ljj = A[j * D + j];
-      for (int i = j + 1 + threadIdx.x; i < D; i += blockDim.x) A[i * D + j] /= ljj;
+      const double rl = 1.0 / A[j * D + j];
+      for (int i = j + 1 + threadIdx.x; i < D; i += blockDim.x) A[i * D + j] *= rl;
       __syncthreads();
-      const int m = D - j - 1;
-      for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
-        int i = j + 1 + idx / m, l = j + 1 + idx % m;
-        if (l <= i) A[i * D + l] -= A[i * D + j] * A[l * D + j];
+      // trailing update of the lower triangle: a thread per row
+      for (int i = j + 1 + threadIdx.x; i < D; i += blockDim.x) {
+        const double lij = A[i * D + j];
+        for (int l = j + 1; l <= i; ++l) A[i * D + l] = fma(-lij, A[l * D + j], A[i * D + l]);
       }
       __syncthreads();
     }
@@ -132,22 +132,95 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
     for (int d = threadIdx.x; d < D; d += blockDim.x) ld += log(A[d * D + d]);
   }
   ld = block_sum(ld, red);
-  // Column j of W = L^-1 by forward substitution of L w = e_j (one thread per column).
-  for (int j = threadIdx.x; j < D; j += blockDim.x) {
-    double wc[128];
-    for (int i = 0; i < D; ++i) {
-      if (fail || i < j) { wc[i] = 0.0; W[(size_t)i * D + j] = 0.0f; continue; }
-      double s = (i == j) ? 1.0 : 0.0;
-      for (int t = j; t < i; ++t) s -= A[i * D + t] * wc[t];
-      wc[i] = s / A[i * D + i];
-      W[(size_t)i * D + j] = (float)wc[i];
+  // W = L^-1 in place, columns from the last: with the trailing block
+  // already inverted, W[i][j] = -(sum_{t=j+1..i} W[i][t] L[t][j]) / L[j][j]
+  // (a thread per row i; every L[t][j] is read before column j changes).
+  if (!fail) {
+    for (int j = D - 1; j >= 0; --j) {
+      const double wjj = 1.0 / A[j * D + j];
+      double v = 0.0;
+      const int i = j + 1 + threadIdx.x;
+      if (i < D) {
+        for (int t = j + 1; t <= i; ++t) v = fma(A[i * D + t], A[t * D + j], v);
+        v = -v * wjj;
+      }
+      __syncthreads();
+      if (i < D) A[i * D + j] = v;
+      if (threadIdx.x == 0) A[j * D + j] = wjj;
+      __syncthreads();
     }
+  }
+  for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+    const int i = e / D, j = e % D;
+    W[e] = (fail || j > i) ? 0.0f : (float)A[e];
   }
   for (int d = threadIdx.x; d < D; d += blockDim.x)
     at<float>(prepared, L.off_mu)[(size_t)k * D + d] = mu[(size_t)k * D + d];
+  if (fc_tc_shape(D, K, GMM_COV_FULL)) {
+    // the tensor-core screen's operands: s_k = 2^e with max |W| / s_k in
+    // [2^14, 2^15), the B image of fp16(W32 / s_k) (W32 the fp32 W the exact
+    // kernels use), b_k = W mu_k and the error-bound coefficients
+    //   ex_k = 1.01 ((2^-11 + 2^-16) |W|_F + 2^-25 s_k D),  em_k = 1.01 2^-18 |W|_F |mu_k|
+    // (fc_screen.cu derives them).
+    double mx = 0.0, f2 = 0.0, m2 = 0.0;
+    for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+      const int i = e / D, j = e % D;
+      if (!fail && j <= i) {
+        const double w = (double)(float)A[e];
+        mx = fmax(mx, fabs(w));
+        f2 += w * w;
+      }
+    }
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      const double m = (double)mu[(size_t)k * D + d];
+      m2 += m * m;
+    }
+    __shared__ double s_mx[4];
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    if ((threadIdx.x & 31) == 0) s_mx[threadIdx.x >> 5] = mx;
+    f2 = block_sum(f2, red);
+    m2 = block_sum(m2, red);
+    double M = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) M = fmax(M, s_mx[w]);
+    int e2 = 0;
+    frexp(M > 0.0 ? M : 1.0, &e2);  // M = f 2^e2, f in [0.5, 1)
+    const float sk = (float)ldexp(1.0, e2 - 15);
+    const float inv = 1.f / sk;
+    float* T = at<float>(prepared, L.off_fcT);
+    unsigned char* B = at<unsigned char>(prepared, L.off_fcB);
+    if (threadIdx.x == 0) {
+      const double F = sqrt(f2) * (1.0 + 1e-6), mun = sqrt(m2) * (1.0 + 1e-6);
+      T[k] = sk;
+      T[3 * kFcMaxK + k] = (float)(1.01 * 3.814697265625e-06 * F * mun);
+      T[2 * kFcMaxK + k] =
+          (float)(1.01 * ((0.00048828125 + 1.52587890625e-05) * F + 2.98023223876953125e-08 * sk * D));
+    }
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+      double b = 0.0;
+      if (!fail)
+        for (int j = 0; j <= i; ++j) b += (double)(float)A[i * D + j] * (double)mu[(size_t)k * D + j];
+      T[4 * kFcMaxK + k * D + i] = (float)b;
+    }
+    for (int u = threadIdx.x; u < D * 8; u += blockDim.x) {
+      const int i = u >> 3, c = u & 7, n = k * D + i;
+      __align__(16) __half h[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int j = 8 * c + t;
+        h[t] = __float2half_rn(!fail && j < D && j <= i ? (float)A[i * D + j] * inv : 0.f);
+      }
+      *reinterpret_cast<uint4*>(B + (size_t)n * 128 + ((c ^ (n & 7)) << 4)) =
+          *reinterpret_cast<const uint4*>(h);
+    }
+  }
   if (threadIdx.x == 0) {
     double p = (double)pi[k];
     double c = (fail || !(p > 0.0)) ? -INFINITY : log(p) - ld - 0.5 * D * kLog2Pi;
+    if (fc_tc_shape(D, K, GMM_COV_FULL)) at<float>(prepared, L.off_fcT)[kFcMaxK + k] = (float)c;
     at<float>(prepared, L.off_c)[k] = (float)c;
     at<int32_t>(prepared, L.off_flags)[k] = flags;
     if (fail && st) raise_status(st, GMM_ERR_NOT_PD);
