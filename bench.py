@@ -110,6 +110,19 @@ def work_model(wl):
             "lse_kernel": dict(flops=pairs * e_flops, bytes=x_bytes + 4 * N, bound="alu"),
             "stats_kernel": dict(flops=pairs * (e_flops + s_flops), bytes=x_bytes + 4 * N,
                                  bound="alu"),
+            # full covariance, few components: the screen contracts every pair
+            # (the triangular W_k x); the exact kernels take the candidate
+            # pairs the status word counts (flops per pair below)
+            "fc_screen_kernel": dict(flops=N * K * D * (D + 1), bytes=x_bytes, bound="tensor",
+                                     unit_note="%d rows" % N),
+            "fc_lse_kernel": dict(pair_flops=D * (D + 1), bound="alu"),
+            "fc_stats_kernel": dict(pair_flops=2 * D * (D + 1) + 2 * D, bound="alu"),
+            # streamed diagonal parameters: the dense-row kernels take the
+            # candidate pairs of the rows the screen left them, the centred form
+            # (x - mu)^2 w: 4 flops a dimension; the statistics recompute it and
+            # add g y and g y^2: 4 more
+            "dense_lse_kernel": dict(pair_flops=4 * D, bound="alu"),
+            "dense_stats_kernel": dict(pair_flops=8 * D, bound="alu"),
         })
 
 
@@ -341,6 +354,7 @@ def config_dict(wl, extra=None):
 
 
 def run_ours(args, wl):
+    import numpy as np
     import torch
     import datagen
     import soft_clustering_gb300 as G
@@ -422,6 +436,16 @@ def run_ours(args, wl):
         tot_ms, n_launch = prof[top]
         avg_s = tot_ms / n_launch / 1e3
         km = wm["kernels"].get(top)
+        if km and "pair_flops" in km:
+            # candidate-driven kernel: replay the timed schedule (untimed, from
+            # theta_0) and count the pairs it evaluated from the status word
+            st.set_params(*theta0)
+            cand_pairs = 0
+            for _ in range(steps):
+                st.step(X)
+                cand_pairs += int(st.ws[16:24].cpu().numpy().view(np.uint64)[0])
+            km = dict(km, flops=cand_pairs * km["pair_flops"] / n_launch,
+                      pairs_per_launch=cand_pairs / n_launch)
         if km and km["bound"] == "tensor":
             # fp16 operands, fp32 accumulation: the dense fp16 rate equals the
             # bf16 rate (nominal ratio 1), so the measured bf16 GEMM peak is used
@@ -441,6 +465,9 @@ def run_ours(args, wl):
                         frac=achieved / alu_peak, traffic=traffic_for(top, wl.name),
                         kernel=top, avg_launch_ms=tot_ms / n_launch,
                         peak_source="fp32 FMA lanes x clock (derived)")
+            if "pairs_per_launch" in km:
+                roof["per_launch"] = "%.4g candidate pairs x %d flops" % (
+                    km["pairs_per_launch"], km["pair_flops"])
     step_roof_s = max(wm["step_flops"] / (peaks["bf16_tflops"] * 1e12),
                       wm["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
 

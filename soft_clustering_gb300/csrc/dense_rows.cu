@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
     mn = __ldg(reinterpret_cast<const uint2*>(a.cmask + ((size_t)row * a.nch + j) * 4 + 2 * hf));
   };
   if (i < n) fetch(i);
+  uint32_t npairs = 0;  // pairs this thread's group evaluated (counted by every lane)
   for (; i < n; i += stride) {
     float x[CPL][4];
 #pragma unroll
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
     // this group's 16 columns
     uint32_t bits = ((grp < 2 ? mn.x : mn.y) >> (16 * (grp & 1))) & 0xffffu;
     if (i + stride < n) fetch(i + stride);
+    npairs += __popc(bits);
     int steps = __popc(bits);
     steps = max(steps, __shfl_xor_sync(0xffffffffu, steps, 8));
     steps = max(steps, __shfl_xor_sync(0xffffffffu, steps, 16));
@@ -199,6 +201,13 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
       a.part[(size_t)i * (2 * a.nch) + blockIdx.x] = make_float2(M, S);
     }
   }
+  // the block's pair count: lane 8 g of each warp holds group g's
+  __shared__ unsigned long long s_pairs;
+  if (tid == 0) s_pairs = 0ull;
+  __syncthreads();
+  if (gl == 0 && npairs) atomicAdd(&s_pairs, (unsigned long long)npairs);
+  __syncthreads();
+  if (tid == 0 && s_pairs) atomicAdd(&a.st->cand_pairs, s_pairs);
 }
 
 __global__ void __launch_bounds__(kThreads) dense_combine_kernel(const DenseArgs a) {

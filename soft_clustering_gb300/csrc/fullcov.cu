@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
     if (sC[k] > -INFINITY) valid |= 1u << k;
   const int64_t ntiles = (a.N + kFcT - 1) / kFcT;
   double ll = 0.0;
+  unsigned long long npairs = 0;  // pairs of this block's tiles (thread 0)
   // the next tile's masks and rows (as stored) are requested while this one is used
   uint32_t mnext = 0u;
   uint4 xnext[XPT];
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
     }
     __syncthreads();
     const int nt = toff[K];
+    if (tid == 0) npairs += (uint32_t)offs[K];
     int kk = 0;
     for (int tk = tid; tk < nt; tk += kFcThreads) {
       while (toff[kk + 1] <= tk) ++kk;
@@ -328,6 +330,7 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
     double s = 0.0;
     for (int w = 0; w < kFcThreads / 32; ++w) s += red[w];
     a.ll_part[blockIdx.x] = s;
+    if (npairs) atomicAdd(&a.st->cand_pairs, npairs);
   }
 }
 

@@ -41,7 +41,9 @@ struct DeviceStatus {
   int32_t detail;      // OR of (1 << gmm_status) for every failure seen
   uint32_t fb_count;   // rows the tensor-core kernel handed to the CUDA-core path
   uint32_t dense_count;  // rows whose candidates went to the dense-row kernels (last slab)
-  int32_t pad[60];
+  unsigned long long cand_pairs;  // (point, candidate) pairs the dense-row or full-covariance
+                                  // log-sum-exp kernels evaluated in this call
+  int32_t pad[58];
 };
 
 __device__ inline void raise_status(DeviceStatus* st, int code) {
