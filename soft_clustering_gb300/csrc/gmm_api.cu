@@ -568,7 +568,8 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
   DeviceStatus* st = static_cast<DeviceStatus*>(ws);
   GMM_TRY(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
   if (tc) {
-    // slabs of rows: screening, then the row list of the slab
+    // slabs of rows on the tensor cores, each marking the rows it hands over
+    // in the bitmap of all rows; then one CUDA-core pass over those rows
     uint32_t* fb = at<uint32_t>(ws, W.off_fb);
     uint32_t* fbm = at<uint32_t>(ws, W.off_fbm);
     const int64_t slab_rows = slab_rows_for(K);
@@ -578,19 +579,17 @@ gmm_status gmm_assign_topm(const void* X, gmm_dtype xdtype, int64_t N, int D, in
       float* ls = lse ? lse + r0 : nullptr;
       int32_t* is = ids + (size_t)r0 * m;
       float* gs = gamma + (size_t)r0 * m;
-      {
-        GMM_PROF("tc_screen_kernel");
-        GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prepared, 1, ls, 0, nullptr, m, is, gs, fbm,
-                          nullptr, nullptr, nullptr, nullptr, 0, st, s));
-      }
-      {
-        GMM_PROFN("fb_compact_kernel", 2);
-        GMM_TRY(fb_compact(fbm, sn, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
-      }
-      GMM_PROF("lse_rows_kernel");
-      GMM_TRY(simt_lse_rows(Xs, xdtype, sn, D, K, cov, prepared, ls, nullptr, m, is, gs, st, fb,
-                            &st->fb_count, kListGrid, s));
+      GMM_PROF("tc_screen_kernel");
+      GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prepared, 1, ls, 0, nullptr, m, is, gs,
+                        fbm + (size_t)(r0 / 128) * 4, nullptr, nullptr, nullptr, nullptr, 0, st, s));
     }
+    {
+      GMM_PROFN("fb_compact_kernel", 2);
+      GMM_TRY(fb_compact(fbm, N, fb, &st->fb_count, at<uint32_t>(ws, W.off_fbseg), s));
+    }
+    GMM_PROF("lse_rows_kernel");
+    GMM_TRY(simt_lse_rows(X, xdtype, N, D, K, cov, prepared, lse, nullptr, m, ids, gamma, st, fb,
+                          &st->fb_count, kListGrid, s));
     return GMM_OK;
   }
   GMM_PROF("lse_topm_kernel");
