@@ -66,7 +66,7 @@ def measured_peaks():
 
 def slab_rows(wl):
     """Rows per screening launch of the tensor-core path (the library's rule)."""
-    return 1 << 20
+    return 1 << 21
 
 
 def tc_path(wl):

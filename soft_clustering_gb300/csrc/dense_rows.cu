@@ -22,8 +22,11 @@
 //   dense_stats   block (group of 8192/D components, partition): a thread
 //                 per (component, 16 dimensions: every eighth 16-byte chunk
 //                 of the row at D = 128) keeps the component's sums
-//                 s0, sum g (x - mu) and sum g (x - mu)^2 in registers over
-//                 the block's points, g = exp(l - LSE_n) recomputed for every
+//                 s0, sum g (x - mu) and sum g v^2 (v = x - c, c a shift
+//                 inside the component's new cluster: the block's first
+//                 candidate point, moved once to its first point of
+//                 responsibility >= 1/2) in registers over the block's points,
+//                 g = exp(l - LSE_n) recomputed for every
 //                 candidate; at the end they join the block's fp64 partial
 //                 slot with the pairwise update of Chan, Golub and LeVeque.
 // Every sum has a fixed order, so the results are the same on every run.
@@ -278,12 +281,23 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
   const unsigned grp_mask = ((1u << TPC) - 1u) << ((tid & 31) & ~(TPC - 1));
   const float ck = kin ? __ldg(a.bias + k) : -INFINITY;
   constexpr int DP = DPT / 2;  // dimension pairs
-  float2 mu[DP], w[DP], s1[DP], s2[DP];
+  // the sums are taken about a shift inside the component's new cluster:
+  // the first candidate point of the block (sf = its x - mu), so that a
+  // component that moves far relative to its spread keeps its second moment
+  // the means live in shared memory (float4 q of thread t at q * threads + t:
+  // consecutive threads, consecutive 16 bytes), the rest in registers
+  extern __shared__ float4 smu[];  // [DPT / 4][kStatThreads] means, then as many shifts
+  float4* ssf = smu + (DPT / 4) * kStatThreads;
+  float2 w[DP], s1[DP], s2[DP];
   float s0 = 0.f;
+  bool shifted = false, heavy = false;
 #pragma unroll
   for (int i = 0; i < DP; ++i) {
     const int d = dim_of(2 * i);  // pairs never straddle a chunk
-    mu[i] = kin ? __ldg(reinterpret_cast<const float2*>(a.mu + (size_t)k * D + d)) : make_float2(0.f, 0.f);
+    const float2 m = kin ? __ldg(reinterpret_cast<const float2*>(a.mu + (size_t)k * D + d)) : make_float2(0.f, 0.f);
+    float* sm4 = reinterpret_cast<float*>(&smu[(i / 2) * kStatThreads + tid]) + 2 * (i & 1);
+    sm4[0] = m.x;
+    sm4[1] = m.y;
     if (!kin) w[i] = make_float2(0.f, 0.f);
     else if (a.iso) w[i] = make_float2(__ldg(a.prec + k), __ldg(a.prec + k));
     else w[i] = __ldg(reinterpret_cast<const float2*>(a.prec + (size_t)k * D + d));
@@ -367,21 +381,53 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
         }
         float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < DP; ++i) {
-          y[i] = sub2(y[i], mu[i]);
-          acc[i & 1] = fma2(mul2(y[i], y[i]), w[i], acc[i & 1]);
+        for (int i = 0; i < DP; i += 2) {
+          const float4 m4 = smu[(i / 2) * kStatThreads + tid];
+          y[i] = sub2(y[i], make_float2(m4.x, m4.y));
+          y[i + 1] = sub2(y[i + 1], make_float2(m4.z, m4.w));
+          acc[0] = fma2(mul2(y[i], y[i]), w[i], acc[0]);
+          acc[1] = fma2(mul2(y[i + 1], y[i + 1]), w[i + 1], acc[1]);
         }
         float d2 = (acc[0].x + acc[1].x) + (acc[0].y + acc[1].y);
 #pragma unroll
         for (int o = 1; o < TPC; o <<= 1) d2 += __shfl_xor_sync(grp_mask, d2, o);
         const float gm = exp2f((ck - 0.5f * d2 - lse_t[r]) * 1.4426950408889634f);
-        s0 += gm;
         const float2 g2 = make_float2(gm, gm);
+        // the second moment is taken about a shift: the first candidate
+        // point, moved once to the first point of responsibility >= 1/2 (the
+        // sum so far carried over: S2 -= 2 d S1c - S0 d^2, with
+        // S1c = S1 - S0 sf the first moment about the old shift); every
+        // thread of the component sees the same points and g.  The first
+        // moment stays about mu.
+        if (!shifted || (!heavy && gm >= 0.5f)) {
 #pragma unroll
-        for (int i = 0; i < DP; ++i) {
-          const float2 gy = mul2(g2, y[i]);
-          s1[i] = add2(s1[i], gy);
-          s2[i] = fma2(gy, y[i], s2[i]);
+          for (int i = 0; i < DP; i += 2) {
+            const float4 old4 = ssf[(i / 2) * kStatThreads + tid];
+            const float2 of0 = shifted ? make_float2(old4.x, old4.y) : make_float2(0.f, 0.f);
+            const float2 of1 = shifted ? make_float2(old4.z, old4.w) : make_float2(0.f, 0.f);
+            const float2 dl0 = sub2(y[i], of0), dl1 = sub2(y[i + 1], of1);
+            const float2 s00 = make_float2(s0, s0);  // S0 before this point
+            const float2 c0 = fma2(make_float2(-s0, -s0), of0, s1[i]);      // S1c
+            const float2 c1 = fma2(make_float2(-s0, -s0), of1, s1[i + 1]);
+            s2[i] = fma2(mul2(s00, dl0), dl0, fma2(make_float2(-2.f * dl0.x, -2.f * dl0.y), c0, s2[i]));
+            s2[i + 1] = fma2(mul2(s00, dl1), dl1,
+                             fma2(make_float2(-2.f * dl1.x, -2.f * dl1.y), c1, s2[i + 1]));
+            ssf[(i / 2) * kStatThreads + tid] = make_float4(y[i].x, y[i].y, y[i + 1].x, y[i + 1].y);
+          }
+          heavy = gm >= 0.5f;
+          shifted = true;
+        }
+        s0 += gm;
+#pragma unroll
+        for (int i = 0; i < DP; i += 2) {
+          const float4 f4 = ssf[(i / 2) * kStatThreads + tid];
+          const float2 v0 = sub2(y[i], make_float2(f4.x, f4.y));  // x - (mu + sf)
+          const float2 v1 = sub2(y[i + 1], make_float2(f4.z, f4.w));
+          s1[i] = fma2(g2, y[i], s1[i]);
+          s1[i + 1] = fma2(g2, y[i + 1], s1[i + 1]);
+          const float2 g0 = mul2(g2, v0), g1 = mul2(g2, v1);
+          s2[i] = fma2(g0, v0, s2[i]);
+          s2[i + 1] = fma2(g1, v1, s2[i + 1]);
         }
       }
     }
@@ -395,9 +441,14 @@ __global__ void __launch_bounds__(kStatThreads, 1) dense_stats_kernel(const Dens
 #pragma unroll
     for (int i = 0; i < DPT; ++i) {
       const int d = dim_of(i);
+      // the first moment about mu; the second about the shift, so the
+      // moment about the block mean comes from the first moment about the
+      // shift (S1 - S0 sf, in fp64)
       const double b1 = (double)((i & 1) ? s1[i / 2].y : s1[i / 2].x);
       const double q2 = (double)((i & 1) ? s2[i / 2].y : s2[i / 2].x);
-      const double m2b = b0 > 0.0 ? q2 - b1 * b1 / b0 : 0.0;
+      const float sfi = shifted ? reinterpret_cast<const float*>(&ssf[(i / 4) * kStatThreads + tid])[i & 3] : 0.f;
+      const double c1 = b1 - b0 * (double)sfi;
+      const double m2b = b0 > 0.0 ? q2 - c1 * c1 / b0 : 0.0;
       double S1 = b1, M2 = m2b;
       if (a.accumulate) {
         const double o1 = o[1 + d], om = o[1 + D + d];
@@ -435,7 +486,11 @@ cudaError_t run_dense(const DenseArgs& a, int pa, int pb, cudaStream_t s) {
   {
     ProfScope prof("dense_stats_kernel", s);
     const int ng = (a.K + DsShape<D>::CPB - 1) / DsShape<D>::CPB;
-    dense_stats_kernel<D, XT><<<dim3(ng, pb), kStatThreads, 0, s>>>(a);
+    const size_t smem_s = 2 * sizeof(float) * DsShape<D>::DPT * kStatThreads;
+    if ((e = cudaFuncSetAttribute(dense_stats_kernel<D, XT>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s)) != cudaSuccess)
+      return e;
+    dense_stats_kernel<D, XT><<<dim3(ng, pb), kStatThreads, smem_s, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

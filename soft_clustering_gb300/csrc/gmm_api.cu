@@ -66,20 +66,19 @@ constexpr int kTargetCtas = 608;   // 4 x 152 SMs: statistics blocks per launch
 constexpr int kListGrid = 304;     // blocks of the CUDA-core pass over handed-over rows
 constexpr int kMaxScreenGrid = 1024;  // upper bound of tc_screen_grid (SM count)
 // Tensor-core path: records {key, exact log joint} per 128-point tile, in
-// eight regions (one per epilogue warp and column half; a warp whose records
-// do not fit hands its rows to the CUDA-core path), and rows per slab (one
-// screening launch; its records are consumed before the next slab).  A tile
-// holds min(K/2, 256) records a point on average (at least 32): the early EM
-// iterations keep tens to about a hundred candidates a point on the
-// 128-dimensional workloads, and the buffer with its sorted copy stays below
-// an N x K fp32 matrix (and at 4 GiB for the largest K).
+// eight regions (one per epilogue warp and column half), and rows per slab
+// (one screening launch; its records are consumed before the next slab).  A
+// point keeps at most 13 (folded parameters) or 2 x 15 (streamed) candidates
+// in its lists, and a point with more goes to the dense-row kernels, so a
+// region of 32 points never needs more than 32 x 15 = 480 records: 32 records
+// a point per tile.
 int rec_cap_for(int K) {
-  const int per_row = K / 2 < 32 ? 32 : (K / 2 > 256 ? 256 : K / 2 / 8 * 8);
-  return 128 * per_row;
+  (void)K;
+  return 128 * 32;
 }
 int64_t slab_rows_for(int K) {
   (void)K;
-  return (int64_t)1 << 20;
+  return (int64_t)1 << 21;
 }
 
 bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
@@ -104,7 +103,7 @@ struct WsLayout {
   int parts;          // statistics partials of the CUDA-core path
   int sp_parts;       // tensor-core path: the records' partial (1) ...
   int lp_parts;       // ... followed by those of the row-list pass ...
-  int dp_parts;       // ... and those of the dense-row kernels (streamed parameters)
+  int dp_parts;       // ... and those of the dense-row kernels
   int64_t lse_rows;
 };
 
@@ -143,13 +142,13 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.parts = stat_parts(rows, D, K, cov);
   W.sp_parts = W.lp_parts = W.dp_parts = 0;
   int slots = W.parts;
-  const bool streamed = tc && !tc_fold((K + kTcChunk - 1) / kTcChunk);
+  const bool dense_rows_on = tc;  // rows whose candidate lists fill go to the dense-row kernels
   if (tc) {
     W.sp_parts = 1;
     const int kc = simt_stat_chunk(D, cov);
     const int chunks = (K + kc - 1) / kc;
     W.lp_parts = (kListGrid + chunks - 1) / chunks;
-    W.dp_parts = streamed ? dense_stat_parts(D, K) : 0;
+    W.dp_parts = dense_rows_on ? dense_stat_parts(D, K) : 0;
     if (W.sp_parts + W.lp_parts + W.dp_parts > slots) slots = W.sp_parts + W.lp_parts + W.dp_parts;
   }
   W.off_part = o;   o = align_up(o + sizeof(double) * (size_t)slots * K * stat_width(D, cov));
@@ -165,13 +164,13 @@ WsLayout ws_layout(int64_t N, int64_t rows, int D, int K, int cov, size_t stage_
   W.off_tcnt = o;   o = align_up(o + sizeof(uint32_t) * 8 * slab_tiles);
   W.off_sws = o;
   o = align_up(o + (tc ? sparse_stats_ws_bytes(slab, D, K, rec_cap_for(K)) : 0));
-  // streamed parameters: every row's candidate masks, the rows left to the
+  // every row's candidate masks, the rows left to the
   // dense-row kernels (bitmap, list) and their per-chunk log-sum-exp
   const size_t nch = (size_t)((K + kTcChunk - 1) / kTcChunk);
-  W.off_cmask = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * 4 * nch * (size_t)slab : 0));
-  W.off_dmask = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * 4 * slab_tiles : 0));
-  W.off_drows = o;  o = align_up(o + (streamed ? sizeof(uint32_t) * (size_t)slab : 0));
-  W.off_dpart = o;  o = align_up(o + (streamed ? sizeof(float2) * 2 * nch * (size_t)slab : 0));
+  W.off_cmask = o;  o = align_up(o + (dense_rows_on ? sizeof(uint32_t) * 4 * nch * (size_t)slab : 0));
+  W.off_dmask = o;  o = align_up(o + (dense_rows_on ? sizeof(uint32_t) * 4 * slab_tiles : 0));
+  W.off_drows = o;  o = align_up(o + (dense_rows_on ? sizeof(uint32_t) * (size_t)slab : 0));
+  W.off_dpart = o;  o = align_up(o + (dense_rows_on ? sizeof(float2) * 2 * nch * (size_t)slab : 0));
   W.off_stage = o;  o = align_up(o + stage_bytes);
   W.bytes = o;
   (void)N;
@@ -267,7 +266,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
     // (single-candidate points), dense-row blocks
     const size_t lls = (size_t)kMaxScreenGrid + (size_t)K + (size_t)dense_ll_parts();
     const size_t nll = (size_t)nslabs * lls + kListGrid;
-    const bool streamed = W.dp_parts > 0;
+    const bool dense_on = W.dp_parts > 0;
     double* dpart = lpart + (size_t)W.lp_parts * K * stat_width(D, cov);
     GMM_TRY(cudaMemsetAsync(llp, 0, sizeof(double) * nll, s));
     for (int64_t si = 0; si < nslabs; ++si) {
@@ -277,8 +276,8 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
       float* ls = lse + r0;
       const int acc = accumulate || r0 > 0;
       double* llp_s = llp + (size_t)si * lls;
-      uint32_t* dmask = streamed ? at<uint32_t>(ws, W.off_dmask) : nullptr;
-      uint32_t* cmask = streamed ? at<uint32_t>(ws, W.off_cmask) : nullptr;
+      uint32_t* dmask = dense_on ? at<uint32_t>(ws, W.off_dmask) : nullptr;
+      uint32_t* cmask = dense_on ? at<uint32_t>(ws, W.off_cmask) : nullptr;
       {
         GMM_PROF("tc_screen_kernel");
         GMM_TRY(tc_screen(Xs, xdtype, sn, D, K, cov, prep, 0, ls, want_lse ? 1 : 0, llp_s, 0,
@@ -287,7 +286,7 @@ gmm_status estep_rows(const void* X, gmm_dtype xdtype, int64_t rows, int D, int 
       }
       GMM_TRY(sparse_stats(Xs, xdtype, sn, D, K, prep, cov, ls, tcnt, recs, rec_cap,
                            at<char>(ws, W.off_sws), part, acc, llp_s + kMaxScreenGrid, st, s));
-      if (streamed) {
+      if (dense_on) {
         uint32_t* drows = at<uint32_t>(ws, W.off_drows);
         {
           GMM_PROFN("fb_compact_kernel", 2);

@@ -83,9 +83,9 @@ struct ScreenArgs {
   float* gamma;          // [N*m] (assign)
   uint32_t* fb_mask;     // assign: [tiles * 4] bit r % 32 of word n / 32: row n
                          // handed to the CUDA-core path
-  uint32_t* cmask;       // EM, streamed parameters: [rows][chunks][4] candidate masks
+  uint32_t* cmask;       // EM: [rows][chunks][4] candidate masks
                          // (word 2h + b: columns 64h + 32b .. + 31 of the chunk)
-  uint32_t* dmask;       // EM, streamed parameters: [tiles * 4] rows left to the dense-row kernels
+  uint32_t* dmask;       // EM: [tiles * 4] rows left to the dense-row kernels
   uint2* recs;           // EM: [tiles][rec_cap] records {key, exact log joint}
   uint32_t* tile_cnt;    // EM: [tiles] records of the tile (> rec_cap: they did not fit)
   int rec_cap;
@@ -696,15 +696,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       int cnt = 0;
       bool ok = true;
       float thr = -INFINITY;  // the point's window, fixed after pass 0
-      // EM: running log-sum-exp of the candidates refined so far, records
-      // written by flushes of a full list, and this warp's region of the
-      // tile's records (regions 2q and 2q + 1 of the eight)
+      // EM: the point's log-sum-exp over its refined candidates, this warp's
+      // region of the tile's records (regions 2q and 2q + 1 of the eight),
+      // the point's candidate masks (every chunk, for the dense-row kernels)
+      // and whether its list filled (the point then goes to those kernels)
       float mx = -INFINITY, ssum = 0.f;
-      int nrec = 0;
-      bool flushed = false;
+      bool deferred = false;
       uint32_t wpos = 0;
       const int rcap = a.rec_cap / 4;
       uint2* region = a.recs + (size_t)tile * a.rec_cap + (size_t)q * rcap;
+      uint32_t* rmask = MODE == MODE_EM ? a.cmask + (size_t)(tile * kBM + r) * nch * 4 : nullptr;
       // pass 0: lower bounds only; pass 1 (a second sweep of the same
       // accumulators): candidates against the point's final window
       for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -780,25 +781,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
               if (!valid) pm = 0u;
               if constexpr (MODE == MODE_EM) {
                 if (!isfinite(rn)) pm = 0u;  // handed over (non-finite input)
-                // append; when a list is full the warp refines its lists,
-                // folds them into the running log-sum-exp and writes their
-                // records (a flush), then goes on appending
-                for (;;) {
-                  while (pm && cnt < kCSG) {
-                    const int kk = c0 + __ffs(pm) - 1;
-                    pm &= pm - 1u;
-                    ck[cnt * kBM + r] = (uint16_t)(j * kBN + kk);
-                    ++cnt;
-                  }
-                  if (!__any_sync(0xffffffffu, pm != 0u)) break;
-                  refine_lists<D, XT>(a.X, tile, q, lane, cnt, cub, ck, g_mu, g_prec, g_c, iso);
-                  fold_lse(cub, r, cnt, &mx, &ssum);
-                  emit_records(lane, r, cnt, cub, ck, &wpos, region, rcap, false);
-                  nrec += cnt;
-                  flushed = flushed || cnt > 0;
-                  cnt = 0;
-                  __syncwarp();
+                if (valid) rmask[j * 4 + (c0 >> 5)] = pm;
+                // append while the list has room; a point with more
+                // candidates goes to the dense-row kernels with its masks
+                while (pm && cnt < kCSG) {
+                  const int kk = c0 + __ffs(pm) - 1;
+                  pm &= pm - 1u;
+                  ck[cnt * kBM + r] = (uint16_t)(j * kBN + kk);
+                  ++cnt;
                 }
+                if (pm) deferred = true;
               } else {
                 while (pm) {
                   const int kk = c0 + __ffs(pm) - 1;
@@ -823,18 +815,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
       __syncwarp();
       if (!ok) break;
       if constexpr (MODE == MODE_EM) {
-        // this warp's record count (flushed + remaining): past its region's
-        // capacity the warp's rows take the CUDA-core path
-        int mine = nrec + cnt;
+        // this warp's record count: past its region's capacity the warp's
+        // rows take the CUDA-core path
+        int mine = deferred ? 0 : cnt;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
         const bool overflow = mine > rcap;
-        const bool exact = valid && isfinite(rn) && (cnt > 0 || flushed) && !overflow;
+        const bool exact = valid && isfinite(rn) && cnt > 0 && !deferred && !overflow;
         // a point with a single candidate has gamma = 1 (every other
         // component lies more than 40 nats below it); unless LSE_n is wanted
         // its exact log joint is not needed here: the statistics give its
         // log-likelihood term
-        const bool single = exact && !flushed && cnt == 1 && !a.want_lse;
+        const bool single = exact && cnt == 1 && !a.want_lse;
         refine_lists<D, XT>(a.X, tile, q, lane, (exact && !single) ? cnt : 0, cub, ck, g_mu,
                             g_prec, g_c, iso);
         if (exact && !single) fold_lse(cub, r, cnt, &mx, &ssum);
@@ -846,10 +838,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_screen_kernel(const ScreenArgs
           ll_acc += (double)lse;
         }
         // rows of an overflowing warp, and rows without a candidate
-        // (non-finite input), go to the CUDA-core path
-        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact);
+        // (non-finite input), go to the CUDA-core path; rows with a full
+        // list to the dense-row kernels
+        const bool dense = valid && isfinite(rn) && deferred && !overflow;
+        const unsigned fbm = __ballot_sync(0xffffffffu, valid && !exact && !dense);
+        const unsigned dbm = __ballot_sync(0xffffffffu, dense);
         if (lane == 0) {
           a.fb_mask[tile * 4 + q] = fbm;
+          a.dmask[tile * 4 + q] = dbm;
           a.tile_cnt[tile * 8 + 2 * q] = overflow ? 0u : (uint32_t)mine;
           a.tile_cnt[tile * 8 + 2 * q + 1] = 0u;
         }
@@ -1525,7 +1521,7 @@ cudaError_t tc_screen(const void* X, int xdtype, int64_t N, int D, int K, int co
   a.recs = recs; a.tile_cnt = tile_cnt; a.rec_cap = rec_cap;
   if (!a.L.tc_chunks || N < 1) return cudaErrorInvalidValue;
   if (mode == MODE_EM && (!recs || !tile_cnt || !lse || rec_cap < kBM)) return cudaErrorInvalidValue;
-  if (mode == MODE_EM && !tc_fold(a.L.tc_chunks) && (!cmask || !dmask)) return cudaErrorInvalidValue;
+  if (mode == MODE_EM && (!cmask || !dmask)) return cudaErrorInvalidValue;
   const int grid = tc_screen_grid(N);
 #define GMM_SCREEN(DD, XX)                                                              \
   return mode == MODE_EM ? run_screen<DD, XX, MODE_EM>(a, grid, s)                      \

@@ -392,14 +392,13 @@ def test_tensor_core_path_matches_cuda_core_path(name, n, cov):
         theta = f32((cc["pi"], cc["mu"], cc["cov"]))
 
 
-def test_full_lists_flush_and_match_oracle():
+def test_full_lists_go_to_dense_rows_and_match_oracle():
     """A point's candidate list in the screening kernel holds 13 (resident
-    parameters) or 15 (streamed, per column half) components; a full list is
-    refined, folded into the point's running log-sum-exp and written out as
-    records, and collection goes on.  24 copies of one component, all within
-    every nearby point's window, force that for many points; the rows stay on
-    the tensor-core path (unless a warp's records outgrow its region of the
-    tile buffer) and the step matches the oracle."""
+    parameters) or 15 (streamed, per column half) components; a point with
+    more goes with its candidate masks to the dense-row kernels.  24 copies of
+    one component, all within every nearby point's window, force that for
+    many points; none is handed to the CUDA-core row list, and the step
+    matches the oracle."""
     for K in (256, 300):
         wl = _workload("embed_diag", n=20000, K=K)
         mix = datagen.planted(wl)
@@ -416,9 +415,10 @@ def test_full_lists_flush_and_match_oracle():
         got = gpu_step(state, to_device(bits, wl.dtype), theta, opts=opts)
         assert got["status"] == 0
         # the library's status word: code, detail, rows handed to the CUDA-core path
-        handed = int(state.ws[8:12].cpu().numpy().view(np.uint32)[0])
+        handed, dense = (int(v) for v in state.ws[8:16].cpu().numpy().view(np.uint32))
         assert handed < wl.N // 4, handed
-        fails = parity.compare_step(got, ref, "flushed lists K=%d" % K, opts["min_s0"])
+        assert dense > 0, dense
+        fails = parity.compare_step(got, ref, "full lists K=%d" % K, opts["min_s0"])
         assert not fails, "\n".join(fails[:10])
 
 

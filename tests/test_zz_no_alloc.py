@@ -57,6 +57,9 @@ def test_noalloc_matches_workspace_entry_point(name, n):
     lse_ref = torch.empty(wl.N, dtype=torch.float32, device="cuda")
     params = theta
     for call in range(2):
+        # both entry points start every call from the same parameters (per-step
+        # parity; each one's own trajectory amplifies last-bit differences)
+        ref_state.set_params(*f32(params))
         ref_in = ref_state.params_numpy()
         ref_state.step(Xd, lse=lse_ref)
         assert ref_state.device_status() == G.GMM_OK
@@ -78,9 +81,6 @@ def test_noalloc_matches_workspace_entry_point(name, n):
             # another fp32 order than the CUDA-core kernels: both paths agree
             # with the oracle's LSE_n to fp32 evaluation error (ten times
             # inside the log-likelihood tolerance of 1e-4 relative).
-            # (each against the oracle at its own input parameters: from the
-            # second call on the two entry points start from their own
-            # updates of the first, which differ in the last bits)
             lo = orc["lse"]
             lo_ws = oracle_step(bits, wl.dtype, ref_in, wl.cov_type, opts=opts, want_lse=True)["lse"]
             scale = np.abs(lo).max()
