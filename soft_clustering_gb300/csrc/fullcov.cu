@@ -177,59 +177,93 @@ __device__ __forceinline__ void stage_w(float* dst, int stride, const float* __r
   }
 }
 
+// The per-tile shared memory of fc_lse (one set per half block).
 template <int D, int XT>
+struct FlTile {
+  static constexpr int RB = D * (XT == GMM_F32 ? 4 : 2);  // bytes of a stored row
+  __host__ __device__ static size_t bytes(int K) {
+    return (size_t)kFcT * RB + sizeof(float) * (size_t)kFcT * K +
+           sizeof(uint32_t) * ((size_t)K * (kFcT / 32) + kFcT) + sizeof(int) * (2 * kFcMaxK + 4) +
+           (((size_t)kFcT * K + 15) / 16) * 16;
+  }
+};
+
+// NH independent halves of the block (NH = 2: warps 0-3 and 4-7) take
+// alternate tiles with their own tile tables and named barriers, so one half
+// evaluates while the other waits at a barrier; W, the means and biases are
+// shared.  With NH = 1 the next tile's rows are prefetched into registers.
+template <int D, int XT, int NH>
 __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
   constexpr int WS = fc_wstride(D), NW = kFcT / 32;
+  constexpr int TH = kFcThreads / NH;          // threads of a half
   constexpr int ESZ = XT == GMM_F32 ? 4 : 2;
   constexpr int RB = D * ESZ;                 // bytes of a stored row
   constexpr int C16 = RB / 16;                // its 16-byte chunks
   constexpr int VPC = 16 / ESZ;               // coordinates per chunk
-  constexpr int XPT = kFcT * C16 / kFcThreads;  // chunks of the tile a thread loads
-  static_assert(XPT >= 1 && XPT * kFcThreads == kFcT * C16, "tile load split");
+  constexpr int XPT = kFcT * C16 / TH;        // chunks of the tile a thread loads
+  constexpr bool PREFETCH = NH == 1;
+  static_assert(TH >= kFcT && XPT * TH == kFcT * C16, "tile split");
   extern __shared__ __align__(16) float sm[];
   const int K = a.K;
   float* sW = sm;                                    // K * WS
   float* sMu = sW + K * WS;                          // K * D
   float* sC = sMu + K * D;                           // kFcMaxK
-  unsigned char* xs = reinterpret_cast<unsigned char*>(sC + kFcMaxK);  // kFcT rows as stored
+  const int tid0 = threadIdx.x, half = tid0 / TH, tid = tid0 % TH;
+  const int lane = tid & 31, warp = tid >> 5;        // within the half
+  unsigned char* xs = reinterpret_cast<unsigned char*>(sC + kFcMaxK) + half * FlTile<D, XT>::bytes(K);
   float* lval = reinterpret_cast<float*>(xs + kFcT * RB);             // kFcT * K
   uint32_t* cm = reinterpret_cast<uint32_t*>(lval + kFcT * K);  // K * NW
   uint32_t* msk = cm + K * NW;                       // kFcT
   int* offs = reinterpret_cast<int*>(msk + kFcT);    // kFcMaxK + 1: pairs
   int* toff = offs + kFcMaxK + 1;                    // kFcMaxK + 1: tasks (two pairs each)
   uint8_t* prow = reinterpret_cast<uint8_t*>(toff + kFcMaxK + 3);  // kFcT * K
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  stage_w<D>(sW, WS, a.W, K, tid, kFcThreads);
-  for (int e = tid; e < K * D; e += kFcThreads) sMu[e] = __ldg(a.mu + e);
-  for (int k = tid; k < kFcMaxK; k += kFcThreads) sC[k] = k < K ? __ldg(a.bias + k) : -INFINITY;
+  auto hsync = [&]() {
+    if constexpr (NH == 1) __syncthreads();
+    else asm volatile("bar.sync %0, %1;" ::"r"(1 + half), "r"(TH) : "memory");
+  };
+  stage_w<D>(sW, WS, a.W, K, tid0, kFcThreads);
+  for (int e = tid0; e < K * D; e += kFcThreads) sMu[e] = __ldg(a.mu + e);
+  for (int k = tid0; k < kFcMaxK; k += kFcThreads) sC[k] = k < K ? __ldg(a.bias + k) : -INFINITY;
   __syncthreads();
   uint32_t valid = 0u;
   for (int k = 0; k < K; ++k)
     if (sC[k] > -INFINITY) valid |= 1u << k;
   const int64_t ntiles = (a.N + kFcT - 1) / kFcT;
   double ll = 0.0;
-  unsigned long long npairs = 0;  // pairs of this block's tiles (thread 0)
-  // the next tile's masks and rows (as stored) are requested while this one is used
+  unsigned long long npairs = 0;  // pairs of this half's tiles (its thread 0)
   uint32_t mnext = 0u;
-  uint4 xnext[XPT];
-  auto fetch = [&](int64_t t) {
+  uint4 xnext[PREFETCH ? XPT : 1];
+  auto load_x = [&](int64_t t, uint4* dst, bool to_smem) {
     const int64_t r0 = t * kFcT;
     const int rows = (int)min((int64_t)kFcT, a.N - r0);
-    if (tid < kFcT) mnext = tid < rows ? __ldg(a.mask + r0 + tid) : 0u;
 #pragma unroll
     for (int c = 0; c < XPT; ++c) {
-      const int e = tid + c * kFcThreads, r = e / C16, q = e % C16;
-      xnext[c] = r < rows ? __ldg(reinterpret_cast<const uint4*>(
-                                static_cast<const unsigned char*>(a.X) + (size_t)(r0 + r) * RB) + q)
-                          : make_uint4(0u, 0u, 0u, 0u);
+      const int e = tid + c * TH, r = e / C16, q = e % C16;
+      const uint4 v = r < rows ? __ldg(reinterpret_cast<const uint4*>(
+                                     static_cast<const unsigned char*>(a.X) + (size_t)(r0 + r) * RB) + q)
+                               : make_uint4(0u, 0u, 0u, 0u);
+      if (to_smem) reinterpret_cast<uint4*>(xs)[e] = v;
+      else dst[c] = v;
     }
   };
-  if ((int64_t)blockIdx.x < ntiles) fetch(blockIdx.x);
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  auto load_mask = [&](int64_t t) {
     const int64_t r0 = t * kFcT;
     const int rows = (int)min((int64_t)kFcT, a.N - r0);
-    __syncthreads();  // the previous tile's tables are no longer read
+    return tid < rows && tid < kFcT ? __ldg(a.mask + r0 + tid) : 0u;
+  };
+  const int64_t t_first = (int64_t)blockIdx.x * NH + half, t_step = (int64_t)gridDim.x * NH;
+  if constexpr (PREFETCH) {
+    if (t_first < ntiles) {
+      mnext = load_mask(t_first);
+      load_x(t_first, xnext, false);
+    }
+  }
+  for (int64_t t = t_first; t < ntiles; t += t_step) {
+    const int64_t r0 = t * kFcT;
+    const int rows = (int)min((int64_t)kFcT, a.N - r0);
+    hsync();  // the previous tile's tables are no longer read
     // masks (component-major bit columns by ballot) and the rows of X
+    if constexpr (!PREFETCH) mnext = load_mask(t);
     if (tid < kFcT) {
       const uint32_t m = mnext & valid;
       msk[tid] = m;
@@ -238,13 +272,17 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
         if (lane == 0) cm[k * NW + warp] = b;
       }
     }
+    if constexpr (PREFETCH) {
 #pragma unroll
-    for (int c = 0; c < XPT; ++c) {
-      const int e = tid + c * kFcThreads;
-      reinterpret_cast<uint4*>(xs)[e] = xnext[c];
+      for (int c = 0; c < XPT; ++c) reinterpret_cast<uint4*>(xs)[tid + c * TH] = xnext[c];
+      if (t + t_step < ntiles) {
+        mnext = load_mask(t + t_step);
+        load_x(t + t_step, xnext, false);
+      }
+    } else {
+      load_x(t, nullptr, true);
     }
-    if (t + gridDim.x < ntiles) fetch(t + gridDim.x);
-    __syncthreads();
+    hsync();
     // pair and task offsets per component (a task: two pairs of a component)
     if (warp == 0) {
       int cnt = 0;
@@ -260,7 +298,7 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
       if (lane < K) { offs[lane + 1] = inc; toff[lane + 1] = tin; }
       if (lane == 0) { offs[0] = 0; toff[0] = 0; }
     }
-    __syncthreads();
+    hsync();
     // the pair list: component-major, rows ascending
     if (tid < kFcT) {
       const uint32_t m = msk[tid], lt = (1u << lane) - 1u;
@@ -271,11 +309,11 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
         prow[pos] = (uint8_t)tid;
       }
     }
-    __syncthreads();
+    hsync();
     const int nt = toff[K];
     if (tid == 0) npairs += (uint32_t)offs[K];
     int kk = 0;
-    for (int tk = tid; tk < nt; tk += kFcThreads) {
+    for (int tk = tid; tk < nt; tk += TH) {
       while (toff[kk + 1] <= tk) ++kk;
       const int p = offs[kk] + 2 * (tk - toff[kk]);
       const bool two = p + 1 < offs[kk + 1];
@@ -302,7 +340,7 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
       lval[p] = __fsub_rn(sC[kk], __fmul_rn(0.5f, da));
       if (two) lval[p + 1] = __fsub_rn(sC[kk], __fmul_rn(0.5f, db));
     }
-    __syncthreads();
+    hsync();
     // LSE_n over the point's candidates in component order
     if (tid < rows) {
       const uint32_t m = msk[tid], lt = (1u << lane) - 1u;
@@ -321,17 +359,18 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
       ll += (double)l;
     }
   }
+  // the block's log-likelihood: warps in order (both halves), fixed
   __shared__ double red[kFcThreads / 32];
   ll = warp_sum(ll);
   __syncthreads();
-  if (lane == 0) red[warp] = ll;
+  if ((tid0 & 31) == 0) red[tid0 >> 5] = ll;
   __syncthreads();
-  if (tid == 0) {
+  if (tid0 == 0) {
     double s = 0.0;
     for (int w = 0; w < kFcThreads / 32; ++w) s += red[w];
     a.ll_part[blockIdx.x] = s;
-    if (npairs) atomicAdd(&a.st->cand_pairs, npairs);
   }
+  if (tid == 0 && npairs) atomicAdd(&a.st->cand_pairs, npairs);
 }
 
 template <int D>
@@ -587,24 +626,27 @@ __global__ void fc_mask_all_kernel(uint32_t* mask, int64_t N, int K, const float
     mask[i] = valid;
 }
 
-size_t fc_lse_smem(int D, int K, int xdtype) {
+// fc_lse shared memory: W, means, biases and nh sets of tile tables.
+size_t fc_lse_smem(int D, int K, int xdtype, int nh) {
   const size_t rb = (size_t)D * (xdtype == GMM_F32 ? 4 : 2);
-  return sizeof(float) * ((size_t)K * fc_wstride(D) + (size_t)K * D + kFcMaxK) + kFcT * rb +
-         sizeof(float) * (size_t)kFcT * K +
-         sizeof(uint32_t) * ((size_t)K * (kFcT / 32) + kFcT) + sizeof(int) * (2 * kFcMaxK + 5) +
-         (size_t)kFcT * K;
+  const size_t tile = (size_t)kFcT * rb + sizeof(float) * (size_t)kFcT * K +
+                      sizeof(uint32_t) * ((size_t)K * (kFcT / 32) + kFcT) +
+                      sizeof(int) * (2 * kFcMaxK + 4) + (((size_t)kFcT * K + 15) / 16) * 16;
+  return sizeof(float) * ((size_t)K * fc_wstride(D) + (size_t)K * D + kFcMaxK) + nh * tile;
 }
 
 template <int D, int XT>
 cudaError_t run_fc(const FcArgs& a, int parts, cudaStream_t s) {
-  const size_t sl = fc_lse_smem(D, a.K, XT);
-  cudaError_t e = cudaFuncSetAttribute(fc_lse_kernel<D, XT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl);
+  // two half blocks when their tile tables fit next to W
+  const bool two = fc_lse_smem(D, a.K, XT, 2) <= (size_t)220 * 1024;
+  const size_t sl = fc_lse_smem(D, a.K, XT, two ? 2 : 1);
+  auto kern = two ? fc_lse_kernel<D, XT, 2> : fc_lse_kernel<D, XT, 1>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl);
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (a.N + kFcT - 1) / kFcT;
   {
     ProfScope prof("fc_lse_kernel", s);
-    fc_lse_kernel<D, XT><<<(int)min((int64_t)kFcGrid, ntiles), kFcThreads, sl, s>>>(a);
+    kern<<<(int)min((int64_t)kFcGrid, ntiles), kFcThreads, sl, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const size_t ss = FsLayout<D>::BYTES;
@@ -631,7 +673,7 @@ cudaError_t fc_screen(const void* X, int64_t N, int D, int K, const void* prepar
 // shared memory of one fc_lse block.
 bool fc_eligible(int D, int K, int cov) {
   if (cov != GMM_COV_FULL || !(D == 16 || D == 32 || D == 64) || K < 1 || K > kFcMaxK) return false;
-  return fc_lse_smem(D, K, GMM_F32) <= (size_t)200 * 1024;
+  return fc_lse_smem(D, K, GMM_F32, 1) <= (size_t)200 * 1024;
 }
 
 // Log-likelihood partials fc_estep writes (fc_lse blocks).
