@@ -78,8 +78,9 @@ typedef struct {
  * full covariance).  min_s0: a component whose responsibility sum s0 is
  * below it keeps its mean and covariance (its weight becomes s0/N).
  * flags: GMM_OPT_CUDA_CORES (bit 0) computes every log-density on CUDA cores
- * even where the tensor-core screening path applies (diagonal / isotropic
- * covariance, D = 64 or 128); other bits reserved, 0. */
+ * even where a tensor-core screening path applies (diagonal / isotropic
+ * covariance with D = 64 or 128; full covariance with D = 32 or 64, K <= 32,
+ * K D <= 1024, fp16 X); other bits reserved, 0. */
 typedef struct {
   float ridge_rel;
   float var_floor;
@@ -139,12 +140,20 @@ gmm_status gmm_prepare(const gmm_params* p, int D, int K, gmm_cov_type cov, cons
  *   M: pi' = s0/N, mu' = c + s1/s0, Sigma' = M2/s0 (the same value as
  *      s2/s0 - mu' mu'^T without its cancellation; iso: mean of the
  *      diagonal), floored at var_floor; empty rule with min_s0.
- *   Where the tensor-core path applies (diagonal / isotropic covariance,
- *   D = 64 or 128), every pair is screened with a rigorous error bound and
- *   the pairs within 40 nats of the point's best log joint are evaluated
- *   exactly in fp32; LSE_n and the statistics use those, and every other pair
- *   carries less than 4.3e-18 of its point's responsibility.  Points with more
- *   candidates than a list holds take the CUDA-core path, which uses all K.
+ *   Where a tensor-core path applies (diagonal / isotropic covariance with
+ *   D = 64 or 128: the contraction [x, x^2] . [mu / var, -1 / (2 var)]; full
+ *   covariance with D = 32 or 64, K <= 32, K D <= 1024 and fp16 X: the
+ *   product W_k x, W = L^-1 ([LP] sec. 1.2)), every pair is screened with a
+ *   rigorous error bound and the pairs within 40 nats of the point's best
+ *   log joint are evaluated exactly in fp32; LSE_n and the statistics use
+ *   those, and every other pair carries less than 4.3e-18 of its point's
+ *   responsibility.  Diagonal points with more candidates than the screen's
+ *   lists hold are evaluated, with their candidate masks, by CUDA-core
+ *   kernels that stage the parameters in shared memory; points with a
+ *   non-finite coordinate take the CUDA-core path, which uses all K.  Full
+ *   covariance outside those shapes (and bf16 / fp32 X, without the screen:
+ *   every component a candidate) uses the same exact kernels or the
+ *   CUDA-core path.
  * params:     in: the current parameters; out: updated in place (stream order).
  * loglik_dev: one double, written with sum_n LSE_n at the INPUT parameters.
  * lse_dev:    optional N floats, LSE_n at the input parameters (NULL: skipped).
