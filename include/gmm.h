@@ -113,8 +113,13 @@ size_t gmm_prepared_bytes(int D, int K, gmm_cov_type cov);
  *         fp32, log|Sigma_k| = 2 sum log L_ii;
  *   diag / iso: inverse variances 1/sigma^2 and sum log sigma^2.
  *   All: bias c_k = log pi_k - log|Sigma_k|/2 - (D/2) log 2 pi, the mean, and
- *   the split fp16 operand blocks the tensor-core kernels read.
- * p:         input parameters (device, fp32).
+ *   the fp16 operand blocks the tensor-core screens read (diagonal: the
+ *   scaled [mu / var, -1 / (2 var)] chunks; full covariance with D = 32 / 64
+ *   and K D <= 1024: fp16(W_k / s_k) and the screen's bound coefficients).
+ * p:         input parameters (device, fp32).  A model stored in fp16 (the
+ *            pages' IVF setting) is passed widened to fp32: every fp16 value
+ *            is an fp32 value, so the preprocessing sees exactly the stored
+ *            model.
  * prepared:  device buffer of gmm_prepared_bytes(D, K, cov) bytes, written.
  * flags_dev: K int32 flag words (GMM_FLAG_RIDGE / GMM_FLAG_NOT_PD), written;
  *            may be NULL.
