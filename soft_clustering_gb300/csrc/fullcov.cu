@@ -20,14 +20,16 @@
 //             per point: LSE_n over its candidates in component order, and
 //             the log-likelihood.
 //   fc_stats  a block per (component, partition of the points): the
-//             partition's candidates of the component, their log joints
-//             recomputed a thread per point (bit-identical to fc_lse),
-//             g = exp(l - LSE_n) and y = x - mu gathered into chunks of up to
-//             256 points; per chunk s0, the chunk mean and the second moment
-//             about it in fp32 (4 x 4 register tiles of the lower triangle),
-//             merged into the block's fp64 sums with the pairwise update of
-//             Chan, Golub and LeVeque.  The partial written per (partition,
-//             component) is [S0 | S1 about mu | M2 about the block mean].
+//             partition's candidates of the component queued in a ring and
+//             taken in chunks of 256 points, their log joints recomputed a
+//             thread per point (bit-identical to fc_lse), g = exp(l - LSE_n)
+//             and y = x - mu; per chunk s0, the chunk mean and the second
+//             moment about it in fp32 (a thread per register block of the
+//             lower triangle and slice of the chunk's points, the slices
+//             then summed in order), merged into the block's fp64 sums with
+//             the pairwise update of Chan, Golub and LeVeque.  The partial
+//             written per (partition, component) is
+//             [S0 | S1 about mu | M2 about the block mean].
 // Every sum has a fixed order, so the results are the same on every run.
 #include <math.h>
 
@@ -44,6 +46,7 @@ constexpr int kFcGrid = 152;       // fc_lse blocks (fixed: the log-likelihood p
 constexpr int kFsThreads = 256;    // fc_stats block
 constexpr int kFsTile = 1024;      // partition points per mask tile (four per thread)
 constexpr int kFsChunk = 256;      // candidate points per fp32 chunk
+constexpr int kFsRing = 2048;      // pending candidates (ring)
 
 // Floats of one component's padded W.  The rows 4m .. 4m + 3 hold 4(m + 1)
 // floats each (zero beyond the diagonal), stored interleaved by 16-byte
@@ -375,16 +378,20 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_lse_kernel(const FcArgs a) {
 
 template <int D>
 struct FsShape {
-  static constexpr int M = D / 4;
-  static constexpr int NB = M * (M + 1) / 2;    // 4 x 4 blocks of the lower triangle
-  static constexpr int YS = D + 4;              // padded chunk row
-  static constexpr int G = kFsThreads / D;      // row groups of the chunk's first moment
-  static_assert(NB <= kFsThreads, "one thread per block of the second moment");
+  static constexpr int BE = D >= 64 ? 8 : 4;     // edge of a second-moment register block
+  static constexpr int MB = D / BE;
+  static constexpr int NBB = MB * (MB + 1) / 2;  // blocks of the lower triangle
+  static constexpr int NS = kFsThreads / NBB;    // slices of the chunk's points
+  static constexpr int BE2 = BE * BE;
+  static constexpr int YS = D + 4;               // padded chunk row
+  static constexpr int G = kFsThreads / D;       // row groups of the chunk's first moment
+  static_assert(NS >= 1, "one thread per block and slice");
+  static_assert(NS * NBB * BE2 <= kFsChunk * YS, "slice partials fit in the chunk rows");
 };
 
 // fc_stats shared memory: the component's W (padded rows) and mean, the
 // chunk (y rows and g), chunk mean, first-moment partials, fp64 running sums
-// and the mask tile's candidate list.
+// and the ring of pending candidates.
 template <int D>
 struct FsLayout {
   using S = FsShape<D>;
@@ -399,17 +406,19 @@ struct FsLayout {
   static constexpr size_t S1R = DM + sizeof(double) * D;
   static constexpr size_t MR = S1R + sizeof(double) * D;
   static constexpr size_t M2R = MR + sizeof(double) * D;
-  static constexpr size_t CAND = M2R + sizeof(double) * S::NB * 16;
-  static constexpr size_t WCNT = CAND + sizeof(uint32_t) * kFsTile;
+  static constexpr size_t CAND = M2R + sizeof(double) * S::NBB * S::BE2;
+  static constexpr size_t WCNT = CAND + sizeof(uint32_t) * kFsRing;
   static constexpr size_t BYTES = WCNT + sizeof(int) * (kFsThreads / 32);
   static_assert(kFsTile == 4 * kFsThreads, "four mask words a thread");
+  static_assert(kFsRing >= kFsChunk + kFsTile && (kFsRing & (kFsRing - 1)) == 0,
+                "a power-of-two ring holding a tile past a partial chunk");
 };
 
 template <int D, int XT>
 __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a, int64_t rows_per_part) {
   using S = FsShape<D>;
   using L = FsLayout<D>;
-  constexpr int YS = S::YS, F = 1 + D + D * (D + 1) / 2;
+  constexpr int YS = S::YS, BE = S::BE, BE2 = S::BE2, F = 1 + D + D * (D + 1) / 2;
   extern __shared__ __align__(16) unsigned char smb[];
   float* sW = reinterpret_cast<float*>(smb + L::W);
   float* sMu = reinterpret_cast<float*>(smb + L::MU);
@@ -441,7 +450,7 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
     s1r[i] = 0.0;
     mr[i] = 0.0;
   }
-  for (int i = tid; i < S::NB * 16; i += kFsThreads) m2r[i] = 0.0;
+  for (int i = tid; i < S::NBB * BE2; i += kFsThreads) m2r[i] = 0.0;
   if (tid == 0) sc[0] = 0.0;
   __syncthreads();
 
@@ -479,48 +488,108 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
     if (tid == 0) sc[2] = sc[0] > 0.0 ? sc[0] * s0c / (sc[0] + s0c) : 0.0;
     __syncthreads();
     if (tid == 0) sc[0] += s0c;
-    if (tid < S::NB) {
-      int A = (int)((sqrtf(8.f * tid + 1.f) - 1.f) * 0.5f);
-      while ((A + 1) * (A + 2) / 2 <= tid) ++A;
-      while (A * (A + 1) / 2 > tid) --A;
-      const int B = tid - A * (A + 1) / 2;
-      const float4 ma = *reinterpret_cast<const float4*>(mc + 4 * A);
-      const float4 mb = *reinterpret_cast<const float4*>(mc + 4 * B);
-      float2 acc[4][2];
+    // the chunk's rows about the chunk mean, in place
+    for (int e = tid; e < fill * D; e += kFsThreads) {
+      const int n = e / D, d = e % D;
+      ys[n * YS + d] = __fsub_rn(ys[n * YS + d], mc[d]);
+    }
+    __syncthreads();
+    // thread (block bi, slice sl): block bi = (A, B) of the lower triangle over
+    // the points sl, sl + NS, ...; g (y_a - m_a) (y_b - m_b) in fp32
+    const int bi = tid % S::NBB, sl = tid / S::NBB;
+    int A = 0;
+    while ((A + 1) * (A + 2) / 2 <= bi) ++A;
+    const int B = bi - A * (A + 1) / 2;
+    float2 acc[BE][BE / 2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
-#pragma unroll 4
-      for (int n = 0; n < fill; ++n) {
+    for (int i = 0; i < BE; ++i)
+#pragma unroll
+      for (int j = 0; j < BE / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+    if (sl < S::NS) {
+#pragma unroll 2
+      for (int n = sl; n < fill; n += S::NS) {
         const float g = gch[n];
-        const float4 ya = *reinterpret_cast<const float4*>(ys + n * YS + 4 * A);
-        const float4 yb = *reinterpret_cast<const float4*>(ys + n * YS + 4 * B);
-        const float2 b01 = sub2(make_float2(yb.x, yb.y), make_float2(mb.x, mb.y));
-        const float2 b23 = sub2(make_float2(yb.z, yb.w), make_float2(mb.z, mb.w));
-        const float ua[4] = {__fmul_rn(g, __fsub_rn(ya.x, ma.x)), __fmul_rn(g, __fsub_rn(ya.y, ma.y)),
-                             __fmul_rn(g, __fsub_rn(ya.z, ma.z)), __fmul_rn(g, __fsub_rn(ya.w, ma.w))};
+        float ca[BE];
+        float2 cb[BE / 2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[i][0] = fma2(make_float2(ua[i], ua[i]), b01, acc[i][0]);
-          acc[i][1] = fma2(make_float2(ua[i], ua[i]), b23, acc[i][1]);
+        for (int v = 0; v < BE / 4; ++v) {
+          const float4 qa = *reinterpret_cast<const float4*>(ys + n * YS + BE * A + 4 * v);
+          const float4 qb = *reinterpret_cast<const float4*>(ys + n * YS + BE * B + 4 * v);
+          ca[4 * v] = qa.x;
+          ca[4 * v + 1] = qa.y;
+          ca[4 * v + 2] = qa.z;
+          ca[4 * v + 3] = qa.w;
+          cb[2 * v] = make_float2(qb.x, qb.y);
+          cb[2 * v + 1] = make_float2(qb.z, qb.w);
+        }
+#pragma unroll
+        for (int i = 0; i < BE; ++i) {
+          const float u = __fmul_rn(g, ca[i]);
+#pragma unroll
+          for (int j = 0; j < BE / 2; ++j) acc[i][j] = fma2(make_float2(u, u), cb[j], acc[i][j]);
         }
       }
-      const double fac = sc[2];
-      double* m2 = m2r + tid * 16;
+    }
+    __syncthreads();  // every read of the rows is done: the slice partials go there
+    float* part = ys;
+    if (sl < S::NS) {
+      float* pp = part + (sl * S::NBB + bi) * BE2;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const double da = dm[4 * A + i];
-        const float v[4] = {acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y};
+      for (int i = 0; i < BE; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) m2[i * 4 + j] += (double)v[j] + fac * da * dm[4 * B + j];
-      }
+        for (int j = 0; j < BE / 4; ++j)
+          *reinterpret_cast<float4*>(pp + i * BE + 4 * j) =
+              make_float4(acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y);
+    }
+    __syncthreads();
+    // the slices summed in order, merged into the fp64 sums
+    const double fac = sc[2];
+    for (int e = tid; e < S::NBB * BE2; e += kFsThreads) {
+      const int bb = e / BE2, r = e % BE2;
+      float v = 0.f;
+      for (int q = 0; q < S::NS; ++q) v = __fadd_rn(v, part[(q * S::NBB + bb) * BE2 + r]);
+      int Ae = 0;
+      while ((Ae + 1) * (Ae + 2) / 2 <= bb) ++Ae;
+      const int Be = bb - Ae * (Ae + 1) / 2;
+      m2r[e] += (double)v + fac * dm[BE * Ae + r / BE] * dm[BE * Be + r % BE];
     }
     __syncthreads();
   };
 
+  // One chunk: a thread per candidate of the ring from `head`: y = x - mu,
+  // the exact log joint (bit-identical to fc_lse) and g = exp(l - LSE_n).
+  auto solve = [&](uint32_t head, int ng) {
+    if (tid < ng) {
+      const uint32_t row = cand[(head + tid) & (kFsRing - 1)];
+      const float lr = __ldg(a.lse + row);
+      float2 y2[D / 2];
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        const float4 xv = load4<XT>(a.X, (size_t)row * D + 4 * c4);
+        const float4 mv = *reinterpret_cast<const float4*>(sMu + 4 * c4);
+        y2[2 * c4] = sub2(make_float2(xv.x, xv.y), make_float2(mv.x, mv.y));
+        y2[2 * c4 + 1] = sub2(make_float2(xv.z, xv.w), make_float2(mv.z, mv.w));
+      }
+      // ((p0 + p1) + (p2 + p3)), as fc_lse
+      const float d2 = __fadd_rn(__fadd_rn(fc_part<D>(sW, y2, 0), fc_part<D>(sW, y2, 1)),
+                                 __fadd_rn(fc_part<D>(sW, y2, 2), fc_part<D>(sW, y2, 3)));
+      const float l = __fsub_rn(ck, __fmul_rn(0.5f, d2));
+      float* yr = ys + tid * YS;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4)
+        *reinterpret_cast<float4*>(yr + 4 * c4) =
+            make_float4(y2[2 * c4].x, y2[2 * c4].y, y2[2 * c4 + 1].x, y2[2 * c4 + 1].y);
+      gch[tid] = expf(l - lr);
+    }
+    __syncthreads();
+    process_chunk(ng);
+  };
+
   // Mask tiles of kFsTile points, four consecutive points a thread (the next
-  // tile's masks are requested before this one is used); candidates of k in
-  // point order; then a thread per candidate, in groups that fill the chunk.
-  int fill = 0;
+  // tile's masks are requested before this one is used); the candidates of k
+  // appended to the ring in point order; every full chunk of the ring taken
+  // at once, so each chunk is evaluated by all the block's threads.
+  uint32_t head = 0u, tail = 0u;
   uint4 mnext = make_uint4(0u, 0u, 0u, 0u);
   auto fetch = [&](int64_t t0) {
     const int64_t rr = t0 + 4 * tid;
@@ -553,42 +622,14 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
       if (w < warp) base += wcnt[w];
       ncand += wcnt[w];
     }
-    for (uint32_t b = bits; b; b &= b - 1u) cand[base++] = (uint32_t)(t0 + 4 * tid + __ffs(b) - 1);
+    // fewer than kFsChunk are pending, so the tile's at most kFsTile fit
+    for (uint32_t b = bits; b; b &= b - 1u)
+      cand[(tail + (uint32_t)base++) & (kFsRing - 1)] = (uint32_t)(t0 + 4 * tid + __ffs(b) - 1);
     __syncthreads();
-    for (int g0 = 0; g0 < ncand;) {
-      const int ng = min(min(kFsThreads, ncand - g0), kFsChunk - fill);
-      if (tid < ng) {
-        const uint32_t row = cand[g0 + tid];
-        const float lr = __ldg(a.lse + row);
-        float2 y2[D / 2];
-#pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-          const float4 xv = load4<XT>(a.X, (size_t)row * D + 4 * c4);
-          const float4 mv = *reinterpret_cast<const float4*>(sMu + 4 * c4);
-          y2[2 * c4] = sub2(make_float2(xv.x, xv.y), make_float2(mv.x, mv.y));
-          y2[2 * c4 + 1] = sub2(make_float2(xv.z, xv.w), make_float2(mv.z, mv.w));
-        }
-        // ((p0 + p1) + (p2 + p3)), as fc_lse
-        const float d2 = __fadd_rn(__fadd_rn(fc_part<D>(sW, y2, 0), fc_part<D>(sW, y2, 1)),
-                                   __fadd_rn(fc_part<D>(sW, y2, 2), fc_part<D>(sW, y2, 3)));
-        const float l = __fsub_rn(ck, __fmul_rn(0.5f, d2));
-        float* yr = ys + (fill + tid) * YS;
-#pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4)
-          *reinterpret_cast<float4*>(yr + 4 * c4) =
-              make_float4(y2[2 * c4].x, y2[2 * c4].y, y2[2 * c4 + 1].x, y2[2 * c4 + 1].y);
-        gch[fill + tid] = expf(l - lr);
-      }
-      __syncthreads();
-      fill += ng;
-      g0 += ng;
-      if (fill == kFsChunk) {
-        process_chunk(fill);
-        fill = 0;
-      }
-    }
+    tail += (uint32_t)ncand;
+    for (; tail - head >= (uint32_t)kFsChunk; head += kFsChunk) solve(head, kFsChunk);
   }
-  if (fill > 0) process_chunk(fill);
+  if (tail != head) solve(head, (int)(tail - head));
   // the block's [S0 | S1 about mu | M2 about the block mean] into slot p
   // (the second moments first: merging reads the old first moments)
   const double S0n = sc[0];
@@ -598,8 +639,8 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
     while ((aa + 1) * (aa + 2) / 2 <= e) ++aa;
     while (aa * (aa + 1) / 2 > e) --aa;
     const int bb = e - aa * (aa + 1) / 2;
-    const int A = aa >> 2, B = bb >> 2;
-    double v = m2r[(A * (A + 1) / 2 + B) * 16 + (aa & 3) * 4 + (bb & 3)];
+    const int A = aa / BE, B = bb / BE;
+    double v = m2r[(A * (A + 1) / 2 + B) * BE2 + (aa % BE) * BE + bb % BE];
     if (a.accumulate) {
       v += out[1 + D + e];
       if (S0o > 0.0 && S0n > 0.0) {
