@@ -383,10 +383,11 @@ struct FsShape {
   static constexpr int NBB = MB * (MB + 1) / 2;  // blocks of the lower triangle
   static constexpr int NS = kFsThreads / NBB;    // slices of the chunk's points
   static constexpr int BE2 = BE * BE;
+  static constexpr int PS = BE2 + 4;             // padded stride of a slice partial
   static constexpr int YS = D + 4;               // padded chunk row
   static constexpr int G = kFsThreads / D;       // row groups of the chunk's first moment
   static_assert(NS >= 1, "one thread per block and slice");
-  static_assert(NS * NBB * BE2 <= kFsChunk * YS, "slice partials fit in the chunk rows");
+  static_assert(NS * NBB * PS <= kFsChunk * YS, "slice partials fit in the chunk rows");
 };
 
 // fc_stats shared memory: the component's W (padded rows) and mean, the
@@ -488,14 +489,9 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
     if (tid == 0) sc[2] = sc[0] > 0.0 ? sc[0] * s0c / (sc[0] + s0c) : 0.0;
     __syncthreads();
     if (tid == 0) sc[0] += s0c;
-    // the chunk's rows about the chunk mean, in place
-    for (int e = tid; e < fill * D; e += kFsThreads) {
-      const int n = e / D, d = e % D;
-      ys[n * YS + d] = __fsub_rn(ys[n * YS + d], mc[d]);
-    }
-    __syncthreads();
     // thread (block bi, slice sl): block bi = (A, B) of the lower triangle over
-    // the points sl, sl + NS, ...; g (y_a - m_a) (y_b - m_b) in fp32
+    // the points sl, sl + NS, ...; g (y_a - m_a) (y_b - m_b) in fp32 about the
+    // chunk mean m
     const int bi = tid % S::NBB, sl = tid / S::NBB;
     int A = 0;
     while ((A + 1) * (A + 2) / 2 <= bi) ++A;
@@ -506,25 +502,28 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
 #pragma unroll
       for (int j = 0; j < BE / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
     if (sl < S::NS) {
-#pragma unroll 2
+      float2 ma[BE / 2], mb[BE / 2];
+#pragma unroll
+      for (int v = 0; v < BE / 2; ++v) {
+        ma[v] = *reinterpret_cast<const float2*>(mc + BE * A + 2 * v);
+        mb[v] = *reinterpret_cast<const float2*>(mc + BE * B + 2 * v);
+      }
+#pragma unroll 1
       for (int n = sl; n < fill; n += S::NS) {
         const float g = gch[n];
-        float ca[BE];
-        float2 cb[BE / 2];
+        float2 ca[BE / 2], cb[BE / 2];
 #pragma unroll
         for (int v = 0; v < BE / 4; ++v) {
           const float4 qa = *reinterpret_cast<const float4*>(ys + n * YS + BE * A + 4 * v);
           const float4 qb = *reinterpret_cast<const float4*>(ys + n * YS + BE * B + 4 * v);
-          ca[4 * v] = qa.x;
-          ca[4 * v + 1] = qa.y;
-          ca[4 * v + 2] = qa.z;
-          ca[4 * v + 3] = qa.w;
-          cb[2 * v] = make_float2(qb.x, qb.y);
-          cb[2 * v + 1] = make_float2(qb.z, qb.w);
+          ca[2 * v] = sub2(make_float2(qa.x, qa.y), ma[2 * v]);
+          ca[2 * v + 1] = sub2(make_float2(qa.z, qa.w), ma[2 * v + 1]);
+          cb[2 * v] = sub2(make_float2(qb.x, qb.y), mb[2 * v]);
+          cb[2 * v + 1] = sub2(make_float2(qb.z, qb.w), mb[2 * v + 1]);
         }
 #pragma unroll
         for (int i = 0; i < BE; ++i) {
-          const float u = __fmul_rn(g, ca[i]);
+          const float u = __fmul_rn(g, (i & 1) ? ca[i / 2].y : ca[i / 2].x);
 #pragma unroll
           for (int j = 0; j < BE / 2; ++j) acc[i][j] = fma2(make_float2(u, u), cb[j], acc[i][j]);
         }
@@ -533,7 +532,7 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
     __syncthreads();  // every read of the rows is done: the slice partials go there
     float* part = ys;
     if (sl < S::NS) {
-      float* pp = part + (sl * S::NBB + bi) * BE2;
+      float* pp = part + (sl * S::NBB + bi) * S::PS;
 #pragma unroll
       for (int i = 0; i < BE; ++i)
 #pragma unroll
@@ -547,7 +546,7 @@ __global__ void __launch_bounds__(kFsThreads, 2) fc_stats_kernel(const FcArgs a,
     for (int e = tid; e < S::NBB * BE2; e += kFsThreads) {
       const int bb = e / BE2, r = e % BE2;
       float v = 0.f;
-      for (int q = 0; q < S::NS; ++q) v = __fadd_rn(v, part[(q * S::NBB + bb) * BE2 + r]);
+      for (int q = 0; q < S::NS; ++q) v = __fadd_rn(v, part[(q * S::NBB + bb) * S::PS + r]);
       int Ae = 0;
       while ((Ae + 1) * (Ae + 2) / 2 <= bb) ++Ae;
       const int Be = bb - Ae * (Ae + 1) / 2;
