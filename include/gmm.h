@@ -255,15 +255,13 @@ gmm_status gmm_last_device_status(void* ws, void* stream);
  * covariance); sizes that need more than 64 MiB are rejected with
  * GMM_ERR_WORKSPACE (and a message on stderr) before anything is queued.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, once per device, with that device current) and
- * keeps it for the life of the process, so the library must not be used
- * across a cudaDeviceReset of that device; make that first call before any
- * stream capture.  Every call shares the one array, so calls that overlap
- * on the GPU (other streams, other host threads) race: serialise them.  The
- * call synchronises `stream` before it returns, and returns the first
- * device-side condition of this call (GMM_ERR_NOT_PD, GMM_ERR_NONFINITE) or
- * GMM_OK.
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress).  Every call shares the one array, so calls that
+ * overlap on the GPU (other streams, other host threads) race: serialise
+ * them.  The call synchronises `stream` before it returns (it reads the
+ * device status into host memory), so it cannot be used under stream
+ * capture, and returns the first device-side condition of this call
+ * (GMM_ERR_NOT_PD, GMM_ERR_NONFINITE) or GMM_OK.
  */
 gmm_status gmm_em_step_noalloc(const void* X, gmm_dtype xdtype, int64_t N, int D, int K,
                                gmm_params* params, gmm_cov_type cov, const gmm_opts* opts,

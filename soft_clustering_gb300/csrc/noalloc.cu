@@ -12,7 +12,6 @@
 // library routine.
 #include <stdio.h>
 
-#include <mutex>
 
 #include "gmm_internal.cuh"
 
@@ -39,23 +38,13 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch per device, looked up once.
-std::mutex g_addr_mu;
-void* g_addr[64] = {};
-
+// Device address of g_noalloc_scratch in the current context, looked up on
+// every call (a cached address would outlive a device reset).
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_addr[dev] = p;
-  }
-  *out = g_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
