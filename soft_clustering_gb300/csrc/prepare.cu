@@ -85,7 +85,8 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
                                     PreparedLayout L, void* prepared, DeviceStatus* st) {
   extern __shared__ double A[];  // D*D
   __shared__ double red[32];
-  __shared__ int s_fail;
+  __shared__ double s_rd[128];   // 1 / L_jj
+  __shared__ double s_col[128];  // the column of W being formed
   const int k = blockIdx.x;
   const float* S = cov + (size_t)k * D * D;
   double tr = 0.0;
@@ -102,27 +103,37 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
     }
     for (int i = threadIdx.x; i < D * D; i += blockDim.x)
       A[i] = (double)S[i] + ((i / D) == (i % D) ? add : 0.0);
-    if (threadIdx.x == 0) s_fail = 0;
     __syncthreads();
+    int bad = 0;
     for (int j = 0; j < D; ++j) {
-      if (threadIdx.x == 0) {
-        double p = A[j * D + j];
-        if (!(p > 0.0) || !isfinite(p)) s_fail = 1;
-        else A[j * D + j] = sqrt(p);
+      // every thread reads the same pivot and takes its root and reciprocal
+      const double p = A[j * D + j];
+      if (!(p > 0.0) || !isfinite(p)) {
+        bad = 1;
+        break;
       }
-      __syncthreads();
-      if (s_fail) break;
-      const double rl = 1.0 / A[j * D + j];
+      const double ljj = sqrt(p), rl = 1.0 / ljj;
       for (int i = j + 1 + threadIdx.x; i < D; i += blockDim.x) A[i * D + j] *= rl;
       __syncthreads();
-      // trailing update of the lower triangle: a thread per row
-      for (int i = j + 1 + threadIdx.x; i < D; i += blockDim.x) {
-        const double lij = A[i * D + j];
-        for (int l = j + 1; l <= i; ++l) A[i * D + l] = fma(-lij, A[l * D + j], A[i * D + l]);
+      if (threadIdx.x == 0) A[j * D + j] = ljj;  // every thread has read the pivot
+      // trailing update of the lower triangle, A[i][l] -= L[i][j] L[l][j] for
+      // j < l <= i, spread evenly: rows j+1+pp and D-1-pp form a pair of
+      // D-j elements in all, taken by four threads
+      const int m = D - 1 - j, npairs = (m + 1) / 2;
+      const int sub = threadIdx.x & 3;
+      for (int pp = threadIdx.x >> 2; pp < npairs; pp += blockDim.x >> 2) {
+        const int ia = j + 1 + pp, ib = D - 1 - pp;
+        const int la = ia - j, tot = ia == ib ? la : la + (ib - j);
+        const double lia = A[ia * D + j], lib = A[ib * D + j];
+        for (int c = sub; c < tot; c += 4) {
+          const bool ra = c < la;
+          const int i = ra ? ia : ib, l = j + 1 + (ra ? c : c - la);
+          A[i * D + l] = fma(-(ra ? lia : lib), A[l * D + j], A[i * D + l]);
+        }
       }
       __syncthreads();
     }
-    fail = s_fail;
+    fail = bad;
     __syncthreads();
   }
   if (fail) flags |= GMM_FLAG_NOT_PD;
@@ -133,19 +144,47 @@ __global__ void prepare_full_kernel(const float* __restrict__ pi, const float* _
   }
   ld = block_sum(ld, red);
   // W = L^-1 in place, columns from the last: with the trailing block
-  // already inverted, W[i][j] = -(sum_{t=j+1..i} W[i][t] L[t][j]) / L[j][j]
-  // (a thread per row i; every L[t][j] is read before column j changes).
+  // already inverted, W[i][j] = -(sum_{t=j+1..i} W[i][t] L[t][j]) / L[j][j].
+  // Rows j+1+pp and D-1-pp form a pair, its dot products split over four
+  // threads (terms sub, sub+4, ... of the pair's terms; partial sums
+  // combined as (s0 + s1) + (s2 + s3)); every L[t][j] is read before column
+  // j changes.
   if (!fail) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) s_rd[d] = 1.0 / A[d * D + d];
+    __syncthreads();
+    const int sub = threadIdx.x & 3;
     for (int j = D - 1; j >= 0; --j) {
-      const double wjj = 1.0 / A[j * D + j];
-      double v = 0.0;
-      const int i = j + 1 + threadIdx.x;
-      if (i < D) {
-        for (int t = j + 1; t <= i; ++t) v = fma(A[i * D + t], A[t * D + j], v);
-        v = -v * wjj;
+      const double wjj = s_rd[j];
+      const int m = D - 1 - j, npairs = (m + 1) / 2;
+      for (int base = 0; base < npairs; base += blockDim.x >> 2) {
+        const int pp = base + (threadIdx.x >> 2);
+        double va = 0.0, vb = 0.0;
+        int ia = 0, ib = 0;
+        if (pp < npairs) {
+          ia = j + 1 + pp;
+          ib = D - 1 - pp;
+          const int la = ia - j, tot = ia == ib ? la : la + (ib - j);
+          for (int c = sub; c < tot; c += 4) {
+            if (c < la) {
+              const int t = j + 1 + c;
+              va = fma(A[ia * D + t], A[t * D + j], va);
+            } else {
+              const int t = j + 1 + c - la;
+              vb = fma(A[ib * D + t], A[t * D + j], vb);
+            }
+          }
+        }
+        va += __shfl_xor_sync(0xffffffffu, va, 1);
+        vb += __shfl_xor_sync(0xffffffffu, vb, 1);
+        va += __shfl_xor_sync(0xffffffffu, va, 2);
+        vb += __shfl_xor_sync(0xffffffffu, vb, 2);
+        if (pp < npairs) {
+          if (sub == 0) s_col[ia] = -va * wjj;
+          if (sub == 1 && ib != ia) s_col[ib] = -vb * wjj;
+        }
       }
       __syncthreads();
-      if (i < D) A[i * D + j] = v;
+      for (int i = j + 1 + threadIdx.x; i < D; i += blockDim.x) A[i * D + j] = s_col[i];
       if (threadIdx.x == 0) A[j * D + j] = wjj;
       __syncthreads();
     }
