@@ -12,8 +12,8 @@
 // window of the rigorous screen), and three kernels take them with the
 // parameters staged in shared memory:
 //   dense_lse     block (half a mask chunk: 64 components, partition): a
-//                 warp per point, its four groups of eight lanes taking the
-//                 candidates of 16 columns each, each evaluated in the
+//                 warp per point, its four groups of eight lanes taking
+//                 every fourth of the point's candidates, each evaluated in the
 //                 centred fp32 form sum_d w_d (x_d - mu_d)^2 (lane: D/8
 //                 dimensions, then a butterfly sum over the group), the
 //                 groups' running max and sum (base 2) combined into the
@@ -124,9 +124,10 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
     s_c[i] = k < a.K ? __ldg(a.bias + k) : -INFINITY;
   }
   __syncthreads();
-  // a warp per point; group q of eight lanes takes the point's candidates
-  // among columns 16 q .. 16 q + 15 of the half chunk, in column order.  The
-  // log-sum-exp runs in base 2 (values l log2(e)).  The next point's row,
+  // a warp per point; group q of eight lanes takes the point's candidates of
+  // rank q, q + 4, q + 8, ... among the half chunk's (column order), so the
+  // four groups' counts differ by at most one.  The log-sum-exp runs in
+  // base 2 (values l log2(e)).  The next point's row,
   // masks and coordinates are requested before this one is evaluated.
   constexpr float kLog2e = 1.4426950408889634f;
   const uint32_t stride = (uint32_t)P * (kThreads / 32);
@@ -147,17 +148,21 @@ __global__ void __launch_bounds__(kThreads, 3) dense_lse_kernel(const DenseArgs 
     for (int c = 0; c < CPL; ++c)
 #pragma unroll
       for (int t = 0; t < 4; ++t) x[c][t] = xn[c][t];
-    // this group's 16 columns
-    uint32_t bits = ((grp < 2 ? mn.x : mn.y) >> (16 * (grp & 1))) & 0xffffu;
+    // the half chunk's candidates dealt over the groups by rank: group q
+    // takes the candidates of rank q, q + 4, ... in column order
+    uint64_t bits = ((uint64_t)mn.y << 32) | mn.x;
     if (i + stride < n) fetch(i + stride);
-    npairs += __popc(bits);
-    int steps = __popc(bits);
-    steps = max(steps, __shfl_xor_sync(0xffffffffu, steps, 8));
-    steps = max(steps, __shfl_xor_sync(0xffffffffu, steps, 16));
+    const int ntot = __popcll(bits);
+    const int steps = (ntot + 3) >> 2;  // the same for every group of the warp
+    npairs += ntot > grp ? (uint32_t)((ntot - grp + 3) >> 2) : 0u;
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+      if (q < grp) bits &= bits - 1u;
     float mx = -INFINITY, sum = 0.f;
     for (int st = 0; st < steps; ++st) {
-      const int col = bits ? 16 * grp + __ffs(bits) - 1 : -1;
-      bits &= bits - 1u;
+      const int col = bits ? __ffsll((long long)bits) - 1 : -1;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) bits &= bits - 1u;
       float acc = 0.f;
       if (col >= 0) {
         float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
